@@ -1,0 +1,494 @@
+#!/usr/bin/env python
+"""Benchmark of the weight-quantized SwiGLU MLP on GB300.
+
+Headline (one JSON line on stdout): microseconds per MLP call of the dense
+27B-class NVFP4 decode MLP (hidden K=5120, intermediate I=17408, M=1 token),
+i.e. the gate/up GEMV with fused SwiGLU followed by the down GEMV, on
+synthetic seeded weights. One "step" = one MLP call. Inputs are resident in
+HBM; the weights rotate over several independent device copies whose total
+exceeds twice the L2 size, so every call streams its weights from HBM.
+
+Also reported: the HBM roofline fraction of the dominant kernel (gate/up
+GEMV, timed with CUDA events on its stream), the end-to-end time through the
+host-buffer entry point, the CPU oracle timed on this host, and secondary
+workloads (tiny NVFP4, FP8 W8A16 decode, routed-expert AWQ, NVFP4 prefill
+when the tensor-core GEMM is available).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from weight_quantized_swiglu_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "MLP us/call (dense NVFP4 decode, M=1)"
+UNIT = "us/call"
+K_HID, I_INT = gen.DENSE_K, gen.DENSE_I
+
+
+def nvfp4_bytes(K, I):
+    """Algorithmic bytes of one NVFP4 MLP call: packed codes + E4M3 scales of
+    gate, up, down + the three fp32 globals (activations excluded)."""
+    return 3 * (I * K // 2 + I * K // 16) + 12
+
+
+def nvfp4_gateup_bytes(K, I):
+    return 2 * (I * K // 2 + I * K // 16)
+
+
+def fp8_bytes(K, I):
+    return 3 * I * K + 4 * (I + I + K)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_src_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d:
+        return None
+    if d.get("src_sha") != kernel_src_sha(d["src_files"]):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(device_index)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# ----------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# measurements
+# ----------------------------------------------------------------------------
+def n_rotating_copies(bytes_per_copy):
+    import torch
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    return max(2, math.ceil(2 * l2 / bytes_per_copy) + 1), l2
+
+
+def bench_headline(args, world, rank, local, pk):
+    import torch
+    import weight_quantized_swiglu_gb300 as q
+    case = gen.workload_case("dense_nvfp4_decode", 0)
+    R, l2 = n_rotating_copies(nvfp4_bytes(K_HID, I_INT))
+    mlps = [q.QuantMLP.from_case(case) for _ in range(R)]
+    x = torch.from_numpy(case.x.view(np.int16)).cuda()
+    out = torch.empty((1, K_HID), dtype=torch.int16, device="cuda")
+    s = torch.cuda.current_stream()
+    for i in range(max(args.warmup, 3)):
+        m = mlps[i % R]
+        m.forward_stage(0, x, None, 1, stream=s)
+        m.forward_stage(1, None, out, 1, stream=s)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    time.sleep(0.25)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        m = mlps[i % R]
+        ev[i][0].record(s)
+        m.forward_stage(0, x, None, 1, stream=s)
+        ev[i][1].record(s)
+        m.forward_stage(1, None, out, 1, stream=s)
+        ev[i][2].record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    gu_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    dn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    total_ms = max_over_ranks(world, total_ms)
+    us_per_call = total_ms * 1e3 / K
+    mlps[0].check()
+
+    # end-to-end through the host-buffer entry point (pinned buffers; the
+    # copies and the completion wait are inside the timed region)
+    xh = torch.from_numpy(case.x.view(np.int16)).pin_memory()
+    oh = torch.empty((1, K_HID), dtype=torch.int16).pin_memory()
+    for i in range(3):
+        mlps[i % R].forward_host(xh, oh)
+    n_e2e = max(10, min(K, 2000))
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        mlps[i % R].forward_host(xh, oh)
+    e2e_s = max_over_ranks(world, time.perf_counter() - t0)
+    for m in mlps:
+        m.close()
+
+    gu_bytes = nvfp4_gateup_bytes(K_HID, I_INT)
+    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    res = {
+        "us_per_call": us_per_call,
+        "ms_per_step": total_ms / K,
+        "gu_us": gu_ms * 1e3,
+        "down_us": dn_ms * 1e3,
+        "hbm_gbs_call": nvfp4_bytes(K_HID, I_INT) / (us_per_call * 1e-6) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<NVFP4,NT=1,gate+up,SwiGLU>",
+                     "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
+                     "algorithmic_bytes_per_launch": gu_bytes,
+                     "traffic": ncu_traffic("gemv_nvfp4_gateup_m1")},
+        "e2e": {"value": e2e_s * 1e6 / n_e2e, "unit": UNIT, "h2d_bytes_per_step": K_HID * 2,
+                "d2h_bytes_per_step": K_HID * 2, "steps": n_e2e},
+        "clocks": clocks,
+        "rotating_copies": R,
+        "l2_bytes": l2,
+        "gpu_launches": 2 * K,
+    }
+    return res, case
+
+
+def bench_dense_secondary(name, variant, reps, fmt_bytes):
+    """us/call of another dense workload (rotating copies, CUDA events)."""
+    import torch
+    import weight_quantized_swiglu_gb300 as q
+    case = gen.workload_case(name, variant)
+    R, _ = n_rotating_copies(fmt_bytes)
+    mlps = [q.QuantMLP.from_case(case) for _ in range(R)]
+    x = torch.from_numpy(case.x.view(np.int16)).cuda()
+    out = torch.empty((case.M, case.K), dtype=torch.int16, device="cuda")
+    for i in range(5):
+        mlps[i % R].forward(x, out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        mlps[i % R].forward(x, out)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    for m in mlps:
+        m.close()
+    return {"M": case.M, "us_per_call": us, "gbs": fmt_bytes / (us * 1e-6) / 1e9, "tokens_per_s": case.M / (us * 1e-6)}
+
+
+def bench_moe(meta_bytes=4):
+    """Routed-expert M=1: CUDA-graph replay of 48 calls, 7 samples, median
+    (hot = the same 10 experts; rotating = 480 experts cycled)."""
+    import torch
+    import weight_quantized_swiglu_gb300 as q
+    c = gen.gen_moe_case(gen.seed_for(4, 0))
+    moe = q.MoeAWQ.from_case(c, meta_bytes)
+    x = torch.from_numpy(c.x_fp16.view(np.int16)).cuda()
+    rw = torch.from_numpy(c.router_w).cuda()
+    hot_ids = torch.from_numpy(c.ids).cuda()
+    rot_ids = torch.from_numpy(np.stack([gen.rotating_ids(k) for k in range(48)])).cuda()
+    out = torch.empty(c.K, dtype=torch.int16, device="cuda")
+    s = torch.cuda.Stream()
+    res = {}
+    for mode in ("hot", "rotating"):
+        with torch.cuda.stream(s):
+            for k in range(3):
+                moe.forward(x, q.DT_FP16, hot_ids if mode == "hot" else rot_ids[k], rw, out, stream=s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for k in range(48):
+                moe.forward(x, q.DT_FP16, hot_ids if mode == "hot" else rot_ids[k], rw, out, stream=s)
+        g.replay()
+        torch.cuda.synchronize()
+        samples = []
+        for _ in range(7):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            samples.append(e0.elapsed_time(e1))
+        ms48 = statistics.median(samples)
+        uniq = len({int(i) for i in (c.ids if mode == "hot" else gen.rotating_ids(0)) if 0 <= i < c.E})
+        per_exp = 2 * c.I * c.K // 2 + 2 * c.I * (c.K // 32) * meta_bytes + c.K * c.I // 2 + c.K * (c.I // 32) * meta_bytes
+        res[mode] = {"ms_per_48_calls": ms48, "us_per_call": ms48 * 1e3 / 48,
+                     "gbs": uniq * per_exp / (ms48 * 1e-3 / 48) / 1e9}
+    moe.close()
+    return res
+
+
+def bench_prefill(M, reps, pk):
+    import torch
+    import weight_quantized_swiglu_gb300 as q
+    case = gen.gen_dense_case("nvfp4", K_HID, I_INT, M, gen.seed_for(3, 0 if M == 512 else 1))
+    mlp = q.QuantMLP.from_case(case)
+    x = torch.from_numpy(case.x.view(np.int16)).cuda()
+    out = torch.empty((M, K_HID), dtype=torch.int16, device="cuda")
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        mlp.forward(x, out, path=q.PATH_GEMM)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mlp.forward(x, out, path=q.PATH_GEMM)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    mlp.check()
+    mlp.close()
+    ms = statistics.median(times)
+    flops = 2.0 * M * 3 * I_INT * K_HID
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"M": M, "ms_per_call": ms, "tflops": tf, "frac_bf16_peak": tf / pk["bf16_tflops_sustained"],
+            "tokens_per_s": M / (ms * 1e-3), "l2": "512 MB buffer written between calls"}
+
+
+def cpu_baseline(case, budget_s=10.0):
+    import oracle
+    oracle.build()
+    oracle.dense_forward(case)  # warm (tables, page-in)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.dense_forward(case)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": el * 1e6 / n, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} full oracle MLP calls (K=5120, I=17408, M=1, fp64) in {el:.1f} s"}
+
+
+# ----------------------------------------------------------------------------
+# the reference arm: the CPU oracle as it stands
+# ----------------------------------------------------------------------------
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    case = gen.workload_case("dense_nvfp4_decode", 0)
+    t0 = time.perf_counter()
+    oracle.dense_forward(case)
+    t_full = time.perf_counter() - t0
+    budget = 150.0
+    frac = min(1.0, budget / max(1e-9, (args.steps + args.warmup) * t_full))
+    sub = None
+    if frac < 1.0:
+        # each step computes a row block of gate, up and down (a fixed fraction
+        # of the weights) with the oracle's projection routine; the time is
+        # scaled by the fraction of weights processed
+        ni = max(16, int(I_INT * frac) // 16 * 16)
+        nk = max(16, int(K_HID * frac) // 16 * 16)
+        cut = lambda p, n: gen.Proj(p.fmt, n, p.K, p.w[:n], p.scale[:n], p.global_scale)
+        sub = (cut(case.gate, ni), cut(case.up, ni), cut(case.down, nk))
+        xact = gen.gen_x_only(7, 1, I_INT)
+        wfrac = (2 * ni * K_HID + nk * I_INT) / (2 * I_INT * K_HID + K_HID * I_INT)
+
+    def step():
+        if sub is None:
+            oracle.dense_forward(case)
+        else:
+            oracle.project(sub[0], case.x)
+            oracle.project(sub[1], case.x)
+            oracle.project(sub[2], xact)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    per_step_us = el * 1e6 / args.steps
+    value = per_step_us if sub is None else per_step_us / wfrac
+    sample = ("full oracle MLP call per step" if sub is None else
+              f"per step: rows 0:{sub[0].N} of gate/up and 0:{sub[2].N} of down ({wfrac:.4f} of the weights); "
+              f"us/call scaled by 1/{wfrac:.4f}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_us / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded NVFP4 weights, x ~ N(0,1) bf16)",
+            "config": {"workload": "dense_nvfp4_decode K=5120 I=17408 M=1", "K": K_HID, "I": I_INT, "M": 1,
+                       "fmt": "nvfp4"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path in this library)")
+    world, rank, local = dist_setup(args.gpus)
+    from weight_quantized_swiglu_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(world)
+    pk = peaks()
+    head, case = bench_headline(args, world, rank, local, pk)
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        import weight_quantized_swiglu_gb300 as q
+        extras["dense_nvfp4_decode_M4"] = bench_dense_secondary("dense_nvfp4_decode", 1, 400, nvfp4_bytes(K_HID, I_INT))
+        extras["dense_fp8_decode_M1"] = bench_dense_secondary("dense_fp8_decode", 0, 300, fp8_bytes(K_HID, I_INT))
+        extras["dense_fp8_decode_M16"] = bench_dense_secondary("dense_fp8_decode", 1, 300, fp8_bytes(K_HID, I_INT))
+        extras["tiny_nvfp4_M1"] = bench_dense_secondary("tiny_nvfp4", 0, 2000, nvfp4_bytes(gen.TINY_K, gen.TINY_I))
+        extras["moe_awq_m1_4B"] = bench_moe(4)
+        extras["moe_awq_m1_3B"] = bench_moe(3)
+        try:
+            extras["nvfp4_prefill_M512"] = bench_prefill(512, 5, pk)
+            extras["nvfp4_prefill_M8192"] = bench_prefill(8192, 3, pk)
+        except q.QmlpError as e:
+            extras["nvfp4_prefill"] = {"unavailable": str(e)}
+        torch.cuda.synchronize()
+
+    cpu = cpu_baseline(case, args.cpu_budget) if rank == 0 else None
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": head["us_per_call"],
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"],
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 weights, fp16 x fp16 -> fp32 MMA, bf16 act/out",
+        "data": "synthetic (seeded NVFP4 weights, x ~ N(0,1) bf16)",
+        "config": {"workload": "dense_nvfp4_decode K=5120 I=17408 M=1", "K": K_HID, "I": I_INT, "M": 1,
+                   "fmt": "nvfp4", "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": f"{head['rotating_copies']} rotating weight copies "
+                         f"({head['rotating_copies'] * nvfp4_bytes(K_HID, I_INT) / 1e6:.0f} MB > 2x L2 "
+                         f"{head['l2_bytes'] / 1e6:.0f} MB)"},
+        "hbm_gbs": head["hbm_gbs_call"],
+        "kernel_us": {"gate_up": head["gu_us"], "down": head["down_us"]},
+        "roofline": head["roofline"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "cpu_baseline": cpu,
+        "extras": extras,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

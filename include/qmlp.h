@@ -1,0 +1,227 @@
+/*
+ * qmlp.h -- C ABI of libqmlp.so, the weight-quantized SwiGLU MLP for GB300
+ * (sm_103a). Plain pointers and sizes only.
+ *
+ * The operation (vllm.cpp issue "tp>1 fp8w tail-MLP shard host-dequantizes
+ * every layer", "Proposed fix"):
+ *   act[m, i] = bf16( SiLU(sigma_g[i] * sum_k x[m,k] Wg[i,k]) *
+ *                          (sigma_u[i] * sum_k x[m,k] Wu[i,k]) )
+ *   out[m, o] = bf16( sigma_d[o] * sum_i act[m,i] Wd[o,i] )
+ * with the weights dequantized on the fly from resident packed bytes:
+ *   NVFP4 (Qwen3.8-27B-NVFP4, "NVFP4 numerics as implemented"):
+ *     W[n,k] = E2M1(nibble) * E4M3(scale[n, k/16]); byte k/2 of row n holds k
+ *     in its low nibble when k is even; sigma = fp32(1 / global_scale).
+ *   FP8 per-channel W8A16 (vllm.cpp issue, "Mechanism on the tp>1 path"):
+ *     W[n,k] = e4m3fn(w[n,k]); sigma[n] = scale[n] (fp32).
+ * SiLU(t) = t / (1 + exp(-t)). Accumulation is fp32 on the GPU; act is
+ * rounded to bf16 before the down projection; out is bf16.
+ *
+ * Conventions for every entry point:
+ *  - A status is returned; no entry point falls back to a CPU computation and
+ *    none aborts the process. QMLP_OK is 0.
+ *  - "device" pointers are CUDA device addresses on the current device;
+ *    "host" pointers are host addresses (pinned or pageable).
+ *  - All device pointers passed to forward calls must be 16-byte aligned.
+ *  - Streams: a CUstream/cudaStream_t value; NULL means the legacy default
+ *    stream. Forward calls only enqueue work (except *_host, which waits).
+ *  - One handle serves one stream at a time: its workspace is shared by all
+ *    calls on it.
+ *  - Validation happens before any launch; a rejected call launches nothing.
+ *  - Launch failures return QMLP_ERR_CUDA. Errors raised asynchronously by a
+ *    kernel surface on a later call or on the caller's synchronization; a
+ *    kernel that gives up a bounded wait records it in the handle, and
+ *    qmlp_check / qmlp_moe_check return QMLP_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef QMLP_H
+#define QMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* qmlp_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    QMLP_OK = 0,
+    QMLP_ERR_INVALID_ARG = 1,     /* null pointer, bad enum, bad count     */
+    QMLP_ERR_ALIGNMENT = 2,       /* a device pointer not 16-byte aligned  */
+    QMLP_ERR_ALIAS = 3,           /* output overlaps an input or workspace */
+    QMLP_ERR_SHAPE = 4,           /* K, I, M, E or topk outside the limits */
+    QMLP_ERR_UNSUPPORTED_ARCH = 5,/* device is not compute capability 10.3 */
+    QMLP_ERR_OOM = 6,             /* device allocation failed at create    */
+    QMLP_ERR_CUDA = 7,            /* a CUDA runtime call or launch failed  */
+    QMLP_ERR_DEVICE_TIMEOUT = 8   /* a kernel gave up a bounded wait       */
+} qmlp_status;
+
+typedef enum { QMLP_FMT_NVFP4 = 1, QMLP_FMT_FP8_PC = 2 } qmlp_format;
+typedef enum { QMLP_DT_BF16 = 1, QMLP_DT_FP16 = 2 } qmlp_dtype;
+typedef enum { QMLP_META_3B = 3, QMLP_META_4B = 4 } qmlp_meta;
+/* Kernel family used by a forward call: AUTO picks the GEMV family for
+ * M <= 16 and the tensor-core GEMM family above (NVFP4). */
+typedef enum { QMLP_PATH_AUTO = 0, QMLP_PATH_GEMV = 1, QMLP_PATH_GEMM = 2 } qmlp_path;
+
+/* One projection [N, K] as the checkpoint stores it. Pointers may be host or
+ * device memory; they are only read during qmlp_create.
+ *  NVFP4: w     = u8 [N, K/2], two E2M1 codes per byte, low nibble = even k
+ *         scale = u8 [N, K/16], E4M3 group scales
+ *         global_scale = fp32; the dequantization factor is 1/global_scale
+ *  FP8:   w     = u8 [N, K], e4m3fn codes
+ *         scale = fp32 [N], per output channel; global_scale is ignored */
+typedef struct {
+    const uint8_t* w;
+    const void* scale;
+    float global_scale;
+} qmlp_proj;
+
+/* Dense MLP description: hidden size K, intermediate size I, largest token
+ * count max_M any forward call will use. gate/up are [I, K], down is [K, I].
+ * Limits: K % 16 == 0, I % 16 == 0, 16 <= K, I <= 65536, 1 <= max_M <= 65536. */
+typedef struct {
+    qmlp_format fmt;
+    int K;
+    int I;
+    int max_M;
+    qmlp_proj gate;
+    qmlp_proj up;
+    qmlp_proj down;
+} qmlp_desc;
+
+typedef struct qmlp_s qmlp_t;
+
+/* Create a dense MLP handle. Copies the weights into memory the handle owns,
+ * reordered for the kernels (create-time repack; the weight bytes are kept
+ * packed, never expanded), computes sigma = fp32(1/global) for NVFP4, and
+ * allocates the forward workspace for max_M tokens. Synchronizes `stream`
+ * before returning, so the caller may free its buffers afterwards.
+ * Errors: INVALID_ARG (null/unknown fmt), SHAPE, UNSUPPORTED_ARCH, OOM, CUDA.
+ * On error *out is NULL and nothing is leaked. */
+qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* desc, qmlp_stream_t stream);
+
+/* Free every buffer owned by the handle (waits for its pending work). NULL is
+ * a no-op. */
+void qmlp_destroy(qmlp_t* h);
+
+/* The MLP block (see the top of this file) on M tokens.
+ *  x   = device bf16 [M, K] (row-major), read only
+ *  out = device bf16 [M, K] (row-major), written
+ * Allocates nothing; enqueues its kernels on `stream`.
+ * Errors: INVALID_ARG (null), ALIGNMENT (x/out not 16-B aligned), ALIAS (out
+ * overlaps x), SHAPE (M < 1 or M > max_M), CUDA. */
+qmlp_status qmlp_forward(qmlp_t* h, const void* x, int M, void* out, qmlp_stream_t stream);
+
+/* As qmlp_forward, forcing a kernel family (tests). GEMM requires NVFP4 and a
+ * handle created with max_M > 16; otherwise SHAPE. */
+qmlp_status qmlp_forward_path(qmlp_t* h, qmlp_path path, const void* x, int M, void* out,
+                              qmlp_stream_t stream);
+
+/* One half of the forward, for callers that overlap or time the two
+ * projections separately (stage 0 followed by stage 1 equals qmlp_forward):
+ *  stage 0: act = SwiGLU(x) into the handle's workspace; x = device bf16
+ *           [M, K]; out must be NULL.
+ *  stage 1: out = the down projection of the workspace act written by the
+ *           previous stage-0 call with the same M; x must be NULL; out =
+ *           device bf16 [M, K].
+ * Errors: as qmlp_forward_path (INVALID_ARG for a wrong NULL pattern). */
+qmlp_status qmlp_forward_stage(qmlp_t* h, int stage, qmlp_path path, const void* x, int M, void* out,
+                               qmlp_stream_t stream);
+
+/* End-to-end call from host buffers: copies x (host bf16 [M, K]) to the
+ * handle's staging buffer, runs the forward, copies the result back to
+ * out (host bf16 [M, K]) and waits for `stream`. Pinned host memory gives
+ * asynchronous copies; pageable memory works but serializes the copies.
+ * Errors: as qmlp_forward. */
+qmlp_status qmlp_forward_host(qmlp_t* h, const void* x_host, int M, void* out_host,
+                              qmlp_stream_t stream);
+
+/* Forward that also returns the intermediate: act = device bf16 [M, I]
+ * (the values the down projection consumed). Errors: as qmlp_forward_path,
+ * plus ALIAS if act overlaps x or out. */
+qmlp_status qmlp_forward_debug(qmlp_t* h, qmlp_path path, const void* x, int M, void* act,
+                               void* out, qmlp_stream_t stream);
+
+/* One projection in isolation, through the same kernels, with no scale
+ * factor applied (no 1/global, no per-channel scale) and fp32 output:
+ *   y[m, n] = sum_k x[m,k] * W[n,k],  W = E2M1*E4M3 (NVFP4) or e4m3fn (FP8)
+ *  which = 0 gate, 1 up (x is [M, K]); 2 down (x is [M, I]).
+ *  x = device bf16 [M, Kp], y = device fp32 [M, N].
+ * With a one-hot x this returns single decoded weights exactly.
+ * Errors: as qmlp_forward_path. */
+qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void* x, int M,
+                               float* y, qmlp_stream_t stream);
+
+/* Synchronize `stream` and report (then clear) a bounded-wait give-up
+ * recorded by this handle's kernels: OK or DEVICE_TIMEOUT (CUDA on a sticky
+ * device error). */
+qmlp_status qmlp_check(qmlp_t* h, qmlp_stream_t stream);
+
+/*
+ * Routed-expert AWQ int4 group-32 MLP, one token (1Cat-vLLM PR "[Kernel][SM70]
+ * Add native-g32 AWQ QPN M1 operator", "What it does"):
+ *   for each route r in router order with 0 <= ids[r] < E:
+ *     h      = x . W13[ids[r]]^T             (fp32 accumulation, N = 2I)
+ *     g, u   = fp16(h[:I]), fp16(h[I:])
+ *     act[r] = fp16(SiLU(g) * u)
+ *     y[r]   = fp16(act[r] . W2[ids[r]]^T)   (fp32 accumulation, N = K)
+ *   out = fp16( sum over valid r, in router order, of router_w[r] * y[r] )
+ *         (fp32 accumulation, no atomics)
+ * Weights: W[e, n, k] = half_fma(q, scale, bias): q is the u4 code (low nibble
+ * = even k), one metadata record per (e, n, k/32): 4-byte {fp16 scale, fp16
+ * bias} or 3-byte {fp16 scale, u8 zero} with bias = half(-zero*scale); records
+ * are little-endian, scale first. Invalid ids (< 0 or >= E) contribute zero;
+ * duplicate valid ids are separate routes with their own router weights.
+ */
+typedef struct {
+    int E;            /* experts                     */
+    int K;            /* hidden size (W13 in, W2 out) */
+    int I;            /* intermediate per expert     */
+    qmlp_meta meta;   /* 3- or 4-byte records        */
+    const uint8_t* w13;       /* [E, 2I, K/2]              host or device */
+    const uint8_t* w13_meta;  /* [E, 2I, K/32] x meta bytes              */
+    const uint8_t* w2;        /* [E, K, I/2]                             */
+    const uint8_t* w2_meta;   /* [E, K, I/32] x meta bytes               */
+} qmlp_moe_desc;
+
+typedef struct qmlp_moe_s qmlp_moe_t;
+
+/* Create a routed-expert handle: copies the banks into handle-owned device
+ * memory (reordered for the kernels, same bytes). Limits: K % 64 == 0,
+ * I % 32 == 0, 32 <= I <= 1024, 64 <= K <= 16384, 1 <= E. Synchronizes.
+ * Errors: INVALID_ARG, SHAPE, UNSUPPORTED_ARCH, OOM, CUDA. */
+qmlp_status qmlp_moe_create(qmlp_moe_t** out, const qmlp_moe_desc* desc, qmlp_stream_t stream);
+void qmlp_moe_destroy(qmlp_moe_t* h);
+
+/* The routed-expert step above for one token.
+ *  x          = device [K], bf16 or fp16 per xdt
+ *  expert_ids = device int32 [topk]  (read on the device: may change between
+ *               CUDA-graph replays)
+ *  router_w   = device fp32 [topk]
+ *  out        = device fp16 [K]
+ * 1 <= topk <= 16. Allocates nothing; graph-capturable.
+ * Errors: INVALID_ARG, ALIGNMENT, ALIAS (out overlaps x, ids or router_w),
+ * SHAPE, CUDA. */
+qmlp_status qmlp_moe_m1_forward(qmlp_moe_t* h, const void* x, qmlp_dtype xdt,
+                                const int32_t* expert_ids, const float* router_w, int topk,
+                                void* out, qmlp_stream_t stream);
+
+/* As qmlp_moe_m1_forward, also writing the per-stage fp16 tensors (device):
+ *  gu [topk, 2I], act [topk, I], y [topk, K]; rows of invalid routes are not
+ *  written. Any of gu/act/y may be NULL. */
+qmlp_status qmlp_moe_debug_stages(qmlp_moe_t* h, const void* x, qmlp_dtype xdt,
+                                  const int32_t* expert_ids, const float* router_w, int topk,
+                                  void* out, void* gu, void* act, void* y, qmlp_stream_t stream);
+
+qmlp_status qmlp_moe_check(qmlp_moe_t* h, qmlp_stream_t stream);
+
+/* Human-readable name of a status ("QMLP_OK", ...). Never NULL. */
+const char* qmlp_status_str(qmlp_status s);
+
+/* ABI version of this header (major * 100 + minor). */
+int qmlp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMLP_H */

@@ -1,0 +1,78 @@
+"""C-ABI library checks that need no GPU: it builds for sm_103a, loads, and
+exports every symbol include/qmlp.h declares; host-side validation rejects
+bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+import weight_quantized_swiglu_gb300 as q
+from weight_quantized_swiglu_gb300 import build as qbuild
+
+
+def declared_symbols():
+    txt = open(os.path.join(ROOT, "include", "qmlp.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmlp_[a-z0-9_]+)\s*\(", txt)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return q.lib()
+
+
+def test_header_declares_the_three_entry_points():
+    syms = declared_symbols()
+    for s in ("qmlp_create", "qmlp_forward", "qmlp_moe_m1_forward"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    syms = declared_symbols()
+    assert len(syms) >= 15
+    missing = [s for s in syms if not hasattr(L, s)]
+    assert not missing, missing
+
+
+def test_binding_signatures_cover_the_header():
+    assert set(declared_symbols()) == set(q._SIGS)
+
+
+def test_status_strings(L):
+    assert q.qmlp_status_str(0) == "QMLP_OK"
+    assert q.qmlp_status_str(8) == "QMLP_ERR_DEVICE_TIMEOUT"
+    assert q.qmlp_abi_version() == 100
+
+
+def test_null_arguments_are_rejected_without_a_device(L):
+    assert L.qmlp_forward(None, None, 1, None, None) == 1
+    assert L.qmlp_moe_m1_forward(None, None, 1, None, None, 1, None, None) == 1
+    h = ctypes.c_void_p()
+    assert L.qmlp_create(ctypes.byref(h), None, None) == 1
+    assert L.qmlp_create(None, None, None) == 1
+    L.qmlp_destroy(None)
+    L.qmlp_moe_destroy(None)
+
+
+def test_bad_shapes_are_rejected_before_the_device(L):
+    h = ctypes.c_void_p()
+    dummy = (ctypes.c_uint8 * 64)()
+    p = q.qmlp_proj(ctypes.addressof(dummy), ctypes.addressof(dummy), 1.0)
+    for K, I, M in ((24, 32, 1), (32, 40, 1), (32, 32, 0), (8, 32, 1)):
+        d = q.qmlp_desc(q.FMT_NVFP4, K, I, M, p, p, p)
+        assert L.qmlp_create(ctypes.byref(h), ctypes.byref(d), None) == 4, (K, I, M)
+    d = q.qmlp_desc(7, 32, 32, 1, p, p, p)
+    assert L.qmlp_create(ctypes.byref(h), ctypes.byref(d), None) == 1
+    m = q.qmlp_moe_desc(4, 100, 160, 4, ctypes.addressof(dummy), ctypes.addressof(dummy),
+                        ctypes.addressof(dummy), ctypes.addressof(dummy))
+    assert L.qmlp_moe_create(ctypes.byref(h), ctypes.byref(m), None) == 4
+    m = q.qmlp_moe_desc(4, 2560, 160, 5, ctypes.addressof(dummy), ctypes.addressof(dummy),
+                        ctypes.addressof(dummy), ctypes.addressof(dummy))
+    assert L.qmlp_moe_create(ctypes.byref(h), ctypes.byref(m), None) == 1
+
+
+def test_library_is_built_for_sm_103a_only():
+    assert qbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,598 @@
+// api.cu -- the C ABI of libqmlp.so (declared in include/qmlp.h).
+//
+// Host side only: argument validation (before any launch), handle ownership,
+// create-time residency and repack, workspace, and dispatch to the kernel
+// families. There is no CPU compute path anywhere in this library: a failed
+// launch returns QMLP_ERR_CUDA.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "internal.h"
+#include "qmlp.h"
+
+using namespace qmlp;
+
+namespace {
+
+constexpr int kMaxGemvM = 16;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+qmlp_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return QMLP_OK;
+    if (e == cudaErrorMemoryAllocation) return QMLP_ERR_OOM;
+    return QMLP_ERR_CUDA;
+}
+
+// Fault injection for host-side tests of the error paths: QMLP_FAULT_INJECT=
+// "alloc" makes device allocations fail, "launch" makes forward calls return
+// QMLP_ERR_CUDA before launching.
+bool fault(const char* what) {
+    const char* v = getenv("QMLP_FAULT_INJECT");
+    return v && strcmp(v, what) == 0;
+}
+
+struct Owner {
+    std::vector<void*> ptrs;
+    cudaError_t alloc(void** p, size_t bytes) {
+        *p = nullptr;
+        if (fault("alloc")) return cudaErrorMemoryAllocation;
+        if (bytes == 0) bytes = 16;
+        cudaError_t e = cudaMalloc(p, bytes);
+        if (e == cudaSuccess) ptrs.push_back(*p);
+        return e;
+    }
+    void release() {
+        for (void* p : ptrs) cudaFree(p);
+        ptrs.clear();
+    }
+};
+
+qmlp_status check_device(int* dev, int* num_sms) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return QMLP_ERR_CUDA;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess)
+        return QMLP_ERR_CUDA;
+    if (major != 10 || minor != 3) return QMLP_ERR_UNSUPPORTED_ARCH;
+    return QMLP_OK;
+}
+
+}  // namespace
+
+struct qmlp_s {
+    int fmt = 0, K = 0, I = 0, max_M = 0, device = 0, num_sms = 0;
+    GemvProj gv[3];  // gate, up, down
+    bool has_gemm = false;
+    GemmProj gm_gu, gm_d;
+    void* act = nullptr;       // bf16 [max_M, I]
+    float* part = nullptr;     // split-K partials
+    size_t part_cap = 0;
+    int* counters = nullptr;   // [Nt(gate/up) + Nt(down)]
+    int* err = nullptr;        // device error word
+    void* x_stage = nullptr;   // bf16 [max_M, K] (forward_host)
+    void* out_stage = nullptr; // bf16 [max_M, K]
+    Owner mem;
+};
+
+struct qmlp_moe_s {
+    int E = 0, K = 0, I = 0, meta = 0, device = 0, num_sms = 0;
+    uint8_t *w13 = nullptr, *w13_meta = nullptr, *w2 = nullptr, *w2_meta = nullptr;
+    __half* act_ws = nullptr;
+    int* err = nullptr;
+    Owner mem;
+};
+
+extern "C" {
+
+const char* qmlp_status_str(qmlp_status s) {
+    switch (s) {
+        case QMLP_OK: return "QMLP_OK";
+        case QMLP_ERR_INVALID_ARG: return "QMLP_ERR_INVALID_ARG";
+        case QMLP_ERR_ALIGNMENT: return "QMLP_ERR_ALIGNMENT";
+        case QMLP_ERR_ALIAS: return "QMLP_ERR_ALIAS";
+        case QMLP_ERR_SHAPE: return "QMLP_ERR_SHAPE";
+        case QMLP_ERR_UNSUPPORTED_ARCH: return "QMLP_ERR_UNSUPPORTED_ARCH";
+        case QMLP_ERR_OOM: return "QMLP_ERR_OOM";
+        case QMLP_ERR_CUDA: return "QMLP_ERR_CUDA";
+        case QMLP_ERR_DEVICE_TIMEOUT: return "QMLP_ERR_DEVICE_TIMEOUT";
+    }
+    return "QMLP_ERR_UNKNOWN";
+}
+
+int qmlp_abi_version(void) { return 100; }
+
+// ---------------------------------------------------------------------------
+// dense MLP
+// ---------------------------------------------------------------------------
+static qmlp_status load_proj(qmlp_t* h, const qmlp_proj& src, int N, int K, GemvProj& dst,
+                             uint8_t** w_tmp, uint8_t** s_tmp, cudaStream_t s) {
+    const bool nv = h->fmt == kNVFP4;
+    const size_t wbytes = (size_t)N * (nv ? K / 2 : K);
+    const size_t sbytes = nv ? (size_t)N * (K / 16) : (size_t)N * sizeof(float);
+    void *wt = nullptr, *st = nullptr, *wc = nullptr, *sc = nullptr;
+    cudaError_t e;
+    if ((e = h->mem.alloc(&wt, wbytes)) != cudaSuccess) return from_cuda(e);
+    if ((e = h->mem.alloc(&st, sbytes)) != cudaSuccess) return from_cuda(e);
+    if ((e = cudaMemcpyAsync(wt, src.w, wbytes, cudaMemcpyDefault, s)) != cudaSuccess) return QMLP_ERR_CUDA;
+    if ((e = cudaMemcpyAsync(st, src.scale, sbytes, cudaMemcpyDefault, s)) != cudaSuccess) return QMLP_ERR_CUDA;
+    if ((e = h->mem.alloc(&wc, gemv_codes_bytes(h->fmt, N, K))) != cudaSuccess) return from_cuda(e);
+    dst.N = N;
+    dst.K = K;
+    dst.Nt = N / kTileRows;
+    dst.Kc = (K + kChunkK - 1) / kChunkK;
+    dst.wc = static_cast<const uint4*>(wc);
+    if (nv) {
+        if ((e = h->mem.alloc(&sc, gemv_scales_bytes(h->fmt, N, K))) != cudaSuccess) return from_cuda(e);
+        dst.sc = static_cast<const uint2*>(sc);
+        dst.inv_g = 1.0f / src.global_scale;
+        e = repack_nvfp4_gemv(static_cast<uint8_t*>(wt), static_cast<uint8_t*>(st), N, K,
+                              static_cast<uint4*>(wc), static_cast<uint2*>(sc), s);
+    } else {
+        dst.chs = static_cast<const float*>(st);  // kept: per-channel scales
+        e = repack_fp8_gemv(static_cast<uint8_t*>(wt), N, K, static_cast<uint4*>(wc), s);
+    }
+    if (e != cudaSuccess) return QMLP_ERR_CUDA;
+    *w_tmp = static_cast<uint8_t*>(wt);
+    *s_tmp = static_cast<uint8_t*>(st);
+    return QMLP_OK;
+}
+
+static void free_tmp(qmlp_t* h, void* p) {
+    if (!p) return;
+    auto it = std::find(h->mem.ptrs.begin(), h->mem.ptrs.end(), p);
+    if (it != h->mem.ptrs.end()) {
+        cudaFree(p);
+        h->mem.ptrs.erase(it);
+    }
+}
+
+qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) {
+    if (!out) return QMLP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!d) return QMLP_ERR_INVALID_ARG;
+    if (d->fmt != QMLP_FMT_NVFP4 && d->fmt != QMLP_FMT_FP8_PC) return QMLP_ERR_INVALID_ARG;
+    if (!d->gate.w || !d->gate.scale || !d->up.w || !d->up.scale || !d->down.w || !d->down.scale)
+        return QMLP_ERR_INVALID_ARG;
+    if (d->K < 16 || d->I < 16 || d->K > 65536 || d->I > 65536 || d->K % 16 || d->I % 16 || d->max_M < 1 ||
+        d->max_M > 65536)
+        return QMLP_ERR_SHAPE;
+    if (d->fmt == QMLP_FMT_NVFP4 &&
+        (!(d->gate.global_scale != 0.0f) || !(d->up.global_scale != 0.0f) || !(d->down.global_scale != 0.0f)))
+        return QMLP_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    qmlp_status st = check_device(&dev, &sms);
+    if (st != QMLP_OK) return st;
+
+    qmlp_t* h = new qmlp_t();
+    h->fmt = d->fmt;
+    h->K = d->K;
+    h->I = d->I;
+    h->max_M = d->max_M;
+    h->device = dev;
+    h->num_sms = sms;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* tmp[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    const qmlp_proj* srcs[3] = {&d->gate, &d->up, &d->down};
+    const int Ns[3] = {d->I, d->I, d->K}, Ks[3] = {d->K, d->K, d->I};
+    cudaError_t e = cudaSuccess;
+    for (int p = 0; p < 3 && st == QMLP_OK; ++p)
+        st = load_proj(h, *srcs[p], Ns[p], Ks[p], h->gv[p], &tmp[2 * p], &tmp[2 * p + 1], s);
+
+    if (st == QMLP_OK && h->fmt == kNVFP4 && d->max_M > kMaxGemvM && gemm_supported(d->K, 2 * d->I) &&
+        gemm_supported(d->I, d->K)) {
+        void *gu = nullptr, *dn = nullptr;
+        if ((e = h->mem.alloc(&gu, gemm_tiles_bytes(2 * d->I, d->K))) != cudaSuccess) st = from_cuda(e);
+        else if ((e = h->mem.alloc(&dn, gemm_tiles_bytes(d->K, d->I))) != cudaSuccess) st = from_cuda(e);
+        else if (repack_nvfp4_gemm(tmp[0], tmp[1], tmp[2], tmp[3], 2 * d->I, d->K, true,
+                                   static_cast<uint8_t*>(gu), s) != cudaSuccess ||
+                 repack_nvfp4_gemm(tmp[4], tmp[5], nullptr, nullptr, d->K, d->I, false,
+                                   static_cast<uint8_t*>(dn), s) != cudaSuccess)
+            st = QMLP_ERR_CUDA;
+        if (st == QMLP_OK) {
+            h->has_gemm = true;
+            h->gm_gu.tiles = static_cast<uint8_t*>(gu);
+            h->gm_gu.N = 2 * d->I;
+            h->gm_gu.K = d->K;
+            h->gm_gu.inv_g0 = h->gv[0].inv_g;
+            h->gm_gu.inv_g1 = h->gv[1].inv_g;
+            h->gm_d.tiles = static_cast<uint8_t*>(dn);
+            h->gm_d.N = d->K;
+            h->gm_d.K = d->I;
+            h->gm_d.inv_g0 = h->gm_d.inv_g1 = h->gv[2].inv_g;
+        }
+    }
+    // workspace
+    if (st == QMLP_OK) {
+        void* p = nullptr;
+        const size_t Ntot = (size_t)(d->I / kTileRows) + (size_t)(d->K / kTileRows);
+        h->part_cap = gemv_part_elems(d->K, d->I, sms);
+        if ((e = h->mem.alloc(&h->act, (size_t)d->max_M * d->I * 2)) != cudaSuccess) st = from_cuda(e);
+        else if ((e = h->mem.alloc(&p, h->part_cap * sizeof(float))) != cudaSuccess) st = from_cuda(e);
+        else {
+            h->part = static_cast<float*>(p);
+            if ((e = h->mem.alloc(&p, Ntot * sizeof(int) + 16)) != cudaSuccess) st = from_cuda(e);
+            else {
+                h->counters = static_cast<int*>(p);
+                if (cudaMemsetAsync(p, 0, Ntot * sizeof(int) + 16, s) != cudaSuccess) st = QMLP_ERR_CUDA;
+            }
+        }
+        if (st == QMLP_OK) {
+            if ((e = h->mem.alloc(&p, 16)) != cudaSuccess) st = from_cuda(e);
+            else {
+                h->err = static_cast<int*>(p);
+                if (cudaMemsetAsync(p, 0, 16, s) != cudaSuccess) st = QMLP_ERR_CUDA;
+            }
+        }
+        if (st == QMLP_OK && (e = h->mem.alloc(&h->x_stage, (size_t)d->max_M * d->K * 2)) != cudaSuccess)
+            st = from_cuda(e);
+        if (st == QMLP_OK && (e = h->mem.alloc(&h->out_stage, (size_t)d->max_M * d->K * 2)) != cudaSuccess)
+            st = from_cuda(e);
+    }
+    if (st == QMLP_OK && cudaStreamSynchronize(s) != cudaSuccess) st = QMLP_ERR_CUDA;
+    // the checkpoint-layout copies are no longer needed (FP8 keeps its scales)
+    if (st == QMLP_OK) {
+        for (int p = 0; p < 3; ++p) {
+            free_tmp(h, tmp[2 * p]);
+            if (h->fmt == kNVFP4) free_tmp(h, tmp[2 * p + 1]);
+        }
+    }
+    if (st != QMLP_OK) {
+        cudaStreamSynchronize(s);
+        h->mem.release();
+        delete h;
+        return st;
+    }
+    *out = h;
+    return QMLP_OK;
+}
+
+void qmlp_destroy(qmlp_t* h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    h->mem.release();
+    delete h;
+}
+
+static qmlp_status validate_fwd(qmlp_t* h, const void* x, int M, const void* out, size_t out_elem_bytes,
+                                int out_cols) {
+    if (!h || !x || !out) return QMLP_ERR_INVALID_ARG;
+    if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(out)) return QMLP_ERR_ALIGNMENT;
+    (void)out_elem_bytes;
+    (void)out_cols;
+    return QMLP_OK;
+}
+
+static bool use_gemm(qmlp_t* h, qmlp_path path, int M) {
+    if (path == QMLP_PATH_GEMV) return false;
+    if (path == QMLP_PATH_GEMM) return true;
+    return h->has_gemm && M > kMaxGemvM;
+}
+
+// stage bit 0: gate/up + SwiGLU (x -> workspace act); bit 1: down (act -> out)
+static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void* x, int M, void* out,
+                              cudaStream_t s) {
+    if (fault("launch")) return QMLP_ERR_CUDA;
+    const bool gemm = use_gemm(h, path, M);
+    if (gemm && !h->has_gemm) return QMLP_ERR_SHAPE;
+    if (gemm) {
+        GemmLaunch g;
+        g.M = M;
+        g.err = h->err;
+        if (stages & 1) {
+            g.epi = kEpiSwiGLU;
+            g.w = h->gm_gu;
+            g.a = x;
+            g.out = h->act;
+            if (launch_gemm(g, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
+        }
+        if (stages & 2) {
+            g.epi = kEpiPlain;
+            g.w = h->gm_d;
+            g.a = h->act;
+            g.out = out;
+            if (launch_gemm(g, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
+        }
+        return QMLP_OK;
+    }
+    const size_t Ntg = (size_t)(h->I / kTileRows);
+    for (int m0 = 0; m0 < M; m0 += kMaxGemvM) {
+        const int mb = std::min(kMaxGemvM, M - m0);
+        GemvLaunch L;
+        L.fmt = h->fmt;
+        L.M = mb;
+        L.part = h->part;
+        L.part_cap = h->part_cap;
+        if (stages & 1) {
+            L.epi = kEpiSwiGLU;
+            L.p0 = h->gv[0];
+            L.p1 = h->gv[1];
+            L.x = static_cast<const uint8_t*>(x) + (size_t)m0 * h->K * 2;
+            L.out = static_cast<uint8_t*>(h->act) + (size_t)m0 * h->I * 2;
+            L.counters = h->counters;
+            if (launch_gemv(L, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
+        }
+        if (stages & 2) {
+            L.epi = kEpiPlain;
+            L.p0 = h->gv[2];
+            L.p1 = GemvProj();
+            L.x = static_cast<const uint8_t*>(h->act) + (size_t)m0 * h->I * 2;
+            L.out = static_cast<uint8_t*>(out) + (size_t)m0 * h->K * 2;
+            L.counters = h->counters + Ntg;
+            if (launch_gemv(L, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
+        }
+    }
+    return QMLP_OK;
+}
+
+static qmlp_status run_forward(qmlp_t* h, qmlp_path path, const void* x, int M, void* out, cudaStream_t s) {
+    return run_stages(h, path, 3, x, M, out, s);
+}
+
+qmlp_status qmlp_forward_path(qmlp_t* h, qmlp_path path, const void* x, int M, void* out,
+                              qmlp_stream_t stream) {
+    qmlp_status st = validate_fwd(h, x, M, out, 2, 0);
+    if (st != QMLP_OK) return st;
+    if (path != QMLP_PATH_AUTO && path != QMLP_PATH_GEMV && path != QMLP_PATH_GEMM) return QMLP_ERR_INVALID_ARG;
+    const size_t xb = (size_t)M * h->K * 2;
+    if (overlaps(x, xb, out, xb)) return QMLP_ERR_ALIAS;
+    if (overlaps(out, xb, h->act, (size_t)h->max_M * h->I * 2)) return QMLP_ERR_ALIAS;
+    return run_forward(h, path, x, M, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmlp_status qmlp_forward_stage(qmlp_t* h, int stage, qmlp_path path, const void* x, int M, void* out,
+                               qmlp_stream_t stream) {
+    if (!h) return QMLP_ERR_INVALID_ARG;
+    if (path != QMLP_PATH_AUTO && path != QMLP_PATH_GEMV && path != QMLP_PATH_GEMM) return QMLP_ERR_INVALID_ARG;
+    if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
+    if (stage == 0) {
+        if (!x || out) return QMLP_ERR_INVALID_ARG;
+        if (!aligned16(x)) return QMLP_ERR_ALIGNMENT;
+        if (overlaps(x, (size_t)M * h->K * 2, h->act, (size_t)h->max_M * h->I * 2)) return QMLP_ERR_ALIAS;
+        return run_stages(h, path, 1, x, M, nullptr, reinterpret_cast<cudaStream_t>(stream));
+    }
+    if (stage == 1) {
+        if (x || !out) return QMLP_ERR_INVALID_ARG;
+        if (!aligned16(out)) return QMLP_ERR_ALIGNMENT;
+        if (overlaps(out, (size_t)M * h->K * 2, h->act, (size_t)h->max_M * h->I * 2)) return QMLP_ERR_ALIAS;
+        return run_stages(h, path, 2, nullptr, M, out, reinterpret_cast<cudaStream_t>(stream));
+    }
+    return QMLP_ERR_INVALID_ARG;
+}
+
+qmlp_status qmlp_forward(qmlp_t* h, const void* x, int M, void* out, qmlp_stream_t stream) {
+    return qmlp_forward_path(h, QMLP_PATH_AUTO, x, M, out, stream);
+}
+
+qmlp_status qmlp_forward_debug(qmlp_t* h, qmlp_path path, const void* x, int M, void* act, void* out,
+                               qmlp_stream_t stream) {
+    qmlp_status st = qmlp_forward_path(h, path, x, M, out, stream);
+    if (st != QMLP_OK) return st;
+    if (!act) return QMLP_ERR_INVALID_ARG;
+    if (!aligned16(act)) return QMLP_ERR_ALIGNMENT;
+    const size_t ab = (size_t)M * h->I * 2;
+    if (overlaps(act, ab, x, (size_t)M * h->K * 2) || overlaps(act, ab, out, (size_t)M * h->K * 2))
+        return QMLP_ERR_ALIAS;
+    return cudaMemcpyAsync(act, h->act, ab, cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? QMLP_OK
+               : QMLP_ERR_CUDA;
+}
+
+qmlp_status qmlp_forward_host(qmlp_t* h, const void* x_host, int M, void* out_host, qmlp_stream_t stream) {
+    if (!h || !x_host || !out_host) return QMLP_ERR_INVALID_ARG;
+    if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)M * h->K * 2;
+    if (cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return QMLP_ERR_CUDA;
+    qmlp_status st = run_forward(h, QMLP_PATH_AUTO, h->x_stage, M, h->out_stage, s);
+    if (st != QMLP_OK) return st;
+    if (cudaMemcpyAsync(out_host, h->out_stage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return QMLP_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? QMLP_OK : QMLP_ERR_CUDA;
+}
+
+qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void* x, int M, float* y,
+                               qmlp_stream_t stream) {
+    if (!h || !x || !y) return QMLP_ERR_INVALID_ARG;
+    if (which < 0 || which > 2) return QMLP_ERR_INVALID_ARG;
+    if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(y)) return QMLP_ERR_ALIGNMENT;
+    const GemvProj& P = h->gv[which];
+    if (overlaps(x, (size_t)M * P.K * 2, y, (size_t)M * P.N * 4)) return QMLP_ERR_ALIAS;
+    if (fault("launch")) return QMLP_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (use_gemm(h, path, M)) {
+        if (!h->has_gemm || which == 1) return QMLP_ERR_SHAPE;
+        GemmLaunch g;
+        g.epi = kEpiRaw;
+        g.w = which == 0 ? h->gm_gu : h->gm_d;
+        g.a = x;
+        g.M = M;
+        g.out = y;
+        g.err = h->err;
+        return launch_gemm(g, h->num_sms, s) == cudaSuccess ? QMLP_OK : QMLP_ERR_CUDA;
+    }
+    const size_t Ntg = (size_t)(h->I / kTileRows);
+    for (int m0 = 0; m0 < M; m0 += kMaxGemvM) {
+        const int mb = std::min(kMaxGemvM, M - m0);
+        GemvLaunch L;
+        L.fmt = h->fmt;
+        L.epi = kEpiRaw;
+        L.p0 = P;
+        L.x = static_cast<const uint8_t*>(x) + (size_t)m0 * P.K * 2;
+        L.M = mb;
+        L.out = y + (size_t)m0 * P.N;
+        L.part = h->part;
+        L.part_cap = h->part_cap;
+        L.counters = which == 2 ? h->counters + Ntg : h->counters;
+        if (launch_gemv(L, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
+    }
+    return QMLP_OK;
+}
+
+qmlp_status qmlp_check(qmlp_t* h, qmlp_stream_t stream) {
+    if (!h) return QMLP_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QMLP_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QMLP_ERR_CUDA;
+    if (v != 0) {
+        cudaMemset(h->err, 0, sizeof(int));
+        return QMLP_ERR_DEVICE_TIMEOUT;
+    }
+    return QMLP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// routed-expert AWQ
+// ---------------------------------------------------------------------------
+qmlp_status qmlp_moe_create(qmlp_moe_t** out, const qmlp_moe_desc* d, qmlp_stream_t stream) {
+    if (!out) return QMLP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!d || !d->w13 || !d->w13_meta || !d->w2 || !d->w2_meta) return QMLP_ERR_INVALID_ARG;
+    if (d->meta != QMLP_META_3B && d->meta != QMLP_META_4B) return QMLP_ERR_INVALID_ARG;
+    if (d->E < 1 || d->K < 64 || d->K > 16384 || d->K % 64 || d->I < 32 || d->I > 1024 || d->I % 32)
+        return QMLP_ERR_SHAPE;
+    int dev = 0, sms = 0;
+    qmlp_status st = check_device(&dev, &sms);
+    if (st != QMLP_OK) return st;
+    qmlp_moe_t* h = new qmlp_moe_t();
+    h->E = d->E;
+    h->K = d->K;
+    h->I = d->I;
+    h->meta = d->meta;
+    h->device = dev;
+    h->num_sms = sms;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t mb = (size_t)d->meta;
+    const size_t w13b = (size_t)d->E * 2 * d->I * (d->K / 2), m13b = (size_t)d->E * 2 * d->I * (d->K / 32) * mb;
+    const size_t w2b = (size_t)d->E * d->K * (d->I / 2), m2b = (size_t)d->E * d->K * (d->I / 32) * mb;
+    void *t0 = nullptr, *t1 = nullptr, *p = nullptr;
+    cudaError_t e = cudaSuccess;
+    auto stage = [&](const void* src, size_t wbytes, const void* msrc, size_t mbytes, int N, int Kr,
+                     uint8_t** wdst, uint8_t** mdst) -> qmlp_status {
+        if ((e = h->mem.alloc(&t0, wbytes)) != cudaSuccess) return from_cuda(e);
+        if ((e = h->mem.alloc(&t1, mbytes)) != cudaSuccess) return from_cuda(e);
+        if (cudaMemcpyAsync(t0, src, wbytes, cudaMemcpyDefault, s) != cudaSuccess) return QMLP_ERR_CUDA;
+        if (cudaMemcpyAsync(t1, msrc, mbytes, cudaMemcpyDefault, s) != cudaSuccess) return QMLP_ERR_CUDA;
+        void *wo = nullptr, *mo = nullptr;
+        if ((e = h->mem.alloc(&wo, wbytes)) != cudaSuccess) return from_cuda(e);
+        if ((e = h->mem.alloc(&mo, mbytes)) != cudaSuccess) return from_cuda(e);
+        if (repack_moe(static_cast<uint8_t*>(t0), static_cast<uint8_t*>(t1), d->meta, d->E, N, Kr,
+                       static_cast<uint8_t*>(wo), static_cast<uint8_t*>(mo), s) != cudaSuccess)
+            return QMLP_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return QMLP_ERR_CUDA;
+        for (void* q : {t0, t1}) {
+            auto it = std::find(h->mem.ptrs.begin(), h->mem.ptrs.end(), q);
+            if (it != h->mem.ptrs.end()) {
+                cudaFree(q);
+                h->mem.ptrs.erase(it);
+            }
+        }
+        *wdst = static_cast<uint8_t*>(wo);
+        *mdst = static_cast<uint8_t*>(mo);
+        return QMLP_OK;
+    };
+    st = stage(d->w13, w13b, d->w13_meta, m13b, 2 * d->I, d->K, &h->w13, &h->w13_meta);
+    if (st == QMLP_OK) st = stage(d->w2, w2b, d->w2_meta, m2b, d->K, d->I, &h->w2, &h->w2_meta);
+    if (st == QMLP_OK) {
+        if ((e = h->mem.alloc(&p, (size_t)16 * d->I * sizeof(__half))) != cudaSuccess) st = from_cuda(e);
+        else h->act_ws = static_cast<__half*>(p);
+    }
+    if (st == QMLP_OK) {
+        if ((e = h->mem.alloc(&p, 16)) != cudaSuccess) st = from_cuda(e);
+        else {
+            h->err = static_cast<int*>(p);
+            if (cudaMemsetAsync(p, 0, 16, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+                st = QMLP_ERR_CUDA;
+        }
+    }
+    if (st != QMLP_OK) {
+        cudaStreamSynchronize(s);
+        h->mem.release();
+        delete h;
+        return st;
+    }
+    *out = h;
+    return QMLP_OK;
+}
+
+void qmlp_moe_destroy(qmlp_moe_t* h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    h->mem.release();
+    delete h;
+}
+
+static qmlp_status moe_run(qmlp_moe_t* h, const void* x, qmlp_dtype xdt, const int32_t* ids, const float* rw,
+                           int topk, void* out, void* gu, void* act, void* y, qmlp_stream_t stream) {
+    if (!h || !x || !ids || !rw || !out) return QMLP_ERR_INVALID_ARG;
+    if (xdt != QMLP_DT_BF16 && xdt != QMLP_DT_FP16) return QMLP_ERR_INVALID_ARG;
+    if (topk < 1 || topk > 16) return QMLP_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(ids) || !aligned16(rw)) return QMLP_ERR_ALIGNMENT;
+    if ((gu && !aligned16(gu)) || (act && !aligned16(act)) || (y && !aligned16(y))) return QMLP_ERR_ALIGNMENT;
+    const size_t ob = (size_t)h->K * 2;
+    if (overlaps(out, ob, x, (size_t)h->K * 2) || overlaps(out, ob, ids, (size_t)topk * 4) ||
+        overlaps(out, ob, rw, (size_t)topk * 4))
+        return QMLP_ERR_ALIAS;
+    if (fault("launch")) return QMLP_ERR_CUDA;
+    MoeLaunch L;
+    L.E = h->E;
+    L.K = h->K;
+    L.I = h->I;
+    L.meta_bytes = h->meta;
+    L.w13 = h->w13;
+    L.w13_meta = h->w13_meta;
+    L.w2 = h->w2;
+    L.w2_meta = h->w2_meta;
+    L.x = x;
+    L.x_is_bf16 = xdt == QMLP_DT_BF16;
+    L.ids = ids;
+    L.rw = rw;
+    L.topk = topk;
+    L.out = static_cast<__half*>(out);
+    L.act_ws = h->act_ws;
+    L.gu_dbg = static_cast<__half*>(gu);
+    L.act_dbg = static_cast<__half*>(act);
+    L.y_dbg = static_cast<__half*>(y);
+    return launch_moe(L, h->num_sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMLP_OK
+                                                                                          : QMLP_ERR_CUDA;
+}
+
+qmlp_status qmlp_moe_m1_forward(qmlp_moe_t* h, const void* x, qmlp_dtype xdt, const int32_t* ids,
+                                const float* rw, int topk, void* out, qmlp_stream_t stream) {
+    return moe_run(h, x, xdt, ids, rw, topk, out, nullptr, nullptr, nullptr, stream);
+}
+
+qmlp_status qmlp_moe_debug_stages(qmlp_moe_t* h, const void* x, qmlp_dtype xdt, const int32_t* ids,
+                                  const float* rw, int topk, void* out, void* gu, void* act, void* y,
+                                  qmlp_stream_t stream) {
+    return moe_run(h, x, xdt, ids, rw, topk, out, gu, act, y, stream);
+}
+
+qmlp_status qmlp_moe_check(qmlp_moe_t* h, qmlp_stream_t stream) {
+    if (!h) return QMLP_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QMLP_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QMLP_ERR_CUDA;
+    if (v != 0) {
+        cudaMemset(h->err, 0, sizeof(int));
+        return QMLP_ERR_DEVICE_TIMEOUT;
+    }
+    return QMLP_OK;
+}
+
+}  // extern "C"

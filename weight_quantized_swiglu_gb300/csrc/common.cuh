@@ -1,0 +1,100 @@
+// common.cuh -- device primitives shared by the qmlp kernels (sm_103a).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define QMLP_DEV __device__ __forceinline__
+
+namespace qmlp {
+
+// ---------------------------------------------------------------------------
+// Element conversions (exact).
+// E2M1 pair -> f16x2: the byte holds the earlier k in its low nibble, which
+// lands in the low half (Qwen3.8-27B-NVFP4, "NVFP4 numerics as implemented").
+// ---------------------------------------------------------------------------
+QMLP_DEV void e2m1x4_to_f16x2x4(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2,
+                                uint32_t& h3) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
+}
+
+// Two E4M3 bytes (low byte -> low half) -> f16x2.
+QMLP_DEV uint32_t e4m3x2_to_f16x2(uint32_t w16) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(r)
+        : "r"(w16));
+    return r;
+}
+
+// Four E4M3 bytes of a word -> two f16x2 (bytes 0,1 -> first; 2,3 -> second).
+QMLP_DEV void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+QMLP_DEV uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// {x.lo, x.lo} and {x.hi, x.hi}
+QMLP_DEV uint32_t dup_lo16(uint32_t x) { return __byte_perm(x, 0, 0x1010); }
+QMLP_DEV uint32_t dup_hi16(uint32_t x) { return __byte_perm(x, 0, 0x3232); }
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core MMA: D[16x8] += A[16x16] (f16, row) * B[16x8] (f16,
+// col), fp32 accumulation.
+// ---------------------------------------------------------------------------
+QMLP_DEV void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                            uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
+// Loads
+// ---------------------------------------------------------------------------
+// Streaming 16-byte global load: read once, do not keep in L1.
+QMLP_DEV uint4 ldg_stream_u4(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+QMLP_DEV uint2 ldg_stream_u2(const uint2* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(r.x), "=r"(r.y)
+                 : "l"(p));
+    return r;
+}
+
+QMLP_DEV float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+
+// Exponent that brings max|v| into [2^14, 2^15): fp16 then holds every bf16
+// value within 2^29 of the maximum exactly (bf16 has 8 significant bits,
+// fp16 11). Zero/non-finite maxima get 0.
+QMLP_DEV int prescale_exponent(float maxabs) {
+    if (!(maxabs > 0.0f) || !isfinite(maxabs)) return 0;
+    int e;
+    frexpf(maxabs, &e);  // maxabs in [2^(e-1), 2^e)
+    return 15 - e;
+}
+
+}  // namespace qmlp

@@ -1,0 +1,467 @@
+// gemv_dec.cu -- decode-path (M <= 16) weight-quantized GEMV kernels.
+//
+// Operation: one or two projections of the SwiGLU MLP (vllm.cpp issue
+// "tp>1 fp8w tail-MLP shard host-dequantizes every layer", "Proposed fix"),
+// y[m, n] = sum_k x[m, k] * W[n, k], with W dequantized on the fly from the
+// resident packed bytes:
+//   NVFP4 (Qwen3.8-27B-NVFP4, "NVFP4 numerics as implemented"):
+//     W = E2M1(nibble) * E4M3(scale[n, k/16]); the 1/global factor is applied
+//     to the fp32 accumulator in the epilogue.
+//   FP8 per-channel (same vllm.cpp issue, "Mechanism on the tp>1 path"):
+//     W = e4m3fn(byte); scale[n] is applied in the epilogue.
+//
+// Design (GB300):
+//  * HBM-bound streaming: every lane issues 16-byte coalesced loads of
+//    packed weights laid out at create time in tensor-core A-fragment order
+//    (one warp load = 512 contiguous bytes = a 16-row x 64-k block of NVFP4).
+//  * Decode in registers with the hardware E2M1/E4M3 -> f16x2 conversions
+//    (exact), the group-16 E4M3 scale applied by one f16x2 multiply (the
+//    product has <= 6 significant bits, exact in fp16), then a warp-level
+//    m16n8k16 tensor-core MMA with fp32 accumulation. Tokens are the n8
+//    operand, so M <= 8 costs one MMA per 256 weights and M <= 16 two.
+//  * Activations: each CTA stages its k-slice of x in shared memory as fp16
+//    scaled by a per-token power of two 2^sigma chosen from the slice's
+//    max|x| (max*2^sigma in [2^14, 2^15)); every bf16 value within 2^29 of
+//    the maximum is then exact in fp16, and the accumulator is multiplied by
+//    2^-sigma (exact) before it leaves the CTA.
+//  * Gate and up are fused: one pass over the staged x feeds both.
+//  * Split-K: 8 warps per CTA take interleaved 64-k chunks and reduce through
+//    shared memory; when the row tiles alone cannot fill the GPU, the k range
+//    is split across CTAs, partial sums go to a workspace and the last CTA of
+//    a row tile (atomic arrival counter, reset by that CTA) adds them in a
+//    fixed order. No floating-point atomics: results are run-to-run
+//    deterministic.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace qmlp {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxStageBytes = 64 * 1024;
+
+struct KArgs {
+    const uint4* wc0;
+    const uint2* sc0;
+    const float* chs0;
+    float inv0;
+    const uint4* wc1;
+    const uint2* sc1;
+    const float* chs1;
+    float inv1;
+    const __nv_bfloat16* x;
+    int M, K, N, Nt, Kc, ksplit, cps;
+    void* out;
+    float* part;
+    int* counters;
+};
+
+// Weights of one chunk (64 k x 16 rows) of one projection, as loaded.
+struct ChunkW {
+    uint4 w0;  // NVFP4: all 4 groups; FP8: groups 0,1
+    uint4 w1;  // FP8: groups 2,3
+    uint2 s;   // NVFP4 scales
+};
+
+template <int FMT>
+QMLP_DEV ChunkW load_chunk(const uint4* wc, const uint2* sc, size_t chunk, int lane) {
+    ChunkW c;
+    if (FMT == kNVFP4) {
+        c.w0 = ldg_stream_u4(wc + chunk * 32 + lane);
+        c.s = ldg_stream_u2(sc + chunk * 8 + (lane >> 2));
+        c.w1 = make_uint4(0, 0, 0, 0);
+    } else {
+        c.w0 = ldg_stream_u4(wc + (chunk * 2 + 0) * 32 + lane);
+        c.w1 = ldg_stream_u4(wc + (chunk * 2 + 1) * 32 + lane);
+        c.s = make_uint2(0, 0);
+    }
+    return c;
+}
+
+QMLP_DEV uint32_t u4_word(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Decode group j (16 k) of a chunk into the four f16x2 A-fragment registers.
+template <int FMT>
+QMLP_DEV void decode_group(const ChunkW& c, int j, uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                           uint32_t& a3) {
+    if (FMT == kNVFP4) {
+        e2m1x4_to_f16x2x4(u4_word(c.w0, j), a0, a1, a2, a3);
+        uint32_t sp = e4m3x2_to_f16x2((j < 2 ? c.s.x : c.s.y) >> (16 * (j & 1)));
+        const uint32_t slo = dup_lo16(sp), shi = dup_hi16(sp);
+        a0 = hmul2_u32(a0, slo);
+        a1 = hmul2_u32(a1, shi);
+        a2 = hmul2_u32(a2, slo);
+        a3 = hmul2_u32(a3, shi);
+    } else {
+        const uint4& v = j < 2 ? c.w0 : c.w1;
+        const int jj = j & 1;
+        e4m3x4_to_f16x2x2(u4_word(v, jj * 2 + 0), a0, a1);
+        e4m3x4_to_f16x2x2(u4_word(v, jj * 2 + 1), a2, a3);
+    }
+}
+
+template <int FMT, int NT, int NP, int EPI>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(const KArgs a) {
+    extern __shared__ __align__(16) uint8_t dyn_smem[];
+    uint4* xs = reinterpret_cast<uint4*>(dyn_smem);  // [cps][2][4*M] fragment slots
+    __shared__ float red[kWarps][NP][NT][32][4];
+    __shared__ int s_maxbits[16];
+    __shared__ int s_sig[16];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x;
+    const int rt = blockIdx.x;
+    const int ks = blockIdx.y;
+    const int M = a.M;
+    const int c0 = ks * a.cps;
+    const int c1 = min(c0 + a.cps, a.Kc);
+    const int nch = c1 - c0;
+    const int kb = c0 * kChunkK;
+    const int ke = min(c1 * kChunkK, a.K);
+    const int kpe = c1 * kChunkK;
+    const int slots = 4 * M;
+
+    // ---- stage x[:, kb:kpe) as prescaled fp16 B fragments ----------------
+    if (tid < 16) s_maxbits[tid] = 0;
+    __syncthreads();
+    const int real8 = (ke - kb) / 8;
+    for (int it = tid; it < M * real8; it += kThreads) {
+        const int m = it / real8, q = it - m * real8;
+        const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + kb + q * 8);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+        atomicMax(&s_maxbits[m], __float_as_int(mx));
+    }
+    __syncthreads();
+    if (tid < M) s_sig[tid] = prescale_exponent(__int_as_float(s_maxbits[tid]));
+    __syncthreads();
+    const int pad8 = (kpe - kb) / 8;
+    for (int it = tid; it < M * pad8; it += kThreads) {
+        const int m = it / pad8, q = it - m * pad8;
+        const int kl = q * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (kb + kl < ke) v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + kb + kl);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+        const int sig = s_sig[m];
+        const int cc = kl / kChunkK, j = (kl % kChunkK) / 16, reg = (kl % 16) / 8;
+        const int half = j >> 1, word = (j & 1) * 2 + reg;
+        uint32_t* base = reinterpret_cast<uint32_t*>(xs + (size_t)(cc * 2 + half) * slots + m * 4);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(h[t]);
+            const __half2 hh = __floats2half2_rn(scalbnf(f.x, sig), scalbnf(f.y, sig));
+            base[t * 4 + word] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+    }
+    __syncthreads();
+
+    // ---- stream weights, decode, MMA ----------------------------------------
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    float acc[NP][NT][4];
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[p][n][i] = 0.0f;
+
+    const size_t tile0 = (size_t)rt * a.Kc + c0;
+    ChunkW cur[NP], nxt[NP];
+    if (warp < nch) {
+        cur[0] = load_chunk<FMT>(a.wc0, a.sc0, tile0 + warp, lane);
+        if (NP == 2) cur[NP - 1] = load_chunk<FMT>(a.wc1, a.sc1, tile0 + warp, lane);
+    }
+    for (int cc = warp; cc < nch; cc += kWarps) {
+        const bool more = cc + kWarps < nch;
+        if (more) {
+            nxt[0] = load_chunk<FMT>(a.wc0, a.sc0, tile0 + cc + kWarps, lane);
+            if (NP == 2) nxt[NP - 1] = load_chunk<FMT>(a.wc1, a.sc1, tile0 + cc + kWarps, lane);
+        }
+        uint4 xb[NT][2];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int m = n * 8 + g;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                xb[n][h] = m < M ? xs[(size_t)(cc * 2 + h) * slots + m * 4 + t] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                uint32_t a0, a1, a2, a3;
+                decode_group<FMT>(cur[p], j, a0, a1, a2, a3);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const uint32_t b0 = u4_word(xb[n][j >> 1], (j & 1) * 2 + 0);
+                    const uint32_t b1 = u4_word(xb[n][j >> 1], (j & 1) * 2 + 1);
+                    mma_f16_16816(acc[p][n], a0, a1, a2, a3, b0, b1);
+                }
+            }
+        }
+        if (more) {
+#pragma unroll
+            for (int p = 0; p < NP; ++p) cur[p] = nxt[p];
+        }
+    }
+
+    // ---- reduce the 8 warps (fixed order) ----------------------------------
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[warp][p][n][lane][i] = acc[p][n][i];
+    __syncthreads();
+
+    // value of (projection p, tile row r, token m) in this CTA
+    auto cta_value = [&](int p, int r, int m) -> float {
+        const int n = m >> 3, mm = m & 7;
+        const int ln = (r & 7) * 4 + (mm >> 1);
+        const int reg = (r >= 8 ? 2 : 0) + (mm & 1);
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += red[w][p][n][ln][reg];
+        return scalbnf(v, -s_sig[m]);
+    };
+
+    const int items = kTileRows * M;
+    if (a.ksplit > 1) {
+        for (int it = tid; it < items; it += kThreads) {
+            const int m = it / kTileRows, r = it - m * kTileRows;
+            const int row = rt * kTileRows + r;
+#pragma unroll
+            for (int p = 0; p < NP; ++p)
+                a.part[((size_t)(ks * NP + p) * M + m) * a.N + row] = cta_value(p, r, m);
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = (atomicAdd(&a.counters[rt], 1) == a.ksplit - 1);
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        if (tid == 0) a.counters[rt] = 0;
+    }
+
+    for (int it = tid; it < items; it += kThreads) {
+        const int m = it / kTileRows, r = it - m * kTileRows;
+        const int row = rt * kTileRows + r;
+        float v[NP];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            if (a.ksplit > 1) {
+                float s = 0.0f;
+                for (int q = 0; q < a.ksplit; ++q)
+                    s += __ldcg(&a.part[((size_t)(q * NP + p) * M + m) * a.N + row]);
+                v[p] = s;
+            } else {
+                v[p] = cta_value(p, r, m);
+            }
+        }
+        if (EPI == kEpiRaw) {
+            reinterpret_cast<float*>(a.out)[(size_t)m * a.N + row] = v[0];
+        } else {
+            const float sg = FMT == kNVFP4 ? a.inv0 : a.chs0[row];
+            const float y0 = v[0] * sg;
+            float res = y0;
+            if (EPI == kEpiSwiGLU) {
+                const float su = FMT == kNVFP4 ? a.inv1 : a.chs1[row];
+                res = silu_f32(y0) * (v[NP - 1] * su);
+            }
+            reinterpret_cast<__nv_bfloat16*>(a.out)[(size_t)m * a.N + row] = __float2bfloat16_rn(res);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Create-time repack into the fragment layout
+// ---------------------------------------------------------------------------
+__global__ void repack_nvfp4_gemv_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ s,
+                                         int N, int K, uint4* __restrict__ wc, uint2* __restrict__ sc) {
+    const int Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK, G = K / 16, rb = K / 2;
+    const size_t total = (size_t)Nt * Kc * 32;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int lane = (int)(idx % 32);
+        const size_t tc = idx / 32;
+        const int c = (int)(tc % Kc), rt = (int)(tc / Kc);
+        const int g = lane >> 2, t = lane & 3;
+        const size_t r0 = (size_t)(rt * kTileRows + g), r8 = r0 + 8;
+        uint32_t words[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gi = 4 * c + j;
+            uint32_t v = 0;
+            if (gi < G) {
+                v = (uint32_t)w[r0 * rb + 8 * gi + t] | ((uint32_t)w[r8 * rb + 8 * gi + t] << 8) |
+                    ((uint32_t)w[r0 * rb + 8 * gi + 4 + t] << 16) |
+                    ((uint32_t)w[r8 * rb + 8 * gi + 4 + t] << 24);
+            }
+            words[j] = v;
+        }
+        wc[idx] = make_uint4(words[0], words[1], words[2], words[3]);
+        if (t == 0) {
+            uint32_t sv[2] = {0, 0};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int gi = 4 * c + j;
+                if (gi < G) {
+                    const uint32_t pair = (uint32_t)s[r0 * G + gi] | ((uint32_t)s[r8 * G + gi] << 8);
+                    sv[j >> 1] |= pair << (16 * (j & 1));
+                }
+            }
+            sc[tc * 8 + g] = make_uint2(sv[0], sv[1]);
+        }
+    }
+}
+
+__global__ void repack_fp8_gemv_kernel(const uint8_t* __restrict__ w, int N, int K,
+                                       uint4* __restrict__ wc) {
+    const int Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK;
+    const size_t total = (size_t)Nt * Kc * 2 * 32;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int lane = (int)(idx % 32);
+        const size_t rest = idx / 32;
+        const int h = (int)(rest % 2);
+        const size_t tc = rest / 2;
+        const int c = (int)(tc % Kc), rt = (int)(tc / Kc);
+        const int g = lane >> 2, t = lane & 3;
+        const size_t r0 = (size_t)(rt * kTileRows + g), r8 = r0 + 8;
+        auto B = [&](size_t row, int k) -> uint32_t { return k < K ? (uint32_t)w[row * K + k] : 0u; };
+        uint32_t words[4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+            const int k = 16 * (4 * c + 2 * h + jj) + 2 * t;
+            words[jj * 2 + 0] = B(r0, k) | (B(r0, k + 1) << 8) | (B(r8, k) << 16) | (B(r8, k + 1) << 24);
+            words[jj * 2 + 1] =
+                B(r0, k + 8) | (B(r0, k + 9) << 8) | (B(r8, k + 8) << 16) | (B(r8, k + 9) << 24);
+        }
+        wc[idx] = make_uint4(words[0], words[1], words[2], words[3]);
+    }
+}
+
+struct Plan {
+    int ksplit, cps, nt;
+    size_t smem;
+};
+
+Plan plan_gemv(int Nt, int Kc, int M, int num_sms) {
+    Plan p;
+    p.nt = M <= 8 ? 1 : 2;
+    const int target = 8 * std::max(num_sms, 1);
+    int ks = std::max(1, (target + Nt - 1) / Nt);
+    const int cap = std::max(1, kMaxStageBytes / (128 * M));
+    ks = std::max(ks, (Kc + cap - 1) / cap);
+    ks = std::min(ks, Kc);
+    p.cps = (Kc + ks - 1) / ks;
+    p.ksplit = (Kc + p.cps - 1) / p.cps;
+    p.smem = (size_t)p.cps * 128 * M;
+    return p;
+}
+
+template <int FMT, int NT, int NP, int EPI>
+cudaError_t launch_one(const KArgs& a, dim3 grid, size_t smem, cudaStream_t s) {
+    auto kern = gemv_kernel<FMT, NT, NP, EPI>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxStageBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    kern<<<grid, kThreads, smem, s>>>(a);
+    return cudaPeekAtLastError();
+}
+
+template <int FMT>
+cudaError_t dispatch(const KArgs& a, int nt, int epi, dim3 grid, size_t smem, cudaStream_t s) {
+    if (epi == kEpiSwiGLU) {
+        return nt == 1 ? launch_one<FMT, 1, 2, kEpiSwiGLU>(a, grid, smem, s)
+                       : launch_one<FMT, 2, 2, kEpiSwiGLU>(a, grid, smem, s);
+    } else if (epi == kEpiPlain) {
+        return nt == 1 ? launch_one<FMT, 1, 1, kEpiPlain>(a, grid, smem, s)
+                       : launch_one<FMT, 2, 1, kEpiPlain>(a, grid, smem, s);
+    }
+    return nt == 1 ? launch_one<FMT, 1, 1, kEpiRaw>(a, grid, smem, s)
+                   : launch_one<FMT, 2, 1, kEpiRaw>(a, grid, smem, s);
+}
+
+}  // namespace
+
+size_t gemv_codes_bytes(int fmt, int N, int K) {
+    const size_t Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK;
+    return Nt * Kc * 32 * 16 * (fmt == kNVFP4 ? 1 : 2);
+}
+
+size_t gemv_scales_bytes(int fmt, int N, int K) {
+    if (fmt != kNVFP4) return 0;
+    const size_t Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK;
+    return Nt * Kc * 8 * 8;
+}
+
+size_t gemv_part_elems(int K, int I, int num_sms) {
+    size_t best = 0;
+    for (int M = 1; M <= 16; ++M) {
+        const Plan gu = plan_gemv(I / kTileRows, (K + kChunkK - 1) / kChunkK, M, num_sms);
+        const Plan dn = plan_gemv(K / kTileRows, (I + kChunkK - 1) / kChunkK, M, num_sms);
+        const Plan dg = plan_gemv(I / kTileRows, (K + kChunkK - 1) / kChunkK, M, num_sms);
+        if (gu.ksplit > 1) best = std::max(best, (size_t)gu.ksplit * 2 * M * I);
+        if (dg.ksplit > 1) best = std::max(best, (size_t)dg.ksplit * M * I);
+        if (dn.ksplit > 1) best = std::max(best, (size_t)dn.ksplit * M * K);
+    }
+    return best;
+}
+
+cudaError_t launch_gemv(const GemvLaunch& L, int num_sms, cudaStream_t s) {
+    if (L.M < 1 || L.M > 16) return cudaErrorInvalidValue;
+    const GemvProj& P = L.p0;
+    const Plan pl = plan_gemv(P.Nt, P.Kc, L.M, num_sms);
+    const int NP = L.epi == kEpiSwiGLU ? 2 : 1;
+    if (pl.ksplit > 1 && (size_t)pl.ksplit * NP * L.M * P.N > L.part_cap) return cudaErrorInvalidValue;
+    KArgs a;
+    a.wc0 = P.wc;
+    a.sc0 = P.sc;
+    a.chs0 = P.chs;
+    a.inv0 = P.inv_g;
+    a.wc1 = L.p1.wc;
+    a.sc1 = L.p1.sc;
+    a.chs1 = L.p1.chs;
+    a.inv1 = L.p1.inv_g;
+    a.x = reinterpret_cast<const __nv_bfloat16*>(L.x);
+    a.M = L.M;
+    a.K = P.K;
+    a.N = P.N;
+    a.Nt = P.Nt;
+    a.Kc = P.Kc;
+    a.ksplit = pl.ksplit;
+    a.cps = pl.cps;
+    a.out = L.out;
+    a.part = L.part;
+    a.counters = L.counters;
+    const dim3 grid(P.Nt, pl.ksplit);
+    return L.fmt == kNVFP4 ? dispatch<kNVFP4>(a, pl.nt, L.epi, grid, pl.smem, s)
+                           : dispatch<kFP8>(a, pl.nt, L.epi, grid, pl.smem, s);
+}
+
+cudaError_t repack_nvfp4_gemv(const uint8_t* w, const uint8_t* scale, int N, int K, uint4* wc, uint2* sc,
+                              cudaStream_t s) {
+    repack_nvfp4_gemv_kernel<<<1024, 256, 0, s>>>(w, scale, N, K, wc, sc);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t repack_fp8_gemv(const uint8_t* w, int N, int K, uint4* wc, cudaStream_t s) {
+    repack_fp8_gemv_kernel<<<1024, 256, 0, s>>>(w, N, K, wc);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace qmlp
