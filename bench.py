@@ -279,19 +279,23 @@ def bench_moe(meta_bytes=4):
     x = torch.from_numpy(c.x_fp16.view(np.int16)).cuda()
     rw = torch.from_numpy(c.router_w).cuda()
     hot_ids = torch.from_numpy(c.ids).cuda()
-    rot_ids = torch.from_numpy(np.stack([gen.rotating_ids(k) for k in range(48)])).cuda()
+    # one 16-entry (64-byte) row per call keeps every row 16-byte aligned
+    rot = np.full((48, 16), -1, np.int32)
+    for k in range(48):
+        rot[k, :10] = gen.rotating_ids(k)
+    rot_ids = torch.from_numpy(rot).cuda()
     out = torch.empty(c.K, dtype=torch.int16, device="cuda")
     s = torch.cuda.Stream()
     res = {}
     for mode in ("hot", "rotating"):
         with torch.cuda.stream(s):
             for k in range(3):
-                moe.forward(x, q.DT_FP16, hot_ids if mode == "hot" else rot_ids[k], rw, out, stream=s)
+                moe.forward(x, q.DT_FP16, hot_ids if mode == "hot" else rot_ids[k, :10], rw, out, stream=s)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for k in range(48):
-                moe.forward(x, q.DT_FP16, hot_ids if mode == "hot" else rot_ids[k], rw, out, stream=s)
+                moe.forward(x, q.DT_FP16, hot_ids if mode == "hot" else rot_ids[k, :10], rw, out, stream=s)
         g.replay()
         torch.cuda.synchronize()
         samples = []

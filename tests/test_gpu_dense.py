@@ -136,7 +136,8 @@ def test_ragged_tails(torch_cuda, fmt, M):
     mlp = q.QuantMLP.from_case(case)
     out, act = run_forward(torch_cuda, mlp, case.x, path=q.PATH_GEMV)
     ref = oracle.dense_forward(case)
-    assert np.abs(oracle.bf16_bits_to_f64(ref["out"])).max() > 1.0
+    # a zero result must not pass: the reference is non-degenerate
+    assert np.count_nonzero(oracle.bf16_bits_to_f64(ref["out"])) > 0.9 * ref["out"].size
     compare(act, ref["act"], what="act")
     compare(out, ref["out"], what="out")
     mlp.close()
