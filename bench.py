@@ -170,6 +170,33 @@ def n_rotating_copies(bytes_per_copy):
     return max(2, math.ceil(2 * l2 / bytes_per_copy) + 1), l2
 
 
+def capture(calls, stream):
+    """CUDA graph of the given zero-argument launch closures (run once first)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for f in calls:
+            f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for f in calls:
+            f()
+    return g
+
+
+def time_graph(g, reps, stream):
+    """Replay `g` reps times on `stream`, timed by CUDA events on that stream."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def bench_headline(args, world, rank, local, pk):
     import torch
     import weight_quantized_swiglu_gb300 as q
@@ -178,75 +205,76 @@ def bench_headline(args, world, rank, local, pk):
     mlps = [q.QuantMLP.from_case(case) for _ in range(R)]
     x = torch.from_numpy(case.x.view(np.int16)).cuda()
     out = torch.empty((1, K_HID), dtype=torch.int16, device="cuda")
-    s = torch.cuda.current_stream()
-    for i in range(max(args.warmup, 3)):
-        m = mlps[i % R]
-        m.forward_stage(0, x, None, 1, stream=s)
-        m.forward_stage(1, None, out, 1, stream=s)
+    s = torch.cuda.Stream()
+    per_graph = R * max(1, 24 // R)
+    g = capture([(lambda m=mlps[i % R]: m.forward(x, out, stream=s)) for i in range(per_graph)], s)
+    reps = max(1, math.ceil(args.steps / per_graph))
+    K = reps * per_graph
+    with torch.cuda.stream(s):
+        for _ in range(max(1, math.ceil(args.warmup / per_graph))):
+            g.replay()
     torch.cuda.synchronize()
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     sampler = ClockSampler(local)
     time.sleep(0.25)
     barrier(world)
     torch.cuda.synchronize()
-    for i in range(K):
-        m = mlps[i % R]
-        ev[i][0].record(s)
-        m.forward_stage(0, x, None, 1, stream=s)
-        ev[i][1].record(s)
-        m.forward_stage(1, None, out, 1, stream=s)
-        ev[i][2].record(s)
-    torch.cuda.synchronize()
+    total_ms = time_graph(g, reps, s)
     barrier(world)
     clocks = sampler.stop()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    gu_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    dn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     total_ms = max_over_ranks(world, total_ms)
     us_per_call = total_ms * 1e3 / K
     mlps[0].check()
+    del g
+
+    # per-projection kernels (stage launches) for diagnostics
+    g0 = capture([(lambda m=mlps[i % R]: m.forward_stage(0, x, None, 1, stream=s)) for i in range(per_graph)], s)
+    g1 = capture([(lambda m=mlps[i % R]: m.forward_stage(1, None, out, 1, stream=s)) for i in range(per_graph)], s)
+    r2 = max(1, reps // 4)
+    gu_us = time_graph(g0, r2, s) * 1e3 / (r2 * per_graph)
+    dn_us = time_graph(g1, r2, s) * 1e3 / (r2 * per_graph)
+    del g0, g1
 
     # end-to-end through the host-buffer entry point (pinned buffers; the
     # copies and the completion wait are inside the timed region)
     xh = torch.from_numpy(case.x.view(np.int16)).pin_memory()
     oh = torch.empty((1, K_HID), dtype=torch.int16).pin_memory()
     for i in range(3):
-        mlps[i % R].forward_host(xh, oh)
+        mlps[i % R].forward_host(xh, oh, stream=s)
     n_e2e = max(10, min(K, 2000))
     barrier(world)
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        mlps[i % R].forward_host(xh, oh)
+        mlps[i % R].forward_host(xh, oh, stream=s)
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     for m in mlps:
         m.close()
 
-    gu_bytes = nvfp4_gateup_bytes(K_HID, I_INT)
-    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    call_bytes = nvfp4_bytes(K_HID, I_INT)
+    achieved = call_bytes / (us_per_call * 1e-6) / 1e9
     res = {
         "us_per_call": us_per_call,
+        "steps": K,
         "ms_per_step": total_ms / K,
-        "gu_us": gu_ms * 1e3,
-        "down_us": dn_ms * 1e3,
-        "hbm_gbs_call": nvfp4_bytes(K_HID, I_INT) / (us_per_call * 1e-6) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<NVFP4,NT=1,gate+up,SwiGLU>",
+        "gu_us": gu_us,
+        "down_us": dn_us,
+        "hbm_gbs_call": achieved,
+        "roofline": {"bound": "hbm", "kernel": "gemv_stream_kernel<NVFP4, fused gate/up+SwiGLU -> down>",
                      "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
-                     "algorithmic_bytes_per_launch": gu_bytes,
-                     "traffic": ncu_traffic("gemv_nvfp4_gateup_m1")},
+                     "algorithmic_bytes_per_launch": call_bytes,
+                     "traffic": ncu_traffic("gemv_stream_fused_nvfp4_m1")},
         "e2e": {"value": e2e_s * 1e6 / n_e2e, "unit": UNIT, "h2d_bytes_per_step": K_HID * 2,
                 "d2h_bytes_per_step": K_HID * 2, "steps": n_e2e},
         "clocks": clocks,
         "rotating_copies": R,
         "l2_bytes": l2,
-        "gpu_launches": 2 * K,
+        "gpu_launches": K,  # one fused cooperative kernel per MLP call at M=1
     }
     return res, case
 
 
 def bench_dense_secondary(name, variant, reps, fmt_bytes):
-    """us/call of another dense workload (rotating copies, CUDA events)."""
+    """us/call of another dense workload (rotating copies, CUDA-graph replay)."""
     import torch
     import weight_quantized_swiglu_gb300 as q
     case = gen.workload_case(name, variant)
@@ -254,19 +282,17 @@ def bench_dense_secondary(name, variant, reps, fmt_bytes):
     mlps = [q.QuantMLP.from_case(case) for _ in range(R)]
     x = torch.from_numpy(case.x.view(np.int16)).cuda()
     out = torch.empty((case.M, case.K), dtype=torch.int16, device="cuda")
-    for i in range(5):
-        mlps[i % R].forward(x, out)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(reps):
-        mlps[i % R].forward(x, out)
-    e1.record()
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / reps
+    s = torch.cuda.Stream()
+    per_graph = R * max(1, 24 // R)
+    g = capture([(lambda m=mlps[i % R]: m.forward(x, out, stream=s)) for i in range(per_graph)], s)
+    time_graph(g, 1, s)
+    n = max(1, reps // per_graph)
+    us = time_graph(g, n, s) * 1e3 / (n * per_graph)
+    del g
     for m in mlps:
         m.close()
-    return {"M": case.M, "us_per_call": us, "gbs": fmt_bytes / (us * 1e-6) / 1e9, "tokens_per_s": case.M / (us * 1e-6)}
+    return {"M": case.M, "us_per_call": us, "gbs": fmt_bytes / (us * 1e-6) / 1e9,
+            "tokens_per_s": case.M / (us * 1e-6)}
 
 
 def bench_moe(meta_bytes=4):
@@ -417,16 +443,70 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------
+# eager launches of one operation, for ncu (no JSON output)
+# ----------------------------------------------------------------------------
+def run_profile(args):
+    import torch
+    import weight_quantized_swiglu_gb300 as q
+    from weight_quantized_swiglu_gb300 import build
+    build.build()
+    n = args.warmup + args.steps
+    if args.profile in ("fused", "stage0", "stage1", "fp8_fused"):
+        name = "dense_fp8_decode" if args.profile == "fp8_fused" else "dense_nvfp4_decode"
+        case = gen.workload_case(name, 0)
+        mlp = q.QuantMLP.from_case(case)
+        x = torch.from_numpy(case.x.view(np.int16)).cuda()
+        out = torch.empty((1, case.K), dtype=torch.int16, device="cuda")
+        for _ in range(n):
+            if args.profile in ("fused", "fp8_fused"):
+                mlp.forward(x, out)
+            elif args.profile == "stage0":
+                mlp.forward_stage(0, x, None, 1)
+            else:
+                mlp.forward_stage(0, x, None, 1)
+                mlp.forward_stage(1, None, out, 1)
+        torch.cuda.synchronize()
+        mlp.check()
+    elif args.profile == "moe":
+        c = gen.gen_moe_case(gen.seed_for(4, 0))
+        moe = q.MoeAWQ.from_case(c, 4)
+        x = torch.from_numpy(c.x_fp16.view(np.int16)).cuda()
+        ids = torch.from_numpy(c.ids).cuda()
+        rw = torch.from_numpy(c.router_w).cuda()
+        out = torch.empty(c.K, dtype=torch.int16, device="cuda")
+        for _ in range(n):
+            moe.forward(x, q.DT_FP16, ids, rw, out)
+        torch.cuda.synchronize()
+        moe.check()
+    elif args.profile.startswith("prefill"):
+        M = int(args.profile[len("prefill"):] or 512)
+        case = gen.gen_dense_case("nvfp4", K_HID, I_INT, M, gen.seed_for(3, 0))
+        mlp = q.QuantMLP.from_case(case)
+        x = torch.from_numpy(case.x.view(np.int16)).cuda()
+        out = torch.empty((M, K_HID), dtype=torch.int16, device="cuda")
+        for _ in range(n):
+            mlp.forward(x, out, path=q.PATH_GEMM)
+        torch.cuda.synchronize()
+        mlp.check()
+    print(f"profile {args.profile}: {n} calls ok", flush=True)
+
+
+# ----------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--profile", default=None,
+                    help="eager launches of one operation for ncu: fused|stage0|stage1|fp8_fused|moe|prefillM")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.profile:
+        run_profile(args)
+        return
 
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -448,10 +528,10 @@ def main():
     extras = {}
     if not args.no_extras and rank == 0:
         import weight_quantized_swiglu_gb300 as q
-        extras["dense_nvfp4_decode_M4"] = bench_dense_secondary("dense_nvfp4_decode", 1, 400, nvfp4_bytes(K_HID, I_INT))
-        extras["dense_fp8_decode_M1"] = bench_dense_secondary("dense_fp8_decode", 0, 300, fp8_bytes(K_HID, I_INT))
-        extras["dense_fp8_decode_M16"] = bench_dense_secondary("dense_fp8_decode", 1, 300, fp8_bytes(K_HID, I_INT))
-        extras["tiny_nvfp4_M1"] = bench_dense_secondary("tiny_nvfp4", 0, 2000, nvfp4_bytes(gen.TINY_K, gen.TINY_I))
+        extras["dense_nvfp4_decode_M4"] = bench_dense_secondary("dense_nvfp4_decode", 1, 2400, nvfp4_bytes(K_HID, I_INT))
+        extras["dense_fp8_decode_M1"] = bench_dense_secondary("dense_fp8_decode", 0, 2400, fp8_bytes(K_HID, I_INT))
+        extras["dense_fp8_decode_M16"] = bench_dense_secondary("dense_fp8_decode", 1, 1200, fp8_bytes(K_HID, I_INT))
+        extras["tiny_nvfp4_M1"] = bench_dense_secondary("tiny_nvfp4", 0, 4800, nvfp4_bytes(gen.TINY_K, gen.TINY_I))
         extras["moe_awq_m1_4B"] = bench_moe(4)
         extras["moe_awq_m1_3B"] = bench_moe(3)
         try:
@@ -469,7 +549,7 @@ def main():
         "value": head["us_per_call"],
         "unit": UNIT,
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": head["steps"],
         "warmup": args.warmup,
         "ms_per_step": head["ms_per_step"],
         "higher_is_better": False,

@@ -82,6 +82,7 @@ struct qmlp_s {
     size_t part_cap = 0;
     int* counters = nullptr;   // [Nt(gate/up) + Nt(down)]
     int* err = nullptr;        // device error word
+    unsigned* bar = nullptr;   // grid barrier {count, generation}
     void* x_stage = nullptr;   // bf16 [max_M, K] (forward_host)
     void* out_stage = nullptr; // bf16 [max_M, K]
     Owner mem;
@@ -117,32 +118,36 @@ int qmlp_abi_version(void) { return 100; }
 // ---------------------------------------------------------------------------
 // dense MLP
 // ---------------------------------------------------------------------------
-static qmlp_status load_proj(qmlp_t* h, const qmlp_proj& src, int N, int K, GemvProj& dst,
+static qmlp_status load_proj(qmlp_t* h, const qmlp_proj& src, int N, int K, int Rr, GemvProj& dst,
                              uint8_t** w_tmp, uint8_t** s_tmp, cudaStream_t s) {
     const bool nv = h->fmt == kNVFP4;
     const size_t wbytes = (size_t)N * (nv ? K / 2 : K);
     const size_t sbytes = nv ? (size_t)N * (K / 16) : (size_t)N * sizeof(float);
-    void *wt = nullptr, *st = nullptr, *wc = nullptr, *sc = nullptr;
+    void *wt = nullptr, *st = nullptr, *wc = nullptr;
     cudaError_t e;
     if ((e = h->mem.alloc(&wt, wbytes)) != cudaSuccess) return from_cuda(e);
     if ((e = h->mem.alloc(&st, sbytes)) != cudaSuccess) return from_cuda(e);
     if ((e = cudaMemcpyAsync(wt, src.w, wbytes, cudaMemcpyDefault, s)) != cudaSuccess) return QMLP_ERR_CUDA;
     if ((e = cudaMemcpyAsync(st, src.scale, sbytes, cudaMemcpyDefault, s)) != cudaSuccess) return QMLP_ERR_CUDA;
-    if ((e = h->mem.alloc(&wc, gemv_codes_bytes(h->fmt, N, K))) != cudaSuccess) return from_cuda(e);
     dst.N = N;
     dst.K = K;
     dst.Nt = N / kTileRows;
     dst.Kc = (K + kChunkK - 1) / kChunkK;
-    dst.wc = static_cast<const uint4*>(wc);
+    dst.TWr = gemv_layout_warps(h->num_sms);
+    dst.Rr = Rr;
+    dst.Lr = (int)(((long)dst.Nt * dst.Kc + dst.TWr - 1) / dst.TWr);
+    dst.Lr = (dst.Lr + dst.Rr - 1) / dst.Rr * dst.Rr;
+    const size_t cbytes = gemv_codes_bytes(h->fmt, N, K, dst.Lr, dst.TWr);
+    if ((e = h->mem.alloc(&wc, cbytes)) != cudaSuccess) return from_cuda(e);
+    if (cudaMemsetAsync(wc, 0, cbytes, s) != cudaSuccess) return QMLP_ERR_CUDA;
+    dst.wc = static_cast<const uint8_t*>(wc);
     if (nv) {
-        if ((e = h->mem.alloc(&sc, gemv_scales_bytes(h->fmt, N, K))) != cudaSuccess) return from_cuda(e);
-        dst.sc = static_cast<const uint2*>(sc);
         dst.inv_g = 1.0f / src.global_scale;
-        e = repack_nvfp4_gemv(static_cast<uint8_t*>(wt), static_cast<uint8_t*>(st), N, K,
-                              static_cast<uint4*>(wc), static_cast<uint2*>(sc), s);
+        e = repack_nvfp4_gemv(static_cast<uint8_t*>(wt), static_cast<uint8_t*>(st), N, K, dst.Lr, dst.TWr,
+                              dst.Rr, static_cast<uint8_t*>(wc), s);
     } else {
         dst.chs = static_cast<const float*>(st);  // kept: per-channel scales
-        e = repack_fp8_gemv(static_cast<uint8_t*>(wt), N, K, static_cast<uint4*>(wc), s);
+        e = repack_fp8_gemv(static_cast<uint8_t*>(wt), N, K, dst.Lr, dst.TWr, dst.Rr, static_cast<uint8_t*>(wc), s);
     }
     if (e != cudaSuccess) return QMLP_ERR_CUDA;
     *w_tmp = static_cast<uint8_t*>(wt);
@@ -189,7 +194,8 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
     const int Ns[3] = {d->I, d->I, d->K}, Ks[3] = {d->K, d->K, d->I};
     cudaError_t e = cudaSuccess;
     for (int p = 0; p < 3 && st == QMLP_OK; ++p)
-        st = load_proj(h, *srcs[p], Ns[p], Ks[p], h->gv[p], &tmp[2 * p], &tmp[2 * p + 1], s);
+        st = load_proj(h, *srcs[p], Ns[p], Ks[p], p < 2 ? kGemvRecsPerStepPair : kGemvRecsPerStepSingle, h->gv[p],
+                       &tmp[2 * p], &tmp[2 * p + 1], s);
 
     if (st == QMLP_OK && h->fmt == kNVFP4 && d->max_M > kMaxGemvM && gemm_supported(d->K, 2 * d->I) &&
         gemm_supported(d->I, d->K)) {
@@ -218,7 +224,7 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
     if (st == QMLP_OK) {
         void* p = nullptr;
         const size_t Ntot = (size_t)(d->I / kTileRows) + (size_t)(d->K / kTileRows);
-        h->part_cap = gemv_part_elems(d->K, d->I, sms);
+        h->part_cap = std::max(gemv_part_elems(d->K, d->I, sms), gemv_stream_part_elems(d->K, d->I, sms));
         if ((e = h->mem.alloc(&h->act, (size_t)d->max_M * d->I * 2)) != cudaSuccess) st = from_cuda(e);
         else if ((e = h->mem.alloc(&p, h->part_cap * sizeof(float))) != cudaSuccess) st = from_cuda(e);
         else {
@@ -230,10 +236,11 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
             }
         }
         if (st == QMLP_OK) {
-            if ((e = h->mem.alloc(&p, 16)) != cudaSuccess) st = from_cuda(e);
+            if ((e = h->mem.alloc(&p, 64)) != cudaSuccess) st = from_cuda(e);
             else {
                 h->err = static_cast<int*>(p);
-                if (cudaMemsetAsync(p, 0, 16, s) != cudaSuccess) st = QMLP_ERR_CUDA;
+                h->bar = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(p) + 32);
+                if (cudaMemsetAsync(p, 0, 64, s) != cudaSuccess) st = QMLP_ERR_CUDA;
             }
         }
         if (st == QMLP_OK && (e = h->mem.alloc(&h->x_stage, (size_t)d->max_M * d->K * 2)) != cudaSuccess)
@@ -311,28 +318,65 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
     const size_t Ntg = (size_t)(h->I / kTileRows);
     for (int m0 = 0; m0 < M; m0 += kMaxGemvM) {
         const int mb = std::min(kMaxGemvM, M - m0);
+        const void* xb = static_cast<const uint8_t*>(x) + (size_t)m0 * h->K * 2;
+        void* ab = static_cast<uint8_t*>(h->act) + (size_t)m0 * h->I * 2;
+        void* ob = static_cast<uint8_t*>(out) + (size_t)m0 * h->K * 2;
+        GemvStreamPhase A, B;
+        A.epi = kEpiSwiGLU;
+        A.p0 = h->gv[0];
+        A.p1 = h->gv[1];
+        A.x = xb;
+        A.out = ab;
+        A.counters = h->counters;
+        B.epi = kEpiPlain;
+        B.p0 = h->gv[2];
+        B.x = ab;
+        B.out = ob;
+        B.counters = h->counters + Ntg;
+        const bool fitA = gemv_stream_fits(h->fmt, mb, h->K, 2, h->gv[0].Rr),
+                   fitB = gemv_stream_fits(h->fmt, mb, h->I, 1, h->gv[2].Rr);
+        const bool fitAB = gemv_stream_fits(h->fmt, mb, std::max(h->K, h->I), 2, h->gv[0].Rr) &&
+                           gemv_stream_fits(h->fmt, mb, std::max(h->K, h->I), 1, h->gv[2].Rr);
+        if (stages == 3 && fitAB) {
+            if (launch_gemv_stream(h->fmt, mb, A, &B, h->part, h->part_cap, h->bar, h->err, h->num_sms, s) !=
+                cudaSuccess)
+                return QMLP_ERR_CUDA;
+            continue;
+        }
         GemvLaunch L;
         L.fmt = h->fmt;
         L.M = mb;
         L.part = h->part;
         L.part_cap = h->part_cap;
         if (stages & 1) {
-            L.epi = kEpiSwiGLU;
-            L.p0 = h->gv[0];
-            L.p1 = h->gv[1];
-            L.x = static_cast<const uint8_t*>(x) + (size_t)m0 * h->K * 2;
-            L.out = static_cast<uint8_t*>(h->act) + (size_t)m0 * h->I * 2;
-            L.counters = h->counters;
-            if (launch_gemv(L, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
+            if (fitA) {
+                if (launch_gemv_stream(h->fmt, mb, A, nullptr, h->part, h->part_cap, h->bar, h->err, h->num_sms,
+                                       s) != cudaSuccess)
+                    return QMLP_ERR_CUDA;
+            } else {
+                L.epi = kEpiSwiGLU;
+                L.p0 = h->gv[0];
+                L.p1 = h->gv[1];
+                L.x = xb;
+                L.out = ab;
+                L.counters = h->counters;
+                if (launch_gemv(L, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
+            }
         }
         if (stages & 2) {
-            L.epi = kEpiPlain;
-            L.p0 = h->gv[2];
-            L.p1 = GemvProj();
-            L.x = static_cast<const uint8_t*>(h->act) + (size_t)m0 * h->I * 2;
-            L.out = static_cast<uint8_t*>(out) + (size_t)m0 * h->K * 2;
-            L.counters = h->counters + Ntg;
-            if (launch_gemv(L, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
+            if (fitB) {
+                if (launch_gemv_stream(h->fmt, mb, B, nullptr, h->part, h->part_cap, h->bar, h->err, h->num_sms,
+                                       s) != cudaSuccess)
+                    return QMLP_ERR_CUDA;
+            } else {
+                L.epi = kEpiPlain;
+                L.p0 = h->gv[2];
+                L.p1 = GemvProj();
+                L.x = ab;
+                L.out = ob;
+                L.counters = h->counters + Ntg;
+                if (launch_gemv(L, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
+            }
         }
     }
     return QMLP_OK;
@@ -428,6 +472,18 @@ qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void*
     const size_t Ntg = (size_t)(h->I / kTileRows);
     for (int m0 = 0; m0 < M; m0 += kMaxGemvM) {
         const int mb = std::min(kMaxGemvM, M - m0);
+        if (gemv_stream_fits(h->fmt, mb, P.K, 1, P.Rr)) {
+            GemvStreamPhase A;
+            A.epi = kEpiRaw;
+            A.p0 = P;
+            A.x = static_cast<const uint8_t*>(x) + (size_t)m0 * P.K * 2;
+            A.out = y + (size_t)m0 * P.N;
+            A.counters = which == 2 ? h->counters + Ntg : h->counters;
+            if (launch_gemv_stream(h->fmt, mb, A, nullptr, h->part, h->part_cap, h->bar, h->err, h->num_sms, s) !=
+                cudaSuccess)
+                return QMLP_ERR_CUDA;
+            continue;
+        }
         GemvLaunch L;
         L.fmt = h->fmt;
         L.epi = kEpiRaw;

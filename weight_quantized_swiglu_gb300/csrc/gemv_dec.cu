@@ -33,8 +33,7 @@
 //    deterministic.
 #include <algorithm>
 
-#include "common.cuh"
-#include "internal.h"
+#include "gemv_frag.cuh"
 
 namespace qmlp {
 namespace {
@@ -44,12 +43,11 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxStageBytes = 64 * 1024;
 
 struct KArgs {
-    const uint4* wc0;
-    const uint2* sc0;
+    int Lr, TWr, Rr;
+    const uint8_t* wc0;
     const float* chs0;
     float inv0;
-    const uint4* wc1;
-    const uint2* sc1;
+    const uint8_t* wc1;
     const float* chs1;
     float inv1;
     const __nv_bfloat16* x;
@@ -58,52 +56,6 @@ struct KArgs {
     float* part;
     int* counters;
 };
-
-// Weights of one chunk (64 k x 16 rows) of one projection, as loaded.
-struct ChunkW {
-    uint4 w0;  // NVFP4: all 4 groups; FP8: groups 0,1
-    uint4 w1;  // FP8: groups 2,3
-    uint2 s;   // NVFP4 scales
-};
-
-template <int FMT>
-QMLP_DEV ChunkW load_chunk(const uint4* wc, const uint2* sc, size_t chunk, int lane) {
-    ChunkW c;
-    if (FMT == kNVFP4) {
-        c.w0 = ldg_stream_u4(wc + chunk * 32 + lane);
-        c.s = ldg_stream_u2(sc + chunk * 8 + (lane >> 2));
-        c.w1 = make_uint4(0, 0, 0, 0);
-    } else {
-        c.w0 = ldg_stream_u4(wc + (chunk * 2 + 0) * 32 + lane);
-        c.w1 = ldg_stream_u4(wc + (chunk * 2 + 1) * 32 + lane);
-        c.s = make_uint2(0, 0);
-    }
-    return c;
-}
-
-QMLP_DEV uint32_t u4_word(const uint4& v, int i) {
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-// Decode group j (16 k) of a chunk into the four f16x2 A-fragment registers.
-template <int FMT>
-QMLP_DEV void decode_group(const ChunkW& c, int j, uint32_t& a0, uint32_t& a1, uint32_t& a2,
-                           uint32_t& a3) {
-    if (FMT == kNVFP4) {
-        e2m1x4_to_f16x2x4(u4_word(c.w0, j), a0, a1, a2, a3);
-        uint32_t sp = e4m3x2_to_f16x2((j < 2 ? c.s.x : c.s.y) >> (16 * (j & 1)));
-        const uint32_t slo = dup_lo16(sp), shi = dup_hi16(sp);
-        a0 = hmul2_u32(a0, slo);
-        a1 = hmul2_u32(a1, shi);
-        a2 = hmul2_u32(a2, slo);
-        a3 = hmul2_u32(a3, shi);
-    } else {
-        const uint4& v = j < 2 ? c.w0 : c.w1;
-        const int jj = j & 1;
-        e4m3x4_to_f16x2x2(u4_word(v, jj * 2 + 0), a0, a1);
-        e4m3x4_to_f16x2x2(u4_word(v, jj * 2 + 1), a2, a3);
-    }
-}
 
 template <int FMT, int NT, int NP, int EPI>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const KArgs a) {
@@ -125,45 +77,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const KArgs a) {
     const int ke = min(c1 * kChunkK, a.K);
     const int kpe = c1 * kChunkK;
     const int slots = 4 * M;
+    (void)tid;
 
-    // ---- stage x[:, kb:kpe) as prescaled fp16 B fragments ----------------
-    if (tid < 16) s_maxbits[tid] = 0;
-    __syncthreads();
-    const int real8 = (ke - kb) / 8;
-    for (int it = tid; it < M * real8; it += kThreads) {
-        const int m = it / real8, q = it - m * real8;
-        const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + kb + q * 8);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-        float mx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(h[i]);
-            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
-        atomicMax(&s_maxbits[m], __float_as_int(mx));
-    }
-    __syncthreads();
-    if (tid < M) s_sig[tid] = prescale_exponent(__int_as_float(s_maxbits[tid]));
-    __syncthreads();
-    const int pad8 = (kpe - kb) / 8;
-    for (int it = tid; it < M * pad8; it += kThreads) {
-        const int m = it / pad8, q = it - m * pad8;
-        const int kl = q * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (kb + kl < ke) v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + kb + kl);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-        const int sig = s_sig[m];
-        const int cc = kl / kChunkK, j = (kl % kChunkK) / 16, reg = (kl % 16) / 8;
-        const int half = j >> 1, word = (j & 1) * 2 + reg;
-        uint32_t* base = reinterpret_cast<uint32_t*>(xs + (size_t)(cc * 2 + half) * slots + m * 4);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const float2 f = __bfloat1622float2(h[t]);
-            const __half2 hh = __floats2half2_rn(scalbnf(f.x, sig), scalbnf(f.y, sig));
-            base[t * 4 + word] = *reinterpret_cast<const uint32_t*>(&hh);
-        }
-    }
-    __syncthreads();
+    stage_x(a.x, M, a.K, kb, ke, kpe, xs, s_maxbits, s_sig);
 
     // ---- stream weights, decode, MMA ----------------------------------------
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -178,37 +94,18 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const KArgs a) {
     const size_t tile0 = (size_t)rt * a.Kc + c0;
     ChunkW cur[NP], nxt[NP];
     if (warp < nch) {
-        cur[0] = load_chunk<FMT>(a.wc0, a.sc0, tile0 + warp, lane);
-        if (NP == 2) cur[NP - 1] = load_chunk<FMT>(a.wc1, a.sc1, tile0 + warp, lane);
+        cur[0] = load_chunk<FMT>(a.wc0, tile0 + warp, a.Lr, a.TWr, a.Rr, lane);
+        if (NP == 2) cur[NP - 1] = load_chunk<FMT>(a.wc1, tile0 + warp, a.Lr, a.TWr, a.Rr, lane);
     }
     for (int cc = warp; cc < nch; cc += kWarps) {
         const bool more = cc + kWarps < nch;
         if (more) {
-            nxt[0] = load_chunk<FMT>(a.wc0, a.sc0, tile0 + cc + kWarps, lane);
-            if (NP == 2) nxt[NP - 1] = load_chunk<FMT>(a.wc1, a.sc1, tile0 + cc + kWarps, lane);
+            nxt[0] = load_chunk<FMT>(a.wc0, tile0 + cc + kWarps, a.Lr, a.TWr, a.Rr, lane);
+            if (NP == 2) nxt[NP - 1] = load_chunk<FMT>(a.wc1, tile0 + cc + kWarps, a.Lr, a.TWr, a.Rr, lane);
         }
         uint4 xb[NT][2];
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            const int m = n * 8 + g;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                xb[n][h] = m < M ? xs[(size_t)(cc * 2 + h) * slots + m * 4 + t] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-            for (int p = 0; p < NP; ++p) {
-                uint32_t a0, a1, a2, a3;
-                decode_group<FMT>(cur[p], j, a0, a1, a2, a3);
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    const uint32_t b0 = u4_word(xb[n][j >> 1], (j & 1) * 2 + 0);
-                    const uint32_t b1 = u4_word(xb[n][j >> 1], (j & 1) * 2 + 1);
-                    mma_f16_16816(acc[p][n], a0, a1, a2, a3, b0, b1);
-                }
-            }
-        }
+        load_xfrag<NT>(xs, cc, M, slots, g, t, xb);
+        mma_chunk<FMT, NT, NP>(cur, xb, acc);
         if (more) {
 #pragma unroll
             for (int p = 0; p < NP; ++p) cur[p] = nxt[p];
@@ -287,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const KArgs a) {
 // Create-time repack into the fragment layout
 // ---------------------------------------------------------------------------
 __global__ void repack_nvfp4_gemv_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ s,
-                                         int N, int K, uint4* __restrict__ wc, uint2* __restrict__ sc) {
+                                         int N, int K, int Lr, int TWr, int Rr, uint8_t* __restrict__ wc) {
     const int Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK, G = K / 16, rb = K / 2;
     const size_t total = (size_t)Nt * Kc * 32;
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
@@ -297,6 +194,7 @@ __global__ void repack_nvfp4_gemv_kernel(const uint8_t* __restrict__ w, const ui
         const int c = (int)(tc % Kc), rt = (int)(tc / Kc);
         const int g = lane >> 2, t = lane & 3;
         const size_t r0 = (size_t)(rt * kTileRows + g), r8 = r0 + 8;
+        uint8_t* rec = wc + gemv_rec_pos(tc, Lr, TWr, Rr) * kRecNVFP4;
         uint32_t words[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -309,7 +207,7 @@ __global__ void repack_nvfp4_gemv_kernel(const uint8_t* __restrict__ w, const ui
             }
             words[j] = v;
         }
-        wc[idx] = make_uint4(words[0], words[1], words[2], words[3]);
+        reinterpret_cast<uint4*>(rec)[lane] = make_uint4(words[0], words[1], words[2], words[3]);
         if (t == 0) {
             uint32_t sv[2] = {0, 0};
 #pragma unroll
@@ -320,13 +218,13 @@ __global__ void repack_nvfp4_gemv_kernel(const uint8_t* __restrict__ w, const ui
                     sv[j >> 1] |= pair << (16 * (j & 1));
                 }
             }
-            sc[tc * 8 + g] = make_uint2(sv[0], sv[1]);
+            reinterpret_cast<uint2*>(rec + 512)[g] = make_uint2(sv[0], sv[1]);
         }
     }
 }
 
-__global__ void repack_fp8_gemv_kernel(const uint8_t* __restrict__ w, int N, int K,
-                                       uint4* __restrict__ wc) {
+__global__ void repack_fp8_gemv_kernel(const uint8_t* __restrict__ w, int N, int K, int Lr, int TWr, int Rr,
+                                       uint8_t* __restrict__ wc) {
     const int Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK;
     const size_t total = (size_t)Nt * Kc * 2 * 32;
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
@@ -347,7 +245,8 @@ __global__ void repack_fp8_gemv_kernel(const uint8_t* __restrict__ w, int N, int
             words[jj * 2 + 1] =
                 B(r0, k + 8) | (B(r0, k + 9) << 8) | (B(r8, k + 8) << 16) | (B(r8, k + 9) << 24);
         }
-        wc[idx] = make_uint4(words[0], words[1], words[2], words[3]);
+        reinterpret_cast<uint4*>(wc + gemv_rec_pos(tc, Lr, TWr, Rr) * kRecFP8 + h * 512)[lane] =
+            make_uint4(words[0], words[1], words[2], words[3]);
     }
 }
 
@@ -398,15 +297,10 @@ cudaError_t dispatch(const KArgs& a, int nt, int epi, dim3 grid, size_t smem, cu
 
 }  // namespace
 
-size_t gemv_codes_bytes(int fmt, int N, int K) {
-    const size_t Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK;
-    return Nt * Kc * 32 * 16 * (fmt == kNVFP4 ? 1 : 2);
-}
-
-size_t gemv_scales_bytes(int fmt, int N, int K) {
-    if (fmt != kNVFP4) return 0;
-    const size_t Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK;
-    return Nt * Kc * 8 * 8;
+size_t gemv_codes_bytes(int fmt, int N, int K, int Lr, int TWr) {
+    (void)N;
+    (void)K;
+    return (size_t)Lr * TWr * (fmt == kNVFP4 ? kRecNVFP4 : kRecFP8);
 }
 
 size_t gemv_part_elems(int K, int I, int num_sms) {
@@ -429,12 +323,13 @@ cudaError_t launch_gemv(const GemvLaunch& L, int num_sms, cudaStream_t s) {
     const int NP = L.epi == kEpiSwiGLU ? 2 : 1;
     if (pl.ksplit > 1 && (size_t)pl.ksplit * NP * L.M * P.N > L.part_cap) return cudaErrorInvalidValue;
     KArgs a;
+    a.Lr = P.Lr;
+    a.TWr = P.TWr;
+    a.Rr = P.Rr;
     a.wc0 = P.wc;
-    a.sc0 = P.sc;
     a.chs0 = P.chs;
     a.inv0 = P.inv_g;
     a.wc1 = L.p1.wc;
-    a.sc1 = L.p1.sc;
     a.chs1 = L.p1.chs;
     a.inv1 = L.p1.inv_g;
     a.x = reinterpret_cast<const __nv_bfloat16*>(L.x);
@@ -453,14 +348,14 @@ cudaError_t launch_gemv(const GemvLaunch& L, int num_sms, cudaStream_t s) {
                            : dispatch<kFP8>(a, pl.nt, L.epi, grid, pl.smem, s);
 }
 
-cudaError_t repack_nvfp4_gemv(const uint8_t* w, const uint8_t* scale, int N, int K, uint4* wc, uint2* sc,
-                              cudaStream_t s) {
-    repack_nvfp4_gemv_kernel<<<1024, 256, 0, s>>>(w, scale, N, K, wc, sc);
+cudaError_t repack_nvfp4_gemv(const uint8_t* w, const uint8_t* scale, int N, int K, int Lr, int TWr, int Rr,
+                              uint8_t* wc, cudaStream_t s) {
+    repack_nvfp4_gemv_kernel<<<1024, 256, 0, s>>>(w, scale, N, K, Lr, TWr, Rr, wc);
     return cudaPeekAtLastError();
 }
 
-cudaError_t repack_fp8_gemv(const uint8_t* w, int N, int K, uint4* wc, cudaStream_t s) {
-    repack_fp8_gemv_kernel<<<1024, 256, 0, s>>>(w, N, K, wc);
+cudaError_t repack_fp8_gemv(const uint8_t* w, int N, int K, int Lr, int TWr, int Rr, uint8_t* wc, cudaStream_t s) {
+    repack_fp8_gemv_kernel<<<1024, 256, 0, s>>>(w, N, K, Lr, TWr, Rr, wc);
     return cudaPeekAtLastError();
 }
 

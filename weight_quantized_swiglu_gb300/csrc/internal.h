@@ -22,19 +22,30 @@ enum GemvEpi {
     kEpiRaw = 2      // one projection -> fp32 acc (no scale), debug
 };
 
-// One projection [N, K] in the GEMV ("fragment-native") layout.
-//  NVFP4: wc = [Nt][Kc][32 lanes][16 B]   E2M1 bytes in mma A-fragment order
-//         sc = [Nt][Kc][8 row pairs][8 B] E4M3 scales (row g, row g+8) x 4 groups
-//  FP8:   wc = [Nt][Kc][2][32 lanes][16 B] e4m3fn bytes in A-fragment order
-//         chs = fp32 [N] per-channel scale
+// One projection [N, K] in the GEMV ("fragment-native") layout: one record
+// per 16-row x 64-k chunk, row-tile-major (see gemv_frag.cuh):
+//  NVFP4: 576 B = 512 B of E2M1 bytes in mma A-fragment order + 64 B of E4M3
+//         scales; FP8: 1024 B of e4m3fn bytes, with chs = fp32 [N] scales.
 // Nt = N/16 row tiles, Kc = ceil(K/64) chunks (zero padded).
+// Records are stored interleaved for the stream kernel: warp w of TWr
+// streaming warps owns the logical records [w*Lr, (w+1)*Lr) (row-tile-major
+// order), taken Rr at a time; logical record u = w*Lr + k is stored at
+// ((k / Rr) * TWr + w) * Rr + k % Rr, so at step j the 16 warps of a CTA
+// find their Rr records each in one contiguous block and the GPU sweeps one
+// contiguous window at a time. Lr is a multiple of Rr.
 struct GemvProj {
-    const uint4* wc = nullptr;
-    const uint2* sc = nullptr;
+    const uint8_t* wc = nullptr;
     const float* chs = nullptr;
     float inv_g = 1.0f;
     int N = 0, K = 0, Nt = 0, Kc = 0;
+    int Lr = 1, TWr = 1, Rr = 1;
 };
+__host__ __device__ inline size_t gemv_rec_pos(size_t u, int Lr, int TWr, int Rr) {
+    const size_t w = u / (size_t)Lr, k = u % (size_t)Lr;
+    return ((k / (size_t)Rr) * (size_t)TWr + w) * (size_t)Rr + k % (size_t)Rr;
+}
+// Streaming warps of the layout on a device with num_sms SMs.
+int gemv_layout_warps(int num_sms);
 
 struct GemvLaunch {
     int fmt;
@@ -50,13 +61,32 @@ struct GemvLaunch {
 
 cudaError_t launch_gemv(const GemvLaunch& L, int num_sms, cudaStream_t s);
 
+// Persistent stream-K GEMV (gemv_stream.cu). One phase = one projection, or
+// gate+up with the SwiGLU epilogue; with a second phase the launch is
+// cooperative and runs gate/up -> grid barrier -> down.
+struct GemvStreamPhase {
+    int epi;
+    GemvProj p0, p1;
+    const void* x;   // bf16 [M, p0.K]
+    void* out;       // bf16 or fp32 [M, p0.N]
+    int* counters;   // >= p0.Nt zeroed ints
+};
+bool gemv_stream_fits(int fmt, int M, int K, int np, int R);
+size_t gemv_stream_part_elems(int K, int I, int num_sms);
+cudaError_t launch_gemv_stream(int fmt, int M, const GemvStreamPhase& A, const GemvStreamPhase* B, float* part,
+                               size_t part_cap, unsigned* bar, int* err, int num_sms, cudaStream_t s);
+
 // Create-time repack into the GEMV layout. src pointers are device copies of
 // the checkpoint layout.
-cudaError_t repack_nvfp4_gemv(const uint8_t* w, const uint8_t* scale, int N, int K, uint4* wc,
-                              uint2* sc, cudaStream_t s);
-cudaError_t repack_fp8_gemv(const uint8_t* w, int N, int K, uint4* wc, cudaStream_t s);
-size_t gemv_codes_bytes(int fmt, int N, int K);
-size_t gemv_scales_bytes(int fmt, int N, int K);
+cudaError_t repack_nvfp4_gemv(const uint8_t* w, const uint8_t* scale, int N, int K, int Lr, int TWr, int Rr,
+                              uint8_t* wc, cudaStream_t s);
+cudaError_t repack_fp8_gemv(const uint8_t* w, int N, int K, int Lr, int TWr, int Rr, uint8_t* wc, cudaStream_t s);
+size_t gemv_codes_bytes(int fmt, int N, int K, int Lr, int TWr);
+// Records per warp per step of the layout: gate/up (streamed in pairs) take
+// 2, a projection streamed alone takes 4, so one step fills the same number
+// of bytes in both cases.
+constexpr int kGemvRecsPerStepPair = 2;
+constexpr int kGemvRecsPerStepSingle = 4;
 // Largest split-K partial buffer (fp32 elements) any GEMV launch of a handle
 // with these sizes can need for M <= 16.
 size_t gemv_part_elems(int K, int I, int num_sms);
