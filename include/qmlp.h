@@ -215,6 +215,29 @@ qmlp_status qmlp_moe_debug_stages(qmlp_moe_t* h, const void* x, qmlp_dtype xdt,
 
 qmlp_status qmlp_moe_check(qmlp_moe_t* h, qmlp_stream_t stream);
 
+/* The routed-expert step of qmlp_moe_m1_forward without a handle, for callers
+ * that cannot allocate device memory when they run it (an allocator-owning
+ * runtime that forbids foreign allocations, or code whose device memory is
+ * fixed after warm-up). It allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library call. The source pages have no counterpart; this is a
+ * library convenience over the same kernels.
+ *  banks = the expert banks as DEVICE pointers in the checkpoint layout of
+ *          qmlp_moe_desc (read directly, never copied), w13/w2 16-byte aligned
+ *  x, expert_ids, router_w, out: as qmlp_moe_m1_forward.
+ * Scratch: the fp16 SwiGLU intermediate lives in one file-scope device array
+ * of 16 x 1024 fp16 (32 KiB) that every GPU loading the library keeps until
+ * exit; hence topk <= 16 and I <= 1024, larger sizes return QMLP_ERR_SHAPE.
+ * The first call on a device looks up the array's device address (once per
+ * device, on the current device); make that first call before any stream
+ * capture. All calls share the array, which keeps the last call's contents
+ * (no call needs it cleared: each route's row is written before it is read);
+ * calls whose kernels overlap on the GPU (other streams, or other threads)
+ * race on it and must be serialized by the caller.
+ * Errors: INVALID_ARG, ALIGNMENT, ALIAS, SHAPE, UNSUPPORTED_ARCH, CUDA. */
+qmlp_status qmlp_moe_m1_forward_noalloc(const qmlp_moe_desc* banks, const void* x, qmlp_dtype xdt,
+                                        const int32_t* expert_ids, const float* router_w, int topk,
+                                        void* out, qmlp_stream_t stream);
+
 /* Human-readable name of a status ("QMLP_OK", ...). Never NULL. */
 const char* qmlp_status_str(qmlp_status s);
 

@@ -73,6 +73,7 @@ _SIGS = {
     "qmlp_moe_m1_forward": ([_VP, _VP, _I, _VP, _VP, _I, _VP, _VP], _I),
     "qmlp_moe_debug_stages": ([_VP, _VP, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _VP], _I),
     "qmlp_moe_check": ([_VP, _VP], _I),
+    "qmlp_moe_m1_forward_noalloc": ([ctypes.POINTER(qmlp_moe_desc), _VP, _I, _VP, _VP, _I, _VP, _VP], _I),
     "qmlp_status_str": ([_I], ctypes.c_char_p),
     "qmlp_abi_version": ([], _I),
 }
@@ -189,6 +190,12 @@ def qmlp_moe_debug_stages(h, x, xdt, ids, rw, topk, out, gu, act, y, stream=None
 
 def qmlp_moe_check(h, stream=None) -> int:
     return lib().qmlp_moe_check(h, _stream(stream))
+
+
+def qmlp_moe_m1_forward_noalloc(banks: qmlp_moe_desc, x, xdt, ids, rw, topk, out, stream=None) -> int:
+    """Routed-expert step on caller-owned device banks; allocates nothing."""
+    return lib().qmlp_moe_m1_forward_noalloc(ctypes.byref(banks), _ptr(x), xdt, _ptr(ids), _ptr(rw), topk,
+                                             _ptr(out), _stream(stream))
 
 
 # ---- convenience handles ------------------------------------------------------
