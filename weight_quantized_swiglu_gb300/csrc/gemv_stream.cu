@@ -128,36 +128,47 @@ __device__ __noinline__ void write_partial(const PhaseArgs* a, float* part, int 
         dst[q * 32 + lane] = make_float4(acc[q * 4 + 0], acc[q * 4 + 1], acc[q * 4 + 2], acc[q * 4 + 3]);
 }
 
-// Announce this warp's (already fenced) partial of tile rt; the last
-// contributor adds all partials in slot (= k) order and applies the epilogue.
+// Announce this warp's (already fenced) partials of the row tiles pend[0..npend)
+// -- one counter per tile, the atomics issued together from separate lanes --
+// and, for each tile where this warp arrived last, add all partials in slot
+// (= k) order and apply the epilogue.
 template <int FMT, int NT, int NP, int EPI>
-__device__ __noinline__ void finish_partial(const PhaseArgs* a, float* part, int M, int rt, int gw,
-                                            const int* s_sig) {
+__device__ __noinline__ void finish_partials(const PhaseArgs* a, float* part, int M, const int* pend, int npend,
+                                             int gw, const int* s_sig) {
     constexpr int Q = NP * NT;
     const int lane = threadIdx.x & 31;
-    int slot, nc;
-    tile_contributors(a, rt, gw, &slot, &nc);
-    int prev = 0;
-    if (lane == 0) prev = atomicAdd(&a->counters[rt], 1);
-    prev = __shfl_sync(0xffffffffu, prev, 0);
-    if (prev != nc - 1) return;
-    __threadfence();
-    if (lane == 0) a->counters[rt] = 0;
-    float v[Q * 4];
-#pragma unroll
-    for (int i = 0; i < Q * 4; ++i) v[i] = 0.0f;
-    const float4* src = reinterpret_cast<const float4*>(part) + (size_t)rt * a->smax * (Q * 32);
-    for (int sl = 0; sl < nc; ++sl) {
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const float4 f = __ldcg(src + ((size_t)sl * Q + q) * 32 + lane);
-            v[q * 4 + 0] += f.x;
-            v[q * 4 + 1] += f.y;
-            v[q * 4 + 2] += f.z;
-            v[q * 4 + 3] += f.w;
-        }
+    int prev = -1;
+    if (lane < npend) {
+        const int rt = lane == 0 ? pend[0] : pend[1];
+        unsigned* ctr = reinterpret_cast<unsigned*>(&a->counters[rt]);
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
     }
-    tile_epilogue<FMT, NT, NP, EPI>(a, M, rt, v, s_sig);
+    __syncwarp();
+    for (int i = 0; i < npend; ++i) {
+        const int rt = i == 0 ? pend[0] : pend[1];
+        int slot, nc;
+        tile_contributors(a, rt, gw, &slot, &nc);
+        const int pv = __shfl_sync(0xffffffffu, prev, i);
+        if (pv != nc - 1) continue;
+        // the acquiring lane saw every partial; order this warp's reads after it
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        if (lane == 0) a->counters[rt] = 0;
+        float v[Q * 4];
+#pragma unroll
+        for (int e = 0; e < Q * 4; ++e) v[e] = 0.0f;
+        const float4* src = reinterpret_cast<const float4*>(part) + (size_t)rt * a->smax * (Q * 32);
+        for (int sl = 0; sl < nc; ++sl) {
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const float4 f = __ldcg(src + ((size_t)sl * Q + q) * 32 + lane);
+                v[q * 4 + 0] += f.x;
+                v[q * 4 + 1] += f.y;
+                v[q * 4 + 2] += f.z;
+                v[q * 4 + 3] += f.w;
+            }
+        }
+        tile_epilogue<FMT, NT, NP, EPI>(a, M, rt, v, s_sig);
+    }
 }
 
 // Ring bookkeeping: global step index q (counting across phases) uses slot
@@ -280,7 +291,7 @@ QMLP_DEV int consume_phase(const PhaseArgs* ap, const Ring& r, int q, float* par
     }
     if (npend > 0) {
         __threadfence();
-        for (int i = 0; i < npend; ++i) finish_partial<FMT, NT, NP, EPI>(ap, part, M, pend[i], gw, s_sig);
+        finish_partials<FMT, NT, NP, EPI>(ap, part, M, pend, npend, gw, s_sig);
     }
     return q + steps;
 }
