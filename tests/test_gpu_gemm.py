@@ -1,0 +1,136 @@
+"""GPU parity of the tensor-core prefill path (GEMM family: NVFP4, M >= 17)
+against the CPU oracle, through the C ABI: exact single-weight decode, raw
+projections, the tiny shape at ragged token counts, the 27B-class prefill
+shape at its token counts (sampled rows), determinism and the automatic
+path choice."""
+import numpy as np
+import pytest
+
+import oracle
+import weight_quantized_swiglu_gb300 as q
+from weight_quantized_swiglu_gb300 import inputs as gen
+from helpers import bits_from_dev, compare, to_dev
+
+pytestmark = pytest.mark.gpu
+
+# GEMM tiles need K % 64 == 0, I % 128 == 0 (gate/up rows in 128-row halves)
+# and hidden K % 256 == 0 (down rows): the tiny shape qualifies.
+TK, TI = gen.TINY_K, gen.TINY_I
+
+
+@pytest.fixture(scope="module")
+def torch_cuda(cuda_available):
+    import torch
+    from weight_quantized_swiglu_gb300 import build
+    build.build()
+    q.lib()
+    return torch
+
+
+def run_forward(torch, mlp, x_bits, path):
+    M = x_bits.shape[0]
+    out = torch.empty((M, mlp.K), dtype=torch.int16, device="cuda")
+    act = torch.empty((M, mlp.I), dtype=torch.int16, device="cuda")
+    mlp.forward_debug(to_dev(x_bits), act, out, path=path)
+    torch.cuda.synchronize()
+    mlp.check()
+    return bits_from_dev(out), bits_from_dev(act)
+
+
+def test_gemm_one_hot_returns_decoded_weights_exactly(torch_cuda):
+    """x = e_k rows: y[r, n] = E2M1 * E4M3 of W[n, k] exactly, for gate, up
+    and down, at k positions on scale-group, k-step and tile boundaries."""
+    torch = torch_cuda
+    case = gen.gen_dense_case("nvfp4", TK, TI, 1, seed=201)
+    mlp = q.QuantMLP.from_case(case, max_M=64)
+    for which, proj in ((0, case.gate), (1, case.up), (2, case.down)):
+        Kp = proj.K
+        ks = [0, 1, 15, 16, 31, 32, 63, 64, 127, 128, Kp - 64, Kp - 17, Kp - 16, Kp - 1, 100, 200,
+              Kp // 2, Kp // 2 + 1, 65, 191]
+        x = np.zeros((len(ks), Kp), dtype=np.uint16)
+        for r, k in enumerate(ks):
+            x[r, k] = 0x3F80  # 1.0
+        y = torch.empty((len(ks), proj.N), dtype=torch.float32, device="cuda")
+        mlp.debug_project(which, to_dev(x), y, path=q.PATH_GEMM)
+        torch.cuda.synchronize()
+        got = y.cpu().numpy().astype(np.float64)
+        ref = oracle.decode_proj(proj)
+        for r, k in enumerate(ks):
+            assert np.array_equal(got[r], ref[:, k]), (which, k)
+    mlp.close()
+
+
+@pytest.mark.parametrize("M", [17, 200])
+def test_gemm_raw_projection_matches_oracle(torch_cuda, M):
+    """Unscaled projections (fp32 out) on random bf16 x, every projection;
+    M = 200 leaves a 72-row ragged second token tile."""
+    torch = torch_cuda
+    case = gen.gen_dense_case("nvfp4", TK, TI, 1, seed=202)
+    mlp = q.QuantMLP.from_case(case, max_M=256)
+    for which, proj in ((0, case.gate), (1, case.up), (2, case.down)):
+        xb = gen.gen_x_only(210 + which + M, M, proj.K)
+        y = torch.empty((M, proj.N), dtype=torch.float32, device="cuda")
+        mlp.debug_project(which, to_dev(xb), y, path=q.PATH_GEMM)
+        torch.cuda.synchronize()
+        ref = oracle.project(proj, xb)
+        got = y.cpu().numpy().astype(np.float64)
+        err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+        assert err < 1e-5, (which, err)
+    mlp.close()
+
+
+@pytest.mark.parametrize("M", [17, 128, 129, 300])
+def test_gemm_parity_tiny(torch_cuda, M):
+    case = gen.gen_dense_case("nvfp4", TK, TI, M, seed=220 + M)
+    mlp = q.QuantMLP.from_case(case)
+    out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM)
+    ref = oracle.dense_forward(case)
+    compare(act, ref["act"], what="act")
+    compare(out, ref["out"], what="out")
+    mlp.close()
+
+
+def test_gemm_is_the_automatic_path_above_16_tokens(torch_cuda):
+    case = gen.gen_dense_case("nvfp4", TK, TI, 40, seed=230)
+    mlp = q.QuantMLP.from_case(case)
+    auto, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
+    gemm, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM)
+    assert np.array_equal(auto, gemm)
+    mlp.close()
+
+
+def test_gemm_activation_magnitudes_keep_precision(torch_cuda):
+    """Rows scaled by 2^-40 and 2^30 and a zero row go through the per-token
+    fp16 prescale without loss (the same staging as the decode path)."""
+    case = gen.gen_dense_case("nvfp4", TK, TI, 48, seed=231)
+    xf = oracle.bf16_bits_to_f64(case.x)
+    xf[:16] *= 2.0 ** -40
+    xf[16:32] *= 2.0 ** 30
+    xf[47] = 0.0
+    case.x = oracle.bf16_rne_array(xf)
+    mlp = q.QuantMLP.from_case(case)
+    out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM)
+    ref = oracle.dense_forward(case)
+    for r in (0, 15, 16, 31, 40):
+        compare(act[r:r + 1], ref["act"][r:r + 1], what=f"act row {r}")
+    assert np.array_equal(oracle.bf16_bits_to_f64(act[47]), oracle.bf16_bits_to_f64(ref["act"][47]))
+    mlp.close()
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_parity_nvfp4_prefill(torch_cuda, variant):
+    """The 27B-class prefill shape (K=5120, I=17408) at M = 512 and 8192 in
+    the launch configuration the bench times; the oracle checks a seeded
+    sample of rows (rows are independent), including tile boundaries."""
+    case = gen.workload_case("nvfp4_prefill", variant)
+    M = case.M
+    mlp = q.QuantMLP.from_case(case)
+    out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
+    rng = np.random.default_rng(240 + variant)
+    rows = np.unique(np.concatenate([[0, 127, 128, M - 1], rng.choice(M, 20, replace=False)])).astype(np.int32)
+    ref = oracle.dense_forward(case, rows=rows)
+    compare(act[rows], ref["act"], what="act")
+    compare(out[rows], ref["out"], what="out")
+    out2, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
+    assert np.array_equal(out, out2)
+    mlp.close()

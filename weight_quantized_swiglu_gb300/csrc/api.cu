@@ -77,6 +77,8 @@ struct qmlp_s {
     GemvProj gv[3];  // gate, up, down
     bool has_gemm = false;
     GemmProj gm_gu, gm_d;
+    void* a16 = nullptr;       // fp16 [max_M, max(K, I)] (GEMM prescaled activations)
+    int* sig = nullptr;        // [max_M] per-token prescale exponents
     void* act = nullptr;       // bf16 [max_M, I]
     float* part = nullptr;     // split-K partials
     size_t part_cap = 0;
@@ -214,10 +216,18 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
             h->gm_gu.K = d->K;
             h->gm_gu.inv_g0 = h->gv[0].inv_g;
             h->gm_gu.inv_g1 = h->gv[1].inv_g;
+            h->gm_gu.interleaved = true;
             h->gm_d.tiles = static_cast<uint8_t*>(dn);
             h->gm_d.N = d->K;
             h->gm_d.K = d->I;
             h->gm_d.inv_g0 = h->gm_d.inv_g1 = h->gv[2].inv_g;
+            // GEMM workspace: prescaled fp16 activations (x, then act) and
+            // the per-token exponents
+            const size_t cols = (size_t)std::max(d->K, d->I);
+            if ((e = h->mem.alloc(&h->a16, (size_t)d->max_M * cols * 2)) != cudaSuccess) st = from_cuda(e);
+            else if ((e = h->mem.alloc(reinterpret_cast<void**>(&h->sig), (size_t)d->max_M * sizeof(int))) !=
+                     cudaSuccess)
+                st = from_cuda(e);
         }
     }
     // workspace
@@ -299,6 +309,8 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
         GemmLaunch g;
         g.M = M;
         g.err = h->err;
+        g.a16 = h->a16;
+        g.sig = h->sig;
         if (stages & 1) {
             g.epi = kEpiSwiGLU;
             g.w = h->gm_gu;
@@ -459,13 +471,16 @@ qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void*
     if (fault("launch")) return QMLP_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (use_gemm(h, path, M)) {
-        if (!h->has_gemm || which == 1) return QMLP_ERR_SHAPE;
+        if (!h->has_gemm) return QMLP_ERR_SHAPE;
         GemmLaunch g;
         g.epi = kEpiRaw;
-        g.w = which == 0 ? h->gm_gu : h->gm_d;
+        g.raw_sel = which == 1 ? 1 : 0;
+        g.w = which < 2 ? h->gm_gu : h->gm_d;
         g.a = x;
         g.M = M;
         g.out = y;
+        g.a16 = h->a16;
+        g.sig = h->sig;
         g.err = h->err;
         return launch_gemm(g, h->num_sms, s) == cudaSuccess ? QMLP_OK : QMLP_ERR_CUDA;
     }

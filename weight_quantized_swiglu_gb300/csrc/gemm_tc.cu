@@ -1,13 +1,596 @@
-// gemm_tc.cu -- tensor-core prefill GEMM (placeholder until the tcgen05
-// kernel lands: reports the GEMM family as unavailable).
+// gemm_tc.cu -- tensor-core prefill GEMM for NVFP4 projections (M >= 17).
+//
+// Operation (Qwen3.8-27B-NVFP4, "NVFP4 numerics as implemented" and the
+// prefill tile discussion; vllm.cpp issue "tp>1 fp8w tail-MLP shard ...",
+// "Proposed fix" for the fused gate/up epilogue):
+//   y[m, n] = sum_k a[m, k] * W[n, k],  W[n, k] = E2M1(code) * E4M3(scale[n, k/16])
+// followed by one of the epilogues
+//   SwiGLU: act[m, i] = bf16( SiLU(y_g[m, i] / g_gate) * (y_u[m, i] / g_up) )
+//   Plain:  out[m, n] = bf16( y[m, n] / g_down )
+//   Raw:    y[m, n] in fp32 (no global factor), debug.
+//
+// GB300 design (sm_103a, one CTA per SM, persistent):
+//  * a (bf16 activations) is first rewritten as fp16 x 2^sigma[m] with one
+//    power of two per token (sigma puts the row maximum in [2^14, 2^15)), so
+//    every bf16 value within 2^29 of the row maximum is held exactly; the
+//    epilogue multiplies by 2^-sigma[m]. W = E2M1 x E4M3 has at most six
+//    significant bits and lies in [2^-10, 2688]: exact in fp16. The MMA is
+//    therefore an fp16 x fp16 -> fp32 product of the same values the bf16
+//    formulation multiplies.
+//  * Tile 128 tokens x 256 weight rows, k-step 64. Warp roles:
+//      warp 0      TMA producer: the activation tile (cp.async.bulk.tensor,
+//                  128-byte swizzle) and the packed weight block of the step
+//                  (one 9 KB cp.async.bulk) into a 3-stage ring;
+//      warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma (M128 N256 K16)
+//                  per step into one of two TMEM accumulators (2 x 256 fp32
+//                  columns), tcgen05.commit frees the stage;
+//      warps 2-5   epilogue: tcgen05.ld of the finished accumulator (warp w
+//                  owns TMEM lanes 32*(w%4)..+31 = 32 token rows), scales,
+//                  SwiGLU, bf16 stores; overlaps the next tile's main loop;
+//      warps 6-13  decoders: packed E2M1 codes + E4M3 scales of the stage ->
+//                  fp16 weights (cvt.rn.f16x2.e2m1x2, then an exact f16x2
+//                  multiply by the group scale) written in the 128-byte
+//                  swizzled K-major layout the MMA descriptor reads.
+//  * Weight block layout (create-time repack): for n-tile j and k-step s a
+//    contiguous 9216-byte block: codes [256 rows][32 B] then scales
+//    [256 rows][4 B]. For gate/up the 256 rows of tile j are gate rows
+//    128j..128j+127 followed by up rows 128j..128j+127, so one accumulator
+//    holds both inputs of 128 SwiGLU outputs per token.
+//  * Every wait is bounded (globaltimer); on expiry the kernel records the
+//    error, every role leaves its loop, in-flight copies and MMAs are waited
+//    for (bounded) and TMEM is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
 #include "internal.h"
 
 namespace qmlp {
-bool gemm_supported(int, int) { return false; }
-size_t gemm_tiles_bytes(int, int) { return 0; }
-cudaError_t repack_nvfp4_gemm(const uint8_t*, const uint8_t*, const uint8_t*, const uint8_t*, int, int, bool,
-                              uint8_t*, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int BM = 128;                 // tokens per tile (TMEM lanes)
+constexpr int BN = 256;                 // weight rows per tile (accumulator columns)
+constexpr int BK = 64;                  // k per step (one 128-byte swizzle row of fp16)
+constexpr int kStages = 3;
+constexpr int kABytes = BM * BK * 2;    // 16 KB
+constexpr int kBBytes = BN * BK * 2;    // 32 KB
+constexpr int kRawCodes = BN * BK / 2;  // 8 KB
+constexpr int kRawBytes = kRawCodes + BN * (BK / 16);  // + 1 KB scales = 9216
+constexpr int kEpiWarps = 4;
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kThreads = (2 + kEpiWarps + kDecWarps) * 32;  // 448
+constexpr int kTmemCols = 2 * BN;                           // two accumulators
+constexpr uint64_t kGemmWaitNs = 2000000000ull;             // 2 s
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kABytes;
+constexpr int kOffRaw = kOffB + kStages * kBBytes;
+constexpr int kOffBar = kOffRaw + kStages * kRawBytes;
+// barriers: full[S], bready[S], empty[S], acc_full[2], acc_empty[2], done
+constexpr int kNumBars = 3 * kStages + 5;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem address, abort flag
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+
+static_assert(kOffB % 1024 == 0 && kOffRaw % 16 == 0 && kOffBar % 8 == 0, "smem layout");
+static_assert(kSmemBytes <= 227 * 1024, "smem budget");
+
+struct Args {
+    const uint8_t* tiles;  // packed weight blocks [Nt][KS][kRawBytes]
+    int M, N, Kd;          // tokens, weight rows (projection outputs), contraction length
+    int epi;               // kEpiSwiGLU / kEpiPlain / kEpiRaw
+    int raw_sel;           // raw on an interleaved gate/up GEMM: 0 gate rows, 1 up rows
+    int interleaved;       // tiles hold gate/up halves
+    float inv0, inv1;      // global factors (gate, up) or (down, down)
+    const int* sig;        // [M] per-token prescale exponent
+    void* out;             // bf16 [M, N_out] or fp32 [M, N_out]
+    int ldo;               // out row length (elements)
+    int* err;
+};
+
+// ---------------------------------------------------------------------------
+// tcgen05 / TMA primitives (inline PTX)
+// ---------------------------------------------------------------------------
+QMLP_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
 }
-cudaError_t launch_gemm(const GemmLaunch&, int, cudaStream_t) { return cudaErrorNotSupported; }
+
+QMLP_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+QMLP_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+QMLP_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+QMLP_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16, one thread.
+QMLP_DEV void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
+QMLP_DEV void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread = lane, v[j] = column col+j.
+QMLP_DEV void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes with
+// the 128-byte swizzle, 8-row groups 1024 bytes apart (SBO), sm100 version
+// bits, swizzle mode 2 (128B).
+QMLP_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1u << 16;                    // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024u >> 4) << 32;          // stride byte offset
+    d |= (uint64_t)1u << 46;                    // descriptor version
+    d |= (uint64_t)2u << 61;                    // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
+// K-major, N = BN, M = BM.
+constexpr uint32_t kIdesc = (1u << 4)                    // D format fp32
+                            | (0u << 7) | (0u << 10)     // A, B fp16
+                            | ((uint32_t)(BN >> 3) << 17)  // N >> 3
+                            | ((uint32_t)(BM >> 4) << 24); // M >> 4
+
+// Wait for phase `parity` of `bar`; false if the CTA's abort flag is raised
+// or the wait ran out (which raises it and records `code`).
+QMLP_DEV bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kGemmWaitNs) {
+            *abort_flag = 1;
+            atomicExch(err, code);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Decode one (row, 32-k half) item of a packed block into the swizzled fp16
+// B tile: 16 code bytes (32 weights, low nibble = even k) and two E4M3
+// scales (k 0..15 and 16..31 of the half).
+QMLP_DEV void decode_item(const uint8_t* raw, uint8_t* bt, int n, int h) {
+    const uint4 c = *reinterpret_cast<const uint4*>(raw + n * 32 + h * 16);
+    const uint32_t s2 = *reinterpret_cast<const uint16_t*>(raw + kRawCodes + n * 4 + h * 2);
+    const uint32_t sf = e4m3x2_to_f16x2(s2);
+    const uint32_t sa = dup_lo16(sf), sb = dup_hi16(sf);
+    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+    uint8_t* row = bt + n * 128;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t f0, f1, f2, f3;
+        e2m1x4_to_f16x2x4(words[j], f0, f1, f2, f3);
+        const uint32_t s = j < 2 ? sa : sb;
+        uint4 o;
+        o.x = hmul2_u32(f0, s);
+        o.y = hmul2_u32(f1, s);
+        o.z = hmul2_u32(f2, s);
+        o.w = hmul2_u32(f3, s);
+        const int chunk = (h * 4 + j) ^ (n & 7);
+        *reinterpret_cast<uint4*>(row + chunk * 16) = o;
+    }
+}
+
+QMLP_DEV uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                   const Args a) {
+    extern __shared__ uint8_t dyn_smem_raw[];
+    const uint32_t base_s = (smem_u32(dyn_smem_raw) + 1023u) & ~1023u;
+    uint8_t* base = dyn_smem_raw + (base_s - smem_u32(dyn_smem_raw));
+    const uint32_t bar0 = base_s + kOffBar;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto bready = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto empty = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
+    auto acc_full = [&](int b) { return bar0 + 8u * (3 * kStages + b); };
+    auto acc_empty = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (3 * kStages + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Mt = (a.M + BM - 1) / BM;
+    const int Nt = a.N / BN;
+    const int KS = a.Kd / BK;
+    const int tiles = Mt * Nt;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(bready(s), kDecThreads);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), kEpiWarps * 32);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&amap)) : "memory");
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int nt = t / Mt, mt = t % Mt;
+                const uint8_t* blk = a.tiles + (size_t)nt * KS * kRawBytes;
+                for (int ks = 0; ks < KS; ++ks, ++it) {
+                    const int s = it % kStages;
+                    if (it >= kStages &&
+                        !wait_or_abort(empty(s), (uint32_t)((it / kStages - 1) & 1), abort_flag, a.err, 11)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full(s), kABytes + kRawBytes);
+                    tma_load_2d(base_s + kOffA + s * kABytes, &amap, ks * BK, mt * BM, full(s));
+                    bulk_g2s(base_s + kOffRaw + s * kRawBytes, blk + (size_t)ks * kRawBytes, kRawBytes, full(s));
+                }
+            }
+            // copies still in flight (only after an abort): wait for the last
+            // one issued into each stage
+            if (!ok) {
+                for (int q = it - 1; q >= 0 && q >= it - kStages; --q)
+                    mbar_wait_bounded(full(q % kStages), (uint32_t)((q / kStages) & 1), kGemmWaitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int it = 0, tc = 0;
+            bool ok = true, issued = false;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
+                const int buf = tc & 1, use = tc >> 1;
+                if (use > 0 &&
+                    !wait_or_abort(acc_empty(buf), (uint32_t)((use - 1) & 1), abort_flag, a.err, 12)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
+                for (int ks = 0; ks < KS; ++ks, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (uint32_t)((it / kStages) & 1);
+                    if (!wait_or_abort(full(s), ph, abort_flag, a.err, 13) ||
+                        !wait_or_abort(bready(s), ph, abort_flag, a.err, 14)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base_s + kOffA + s * kABytes;
+                    const uint32_t sb = base_s + kOffB + s * kBBytes;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        umma_f16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), kIdesc,
+                                 (ks | k) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    umma_commit(empty(s));
+                }
+                if (!ok) break;
+                umma_commit(acc_full(buf));
+            }
+            // every MMA this thread issued must be finished before TMEM is freed
+            if (issued) {
+                umma_commit(done_bar);
+                mbar_wait_bounded(done_bar, 0, kGemmWaitNs);
+            }
+        }
+    } else if (warp < 2 + kEpiWarps) {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        const int row_in_tile = q * 32 + lane;
+        int tc = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
+            const int nt = t / Mt, mt = t % Mt;
+            const int buf = tc & 1, use = tc >> 1;
+            // warp-uniform: the TMEM loads below are .sync.aligned
+            const bool ready = wait_or_abort(acc_full(buf), (uint32_t)(use & 1), abort_flag, a.err, 15);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const int m = mt * BM + row_in_tile;
+            const bool live = m < a.M;
+            const int sg = live ? a.sig[m] : 0;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+            if (a.epi == kEpiSwiGLU) {
+                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+                    float g[32], u[32];
+                    tmem_ld32(tbase + c0, g);
+                    tmem_ld32(tbase + BN / 2 + c0, u);
+                    if (live) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            float r2[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float gv = scalbnf(g[j + e], -sg) * a.inv0;
+                                const float uv = scalbnf(u[j + e], -sg) * a.inv1;
+                                r2[e] = silu_f32(gv) * uv;
+                            }
+                            pk[j / 2] = pack_bf16x2(r2[0], r2[1]);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * (BN / 2) + c0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+            } else if (a.epi == kEpiPlain) {
+                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    float y[32];
+                    tmem_ld32(tbase + c0, y);
+                    if (live) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2)
+                            pk[j / 2] = pack_bf16x2(scalbnf(y[j], -sg) * a.inv0, scalbnf(y[j + 1], -sg) * a.inv0);
+                        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * BN + c0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+            } else {
+                float* out = reinterpret_cast<float*>(a.out);
+                const int cbeg = a.interleaved ? a.raw_sel * (BN / 2) : 0;
+                const int cend = a.interleaved ? cbeg + BN / 2 : BN;
+                const int ocol = a.interleaved ? nt * (BN / 2) : nt * BN;
+#pragma unroll 1
+                for (int c0 = cbeg; c0 < cend; c0 += 32) {
+                    float y[32];
+                    tmem_ld32(tbase + c0, y);
+                    if (live) {
+                        float4* dst = reinterpret_cast<float4*>(out + (size_t)m * a.ldo + ocol + (c0 - cbeg));
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(scalbnf(y[4 * v], -sg), scalbnf(y[4 * v + 1], -sg),
+                                                 scalbnf(y[4 * v + 2], -sg), scalbnf(y[4 * v + 3], -sg));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acc_empty(buf));
+        }
+    } else {
+        // ---------------- decoders ----------------
+        const int d = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. kDecThreads-1
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            for (int ks = 0; ks < KS; ++ks, ++it) {
+                const int s = it % kStages;
+                if (!wait_or_abort(full(s), (uint32_t)((it / kStages) & 1), abort_flag, a.err, 16)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* raw = base + kOffRaw + s * kRawBytes;
+                uint8_t* bt = base + kOffB + s * kBBytes;
+#pragma unroll
+                for (int j = 0; j < (BN * 2) / kDecThreads; ++j) {
+                    const int item = d + j * kDecThreads;
+                    decode_item(raw, bt, item >> 1, item & 1);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(bready(s));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// a (bf16 [M, C]) -> a16 (fp16 [M, C]) * 2^sig[m], sig[m] = the exponent
+// that brings max|a[m, :]| into [2^14, 2^15). One CTA per row.
+__global__ void __launch_bounds__(256) prescale_rows_kernel(const __nv_bfloat16* __restrict__ a, __half* a16,
+                                                            int* sig, int M, int C) {
+    __shared__ float red[8];
+    for (int m = blockIdx.x; m < M; m += gridDim.x) {
+        const uint4* row = reinterpret_cast<const uint4*>(a + (size_t)m * C);
+        float mx = 0.0f;
+        for (int i = threadIdx.x; i < C / 8; i += blockDim.x) {
+            const uint4 v = row[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                mx = fmaxf(mx, fabsf(__uint_as_float(w[j] << 16)));
+                mx = fmaxf(mx, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+        __syncthreads();
+        float rmax = 0.0f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) rmax = fmaxf(rmax, red[i]);
+        const int e = prescale_exponent(rmax);
+        if (threadIdx.x == 0) sig[m] = e;
+        uint4* orow = reinterpret_cast<uint4*>(a16 + (size_t)m * C);
+        for (int i = threadIdx.x; i < C / 8; i += blockDim.x) {
+            const uint4 v = row[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float lo = scalbnf(__uint_as_float(w[j] << 16), e);
+                const float hi = scalbnf(__uint_as_float(w[j] & 0xFFFF0000u), e);
+                const __half2 h = __floats2half2_rn(lo, hi);
+                o[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            orow[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        __syncthreads();  // red[] is reused by the next row
+    }
+}
+
+// Create-time repack into the weight-block layout (see the top of the file).
+__global__ void repack_gemm_kernel(const uint8_t* __restrict__ w0, const uint8_t* __restrict__ s0,
+                                   const uint8_t* __restrict__ w1, const uint8_t* __restrict__ s1, int N, int K,
+                                   int interleave, uint8_t* __restrict__ tiles) {
+    const int KS = K / BK;
+    const long total = (long)(N / BN) * KS * BN;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const int r = (int)(idx % BN);
+        const long blk = idx / BN;  // = j * KS + ks
+        const int ks = (int)(blk % KS);
+        const int j = (int)(blk / KS);
+        const uint8_t* w;
+        const uint8_t* s;
+        int row;
+        if (interleave) {
+            const bool up = r >= BN / 2;
+            w = up ? w1 : w0;
+            s = up ? s1 : s0;
+            row = j * (BN / 2) + (r - (up ? BN / 2 : 0));
+        } else {
+            w = w0;
+            s = s0;
+            row = j * BN + r;
+        }
+        uint8_t* dst = tiles + blk * kRawBytes;
+        const uint4* src = reinterpret_cast<const uint4*>(w + (size_t)row * (K / 2) + ks * (BK / 2));
+        uint4* dc = reinterpret_cast<uint4*>(dst + r * 32);
+        dc[0] = src[0];
+        dc[1] = src[1];
+        *reinterpret_cast<uint32_t*>(dst + kRawCodes + r * 4) =
+            *reinterpret_cast<const uint32_t*>(s + (size_t)row * (K / 16) + ks * (BK / 16));
+    }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool gemm_supported(int K, int N) { return K >= BK && K % BK == 0 && N >= BN && N % BN == 0; }
+
+size_t gemm_tiles_bytes(int N, int K) { return (size_t)(N / BN) * (K / BK) * kRawBytes; }
+
+cudaError_t repack_nvfp4_gemm(const uint8_t* w0, const uint8_t* s0, const uint8_t* w1, const uint8_t* s1, int N,
+                              int K, bool interleave, uint8_t* tiles, cudaStream_t s) {
+    if (!gemm_supported(K, N) || (interleave && (!w1 || !s1))) return cudaErrorInvalidValue;
+    const long total = (long)(N / BN) * (K / BK) * BN;
+    const int grid = (int)std::min<long>((total + 255) / 256, 65535);
+    repack_gemm_kernel<<<grid, 256, 0, s>>>(w0, s0, w1, s1, N, K, interleave ? 1 : 0, tiles);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
+    const GemmProj& P = L.w;
+    if (!gemm_supported(P.K, P.N) || L.M < 1 || !L.a16 || !L.sig) return cudaErrorInvalidValue;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+
+    // 1. per-token fp16 prescale of the activations
+    const int pgrid = std::min(L.M, 8 * std::max(num_sms, 1));
+    prescale_rows_kernel<<<pgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(L.a),
+                                                static_cast<__half*>(L.a16), L.sig, L.M, P.K);
+    cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+
+    // 2. tensor map of the fp16 activations: [M rows, K] row-major, box 64 x 128
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)P.K, (cuuint64_t)L.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)P.K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.a16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    // 3. the GEMM
+    Args a;
+    a.tiles = P.tiles;
+    a.M = L.M;
+    a.N = P.N;
+    a.Kd = P.K;
+    a.epi = L.epi;
+    a.raw_sel = L.raw_sel;
+    a.interleaved = P.interleaved ? 1 : 0;
+    a.inv0 = P.inv_g0;
+    a.inv1 = P.inv_g1;
+    a.sig = L.sig;
+    a.out = L.out;
+    a.ldo = L.epi == kEpiSwiGLU ? P.N / 2 : (L.epi == kEpiRaw && P.interleaved ? P.N / 2 : P.N);
+    a.err = L.err;
+    static bool attr = false;
+    if (!attr) {
+        e = cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int tiles = ((L.M + BM - 1) / BM) * (P.N / BN);
+    const int grid = std::min(tiles, std::max(num_sms, 1));
+    gemm_nvfp4_kernel<<<grid, kThreads, kSmemBytes, s>>>(map, a);
+    return cudaPeekAtLastError();
+}
+
 }  // namespace qmlp

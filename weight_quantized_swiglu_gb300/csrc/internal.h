@@ -95,21 +95,25 @@ size_t gemv_part_elems(int K, int I, int num_sms);
 // Tensor-core prefill GEMM (NVFP4, tcgen05)
 // ---------------------------------------------------------------------------
 struct GemmProj {
-    const uint8_t* tiles = nullptr;  // [N/BN][K/BK][BN rows][BK/2 B codes] + scales, see gemm_tc.cu
-    float inv_g0 = 1.0f, inv_g1 = 1.0f;  // column halves (gate, up) or both = down
-    int N = 0, K = 0;
+    const uint8_t* tiles = nullptr;  // packed weight blocks [N/256][K/64][9216 B], see gemm_tc.cu
+    float inv_g0 = 1.0f, inv_g1 = 1.0f;  // global factors: (gate, up) when interleaved, else both = down
+    int N = 0, K = 0;                    // N weight rows (2I when interleaved), K contraction length
+    bool interleaved = false;            // tile rows = 128 gate rows then the same 128 up rows
 };
 size_t gemm_tiles_bytes(int N, int K);
 cudaError_t repack_nvfp4_gemm(const uint8_t* w0, const uint8_t* s0, const uint8_t* w1,
                               const uint8_t* s1, int N, int K, bool interleave, uint8_t* tiles,
                               cudaStream_t s);
 struct GemmLaunch {
-    int epi;            // kEpiSwiGLU / kEpiPlain / kEpiRaw
+    int epi = kEpiPlain;  // kEpiSwiGLU / kEpiPlain / kEpiRaw
+    int raw_sel = 0;      // kEpiRaw on an interleaved GEMM: 0 = gate rows, 1 = up rows
     GemmProj w;
-    const void* a;      // bf16 [M, K]
-    int M;
-    void* out;          // bf16 [M, N_out] or fp32 [M, N_out] (raw)
-    int* err;           // device error word
+    const void* a = nullptr;  // bf16 [M, K]
+    int M = 0;
+    void* out = nullptr;      // bf16 [M, N_out] or fp32 [M, N_out] (raw)
+    void* a16 = nullptr;      // workspace fp16 [M, K]: prescaled activations
+    int* sig = nullptr;       // workspace [M]: per-token prescale exponents
+    int* err = nullptr;       // device error word
 };
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s);
 bool gemm_supported(int K, int N);
