@@ -499,6 +499,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--extras", default="all",
+                    help="comma list of extra workloads to time (decode,fp8,tiny,moe,prefill) or 'all'")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile", default=None,
                     help="eager launches of one operation for ncu: fused|stage0|stage1|fp8_fused|moe|prefillM")
@@ -528,17 +530,25 @@ def main():
     extras = {}
     if not args.no_extras and rank == 0:
         import weight_quantized_swiglu_gb300 as q
-        extras["dense_nvfp4_decode_M4"] = bench_dense_secondary("dense_nvfp4_decode", 1, 2400, nvfp4_bytes(K_HID, I_INT))
-        extras["dense_fp8_decode_M1"] = bench_dense_secondary("dense_fp8_decode", 0, 2400, fp8_bytes(K_HID, I_INT))
-        extras["dense_fp8_decode_M16"] = bench_dense_secondary("dense_fp8_decode", 1, 1200, fp8_bytes(K_HID, I_INT))
-        extras["tiny_nvfp4_M1"] = bench_dense_secondary("tiny_nvfp4", 0, 4800, nvfp4_bytes(gen.TINY_K, gen.TINY_I))
-        extras["moe_awq_m1_4B"] = bench_moe(4)
-        extras["moe_awq_m1_3B"] = bench_moe(3)
-        try:
-            extras["nvfp4_prefill_M512"] = bench_prefill(512, 5, pk)
-            extras["nvfp4_prefill_M8192"] = bench_prefill(8192, 3, pk)
-        except q.QmlpError as e:
-            extras["nvfp4_prefill"] = {"unavailable": str(e)}
+        want = set(args.extras.split(",")) if args.extras != "all" else {"decode", "fp8", "tiny", "moe", "prefill"}
+        if "decode" in want:
+            extras["dense_nvfp4_decode_M4"] = bench_dense_secondary("dense_nvfp4_decode", 1, 2400,
+                                                                    nvfp4_bytes(K_HID, I_INT))
+        if "fp8" in want:
+            extras["dense_fp8_decode_M1"] = bench_dense_secondary("dense_fp8_decode", 0, 2400, fp8_bytes(K_HID, I_INT))
+            extras["dense_fp8_decode_M16"] = bench_dense_secondary("dense_fp8_decode", 1, 1200,
+                                                                   fp8_bytes(K_HID, I_INT))
+        if "tiny" in want:
+            extras["tiny_nvfp4_M1"] = bench_dense_secondary("tiny_nvfp4", 0, 4800, nvfp4_bytes(gen.TINY_K, gen.TINY_I))
+        if "moe" in want:
+            extras["moe_awq_m1_4B"] = bench_moe(4)
+            extras["moe_awq_m1_3B"] = bench_moe(3)
+        if "prefill" in want:
+            try:
+                extras["nvfp4_prefill_M512"] = bench_prefill(512, 5, pk)
+                extras["nvfp4_prefill_M8192"] = bench_prefill(8192, 3, pk)
+            except q.QmlpError as e:
+                extras["nvfp4_prefill"] = {"unavailable": str(e)}
         torch.cuda.synchronize()
 
     cpu = cpu_baseline(case, args.cpu_budget) if rank == 0 else None

@@ -20,17 +20,20 @@
 //  * Tile 128 tokens x 256 weight rows, k-step 64. Warp roles:
 //      warp 0      TMA producer: the activation tile (cp.async.bulk.tensor,
 //                  128-byte swizzle) and the packed weight block of the step
-//                  (one 9 KB cp.async.bulk) into a 3-stage ring;
+//                  (one 9 KB cp.async.bulk) into a 6-stage load ring (TMA
+//                  and L2 latency is several MMA steps long);
 //      warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma (M128 N256 K16)
 //                  per step into one of two TMEM accumulators (2 x 256 fp32
-//                  columns), tcgen05.commit frees the stage;
+//                  columns), tcgen05.commit frees the load stage and the
+//                  decoded stage;
 //      warps 2-5   epilogue: tcgen05.ld of the finished accumulator (warp w
 //                  owns TMEM lanes 32*(w%4)..+31 = 32 token rows), scales,
 //                  SwiGLU, bf16 stores; overlaps the next tile's main loop;
 //      warps 6-13  decoders: packed E2M1 codes + E4M3 scales of the stage ->
 //                  fp16 weights (cvt.rn.f16x2.e2m1x2, then an exact f16x2
 //                  multiply by the group scale) written in the 128-byte
-//                  swizzled K-major layout the MMA descriptor reads.
+//                  swizzled K-major layout the MMA descriptor reads, into a
+//                  2-stage ring (decoding step i+1 overlaps the MMAs of step i).
 //  * Weight block layout (create-time repack): for n-tile j and k-step s a
 //    contiguous 9216-byte block: codes [256 rows][32 B] then scales
 //    [256 rows][4 B]. For gate/up the 256 rows of tile j are gate rows
@@ -53,7 +56,8 @@ namespace {
 constexpr int BM = 128;                 // tokens per tile (TMEM lanes)
 constexpr int BN = 256;                 // weight rows per tile (accumulator columns)
 constexpr int BK = 64;                  // k per step (one 128-byte swizzle row of fp16)
-constexpr int kStages = 3;
+constexpr int kLStages = 6;             // load ring: activation tile + packed weight block
+constexpr int kBStages = 2;             // decoded-weight ring
 constexpr int kABytes = BM * BK * 2;    // 16 KB
 constexpr int kBBytes = BN * BK * 2;    // 32 KB
 constexpr int kRawCodes = BN * BK / 2;  // 8 KB
@@ -67,11 +71,11 @@ constexpr uint64_t kGemmWaitNs = 2000000000ull;             // 2 s
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kABytes;
-constexpr int kOffRaw = kOffB + kStages * kBBytes;
-constexpr int kOffBar = kOffRaw + kStages * kRawBytes;
-// barriers: full[S], bready[S], empty[S], acc_full[2], acc_empty[2], done
-constexpr int kNumBars = 3 * kStages + 5;
+constexpr int kOffB = kOffA + kLStages * kABytes;
+constexpr int kOffRaw = kOffB + kBStages * kBBytes;
+constexpr int kOffBar = kOffRaw + kLStages * kRawBytes;
+// barriers: full[L], empty[L], bfull[B], bempty[B], acc_full[2], acc_empty[2], done
+constexpr int kNumBars = 2 * kLStages + 2 * kBStages + 5;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem address, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 
@@ -217,11 +221,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
     uint8_t* base = dyn_smem_raw + (base_s - smem_u32(dyn_smem_raw));
     const uint32_t bar0 = base_s + kOffBar;
     auto full = [&](int s) { return bar0 + 8u * s; };
-    auto bready = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto empty = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
-    auto acc_full = [&](int b) { return bar0 + 8u * (3 * kStages + b); };
-    auto acc_empty = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };
-    const uint32_t done_bar = bar0 + 8u * (3 * kStages + 4);
+    auto empty = [&](int s) { return bar0 + 8u * (kLStages + s); };
+    auto bfull = [&](int b) { return bar0 + 8u * (2 * kLStages + b); };
+    auto bempty = [&](int b) { return bar0 + 8u * (2 * kLStages + kBStages + b); };
+    auto acc_full = [&](int b) { return bar0 + 8u * (2 * kLStages + 2 * kBStages + b); };
+    auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kLStages + 2 * kBStages + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kLStages + 2 * kBStages + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
 
@@ -232,10 +237,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
     const int tiles = Mt * Nt;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kLStages; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(bready(s), kDecThreads);
             mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < kBStages; ++b) {
+            mbar_init(bfull(b), kDecThreads);
+            mbar_init(bempty(b), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full(b), 1);
@@ -261,9 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
                 const int nt = t / Mt, mt = t % Mt;
                 const uint8_t* blk = a.tiles + (size_t)nt * KS * kRawBytes;
                 for (int ks = 0; ks < KS; ++ks, ++it) {
-                    const int s = it % kStages;
-                    if (it >= kStages &&
-                        !wait_or_abort(empty(s), (uint32_t)((it / kStages - 1) & 1), abort_flag, a.err, 11)) {
+                    const int s = it % kLStages;
+                    if (it >= kLStages &&
+                        !wait_or_abort(empty(s), (uint32_t)((it / kLStages - 1) & 1), abort_flag, a.err, 11)) {
                         ok = false;
                         break;
                     }
@@ -275,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
             // copies still in flight (only after an abort): wait for the last
             // one issued into each stage
             if (!ok) {
-                for (int q = it - 1; q >= 0 && q >= it - kStages; --q)
-                    mbar_wait_bounded(full(q % kStages), (uint32_t)((q / kStages) & 1), kGemmWaitNs);
+                for (int q = it - 1; q >= 0 && q >= it - kLStages; --q)
+                    mbar_wait_bounded(full(q % kLStages), (uint32_t)((q / kLStages) & 1), kGemmWaitNs);
             }
         }
     } else if (warp == 1) {
@@ -294,16 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
                 for (int ks = 0; ks < KS; ++ks, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (uint32_t)((it / kStages) & 1);
-                    if (!wait_or_abort(full(s), ph, abort_flag, a.err, 13) ||
-                        !wait_or_abort(bready(s), ph, abort_flag, a.err, 14)) {
+                    const int s = it % kLStages, b = it % kBStages;
+                    if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 13) ||
+                        !wait_or_abort(bfull(b), (uint32_t)((it / kBStages) & 1), abort_flag, a.err, 14)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sa = base_s + kOffA + s * kABytes;
-                    const uint32_t sb = base_s + kOffB + s * kBBytes;
+                    const uint32_t sb = base_s + kOffB + b * kBBytes;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         umma_f16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), kIdesc,
@@ -311,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
                     }
                     issued = true;
                     umma_commit(empty(s));
+                    umma_commit(bempty(b));
                 }
                 if (!ok) break;
                 umma_commit(acc_full(buf));
@@ -408,20 +416,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
         bool ok = true;
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
             for (int ks = 0; ks < KS; ++ks, ++it) {
-                const int s = it % kStages;
-                if (!wait_or_abort(full(s), (uint32_t)((it / kStages) & 1), abort_flag, a.err, 16)) {
+                const int s = it % kLStages, b = it % kBStages;
+                if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 16) ||
+                    (it >= kBStages &&
+                     !wait_or_abort(bempty(b), (uint32_t)((it / kBStages - 1) & 1), abort_flag, a.err, 17))) {
                     ok = false;
                     break;
                 }
                 const uint8_t* raw = base + kOffRaw + s * kRawBytes;
-                uint8_t* bt = base + kOffB + s * kBBytes;
+                uint8_t* bt = base + kOffB + b * kBBytes;
 #pragma unroll
                 for (int j = 0; j < (BN * 2) / kDecThreads; ++j) {
                     const int item = d + j * kDecThreads;
                     decode_item(raw, bt, item >> 1, item & 1);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(bready(s));
+                mbar_arrive(bfull(b));
             }
         }
     }
