@@ -152,6 +152,13 @@ qmlp_status qmlp_forward_debug(qmlp_t* h, qmlp_path path, const void* x, int M, 
 qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void* x, int M,
                                float* y, qmlp_stream_t stream);
 
+/* CTAs of the single-launch decode kernel that partitions the intermediate
+ * dimension (each CTA computes gate/up for its slice of I and the down
+ * projection over that slice; the partial outputs are reduced in a fixed
+ * order after one grid barrier). 0 when the shape has no such partition on
+ * this device (the stream-K kernel is used instead). Used for M <= 8. */
+int qmlp_decode_ctas(qmlp_t* h);
+
 /* Synchronize `stream` and report (then clear) a bounded-wait give-up
  * recorded by this handle's kernels: OK or DEVICE_TIMEOUT (CUDA on a sticky
  * device error). */

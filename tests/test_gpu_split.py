@@ -1,0 +1,90 @@
+"""GPU parity of the single-launch decode kernel that partitions the
+intermediate dimension across CTAs (each CTA: gate/up for its slice of I,
+then the down projection over that slice; partial outputs reduced in a
+fixed order after one grid barrier), against the CPU oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import weight_quantized_swiglu_gb300 as q
+from weight_quantized_swiglu_gb300 import inputs as gen
+from helpers import bits_from_dev, compare, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda(cuda_available):
+    import torch
+    from weight_quantized_swiglu_gb300 import build
+    build.build()
+    q.lib()
+    return torch
+
+
+def run_forward(torch, mlp, x_bits):
+    M = x_bits.shape[0]
+    out = torch.empty((M, mlp.K), dtype=torch.int16, device="cuda")
+    act = torch.empty((M, mlp.I), dtype=torch.int16, device="cuda")
+    mlp.forward_debug(to_dev(x_bits), act, out, path=q.PATH_GEMV)
+    torch.cuda.synchronize()
+    mlp.check()
+    return bits_from_dev(out), bits_from_dev(act)
+
+
+def sm_count(torch):
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def test_plan_of_the_27b_shape(torch_cuda):
+    """K=5120, I=17408 on a 152-SM GB300: 136 CTAs x 8 gate/up row tiles."""
+    if sm_count(torch_cuda) != 152:
+        pytest.skip("the expected partition is for a 152-SM device")
+    case = gen.workload_case("dense_nvfp4_decode", 0)
+    mlp = q.QuantMLP.from_case(case)
+    assert mlp.decode_ctas() == 136
+    mlp.close()
+
+
+# (K, I): tiles of 4 CTA-local gate/up tiles spanning 4 warps each (1024,
+# 7680 -> 120 CTAs); down tiles split at warp boundaries with padding records
+# (1536, 23040 -> 120 CTAs, 3 down chunks per CTA, 20 records per warp).
+SHAPES = [(1024, 7680), (1536, 23040)]
+
+
+@pytest.mark.parametrize("K,I", SHAPES)
+@pytest.mark.parametrize("fmt,M", [("nvfp4", 1), ("nvfp4", 3), ("nvfp4", 8), ("fp8", 1), ("fp8", 5)])
+def test_split_parity(torch_cuda, K, I, fmt, M):
+    case = gen.gen_dense_case(fmt, K, I, M, seed=310 + M + K // 512)
+    mlp = q.QuantMLP.from_case(case)
+    if mlp.decode_ctas() == 0:
+        pytest.skip("no I partition for this shape on this device")
+    out, act = run_forward(torch_cuda, mlp, case.x)
+    ref = oracle.dense_forward(case)
+    compare(act, ref["act"], what="act")
+    compare(out, ref["out"], what="out")
+    out2, act2 = run_forward(torch_cuda, mlp, case.x)
+    assert np.array_equal(out, out2) and np.array_equal(act, act2)
+    mlp.close()
+
+
+def test_split_many_calls_keep_the_barrier_aligned(torch_cuda):
+    """200 back-to-back launches (the ticket counter keeps counting) give the
+    same bits as the first, with changing inputs in between."""
+    torch = torch_cuda
+    K, I = SHAPES[0]
+    case = gen.gen_dense_case("nvfp4", K, I, 2, seed=320)
+    mlp = q.QuantMLP.from_case(case)
+    if mlp.decode_ctas() == 0:
+        pytest.skip("no I partition for this shape on this device")
+    first, _ = run_forward(torch, mlp, case.x)
+    x2 = gen.gen_x_only(321, 2, K)
+    xd, x2d = to_dev(case.x), to_dev(x2)
+    out = torch.empty((2, K), dtype=torch.int16, device="cuda")
+    for i in range(200):
+        mlp.forward(x2d if i % 2 else xd, out)
+    torch.cuda.synchronize()
+    mlp.check()
+    last, _ = run_forward(torch, mlp, case.x)
+    assert np.array_equal(first, last)
+    mlp.close()

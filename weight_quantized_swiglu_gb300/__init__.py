@@ -68,6 +68,7 @@ _SIGS = {
     "qmlp_forward_debug": ([_VP, _I, _VP, _I, _VP, _VP, _VP], _I),
     "qmlp_debug_project": ([_VP, _I, _I, _VP, _I, _VP, _VP], _I),
     "qmlp_check": ([_VP, _VP], _I),
+    "qmlp_decode_ctas": ([_VP], _I),
     "qmlp_moe_create": ([ctypes.POINTER(_VP), ctypes.POINTER(qmlp_moe_desc), _VP], _I),
     "qmlp_moe_destroy": ([_VP], None),
     "qmlp_moe_m1_forward": ([_VP, _VP, _I, _VP, _VP, _I, _VP, _VP], _I),
@@ -168,6 +169,10 @@ def qmlp_check(h, stream=None) -> int:
     return lib().qmlp_check(h, _stream(stream))
 
 
+def qmlp_decode_ctas(h) -> int:
+    return lib().qmlp_decode_ctas(h)
+
+
 def qmlp_moe_create(desc: qmlp_moe_desc, stream=None) -> int:
     h = ctypes.c_void_p()
     st = lib().qmlp_moe_create(ctypes.byref(h), ctypes.byref(desc), _stream(stream))
@@ -255,6 +260,10 @@ class QuantMLP:
 
     def check(self, stream=None):
         _chk(qmlp_check(self.h, stream), "qmlp_check")
+
+    def decode_ctas(self):
+        """CTAs of the I-partitioned single-launch decode kernel (0: not used)."""
+        return qmlp_decode_ctas(self.h)
 
     def close(self):
         if getattr(self, "h", None):

@@ -20,6 +20,9 @@ using namespace qmlp;
 namespace {
 
 constexpr int kMaxGemvM = 16;
+// Largest token block the I-partitioned fused decode kernel takes (its
+// cross-CTA partials grow with M; larger blocks use the stream-K kernel).
+constexpr int kMaxSplitM = 8;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -75,6 +78,11 @@ qmlp_status check_device(int* dev, int* num_sms) {
 struct qmlp_s {
     int fmt = 0, K = 0, I = 0, max_M = 0, device = 0, num_sms = 0;
     GemvProj gv[3];  // gate, up, down
+    int layout_warps = 0;       // streaming warps of the GEMV record layout
+    SplitPlan sp;               // I-partitioned decode plan (sp.G == 0: none)
+    uint8_t* wsplit = nullptr;  // down records in the CTA-sliced layout
+    float* spart = nullptr;     // [G][16][K] fp32 partial outputs
+    unsigned long long* ticket = nullptr;  // grid-barrier ticket counter
     bool has_gemm = false;
     GemmProj gm_gu, gm_d;
     void* a16 = nullptr;       // fp16 [max_M, max(K, I)] (GEMM prescaled activations)
@@ -135,7 +143,7 @@ static qmlp_status load_proj(qmlp_t* h, const qmlp_proj& src, int N, int K, int 
     dst.K = K;
     dst.Nt = N / kTileRows;
     dst.Kc = (K + kChunkK - 1) / kChunkK;
-    dst.TWr = gemv_layout_warps(h->num_sms);
+    dst.TWr = h->layout_warps;
     dst.Rr = Rr;
     dst.Lr = (int)(((long)dst.Nt * dst.Kc + dst.TWr - 1) / dst.TWr);
     dst.Lr = (dst.Lr + dst.Rr - 1) / dst.Rr * dst.Rr;
@@ -190,6 +198,8 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
     h->max_M = d->max_M;
     h->device = dev;
     h->num_sms = sms;
+    h->sp = plan_split(d->K, d->I, sms);
+    h->layout_warps = h->sp.G ? h->sp.G * 16 : gemv_layout_warps(sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* tmp[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     const qmlp_proj* srcs[3] = {&d->gate, &d->up, &d->down};
@@ -198,6 +208,27 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
     for (int p = 0; p < 3 && st == QMLP_OK; ++p)
         st = load_proj(h, *srcs[p], Ns[p], Ks[p], p < 2 ? kGemvRecsPerStepPair : kGemvRecsPerStepSingle, h->gv[p],
                        &tmp[2 * p], &tmp[2 * p + 1], s);
+
+    // the CTA-sliced copy of the down projection for the I-partitioned kernel
+    if (st == QMLP_OK && h->sp.G) {
+        void *wsp = nullptr, *part = nullptr, *tk = nullptr;
+        const size_t wb = split_codes_bytes(h->fmt, h->sp);
+        if ((e = h->mem.alloc(&wsp, wb)) != cudaSuccess) st = from_cuda(e);
+        else if ((e = h->mem.alloc(&part, split_part_elems(d->K, h->sp) * sizeof(float))) != cudaSuccess)
+            st = from_cuda(e);
+        else if ((e = h->mem.alloc(&tk, 64)) != cudaSuccess) st = from_cuda(e);
+        else if (cudaMemsetAsync(wsp, 0, wb, s) != cudaSuccess || cudaMemsetAsync(tk, 0, 64, s) != cudaSuccess)
+            st = QMLP_ERR_CUDA;
+        else if ((h->fmt == kNVFP4 ? repack_nvfp4_split(tmp[4], tmp[5], d->K, d->I, h->sp, static_cast<uint8_t*>(wsp), s)
+                                   : repack_fp8_split(tmp[4], d->K, d->I, h->sp, static_cast<uint8_t*>(wsp), s)) !=
+                 cudaSuccess)
+            st = QMLP_ERR_CUDA;
+        if (st == QMLP_OK) {
+            h->wsplit = static_cast<uint8_t*>(wsp);
+            h->spart = static_cast<float*>(part);
+            h->ticket = static_cast<unsigned long long*>(tk);
+        }
+    }
 
     if (st == QMLP_OK && h->fmt == kNVFP4 && d->max_M > kMaxGemvM && gemm_supported(d->K, 2 * d->I) &&
         gemm_supported(d->I, d->K)) {
@@ -349,6 +380,26 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
                    fitB = gemv_stream_fits(h->fmt, mb, h->I, 1, h->gv[2].Rr);
         const bool fitAB = gemv_stream_fits(h->fmt, mb, std::max(h->K, h->I), 2, h->gv[0].Rr) &&
                            gemv_stream_fits(h->fmt, mb, std::max(h->K, h->I), 1, h->gv[2].Rr);
+        if (stages == 3 && h->sp.G && mb <= kMaxSplitM && split_fits(h->fmt, mb, h->K, h->sp)) {
+            SplitLaunch S;
+            S.fmt = h->fmt;
+            S.M = mb;
+            S.K = h->K;
+            S.I = h->I;
+            S.gate = h->gv[0];
+            S.up = h->gv[1];
+            S.wdown = h->wsplit;
+            S.chsd = h->gv[2].chs;
+            S.invd = h->gv[2].inv_g;
+            S.x = xb;
+            S.act_out = ab;  // the workspace act (qmlp_forward_debug returns it)
+            S.out = ob;
+            S.part = h->spart;
+            S.ticket = h->ticket;
+            S.err = h->err;
+            if (launch_split(S, h->sp, s) != cudaSuccess) return QMLP_ERR_CUDA;
+            continue;
+        }
         if (stages == 3 && fitAB) {
             if (launch_gemv_stream(h->fmt, mb, A, &B, h->part, h->part_cap, h->bar, h->err, h->num_sms, s) !=
                 cudaSuccess)
@@ -522,10 +573,15 @@ qmlp_status qmlp_check(qmlp_t* h, qmlp_stream_t stream) {
     if (cudaMemcpy(&v, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QMLP_ERR_CUDA;
     if (v != 0) {
         cudaMemset(h->err, 0, sizeof(int));
+        // a launch that gave up may have left the grid-barrier ticket off a
+        // multiple of the CTA count: start the count again
+        if (h->ticket) cudaMemset(h->ticket, 0, sizeof(unsigned long long));
         return QMLP_ERR_DEVICE_TIMEOUT;
     }
     return QMLP_OK;
 }
+
+int qmlp_decode_ctas(qmlp_t* h) { return h ? h->sp.G : 0; }
 
 // ---------------------------------------------------------------------------
 // routed-expert AWQ

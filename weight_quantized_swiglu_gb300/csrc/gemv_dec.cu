@@ -183,8 +183,23 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const KArgs a) {
 // ---------------------------------------------------------------------------
 // Create-time repack into the fragment layout
 // ---------------------------------------------------------------------------
+// Record position of (row tile rt, chunk c): the row-tile-major stream
+// layout (split = false) or the CTA-sliced layout of the I-partitioned MLP.
+struct RecPos {
+    int Lr, TWr, Rr;        // stream layout
+    bool split;
+    int Cb, LB;             // CTA-sliced layout (TWr = 16G, Rr = 4)
+    __device__ size_t operator()(int rt, int c, int Kc) const {
+        if (!split) return gemv_rec_pos((size_t)rt * Kc + c, Lr, TWr, Rr);
+        const int b = c / Cb;
+        const long u = (long)rt * Cb + c % Cb;
+        const int w = (int)(u / LB), k = (int)(u % LB);
+        return ((size_t)(k / Rr) * TWr + (size_t)b * 16 + w) * Rr + k % Rr;
+    }
+};
+
 __global__ void repack_nvfp4_gemv_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ s,
-                                         int N, int K, int Lr, int TWr, int Rr, uint8_t* __restrict__ wc) {
+                                         int N, int K, RecPos pos, uint8_t* __restrict__ wc) {
     const int Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK, G = K / 16, rb = K / 2;
     const size_t total = (size_t)Nt * Kc * 32;
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
@@ -194,7 +209,7 @@ __global__ void repack_nvfp4_gemv_kernel(const uint8_t* __restrict__ w, const ui
         const int c = (int)(tc % Kc), rt = (int)(tc / Kc);
         const int g = lane >> 2, t = lane & 3;
         const size_t r0 = (size_t)(rt * kTileRows + g), r8 = r0 + 8;
-        uint8_t* rec = wc + gemv_rec_pos(tc, Lr, TWr, Rr) * kRecNVFP4;
+        uint8_t* rec = wc + pos(rt, c, Kc) * kRecNVFP4;
         uint32_t words[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -223,7 +238,7 @@ __global__ void repack_nvfp4_gemv_kernel(const uint8_t* __restrict__ w, const ui
     }
 }
 
-__global__ void repack_fp8_gemv_kernel(const uint8_t* __restrict__ w, int N, int K, int Lr, int TWr, int Rr,
+__global__ void repack_fp8_gemv_kernel(const uint8_t* __restrict__ w, int N, int K, RecPos pos,
                                        uint8_t* __restrict__ wc) {
     const int Nt = N / kTileRows, Kc = (K + kChunkK - 1) / kChunkK;
     const size_t total = (size_t)Nt * Kc * 2 * 32;
@@ -245,7 +260,7 @@ __global__ void repack_fp8_gemv_kernel(const uint8_t* __restrict__ w, int N, int
             words[jj * 2 + 1] =
                 B(r0, k + 8) | (B(r0, k + 9) << 8) | (B(r8, k + 8) << 16) | (B(r8, k + 9) << 24);
         }
-        reinterpret_cast<uint4*>(wc + gemv_rec_pos(tc, Lr, TWr, Rr) * kRecFP8 + h * 512)[lane] =
+        reinterpret_cast<uint4*>(wc + pos(rt, c, Kc) * kRecFP8 + h * 512)[lane] =
             make_uint4(words[0], words[1], words[2], words[3]);
     }
 }
@@ -350,12 +365,30 @@ cudaError_t launch_gemv(const GemvLaunch& L, int num_sms, cudaStream_t s) {
 
 cudaError_t repack_nvfp4_gemv(const uint8_t* w, const uint8_t* scale, int N, int K, int Lr, int TWr, int Rr,
                               uint8_t* wc, cudaStream_t s) {
-    repack_nvfp4_gemv_kernel<<<1024, 256, 0, s>>>(w, scale, N, K, Lr, TWr, Rr, wc);
+    repack_nvfp4_gemv_kernel<<<1024, 256, 0, s>>>(w, scale, N, K, RecPos{Lr, TWr, Rr, false, 0, 0}, wc);
     return cudaPeekAtLastError();
 }
 
 cudaError_t repack_fp8_gemv(const uint8_t* w, int N, int K, int Lr, int TWr, int Rr, uint8_t* wc, cudaStream_t s) {
-    repack_fp8_gemv_kernel<<<1024, 256, 0, s>>>(w, N, K, Lr, TWr, Rr, wc);
+    repack_fp8_gemv_kernel<<<1024, 256, 0, s>>>(w, N, K, RecPos{Lr, TWr, Rr, false, 0, 0}, wc);
+    return cudaPeekAtLastError();
+}
+
+// The CTA-sliced down layout of the I-partitioned MLP (see SplitPlan); the
+// padding records past Nt*Cb of each CTA must be zeroed by the caller.
+cudaError_t repack_nvfp4_split(const uint8_t* w, const uint8_t* scale, int N, int K, const SplitPlan& P,
+                               uint8_t* wc, cudaStream_t s) {
+    if (!P.G || (K / kChunkK) != P.G * P.Cb || K % kChunkK) return cudaErrorInvalidValue;
+    repack_nvfp4_gemv_kernel<<<1024, 256, 0, s>>>(w, scale, N, K,
+                                                  RecPos{P.LB, P.G * 16, kGemvRecsPerStepSingle, true, P.Cb, P.LB},
+                                                  wc);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t repack_fp8_split(const uint8_t* w, int N, int K, const SplitPlan& P, uint8_t* wc, cudaStream_t s) {
+    if (!P.G || (K / kChunkK) != P.G * P.Cb || K % kChunkK) return cudaErrorInvalidValue;
+    repack_fp8_gemv_kernel<<<1024, 256, 0, s>>>(w, N, K,
+                                                RecPos{P.LB, P.G * 16, kGemvRecsPerStepSingle, true, P.Cb, P.LB}, wc);
     return cudaPeekAtLastError();
 }
 

@@ -1,0 +1,594 @@
+// gemv_split.cu -- the whole decode MLP (M <= 16) in one persistent launch,
+// with the intermediate dimension partitioned across CTAs.
+//
+// Operation (vllm.cpp issue "tp>1 fp8w tail-MLP shard ...", "Proposed fix";
+// Qwen3.8-27B-NVFP4, "NVFP4 numerics as implemented"):
+//   act[m, i] = bf16( SiLU(sg * x[m].Wg[i]) * (su * x[m].Wu[i]) )
+//   out[m, n] = bf16( sd * sum_i act[m, i] Wd[n, i] )
+// with W decoded on the fly (NVFP4: E2M1 x E4M3, s = 1/global; FP8: e4m3fn,
+// s = per-channel scale).
+//
+// Schedule: CTA b of G owns the T gate/up row tiles [T*b, T*(b+1)) -- the
+// act slice i in [16*T*b, 16*T*(b+1)) -- and the matching T*16 columns of
+// the down projection. The dependency between the projections is then local
+// to the CTA:
+//  1. stream gate/up (16 consumer warps, L_A records each, tiles split
+//     between warps are combined in shared memory) -> SwiGLU -> the CTA's
+//     act slice in shared memory (bf16 values);
+//  2. restage the slice as prescaled fp16 fragments, stream the down
+//     records of the slice (every output row tile, Cb = T/4 k-chunks) ->
+//     the CTA's partial out[m, n] over its slice, fp32, to global memory;
+//  3. one grid-wide barrier (a 64-bit ticket counter: one atomic per CTA),
+//     then every CTA reduces a share of the outputs over the G partials in
+//     a fixed order and applies the down scale.
+// The producer warp streams the gate/up records and then the down records
+// without a pause (the down weights do not depend on act), one bulk-async
+// copy per projection and step into a shared-memory ring, as in
+// gemv_stream.cu. No float atomics: every sum has a fixed order.
+// Every wait is bounded (globaltimer); on expiry the CTA records the error,
+// still arrives at the grid barrier exactly once, waits for its own copies
+// in flight and leaves.
+#include <algorithm>
+
+#include "gemv_frag.cuh"
+
+namespace qmlp {
+namespace {
+
+constexpr int kW = 16;                // consumer warps
+constexpr int kCT = kW * 32;          // consumer threads
+constexpr int kThr = kCT + 32;        // + one producer warp
+constexpr int kDepthMax = 16;
+constexpr int kBudget = 220 * 1024;
+constexpr int kBars = 2 * kDepthMax * 8;
+constexpr int kRA = kGemvRecsPerStepPair;  // gate/up records per warp per step
+constexpr uint64_t kLimit = 2000000000ull;  // 2 s
+
+struct Args {
+    // phase A: gate (wc0) and up (wc1), row-tile-major layout over 16*G warps
+    const uint8_t* wa0;
+    const uint8_t* wa1;
+    const float* chs0;
+    const float* chs1;
+    float inv0, inv1;
+    // phase B: down in the CTA-sliced layout
+    const uint8_t* wb;
+    const float* chsd;
+    float invd;
+    const __nv_bfloat16* x;    // [M, K]
+    __nv_bfloat16* act_out;    // optional [M, I]
+    __nv_bfloat16* out;        // [M, K]
+    float* part;               // [G][M][K]
+    unsigned long long* ticket;
+    int* err;
+    int M, K, I;
+    int G, T, KcA, LA, Cb, NtD, LB;
+    int xs_bytes;              // x staging (phase A) region
+    int pa_off, act_off, pb_off;  // byte offsets of the combine / act regions
+    int ring_off, slot_bytes, depth;
+    int SA;                    // partial slots per gate/up tile
+};
+
+struct Ring {
+    uint8_t* base;
+    uint32_t base_s, full0, empty0;
+    int slot_bytes, depth;
+};
+
+// Producer: steps [0, steps) of one phase; step j of CTA b is the 16 warps'
+// records R*j..R*j+R-1, contiguous in the interleaved layout.
+template <int FMT, int NP>
+QMLP_DEV int produce(const uint8_t* w0, const uint8_t* w1, int R, int steps, int TW, const Ring& r, int q,
+                     int* err) {
+    constexpr uint32_t rec = rec_bytes<FMT>();
+    const uint32_t step_bytes = kW * R * rec;
+    const size_t stride = (size_t)TW * R * rec;
+    const uint8_t* s0 = w0 + (size_t)blockIdx.x * kW * R * rec;
+    const uint8_t* s1 = NP == 2 ? w1 + (size_t)blockIdx.x * kW * R * rec : nullptr;
+    int slot = q % r.depth, round = q / r.depth;
+    for (int j = 0; j < steps; ++j, ++q) {
+        if (round > 0 && !mbar_wait_bounded(r.empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kLimit)) {
+            atomicExch(err, 24);
+            return -(q + 1);
+        }
+        const uint32_t full = r.full0 + 8u * slot;
+        const uint32_t dst = r.base_s + (uint32_t)slot * r.slot_bytes;
+        mbar_arrive_expect_tx(full, NP * step_bytes);
+        bulk_g2s(dst, s0 + (size_t)j * stride, step_bytes, full);
+        if (NP == 2) bulk_g2s(dst + step_bytes, s1 + (size_t)j * stride, step_bytes, full);
+        if (++slot == r.depth) {
+            slot = 0;
+            ++round;
+        }
+    }
+    return q;
+}
+
+// Fragment element (p, n, e) of lane (g, t): token m = 8n + 2t + (e & 1),
+// row g + 8*(e >> 1). Compact partial layout: [p][m][16 rows] fp32.
+template <int NT, int NP>
+QMLP_DEV void store_compact(float* dst, int M, const float (&acc)[NP][NT][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = n * 8 + 2 * t + (e & 1);
+                if (m < M) dst[(p * M + m) * 16 + g + 8 * (e >> 1)] = acc[p][n][e];
+            }
+}
+template <int NT, int NP>
+QMLP_DEV void add_compact(const float* src, int M, float (&v)[NP][NT][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = n * 8 + 2 * t + (e & 1);
+                if (m < M) v[p][n][e] += src[(p * M + m) * 16 + g + 8 * (e >> 1)];
+            }
+}
+
+// Combine a tile's partial through shared memory: store this warp's part in
+// its slot, count arrivals; the last of `nc` contributors gets true and the
+// slot-ordered sum in `v`.
+template <int NT, int NP>
+QMLP_DEV bool combine_smem(float* slots, int slot_floats, int slot, int nc, int* cnt, int M, float (&v)[NP][NT][4]) {
+    const int lane = threadIdx.x & 31;
+    store_compact<NT, NP>(slots + slot * slot_floats, M, v);
+    __syncwarp();
+    int prev = 0;
+    if (lane == 0) {
+        __threadfence_block();
+        prev = atomicAdd(cnt, 1);
+    }
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev != nc - 1) return false;
+    __threadfence_block();
+    if (lane == 0) *cnt = 0;
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[p][n][e] = 0.0f;
+    for (int sl = 0; sl < nc; ++sl) add_compact<NT, NP>(slots + sl * slot_floats, M, v);
+    return true;
+}
+
+// Phase-A epilogue of local tile lt: act = bf16(SiLU(g)*u) into the CTA's
+// act slice (and optionally the global act).
+template <int FMT, int NT>
+QMLP_DEV void epilogue_a(const Args& a, int M, int lt, const float (&v)[2][NT][4], const int* s_sig,
+                         float* s_act) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int tslice = a.T * 16;
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int m = n * 8 + 2 * t + (e & 1);
+            if (m >= M) continue;
+            const int r = lt * 16 + g + 8 * (e >> 1);  // row within the CTA's slice
+            const int i = blockIdx.x * tslice + r;     // intermediate index
+            const float s0 = FMT == kNVFP4 ? a.inv0 : a.chs0[i];
+            const float s1 = FMT == kNVFP4 ? a.inv1 : a.chs1[i];
+            const float gv = scalbnf(v[0][n][e], -s_sig[m]) * s0;
+            const float uv = scalbnf(v[1][n][e], -s_sig[m]) * s1;
+            const __nv_bfloat16 act = __float2bfloat16_rn(silu_f32(gv) * uv);
+            s_act[m * tslice + r] = __bfloat162float(act);
+            if (a.act_out) a.act_out[(size_t)m * a.I + i] = act;
+        }
+}
+
+// Phase-B result of down row tile rt over this CTA's slice -> global partial.
+template <int NT>
+QMLP_DEV void store_part_b(const Args& a, int M, int rt, const float (&v)[1][NT][4], const int* s_sigb) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    float* dst = a.part + (size_t)blockIdx.x * M * a.K;
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int m = n * 8 + 2 * t + (e & 1);
+            if (m < M) dst[(size_t)m * a.K + rt * 16 + g + 8 * (e >> 1)] = scalbnf(v[0][n][e], -s_sigb[m]);
+        }
+}
+
+template <int NT, int NP>
+QMLP_DEV void zero_acc(float (&acc)[NP][NT][4]) {
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[p][n][e] = 0.0f;
+}
+
+QMLP_DEV unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <int FMT, int NT, bool M1>
+__global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_constant__ Args a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_maxbits[16];
+    __shared__ int s_sig[16];
+    __shared__ int s_sigb[16];
+    __shared__ int s_cnta[64];
+    __shared__ int s_cntb[kW];
+    __shared__ float s_red[kW][32];
+    __shared__ int s_fail;
+    __shared__ int s_pass;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int M = a.M;
+    Ring r;
+    r.base = smem + a.ring_off;
+    r.base_s = smem_u32(r.base);
+    r.slot_bytes = a.slot_bytes;
+    r.depth = a.depth;
+    r.full0 = smem_u32(r.base + (size_t)a.depth * a.slot_bytes);
+    r.empty0 = r.full0 + 8u * kDepthMax;
+    const int stepsA = a.LA / kRA, stepsB = a.LB / kGemvRecsPerStepSingle;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.depth; ++i) {
+            mbar_init(r.full0 + 8u * i, 1);
+            mbar_init(r.empty0 + 8u * i, kW);
+        }
+        fence_mbar_init();
+        s_fail = 0;
+    }
+    if (threadIdx.x < 64) s_cnta[threadIdx.x] = 0;
+    if (threadIdx.x < kW) s_cntb[threadIdx.x] = 0;
+    __syncthreads();  // the last CTA-wide barrier: the producer never waits on the consumers
+
+    if (warp == kW) {
+        if (lane == 0) {
+            int q = produce<FMT, 2>(a.wa0, a.wa1, kRA, stepsA, a.G * kW, r, 0, a.err);
+            if (q >= 0) q = produce<FMT, 1>(a.wb, nullptr, kGemvRecsPerStepSingle, stepsB, a.G * kW, r, q, a.err);
+            if (q < 0) {
+                const int issued = -q - 1;
+                for (int qq = issued - 1; qq >= 0 && qq >= issued - a.depth; --qq)
+                    mbar_wait_bounded(r.full0 + 8u * (qq % a.depth), (uint32_t)((qq / a.depth) & 1), kLimit);
+            }
+        }
+        return;
+    }
+
+    constexpr int rec = rec_bytes<FMT>();
+    uint4* xs = reinterpret_cast<uint4*>(smem);
+    float* s_pa = reinterpret_cast<float*>(smem + a.pa_off);
+    float* s_act = reinterpret_cast<float*>(smem + a.act_off);
+    float* s_pb = reinterpret_cast<float*>(smem + a.pb_off);
+    const int g = lane >> 2, t = lane & 3;
+    bool ok = true;
+
+    // ---------------- phase A: gate/up over this CTA's tiles ----------------
+    stage_x(a.x, M, a.K, 0, a.K, a.KcA * kChunkK, xs, s_maxbits, s_sig, kCT);
+    int q = 0;
+    {
+        const int slots = 4 * M;
+        const int pa_floats = 2 * M * 16;
+        const uint32_t step_bytes = (uint32_t)kW * kRA * rec;
+        float acc[2][NT][4];
+        zero_acc<NT, 2>(acc);
+        const int u0 = warp * a.LA;  // local record index of this warp's first record
+        int lt = u0 / a.KcA, c = u0 % a.KcA, cs = c;
+        int slot = 0;
+        uint32_t parity = 0;
+        int k = 0;
+        for (int j = 0; j < stepsA && ok; ++j) {
+            if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, kLimit)) {
+                if (lane == 0) atomicExch(a.err, 21);
+                ok = false;
+                break;
+            }
+            const uint8_t* sb = r.base + (uint32_t)slot * (uint32_t)r.slot_bytes + (uint32_t)warp * kRA * rec;
+            for (int kk = 0; kk < kRA; ++kk, ++k, sb += rec) {
+                ChunkW w[2];
+                w[0] = lds_chunk<FMT>(sb, lane);
+                w[1] = lds_chunk<FMT>(sb + step_bytes, lane);
+                uint4 xb[NT][2];
+                load_xfrag<NT>(xs, c, M, slots, g, t, xb);
+                mma_chunk<FMT, NT, 2, M1>(w, xb, acc);
+                if (++c == a.KcA || k == a.LA - 1) {
+                    if (cs == 0 && c == a.KcA) {
+                        epilogue_a<FMT, NT>(a, M, lt, acc, s_sig, s_act);
+                    } else {
+                        const int w0 = (lt * a.KcA) / a.LA, w1 = ((lt + 1) * a.KcA - 1) / a.LA;
+                        if (combine_smem<NT, 2>(s_pa + (size_t)lt * a.SA * pa_floats, pa_floats, warp - w0,
+                                                w1 - w0 + 1, &s_cnta[lt], M, acc))
+                            epilogue_a<FMT, NT>(a, M, lt, acc, s_sig, s_act);
+                    }
+                    zero_acc<NT, 2>(acc);
+                    ++lt;
+                    c = 0;
+                    cs = 0;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(r.empty0 + 8u * slot);
+            if (++slot == r.depth) {
+                slot = 0;
+                parity ^= 1u;
+            }
+        }
+        q = stepsA;
+    }
+    if (!ok && lane == 0) s_fail = 1;
+    named_bar_sync(1, kCT);  // the CTA's act slice is complete
+
+    // ---------------- restage act (prescaled fp16 fragments) ----------------
+    const int tslice = a.T * 16;
+    if (s_fail == 0) {
+        if (threadIdx.x < 16) s_maxbits[threadIdx.x] = 0;
+        named_bar_sync(1, kCT);
+        for (int m = 0; m < M; ++m) {
+            float mx = 0.0f;
+            for (int i = threadIdx.x; i < tslice; i += kCT) mx = fmaxf(mx, fabsf(s_act[m * tslice + i]));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0 && mx > 0.0f) atomicMax(&s_maxbits[m], __float_as_int(mx));
+        }
+        named_bar_sync(1, kCT);
+        if (threadIdx.x < M) s_sigb[threadIdx.x] = prescale_exponent(__int_as_float(s_maxbits[threadIdx.x]));
+        named_bar_sync(1, kCT);
+        const int slots = 4 * M;
+        for (int it = threadIdx.x; it < M * (tslice / 8); it += kCT) {
+            const int m = it / (tslice / 8), k8 = (it % (tslice / 8)) * 8;
+            const float* src = s_act + m * tslice + k8;
+            uint4 v;
+            uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(src[2 * h], src[2 * h + 1]);  // exact: bf16 values
+                vw[h] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            stage_store8(xs, slots, m, k8, s_sigb[m], v);
+        }
+        named_bar_sync(1, kCT);
+    }
+
+    // ---------------- phase B: down over this CTA's act slice ----------------
+    if (s_fail == 0) {
+        const int slots = 4 * M;
+        const int pb_floats = M * 16;
+        float acc[1][NT][4];
+        zero_acc<NT, 1>(acc);
+        const int nrec = a.NtD * a.Cb;          // real records of the CTA
+        const int u0 = warp * a.LB;
+        const int n = max(0, min(a.LB, nrec - u0));  // real records of this warp
+        int rt = u0 / a.Cb, c = u0 % a.Cb, cs = c;
+        int slot = q % r.depth;
+        uint32_t parity = (uint32_t)((q / r.depth) & 1);
+        int k = 0;
+        for (int j = 0; j < stepsB && ok; ++j) {
+            if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, kLimit)) {
+                if (lane == 0) atomicExch(a.err, 22);
+                ok = false;
+                break;
+            }
+            const uint8_t* sb = r.base + (uint32_t)slot * (uint32_t)r.slot_bytes +
+                                (uint32_t)warp * kGemvRecsPerStepSingle * rec;
+            const int kend = min(k + kGemvRecsPerStepSingle, n);
+            for (; k < kend; ++k, sb += rec) {
+                ChunkW w[1];
+                w[0] = lds_chunk<FMT>(sb, lane);
+                uint4 xb[NT][2];
+                load_xfrag<NT>(xs, c, M, slots, g, t, xb);
+                mma_chunk<FMT, NT, 1, M1>(w, xb, acc);
+                if (++c == a.Cb || k == n - 1) {
+                    if (cs == 0 && c == a.Cb) {
+                        store_part_b<NT>(a, M, rt, acc, s_sigb);
+                    } else {
+                        // a tile split at a warp boundary: two contributors
+                        const int wb = (cs == 0) ? warp : warp - 1;  // boundary after warp wb
+                        if (combine_smem<NT, 1>(s_pb + (size_t)wb * 2 * pb_floats, pb_floats, cs == 0 ? 0 : 1, 2,
+                                                &s_cntb[wb], M, acc))
+                            store_part_b<NT>(a, M, rt, acc, s_sigb);
+                    }
+                    zero_acc<NT, 1>(acc);
+                    ++rt;
+                    c = 0;
+                    cs = 0;
+                }
+            }
+            k = max(k, (j + 1) * kGemvRecsPerStepSingle);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(r.empty0 + 8u * slot);
+            if (++slot == r.depth) {
+                slot = 0;
+                parity ^= 1u;
+            }
+        }
+    }
+    if (!ok && lane == 0) s_fail = 1;
+
+    // ---------------- grid barrier (every CTA arrives exactly once) ----------------
+    __threadfence();
+    named_bar_sync(1, kCT);
+    if (threadIdx.x == 0) {
+        const unsigned long long tk = atomicAdd(a.ticket, 1ull);
+        const unsigned long long target = (tk / (unsigned long long)a.G + 1ull) * (unsigned long long)a.G;
+        int pass = 1;
+        if (tk + 1ull != target) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_u64(a.ticket) < target) {
+                if (globaltimer_ns() - t0 > kLimit) {
+                    atomicExch(a.err, 23);
+                    pass = 0;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        s_pass = pass;
+    }
+    named_bar_sync(1, kCT);
+    if (s_pass == 0) return;
+    // a CTA that failed still reduces: every partial it could not write is
+    // reported through the error word, and outputs are never left unwritten
+
+    // ---------------- reduction over the G partials ----------------
+    const int units_n = (a.K + 31) / 32;
+    const int units = M * units_n;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int m = u / units_n, n = (u % units_n) * 32 + lane;
+        float sum = 0.0f;
+        if (n < a.K) {
+            const float* src = a.part + (size_t)m * a.K + n;
+            const size_t bstride = (size_t)M * a.K;
+            for (int b = warp; b < a.G; b += kW) sum += __ldcg(src + (size_t)b * bstride);
+        }
+        s_red[warp][lane] = sum;
+        named_bar_sync(1, kCT);
+        if (warp == 0 && n < a.K) {
+            float tot = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kW; ++w) tot += s_red[w][lane];
+            const float sd = FMT == kNVFP4 ? a.invd : a.chsd[n];
+            a.out[(size_t)m * a.K + n] = __float2bfloat16_rn(tot * sd);
+        }
+        named_bar_sync(1, kCT);
+    }
+}
+
+template <int FMT, int NT, bool M1>
+cudaError_t launch_t(const Args& a, size_t smem, cudaStream_t s) {
+    auto kern = gemv_split_kernel<FMT, NT, M1>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBudget);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.G);
+    cfg.blockDim = dim3(kThr);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+struct Layout {
+    int xs, pa, act, pb, ring, slot, depth, sa;
+    size_t total;
+};
+
+Layout layout_for(int fmt, int M, int K, const SplitPlan& P) {
+    Layout L;
+    const int kca = (K + kChunkK - 1) / kChunkK;
+    const int rec = fmt == kNVFP4 ? kRecNVFP4 : kRecFP8;
+    auto al = [](size_t v) { return (int)((v + 127) & ~(size_t)127); };
+    L.xs = al((size_t)std::max(kca, P.Cb) * 128 * M);
+    L.sa = (kca + P.LA - 1) / P.LA + 1;  // contributors per gate/up tile (upper bound)
+    L.pa = L.xs;
+    L.act = L.pa + al((size_t)P.T * L.sa * 2 * M * 16 * 4);
+    L.pb = L.act + al((size_t)M * P.T * 16 * 4);
+    L.ring = L.pb + al((size_t)kW * 2 * M * 16 * 4);
+    L.slot = std::max(2 * kW * kRA * rec, kW * kGemvRecsPerStepSingle * rec);
+    const long avail = (long)kBudget - L.ring - kBars - 1024;
+    L.depth = avail > 0 ? (int)std::min<long>(kDepthMax, avail / L.slot) : 0;
+    L.total = (size_t)L.ring + (size_t)L.depth * L.slot + kBars;
+    return L;
+}
+
+}  // namespace
+
+SplitPlan plan_split(int K, int I, int num_sms) {
+    SplitPlan P;
+    if (K % 16 || I % 16 || num_sms < 1) return P;
+    const int nta = I / 16, kca = (K + kChunkK - 1) / kChunkK, ntd = K / 16;
+    for (int T = 4; T <= nta; T += 4) {
+        if (nta % T) continue;
+        const int G = nta / T;
+        if (G > num_sms) continue;
+        // the smallest T with G <= SMs: the most CTAs; too few CTAs cannot
+        // pull the bandwidth (each SM's consumers decode ~1.4x the HBM rate)
+        if (4 * G < 3 * num_sms) return P;
+        if ((T * kca) % (16 * kRA) != 0) return P;  // gate/up: whole steps, no padding
+        if (ntd < 16 || T > 64) return P;
+        P.G = G;
+        P.T = T;
+        P.Cb = T / 4;
+        P.LA = T * kca / 16;
+        const int lb = (ntd * P.Cb + 15) / 16;
+        P.LB = (lb + kGemvRecsPerStepSingle - 1) / kGemvRecsPerStepSingle * kGemvRecsPerStepSingle;
+        return P;
+    }
+    return P;
+}
+
+bool split_fits(int fmt, int M, int K, const SplitPlan& P) {
+    if (!P.G || M < 1 || M > 16) return false;
+    return layout_for(fmt, M, K, P).depth >= 2;
+}
+
+size_t split_part_elems(int K, const SplitPlan& P) { return (size_t)P.G * 16 * K; }
+
+size_t split_codes_bytes(int fmt, const SplitPlan& P) {
+    return (size_t)P.G * kW * P.LB * (fmt == kNVFP4 ? kRecNVFP4 : kRecFP8);
+}
+
+cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t s) {
+    if (!split_fits(L.fmt, L.M, L.K, P)) return cudaErrorInvalidValue;
+    if (L.gate.TWr != P.G * kW || L.gate.Lr != P.LA || L.gate.Rr != kRA || L.up.TWr != P.G * kW)
+        return cudaErrorInvalidValue;
+    const Layout lay = layout_for(L.fmt, L.M, L.K, P);
+    if (P.T > 64) return cudaErrorInvalidValue;
+    Args a;
+    a.wa0 = L.gate.wc;
+    a.wa1 = L.up.wc;
+    a.chs0 = L.gate.chs;
+    a.chs1 = L.up.chs;
+    a.inv0 = L.gate.inv_g;
+    a.inv1 = L.up.inv_g;
+    a.wb = L.wdown;
+    a.chsd = L.chsd;
+    a.invd = L.invd;
+    a.x = static_cast<const __nv_bfloat16*>(L.x);
+    a.act_out = static_cast<__nv_bfloat16*>(L.act_out);
+    a.out = static_cast<__nv_bfloat16*>(L.out);
+    a.part = L.part;
+    a.ticket = L.ticket;
+    a.err = L.err;
+    a.M = L.M;
+    a.K = L.K;
+    a.I = L.I;
+    a.G = P.G;
+    a.T = P.T;
+    a.KcA = (L.K + kChunkK - 1) / kChunkK;
+    a.LA = P.LA;
+    a.Cb = P.Cb;
+    a.NtD = L.K / 16;
+    a.LB = P.LB;
+    a.xs_bytes = lay.xs;
+    a.pa_off = lay.pa;
+    a.act_off = lay.act;
+    a.pb_off = lay.pb;
+    a.ring_off = lay.ring;
+    a.slot_bytes = lay.slot;
+    a.depth = lay.depth;
+    a.SA = lay.sa;
+    const int nt = L.M <= 8 ? 1 : 2;
+    const bool m1 = L.M == 1;
+    if (L.fmt == kNVFP4) {
+        if (nt == 2) return launch_t<kNVFP4, 2, false>(a, lay.total, s);
+        return m1 ? launch_t<kNVFP4, 1, true>(a, lay.total, s) : launch_t<kNVFP4, 1, false>(a, lay.total, s);
+    }
+    if (nt == 2) return launch_t<kFP8, 2, false>(a, lay.total, s);
+    return m1 ? launch_t<kFP8, 1, true>(a, lay.total, s) : launch_t<kFP8, 1, false>(a, lay.total, s);
+}
+
+}  // namespace qmlp

@@ -534,8 +534,11 @@ cudaError_t launch_gemv_stream(int fmt, int M, const GemvStreamPhase& A, const G
     cudaError_t e = dispatch(fmt, nt, m1, mode, nullptr, smem, &blocks, true, s, 0);
     if (e != cudaSuccess) return e;
     if (blocks < 1) return cudaErrorInvalidConfiguration;
-    const int grid = num_sms;  // one CTA per SM: the rings fill its shared memory
-    if (A.p0.TWr != grid * kSWarps || (B && B->p0.TWr != grid * kSWarps)) return cudaErrorInvalidValue;
+    // one CTA per streaming-warp group of the layout (at most one per SM: the
+    // rings fill its shared memory, and the fused launch is cooperative)
+    const int grid = A.p0.TWr / kSWarps;
+    if (grid < 1 || grid > num_sms || A.p0.TWr != grid * kSWarps || (B && B->p0.TWr != grid * kSWarps))
+        return cudaErrorInvalidValue;
     StreamArgs a;
     fill_phase(a.A, A, grid * kSWarps, depth);
     size_t need = phase_part_elems(a.A, npa, nt);

@@ -92,6 +92,42 @@ constexpr int kGemvRecsPerStepSingle = 4;
 size_t gemv_part_elems(int K, int I, int num_sms);
 
 // ---------------------------------------------------------------------------
+// I-partitioned fused decode MLP (gemv_split.cu): CTA b of G owns gate/up
+// row tiles [T*b, T*(b+1)) and the matching Cb = T/4 down k-chunks.
+// ---------------------------------------------------------------------------
+struct SplitPlan {
+    int G = 0;        // CTAs (0: no plan for this shape / device)
+    int T = 0;        // gate/up row tiles per CTA
+    int Cb = 0;       // down 64-k chunks per CTA
+    int LA = 0;       // gate/up records per warp (= T*Kc/16; the gate/up layout uses Lr = LA, TWr = 16G)
+    int LB = 0;       // down records per warp in the CTA-sliced layout (multiple of 4)
+};
+SplitPlan plan_split(int K, int I, int num_sms);
+bool split_fits(int fmt, int M, int K, const SplitPlan& P);
+size_t split_part_elems(int K, const SplitPlan& P);       // fp32 partials for M <= 16
+size_t split_codes_bytes(int fmt, const SplitPlan& P);     // down records, CTA-sliced
+// Down projection [K, I] into the CTA-sliced layout: local record u = w*LB + k
+// of CTA b (u < Nt*Cb) is (row tile u / Cb, chunk Cb*b + u % Cb), stored at
+// ((k / 4) * 16G + 16b + w) * 4 + k % 4; records past Nt*Cb are zero.
+cudaError_t repack_nvfp4_split(const uint8_t* w, const uint8_t* scale, int N, int K, const SplitPlan& P,
+                               uint8_t* wc, cudaStream_t s);
+cudaError_t repack_fp8_split(const uint8_t* w, int N, int K, const SplitPlan& P, uint8_t* wc, cudaStream_t s);
+struct SplitLaunch {
+    int fmt = 0, M = 0, K = 0, I = 0;
+    GemvProj gate, up;               // GEMV layout with TWr = 16G, Lr = LA
+    const uint8_t* wdown = nullptr;  // CTA-sliced down records
+    const float* chsd = nullptr;     // FP8 down per-channel scales
+    float invd = 1.0f;               // NVFP4 down 1/global
+    const void* x = nullptr;         // bf16 [M, K]
+    void* act_out = nullptr;         // optional bf16 [M, I]
+    void* out = nullptr;             // bf16 [M, K]
+    float* part = nullptr;           // >= split_part_elems
+    unsigned long long* ticket = nullptr;  // grid-barrier ticket counter (zeroed at create)
+    int* err = nullptr;
+};
+cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // Tensor-core prefill GEMM (NVFP4, tcgen05)
 // ---------------------------------------------------------------------------
 struct GemmProj {
