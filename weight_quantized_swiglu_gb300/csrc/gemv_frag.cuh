@@ -196,8 +196,14 @@ QMLP_DEV float absmax8(const uint4& v) {
     return mx;
 }
 
+// 16 bytes of x: from global memory (L2, no L1 allocation) or, when x was
+// first copied into shared memory, a plain load.
+QMLP_DEV uint4 ld_x16(const __nv_bfloat16* p, bool smem_src) {
+    return smem_src ? *reinterpret_cast<const uint4*>(p) : __ldcg(reinterpret_cast<const uint4*>(p));
+}
+
 QMLP_DEV void stage_x(const __nv_bfloat16* x, int M, int ld, int kb, int ke, int kpe, uint4* xs, int* s_maxbits,
-                      int* s_sig, int nth = -1) {
+                      int* s_sig, int nth = -1, bool smem_src = false) {
     if (nth < 0) nth = blockDim.x;
     const int tid = threadIdx.x;
     const int slots = 4 * M;
@@ -214,7 +220,7 @@ QMLP_DEV void stage_x(const __nv_bfloat16* x, int M, int ld, int kb, int ke, int
         v[i] = make_uint4(0, 0, 0, 0);
         if (in_regs && it < total) {
             const int m = it / real8, q = it - m * real8;
-            v[i] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)m * ld + kb + q * 8));
+            v[i] = ld_x16(x + (size_t)m * ld + kb + q * 8, smem_src);
         }
     }
     stage_sync(nth);
@@ -230,7 +236,7 @@ QMLP_DEV void stage_x(const __nv_bfloat16* x, int M, int ld, int kb, int ke, int
             }
         } else {
             for (int q = tid; q < real8; q += nth)
-                mx = fmaxf(mx, absmax8(__ldcg(reinterpret_cast<const uint4*>(x + (size_t)m * ld + kb + q * 8))));
+                mx = fmaxf(mx, absmax8(ld_x16(x + (size_t)m * ld + kb + q * 8, smem_src)));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -258,7 +264,7 @@ QMLP_DEV void stage_x(const __nv_bfloat16* x, int M, int ld, int kb, int ke, int
         for (int it = tid; it < M * pad8; it += nth) {
             const int m = it / pad8, q = it - m * pad8;
             uint4 w = make_uint4(0, 0, 0, 0);
-            if (q < real8) w = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)m * ld + kb + q * 8));
+            if (q < real8) w = ld_x16(x + (size_t)m * ld + kb + q * 8, smem_src);
             stage_store8(xs, slots, m, q * 8, s_sig[m], w);
         }
     }

@@ -40,7 +40,7 @@ constexpr int kCT = kW * 32;          // consumer threads
 constexpr int kThr = kCT + 32;        // + one producer warp
 constexpr int kDepthMax = 16;
 constexpr int kBudget = 220 * 1024;
-constexpr int kBars = 2 * kDepthMax * 8;
+constexpr int kBars = 2 * kDepthMax * 8 + 16;  // full, empty, x
 constexpr int kRA = kGemvRecsPerStepPair;  // gate/up records per warp per step
 constexpr uint64_t kLimit = 2000000000ull;  // 2 s
 
@@ -67,41 +67,57 @@ struct Args {
     int pa_off, act_off, pb_off;  // byte offsets of the combine / act regions
     int ring_off, slot_bytes, depth;
     int SA;                    // partial slots per gate/up tile
+    int xraw_off, xraw_bytes;  // raw bf16 x copied to shared memory (0: staged from global)
 };
 
 struct Ring {
     uint8_t* base;
     uint32_t base_s, full0, empty0;
+    uint32_t xbar;  // completion of the x copy
     int slot_bytes, depth;
 };
 
-// Producer: steps [0, steps) of one phase; step j of CTA b is the 16 warps'
-// records R*j..R*j+R-1, contiguous in the interleaved layout.
-template <int FMT, int NP>
-QMLP_DEV int produce(const uint8_t* w0, const uint8_t* w1, int R, int steps, int TW, const Ring& r, int q,
-                     int* err) {
-    constexpr uint32_t rec = rec_bytes<FMT>();
-    const uint32_t step_bytes = kW * R * rec;
-    const size_t stride = (size_t)TW * R * rec;
-    const uint8_t* s0 = w0 + (size_t)blockIdx.x * kW * R * rec;
-    const uint8_t* s1 = NP == 2 ? w1 + (size_t)blockIdx.x * kW * R * rec : nullptr;
-    int slot = q % r.depth, round = q / r.depth;
-    for (int j = 0; j < steps; ++j, ++q) {
+// The producer's view of the two phases: step q < steps_a is the gate and up
+// blocks of gate/up step q, later steps are down blocks. Step j of CTA b is
+// the 16 warps' records R*j..R*j+R-1, contiguous in the interleaved layout.
+struct Steps {
+    const uint8_t* a0;
+    const uint8_t* a1;
+    const uint8_t* b;
+    size_t stride_a, stride_b;
+    uint32_t bytes_a, bytes_b;  // per block
+    int steps_a, steps;
+};
+
+// Producer (one thread): every step of both phases into the ring, without a
+// pause between the phases (the down weights do not depend on act). Returns
+// the number of steps issued, or -(issued + 1) after an expired wait.
+// (Measured: L2 prefetches of later steps, of both phases or of the down
+// steps only, slow the call down by 2-8 us; the bulk copies alone are kept.)
+template <int FMT>
+QMLP_DEV int produce(const Steps& st, const Ring& r, int* err) {
+    int slot = 0, round = 0;
+    for (int q = 0; q < st.steps; ++q) {
         if (round > 0 && !mbar_wait_bounded(r.empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kLimit)) {
             atomicExch(err, 24);
             return -(q + 1);
         }
         const uint32_t full = r.full0 + 8u * slot;
         const uint32_t dst = r.base_s + (uint32_t)slot * r.slot_bytes;
-        mbar_arrive_expect_tx(full, NP * step_bytes);
-        bulk_g2s(dst, s0 + (size_t)j * stride, step_bytes, full);
-        if (NP == 2) bulk_g2s(dst + step_bytes, s1 + (size_t)j * stride, step_bytes, full);
+        if (q < st.steps_a) {
+            mbar_arrive_expect_tx(full, 2 * st.bytes_a);
+            bulk_g2s(dst, st.a0 + (size_t)q * st.stride_a, st.bytes_a, full);
+            bulk_g2s(dst + st.bytes_a, st.a1 + (size_t)q * st.stride_a, st.bytes_a, full);
+        } else {
+            mbar_arrive_expect_tx(full, st.bytes_b);
+            bulk_g2s(dst, st.b + (size_t)(q - st.steps_a) * st.stride_b, st.bytes_b, full);
+        }
         if (++slot == r.depth) {
             slot = 0;
             ++round;
         }
     }
-    return q;
+    return st.steps;
 }
 
 // Fragment element (p, n, e) of lane (g, t): token m = 8n + 2t + (e & 1),
@@ -200,6 +216,55 @@ QMLP_DEV void store_part_b(const Args& a, int M, int rt, const float (&v)[1][NT]
 }
 
 template <int NT, int NP>
+QMLP_DEV void zero_acc(float (&acc)[NP][NT][4]);
+
+// Phase B when the CTA's slice is CB = 1, 2 or 4 down chunks: every warp's
+// range starts on a row-tile boundary (LB is a multiple of 4), a step's 4
+// records are 4/CB whole tiles, and the CB activation fragments are the same
+// for every record, so they are loaded once and stay in registers. Records
+// past the CTA's real ones are zero and their tiles are not stored.
+template <int FMT, int NT, bool M1, int CB>
+QMLP_DEV bool phase_b_fixed(const Args& a, const Ring& r, int q, int steps, const uint4* xs, const int* s_sigb,
+                            int M, int warp) {
+    constexpr int rec = rec_bytes<FMT>();
+    constexpr int R = kGemvRecsPerStepSingle;
+    static_assert(R % CB == 0, "whole tiles per step");
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    uint4 xb[CB][NT][2];
+#pragma unroll
+    for (int c = 0; c < CB; ++c) load_xfrag<NT>(xs, c, M, 4 * M, g, t, xb[c]);
+    int rt = warp * a.LB / CB;
+    int slot = q % r.depth;
+    uint32_t parity = (uint32_t)((q / r.depth) & 1);
+    for (int j = 0; j < steps; ++j) {
+        if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, kLimit)) {
+            if (lane == 0) atomicExch(a.err, 22);
+            return false;
+        }
+        const uint8_t* sb = r.base + (uint32_t)slot * (uint32_t)r.slot_bytes + (uint32_t)warp * R * rec;
+#pragma unroll
+        for (int tt = 0; tt < R / CB; ++tt, ++rt) {
+            float acc[1][NT][4];
+            zero_acc<NT, 1>(acc);
+#pragma unroll
+            for (int c = 0; c < CB; ++c) {
+                ChunkW w[1];
+                w[0] = lds_chunk<FMT>(sb + (tt * CB + c) * rec, lane);
+                mma_chunk<FMT, NT, 1, M1>(w, xb[c], acc);
+            }
+            if (rt < a.NtD) store_part_b<NT>(a, M, rt, acc, s_sigb);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(r.empty0 + 8u * slot);
+        if (++slot == r.depth) {
+            slot = 0;
+            parity ^= 1u;
+        }
+    }
+    return true;
+}
+
+template <int NT, int NP>
 QMLP_DEV void zero_acc(float (&acc)[NP][NT][4]) {
 #pragma unroll
     for (int p = 0; p < NP; ++p)
@@ -235,12 +300,14 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     r.depth = a.depth;
     r.full0 = smem_u32(r.base + (size_t)a.depth * a.slot_bytes);
     r.empty0 = r.full0 + 8u * kDepthMax;
+    r.xbar = r.empty0 + 8u * kDepthMax;
     const int stepsA = a.LA / kRA, stepsB = a.LB / kGemvRecsPerStepSingle;
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.depth; ++i) {
             mbar_init(r.full0 + 8u * i, 1);
             mbar_init(r.empty0 + 8u * i, kW);
         }
+        mbar_init(r.xbar, 1);
         fence_mbar_init();
         s_fail = 0;
     }
@@ -250,8 +317,24 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
 
     if (warp == kW) {
         if (lane == 0) {
-            int q = produce<FMT, 2>(a.wa0, a.wa1, kRA, stepsA, a.G * kW, r, 0, a.err);
-            if (q >= 0) q = produce<FMT, 1>(a.wb, nullptr, kGemvRecsPerStepSingle, stepsB, a.G * kW, r, q, a.err);
+            // x first (when it fits the raw buffer), then the weights
+            if (a.xraw_bytes) {
+                mbar_arrive_expect_tx(r.xbar, a.xraw_bytes);
+                bulk_g2s(smem_u32(smem + a.xraw_off), a.x, a.xraw_bytes, r.xbar);
+            }
+            Steps st;
+            const uint32_t rec = rec_bytes<FMT>();
+            st.bytes_a = kW * kRA * rec;
+            st.bytes_b = kW * kGemvRecsPerStepSingle * rec;
+            st.stride_a = (size_t)a.G * st.bytes_a;
+            st.stride_b = (size_t)a.G * st.bytes_b;
+            st.a0 = a.wa0 + (size_t)blockIdx.x * st.bytes_a;
+            st.a1 = a.wa1 + (size_t)blockIdx.x * st.bytes_a;
+            st.b = a.wb + (size_t)blockIdx.x * st.bytes_b;
+            st.steps_a = stepsA;
+            st.steps = stepsA + stepsB;
+            int q = produce<FMT>(st, r, a.err);
+            if (a.xraw_bytes) mbar_wait_bounded(r.xbar, 0, kLimit);  // the x copy is never left in flight
             if (q < 0) {
                 const int issued = -q - 1;
                 for (int qq = issued - 1; qq >= 0 && qq >= issued - a.depth; --qq)
@@ -270,7 +353,18 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     bool ok = true;
 
     // ---------------- phase A: gate/up over this CTA's tiles ----------------
-    stage_x(a.x, M, a.K, 0, a.K, a.KcA * kChunkK, xs, s_maxbits, s_sig, kCT);
+    if (a.xraw_bytes) {
+        if (!mbar_wait_bounded(r.xbar, 0, kLimit)) {
+            if (lane == 0) atomicExch(a.err, 25);
+            ok = false;
+        }
+        // (after a failed wait x reads as whatever is there; the error word
+        // reports the call)
+        stage_x(reinterpret_cast<const __nv_bfloat16*>(smem + a.xraw_off), M, a.K, 0, a.K, a.KcA * kChunkK, xs,
+                s_maxbits, s_sig, kCT, true);
+    } else {
+        stage_x(a.x, M, a.K, 0, a.K, a.KcA * kChunkK, xs, s_maxbits, s_sig, kCT);
+    }
     int q = 0;
     {
         const int slots = 4 * M;
@@ -356,7 +450,11 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     }
 
     // ---------------- phase B: down over this CTA's act slice ----------------
-    if (s_fail == 0) {
+    if (s_fail == 0 && (a.Cb == 1 || a.Cb == 2 || a.Cb == 4)) {
+        ok = a.Cb == 1   ? phase_b_fixed<FMT, NT, M1, 1>(a, r, q, stepsB, xs, s_sigb, M, warp)
+             : a.Cb == 2 ? phase_b_fixed<FMT, NT, M1, 2>(a, r, q, stepsB, xs, s_sigb, M, warp)
+                         : phase_b_fixed<FMT, NT, M1, 4>(a, r, q, stepsB, xs, s_sigb, M, warp);
+    } else if (s_fail == 0) {
         const int slots = 4 * M;
         const int pb_floats = M * 16;
         float acc[1][NT][4];
@@ -482,9 +580,10 @@ cudaError_t launch_t(const Args& a, size_t smem, cudaStream_t s) {
 }
 
 struct Layout {
-    int xs, pa, act, pb, ring, slot, depth, sa;
+    int xs, pa, act, pb, xraw, xraw_bytes, ring, slot, depth, sa;
     size_t total;
 };
+constexpr int kXRawMax = 16 * 1024;  // raw x copied to shared memory up to this size
 
 Layout layout_for(int fmt, int M, int K, const SplitPlan& P) {
     Layout L;
@@ -496,7 +595,9 @@ Layout layout_for(int fmt, int M, int K, const SplitPlan& P) {
     L.pa = L.xs;
     L.act = L.pa + al((size_t)P.T * L.sa * 2 * M * 16 * 4);
     L.pb = L.act + al((size_t)M * P.T * 16 * 4);
-    L.ring = L.pb + al((size_t)kW * 2 * M * 16 * 4);
+    L.xraw = L.pb + al((size_t)kW * 2 * M * 16 * 4);
+    L.xraw_bytes = (size_t)M * K * 2 <= (size_t)kXRawMax ? M * K * 2 : 0;
+    L.ring = L.xraw + al((size_t)L.xraw_bytes);
     L.slot = std::max(2 * kW * kRA * rec, kW * kGemvRecsPerStepSingle * rec);
     const long avail = (long)kBudget - L.ring - kBars - 1024;
     L.depth = avail > 0 ? (int)std::min<long>(kDepthMax, avail / L.slot) : 0;
@@ -581,6 +682,8 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
     a.slot_bytes = lay.slot;
     a.depth = lay.depth;
     a.SA = lay.sa;
+    a.xraw_off = lay.xraw;
+    a.xraw_bytes = lay.xraw_bytes;
     const int nt = L.M <= 8 ? 1 : 2;
     const bool m1 = L.M == 1;
     if (L.fmt == kNVFP4) {
