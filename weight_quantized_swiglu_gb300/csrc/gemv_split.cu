@@ -120,6 +120,12 @@ QMLP_DEV int produce(const Steps& st, const Ring& r, int* err) {
     return st.steps;
 }
 
+// 2^-s as a float (exact for every exponent the prescale produces); the
+// product v * 2^-s is the correctly rounded v scaled by 2^-s, as scalbnf.
+QMLP_DEV float pow2_neg(int s) {
+    return (s >= -126 && s <= 126) ? __int_as_float((127 - s) << 23) : scalbnf(1.0f, -s);
+}
+
 // Fragment element (p, n, e) of lane (g, t): token m = 8n + 2t + (e & 1),
 // row g + 8*(e >> 1). Compact partial layout: [p][m][16 rows] fp32.
 template <int NT, int NP>
@@ -193,12 +199,34 @@ QMLP_DEV void epilogue_a(const Args& a, int M, int lt, const float (&v)[2][NT][4
             const int i = blockIdx.x * tslice + r;     // intermediate index
             const float s0 = FMT == kNVFP4 ? a.inv0 : a.chs0[i];
             const float s1 = FMT == kNVFP4 ? a.inv1 : a.chs1[i];
-            const float gv = scalbnf(v[0][n][e], -s_sig[m]) * s0;
-            const float uv = scalbnf(v[1][n][e], -s_sig[m]) * s1;
+            const float pw = pow2_neg(s_sig[m]);
+            const float gv = v[0][n][e] * pw * s0;
+            const float uv = v[1][n][e] * pw * s1;
             const __nv_bfloat16 act = __float2bfloat16_rn(silu_f32(gv) * uv);
             s_act[m * tslice + r] = __bfloat162float(act);
             if (a.act_out) a.act_out[(size_t)m * a.I + i] = act;
         }
+}
+
+// End of this warp's part of gate/up tile lt: the epilogue when the warp
+// covered the whole tile, else the shared-memory combine (the last
+// contributor applies the epilogue). Out of line: it runs once per tile
+// part, and keeping it out of the streaming loop keeps that loop small.
+template <int NT>
+struct AccA {
+    float v[2][NT][4];
+};
+template <int FMT, int NT>
+__device__ __noinline__ void finish_tile_a(const Args& a, int M, int lt, bool whole, int warp, AccA<NT> acc,
+                                           float* s_pa, int pa_floats, int* s_cnta, const int* s_sig, float* s_act) {
+    if (whole) {
+        epilogue_a<FMT, NT>(a, M, lt, acc.v, s_sig, s_act);
+        return;
+    }
+    const int w0 = (lt * a.KcA) / a.LA, w1 = ((lt + 1) * a.KcA - 1) / a.LA;
+    if (combine_smem<NT, 2>(s_pa + (size_t)lt * a.SA * pa_floats, pa_floats, warp - w0, w1 - w0 + 1, &s_cnta[lt], M,
+                            acc.v))
+        epilogue_a<FMT, NT>(a, M, lt, acc.v, s_sig, s_act);
 }
 
 // Phase-B result of down row tile rt over this CTA's slice -> global partial.
@@ -211,7 +239,7 @@ QMLP_DEV void store_part_b(const Args& a, int M, int rt, const float (&v)[1][NT]
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int m = n * 8 + 2 * t + (e & 1);
-            if (m < M) dst[(size_t)m * a.K + rt * 16 + g + 8 * (e >> 1)] = scalbnf(v[0][n][e], -s_sigb[m]);
+            if (m < M) dst[(size_t)m * a.K + rt * 16 + g + 8 * (e >> 1)] = v[0][n][e] * pow2_neg(s_sigb[m]);
         }
 }
 
@@ -292,7 +320,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     __shared__ int s_fail;
     __shared__ int s_pass;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int M = a.M;
+    const int M = M1 ? 1 : a.M;  // a compile-time constant in the one-token kernel
     Ring r;
     r.base = smem + a.ring_off;
     r.base_s = smem_u32(r.base);
@@ -392,14 +420,15 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                 load_xfrag<NT>(xs, c, M, slots, g, t, xb);
                 mma_chunk<FMT, NT, 2, M1>(w, xb, acc);
                 if (++c == a.KcA || k == a.LA - 1) {
-                    if (cs == 0 && c == a.KcA) {
-                        epilogue_a<FMT, NT>(a, M, lt, acc, s_sig, s_act);
-                    } else {
-                        const int w0 = (lt * a.KcA) / a.LA, w1 = ((lt + 1) * a.KcA - 1) / a.LA;
-                        if (combine_smem<NT, 2>(s_pa + (size_t)lt * a.SA * pa_floats, pa_floats, warp - w0,
-                                                w1 - w0 + 1, &s_cnta[lt], M, acc))
-                            epilogue_a<FMT, NT>(a, M, lt, acc, s_sig, s_act);
-                    }
+                    AccA<NT> av;
+#pragma unroll
+                    for (int p = 0; p < 2; ++p)
+#pragma unroll
+                        for (int n = 0; n < NT; ++n)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) av.v[p][n][e] = acc[p][n][e];
+                    finish_tile_a<FMT, NT>(a, M, lt, cs == 0 && c == a.KcA, warp, av, s_pa, pa_floats, s_cnta, s_sig,
+                                           s_act);
                     zero_acc<NT, 2>(acc);
                     ++lt;
                     c = 0;
