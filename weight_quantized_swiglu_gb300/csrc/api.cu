@@ -359,8 +359,13 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
         return QMLP_OK;
     }
     const size_t Ntg = (size_t)(h->I / kTileRows);
-    for (int m0 = 0; m0 < M; m0 += kMaxGemvM) {
-        const int mb = std::min(kMaxGemvM, M - m0);
+    // the whole MLP in token blocks: up to 8 tokens per launch of the
+    // I-partitioned kernel when the shape has a partition (its shared-memory
+    // staging of x grows with M), else 16 per stream-K / split-K pass
+    const bool split = stages == 3 && h->sp.G && split_fits(h->fmt, 1, h->K, h->sp);
+    const int block = split ? kMaxSplitM : kMaxGemvM;
+    for (int m0 = 0; m0 < M; m0 += block) {
+        const int mb = std::min(block, M - m0);
         const void* xb = static_cast<const uint8_t*>(x) + (size_t)m0 * h->K * 2;
         void* ab = static_cast<uint8_t*>(h->act) + (size_t)m0 * h->I * 2;
         void* ob = static_cast<uint8_t*>(out) + (size_t)m0 * h->K * 2;
@@ -380,7 +385,7 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
                    fitB = gemv_stream_fits(h->fmt, mb, h->I, 1, h->gv[2].Rr);
         const bool fitAB = gemv_stream_fits(h->fmt, mb, std::max(h->K, h->I), 2, h->gv[0].Rr) &&
                            gemv_stream_fits(h->fmt, mb, std::max(h->K, h->I), 1, h->gv[2].Rr);
-        if (stages == 3 && h->sp.G && mb <= kMaxSplitM && split_fits(h->fmt, mb, h->K, h->sp)) {
+        if (split && split_fits(h->fmt, mb, h->K, h->sp)) {
             SplitLaunch S;
             S.fmt = h->fmt;
             S.M = mb;

@@ -15,43 +15,39 @@
 //   Invalid ids (< 0 or >= E) contribute zero; duplicate ids are separate
 //   routes with their own router weights.
 //
-// GB300 shape of the work: 10 routes x (320 x 2560 + 2560 x 160) weights,
-// about 6 MB per call, so the step is latency-bound rather than bandwidth-
-// bound. W13 runs one CTA per (route, 8 intermediate columns) with a warp
-// per column computing gate and up together (so SiLU(g)*u is formed in the
-// warp), W2 one CTA per 16 output rows looping over the routes. Each lane
-// streams 8 consecutive k (4 code bytes) per step with coalesced warp
-// accesses; products are exact in fp32 (fp16 weight x fp16/bf16 x) and
-// every reduction has a fixed order.
+// GB300 design. 10 routes x (320 x 2560 + 2560 x 160) weights, ~7.7 MB per
+// call: a latency problem. The dot products run on the tensor cores
+// (mma.sync m16n8k16, fp16 x fp16 -> fp32, the token in column 0), so a
+// weight costs ~2 instructions of decode instead of a scalar half_fma,
+// conversion and fp32 FMA each, and the work spreads over thousands of
+// warps:
+//  * A fragments straight from the checkpoint layout: lane (g, t) of a
+//    16-row tile needs byte t of every 32-bit word of rows g and g+8 (the k
+//    pairs 2t..2t+1 and 8+2t..9+2t of each k16 group). One PRMT copies that
+//    byte into both halves of a register, one LOP3 turns it into the fp16
+//    pair (1024 + q_lo, 1024 + 16 q_hi), one exact HFMA2 recovers (q_lo,
+//    q_hi) and one HFMA2 forms half_fma(q, s, b) for both -- the same
+//    single rounding as the scalar definition.
+//  * B fragment = the token: x as fp16 (fp16 input as is; bf16 input times a
+//    power of two per call, exact for every value within 2^29 of max|x|),
+//    the intermediate act as fp16 (exact).
+//  * W13: a CTA per (route, 16-row gate/up tile pair); each warp takes one
+//    of the two tiles over a tenth of K, and the partial sums are added in a
+//    fixed order in shared memory.
+//  * W2: a CTA per 16 output rows with one warp per route; the fp16 route
+//    results are added in router order by one thread per output row.
+//  * Programmatic dependent launch: the W2 grid starts while W13 runs, reads
+//    the ids and loads its codes and metadata into registers, and only then
+//    waits (griddepcontrol.wait) for the intermediate.
 #include "common.cuh"
 #include "internal.h"
 
 namespace qmlp {
 namespace {
 
-constexpr int kW13Cols = 8;           // intermediate columns per W13 CTA (one warp each)
-constexpr int kW2Rows = 16;           // output rows per W2 CTA
-constexpr int kW2Threads = 256;
-
-// Decode the 8 weights of code word `w` (nibble i = k offset i, low nibble
-// first) of one group record into fp32.
-template <int MB>
-QMLP_DEV void awq_decode8(uint32_t w, const uint8_t* rec, float (&out)[8]) {
-    const __half s = __ushort_as_half((unsigned short)(rec[0] | (rec[1] << 8)));
-    __half b;
-    if (MB == 4) {
-        b = __ushort_as_half((unsigned short)(rec[2] | (rec[3] << 8)));
-    } else {
-        // half(-zero * scale): the product of a 4-bit integer and an fp16 is
-        // exact in fp32, so one rounding to fp16 matches half arithmetic.
-        b = __float2half_rn(-(float)rec[2] * __half2float(s));
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const __half q = __ushort2half_rn((unsigned short)((w >> (4 * i)) & 0xF));
-        out[i] = __half2float(__hfma(q, s, b));
-    }
-}
+constexpr int kK13 = 10;  // W13 K splits: a CTA has 2 x kK13 warps (gate and up tiles)
+constexpr int kC13 = 2;   // 64-k chunks a W13 warp loads at once
+constexpr int kG2 = 10;   // k16 groups a W2 warp loads at once
 
 struct Args {
     int E, K, I;
@@ -61,6 +57,7 @@ struct Args {
     const uint8_t* w2_meta;
     const void* x;
     int x_is_bf16;
+    int meta_al4;  // 4-byte records are 4-byte aligned (one load each)
     const int32_t* ids;
     const float* rw;
     int topk;
@@ -71,134 +68,310 @@ struct Args {
     __half* y_dbg;
 };
 
-QMLP_DEV float warp_sum(float v) {
+// Programmatic dependent launch: let the next kernel of the stream start /
+// wait until the previous kernel's memory is visible.
+QMLP_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+QMLP_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// One metadata record (little-endian fp16 scale, then fp16 bias or u8 zero)
+// as its raw bytes, low byte first.
+template <int MB>
+QMLP_DEV uint32_t load_meta(const uint8_t* p, bool al4) {
+    if (MB == 4 && al4) return __ldg(reinterpret_cast<const unsigned int*>(p));
+    uint32_t v = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int i = 0; i < MB; ++i) v |= (uint32_t)__ldg(p + i) << (8 * i);
     return v;
 }
 
-// Dot product of the staged fp32 vector xs[0:Kr) with row `row` of expert e
-// of a [E, N, Kr] bank, reduced over the warp (every lane gets the sum).
+// {scale, scale} and {bias, bias} of a record as f16x2: the bias is stored
+// (4-byte) or half(-zero*scale) -- the product of a 4-bit integer and an fp16
+// is exact in fp32, so one rounding to fp16 matches half arithmetic.
 template <int MB>
-QMLP_DEV float awq_row_dot(const uint8_t* __restrict__ w, const uint8_t* __restrict__ meta, int N, int Kr,
-                           int e, int row, const float* xs, int lane) {
-    const size_t rbase = (size_t)e * N + row;
-    const uint8_t* wr = w + rbase * (Kr / 2);
-    const uint8_t* mr = meta + rbase * (Kr / 32) * MB;
-    float acc = 0.0f;
-    for (int k0 = lane * 8; k0 < Kr; k0 += 256) {
-        const uint32_t code = __ldg(reinterpret_cast<const uint32_t*>(wr + k0 / 2));
-        float wv[8];
-        awq_decode8<MB>(code, mr + (size_t)(k0 / 32) * MB, wv);
-        const float4 xa = *reinterpret_cast<const float4*>(xs + k0);
-        const float4 xb = *reinterpret_cast<const float4*>(xs + k0 + 4);
-        acc = fmaf(xa.x, wv[0], acc);
-        acc = fmaf(xa.y, wv[1], acc);
-        acc = fmaf(xa.z, wv[2], acc);
-        acc = fmaf(xa.w, wv[3], acc);
-        acc = fmaf(xb.x, wv[4], acc);
-        acc = fmaf(xb.y, wv[5], acc);
-        acc = fmaf(xb.z, wv[6], acc);
-        acc = fmaf(xb.w, wv[7], acc);
+QMLP_DEV void meta_sb2(uint32_t m, uint32_t& s2, uint32_t& b2) {
+    const uint32_t s = m & 0xFFFFu;
+    uint32_t b;
+    if (MB == 4) {
+        b = m >> 16;
+    } else {
+        const float bf = -(float)((m >> 16) & 0xFFu) * __half2float(__ushort_as_half((unsigned short)s));
+        b = __half_as_ushort(__float2half_rn(bf));
     }
-    return warp_sum(acc);
+    s2 = s | (s << 16);
+    b2 = b | (b << 16);
 }
 
+QMLP_DEV uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// The byte of word w that `sel` (pair_selector) picks -- two u4 codes, the
+// low nibble the earlier k -- to f16x2 {half_fma(q_lo, s, b), half_fma(q_hi, s, b)}.
+QMLP_DEV uint32_t awq_pair(uint32_t w, uint32_t sel, uint32_t s2, uint32_t b2) {
+    const uint32_t m = __byte_perm(w, 0u, sel);                // [b, 0, b, 0]
+    const uint32_t h = (m & 0x00F0000Fu) | 0x64006400u;        // {1024 + q_lo, 1024 + 16 q_hi}
+    const uint32_t q = hfma2_u32(h, 0x2C003C00u, 0xD400E400u);  // {q_lo, q_hi} = h * {1, 1/16} - {1024, 64}
+    return hfma2_u32(q, s2, b2);
+}
+
+// PRMT selector placing byte t of a word in bytes 0 and 2 (bytes 1, 3 zero).
+QMLP_DEV uint32_t pair_selector(int t) {
+    return (uint32_t)t | (4u << 4) | ((uint32_t)t << 8) | (4u << 12);
+}
+
+// ---------------------------------------------------------------------------
+// W13 + SwiGLU
+// ---------------------------------------------------------------------------
 template <int MB>
-__global__ void __launch_bounds__(kW13Cols * 32) moe_w13_kernel(const Args a) {
-    extern __shared__ __align__(16) float xs[];  // [K]
+__global__ void __launch_bounds__(2 * kK13 * 32) moe_w13_kernel(const Args a) {
+    extern __shared__ __align__(16) uint32_t x16[];  // [K/2] fp16 pairs
+    __shared__ float part[2 * kK13][16];            // [warp][row of its tile]
+    __shared__ int s_max;
+    // the ids, x and (through the intermediate) the previous call's W2
+    // stage belong to the kernels before this one
+    pdl_wait();
+    pdl_launch_dependents();
     const int r = blockIdx.y;
     const int id = a.ids[r];
     if (id < 0 || id >= a.E) return;
-    for (int k = threadIdx.x; k < a.K; k += blockDim.x) {
-        const unsigned short b = reinterpret_cast<const unsigned short*>(a.x)[k];
-        xs[k] = a.x_is_bf16 ? __bfloat162float(__ushort_as_bfloat16(b)) : __half2float(__ushort_as_half(b));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    // warp = (tile, K split): tile 0 = gate rows 16*bx.., tile 1 = up rows I + 16*bx..
+    const int tile = warp / kK13, ks = warp % kK13;
+    const int Kc = a.K / 64, gpr = a.K / 32, N = 2 * a.I;
+    const int cpw = (Kc + kK13 - 1) / kK13;  // chunks per warp
+    const int c0 = ks * cpw, c1 = min(Kc, c0 + cpw);
+    const bool al4 = a.meta_al4 != 0;
+    const size_t row0 = (size_t)id * N + tile * a.I + 16 * blockIdx.x + g;
+    const size_t rows[2] = {row0, row0 + 8};
+    uint4 cw[kC13][2][2];  // two 16-byte halves of each row's 32-byte chunk
+    uint32_t mw[kC13][2][2];
+    auto load_batch = [&](int cb) {
+#pragma unroll
+        for (int i = 0; i < kC13; ++i) {
+            const int c = cb + i;
+            if (c < c1) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint4* src = reinterpret_cast<const uint4*>(a.w13 + rows[q] * (a.K / 2) + c * 32);
+                    cw[i][q][0] = __ldg(src);
+                    cw[i][q][1] = __ldg(src + 1);
+                    const uint8_t* m = a.w13_meta + (rows[q] * gpr + 2 * c) * MB;
+                    mw[i][q][0] = load_meta<MB>(m, al4);
+                    mw[i][q][1] = load_meta<MB>(m + MB, al4);
+                }
+            }
+        }
+    };
+    load_batch(c0);  // issued before x is staged: the two round trips overlap
+
+    // x -> fp16 pairs (bf16: times 2^sig so that max|x| lies in [2^14, 2^15))
+    const unsigned short* xin = reinterpret_cast<const unsigned short*>(a.x);
+    if (threadIdx.x == 0) s_max = 0;
+    __syncthreads();
+    if (a.x_is_bf16) {
+        float mx = 0.0f;
+        for (int k = threadIdx.x; k < a.K; k += blockDim.x)
+            mx = fmaxf(mx, fabsf(__bfloat162float(__ushort_as_bfloat16(xin[k]))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0 && mx > 0.0f) atomicMax(&s_max, __float_as_int(mx));
+        __syncthreads();
+    }
+    const int sig = a.x_is_bf16 ? prescale_exponent(__int_as_float(s_max)) : 0;
+    for (int k2 = threadIdx.x; k2 < a.K / 2; k2 += blockDim.x) {
+        const uint32_t v = reinterpret_cast<const uint32_t*>(xin)[k2];
+        if (a.x_is_bf16) {
+            const float lo = scalbnf(__uint_as_float(v << 16), sig);
+            const float hi = scalbnf(__uint_as_float(v & 0xFFFF0000u), sig);
+            const __half2 h = __floats2half2_rn(lo, hi);
+            x16[k2] = *reinterpret_cast<const uint32_t*>(&h);
+        } else {
+            x16[k2] = v;
+        }
     }
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q = blockIdx.x * kW13Cols + warp;
-    if (q >= a.I) return;
-    const int N13 = 2 * a.I;
-    const float hg = awq_row_dot<MB>(a.w13, a.w13_meta, N13, a.K, id, q, xs, lane);
-    const float hu = awq_row_dot<MB>(a.w13, a.w13_meta, N13, a.K, id, a.I + q, xs, lane);
-    if (lane == 0) {
-        const __half g = __float2half_rn(hg), u = __float2half_rn(hu);
-        const __half act = __float2half_rn(silu_f32(__half2float(g)) * __half2float(u));
+
+    const uint32_t sel = pair_selector(t);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int cb = c0; cb < c1; cb += kC13) {
+        if (cb != c0) load_batch(cb);
+#pragma unroll
+        for (int i = 0; i < kC13; ++i) {
+            const int c = cb + i;
+            if (c < c1) {
+                uint32_t s2[2][2], b2[2][2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    meta_sb2<MB>(mw[i][q][0], s2[q][0], b2[q][0]);
+                    meta_sb2<MB>(mw[i][q][1], s2[q][1], b2[q][1]);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {  // k16 group j: AWQ group j/2, words 2j, 2j+1 of the chunk
+                    const int h = j >> 1;
+                    const uint32_t wa0 = (j & 1) ? cw[i][0][h].z : cw[i][0][h].x;
+                    const uint32_t wb0 = (j & 1) ? cw[i][0][h].w : cw[i][0][h].y;
+                    const uint32_t wa1 = (j & 1) ? cw[i][1][h].z : cw[i][1][h].x;
+                    const uint32_t wb1 = (j & 1) ? cw[i][1][h].w : cw[i][1][h].y;
+                    uint32_t x0 = 0, x1 = 0;
+                    if (g == 0) {
+                        const int k2 = (c * 64 + 16 * j) / 2 + t;
+                        x0 = x16[k2];
+                        x1 = x16[k2 + 4];
+                    }
+                    mma_f16_16816(d, awq_pair(wa0, sel, s2[0][h], b2[0][h]), awq_pair(wa1, sel, s2[1][h], b2[1][h]),
+                                  awq_pair(wb0, sel, s2[0][h], b2[0][h]), awq_pair(wb1, sel, s2[1][h], b2[1][h]), x0,
+                                  x1);
+                }
+            }
+        }
+    }
+    // the token is column 0: lanes t == 0 hold rows g (d[0]) and g+8 (d[2])
+    if (t == 0) {
+        part[warp][g] = d[0];
+        part[warp][g + 8] = d[2];
+    }
+    __syncthreads();
+    if (threadIdx.x < 16) {
+        const int j = threadIdx.x;
+        float hg = 0.0f, hu = 0.0f;
+        for (int w = 0; w < kK13; ++w) {
+            hg += part[w][j];
+            hu += part[kK13 + w][j];
+        }
+        const int q = 16 * blockIdx.x + j;
+        const __half gh = __float2half_rn(scalbnf(hg, -sig)), uh = __float2half_rn(scalbnf(hu, -sig));
+        const __half act = __float2half_rn(silu_f32(__half2float(gh)) * __half2float(uh));
         a.act_ws[(size_t)r * a.I + q] = act;
         if (a.gu_dbg) {
-            a.gu_dbg[(size_t)r * N13 + q] = g;
-            a.gu_dbg[(size_t)r * N13 + a.I + q] = u;
+            a.gu_dbg[(size_t)r * 2 * a.I + q] = gh;
+            a.gu_dbg[(size_t)r * 2 * a.I + a.I + q] = uh;
         }
         if (a.act_dbg) a.act_dbg[(size_t)r * a.I + q] = act;
     }
 }
 
+// ---------------------------------------------------------------------------
+// W2 + ordered router-weighted sum
+// ---------------------------------------------------------------------------
 template <int MB>
-__global__ void __launch_bounds__(kW2Threads) moe_w2_kernel(const Args a) {
-    extern __shared__ __align__(16) float acts[];  // [topk][I]
-    __shared__ float ys[16][kW2Rows];
-    __shared__ int s_ids[16];
-    const int tid = threadIdx.x;
-    if (tid < a.topk) s_ids[tid] = a.ids[tid];
-    __syncthreads();
-    for (int i = tid; i < a.topk * a.I; i += blockDim.x) {
-        const int r = i / a.I;
-        const int id = s_ids[r];
-        acts[i] = (id >= 0 && id < a.E) ? __half2float(a.act_ws[i]) : 0.0f;
+__global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
+    __shared__ float ys[16][16];
+    const int r = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int n0 = 16 * blockIdx.x;
+    // prologue, overlapping the W13 stage: the ids (final before W13
+    // released this grid) and the first batch of codes and metadata
+    const int id = a.ids[r];
+    const bool valid = id >= 0 && id < a.E;
+    const int ng = a.I / 16, gpr = a.I / 32;
+    const size_t row0 = (size_t)(valid ? id : 0) * a.K + n0 + g;
+    const uint2* c0p = reinterpret_cast<const uint2*>(a.w2 + row0 * (a.I / 2));
+    const uint2* c8p = reinterpret_cast<const uint2*>(a.w2 + (row0 + 8) * (a.I / 2));
+    const uint8_t* m0p = a.w2_meta + row0 * gpr * MB;
+    const uint8_t* m8p = a.w2_meta + (row0 + 8) * gpr * MB;
+    const bool al4 = a.meta_al4 != 0;
+    uint2 cw[kG2][2];         // words 2j, 2j+1 of rows g and g+8 for k16 group j
+    uint32_t mw[kG2 / 2][2];  // the AWQ records of the batch
+    auto load_batch = [&](int gb) {  // gb is a multiple of kG2 (even)
+#pragma unroll
+        for (int i = 0; i < kG2; ++i) {
+            if (valid && gb + i < ng) {
+                cw[i][0] = __ldg(c0p + gb + i);
+                cw[i][1] = __ldg(c8p + gb + i);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kG2 / 2; ++i) {
+            const int ag = gb / 2 + i;
+            if (valid && ag < gpr) {
+                mw[i][0] = load_meta<MB>(m0p + (size_t)ag * MB, al4);
+                mw[i][1] = load_meta<MB>(m8p + (size_t)ag * MB, al4);
+            }
+        }
+    };
+    load_batch(0);
+    pdl_wait();  // the W13 stage (act) is complete and visible
+    pdl_launch_dependents();
+    const uint32_t sel = pair_selector(t);
+    const uint32_t* act = reinterpret_cast<const uint32_t*>(a.act_ws + (size_t)r * a.I);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    if (valid) {
+        for (int gb = 0; gb < ng; gb += kG2) {
+            if (gb > 0) load_batch(gb);
+#pragma unroll
+            for (int i = 0; i < kG2; ++i) {
+                const int j = gb + i;
+                if (j < ng) {
+                    uint32_t s0, b0, s8, b8;
+                    meta_sb2<MB>(mw[i / 2][0], s0, b0);
+                    meta_sb2<MB>(mw[i / 2][1], s8, b8);
+                    uint32_t x0 = 0, x1 = 0;
+                    if (g == 0) {
+                        x0 = act[8 * j + t];
+                        x1 = act[8 * j + 4 + t];
+                    }
+                    mma_f16_16816(d, awq_pair(cw[i][0].x, sel, s0, b0), awq_pair(cw[i][1].x, sel, s8, b8),
+                                  awq_pair(cw[i][0].y, sel, s0, b0), awq_pair(cw[i][1].y, sel, s8, b8), x0, x1);
+                }
+            }
+        }
     }
-    __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-    const int n0 = blockIdx.x * kW2Rows;
-    for (int item = warp; item < a.topk * kW2Rows; item += nw) {
-        const int r = item / kW2Rows, j = item - r * kW2Rows;
-        const int id = s_ids[r];
-        const int n = n0 + j;
-        if (id < 0 || id >= a.E || n >= a.K) continue;
-        const float v = awq_row_dot<MB>(a.w2, a.w2_meta, a.K, a.I, id, n, acts + (size_t)r * a.I, lane);
-        if (lane == 0) {
-            const __half y = __float2half_rn(v);
-            ys[r][j] = __half2float(y);
-            if (a.y_dbg) a.y_dbg[(size_t)r * a.K + n] = y;
+    if (t == 0) {
+        const __half y0 = __float2half_rn(d[0]), y8 = __float2half_rn(d[2]);
+        ys[r][g] = __half2float(y0);
+        ys[r][g + 8] = __half2float(y8);
+        if (a.y_dbg && valid) {
+            a.y_dbg[(size_t)r * a.K + n0 + g] = y0;
+            a.y_dbg[(size_t)r * a.K + n0 + g + 8] = y8;
         }
     }
     __syncthreads();
-    if (tid < kW2Rows && n0 + tid < a.K) {
+    if (threadIdx.x < 16) {
         float s = 0.0f;
-        for (int r = 0; r < a.topk; ++r) {
-            const int id = s_ids[r];
-            if (id >= 0 && id < a.E) s = fmaf(a.rw[r], ys[r][tid], s);
+        for (int rr = 0; rr < a.topk; ++rr) {
+            const int idr = a.ids[rr];
+            if (idr >= 0 && idr < a.E) s = fmaf(a.rw[rr], ys[rr][threadIdx.x], s);
         }
-        a.out[n0 + tid] = __float2half_rn(s);
+        a.out[n0 + threadIdx.x] = __float2half_rn(s);
     }
 }
 
 template <int MB>
 cudaError_t launch_mb(const Args& a, cudaStream_t s) {
-    const size_t smem13 = (size_t)a.K * sizeof(float);
-    const size_t smem2 = (size_t)a.topk * a.I * sizeof(float);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(moe_w13_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             16384 * (int)sizeof(float));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(moe_w2_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 16 * 1024 * (int)sizeof(float));
+                                             16384 * 2);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const dim3 g13((a.I + kW13Cols - 1) / kW13Cols, a.topk);
-    moe_w13_kernel<MB><<<g13, kW13Cols * 32, smem13, s>>>(a);
-    cudaError_t e = cudaPeekAtLastError();
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t c13 = {};
+    c13.gridDim = dim3(a.I / 16, a.topk);
+    c13.blockDim = dim3(2 * kK13 * 32);
+    c13.dynamicSmemBytes = (size_t)a.K * 2;
+    c13.stream = s;
+    c13.attrs = pdl;
+    c13.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&c13, moe_w13_kernel<MB>, a);
     if (e != cudaSuccess) return e;
-    const dim3 g2((a.K + kW2Rows - 1) / kW2Rows);
-    moe_w2_kernel<MB><<<g2, kW2Threads, smem2, s>>>(a);
-    return cudaPeekAtLastError();
+    cudaLaunchConfig_t c2 = {};
+    c2.gridDim = dim3(a.K / 16);
+    c2.blockDim = dim3(32 * a.topk);
+    c2.stream = s;
+    c2.attrs = pdl;
+    c2.numAttrs = 1;
+    return cudaLaunchKernelEx(&c2, moe_w2_kernel<MB>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_moe(const MoeLaunch& L, int num_sms, cudaStream_t s) {
     (void)num_sms;
+    if (L.topk < 1 || L.topk > 16 || L.K % 64 || L.I % 32 || L.K > 16384) return cudaErrorInvalidValue;
     Args a;
     a.E = L.E;
     a.K = L.K;
@@ -209,6 +382,7 @@ cudaError_t launch_moe(const MoeLaunch& L, int num_sms, cudaStream_t s) {
     a.w2_meta = L.w2_meta;
     a.x = L.x;
     a.x_is_bf16 = L.x_is_bf16;
+    a.meta_al4 = ((reinterpret_cast<uintptr_t>(L.w13_meta) | reinterpret_cast<uintptr_t>(L.w2_meta)) & 3u) == 0;
     a.ids = L.ids;
     a.rw = L.rw;
     a.topk = L.topk;
