@@ -128,10 +128,12 @@ qmlp_status qmlp_forward_path(qmlp_t* h, qmlp_path path, const void* x, int M, v
 qmlp_status qmlp_forward_stage(qmlp_t* h, int stage, qmlp_path path, const void* x, int M, void* out,
                                qmlp_stream_t stream);
 
-/* End-to-end call from host buffers: copies x (host bf16 [M, K]) to the
- * handle's staging buffer, runs the forward, copies the result back to
- * out (host bf16 [M, K]) and waits for `stream`. Pinned host memory gives
- * asynchronous copies; pageable memory works but serializes the copies.
+/* End-to-end call from host buffers (x: host bf16 [M, K], out: host bf16
+ * [M, K]); returns after `stream` has finished. Pinned (device-mapped) host
+ * buffers, 16-byte aligned and not overlapping, are read and written in place
+ * by the kernels over the coherent CPU-GPU link; otherwise x is copied to
+ * the handle's staging buffer and the result copied back (pageable memory
+ * works but serializes the copies).
  * Errors: as qmlp_forward. */
 qmlp_status qmlp_forward_host(qmlp_t* h, const void* x_host, int M, void* out_host,
                               qmlp_stream_t stream);

@@ -88,3 +88,24 @@ def test_split_many_calls_keep_the_barrier_aligned(torch_cuda):
     last, _ = run_forward(torch, mlp, case.x)
     assert np.array_equal(first, last)
     mlp.close()
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_split_host_buffers_match_device(torch_cuda, pinned):
+    """qmlp_forward_host on the I-partitioned kernel: pinned buffers are read
+    and written in place by the kernel, pageable ones go through the staging
+    copies; both give the device-buffer result bit for bit."""
+    torch = torch_cuda
+    K, I = SHAPES[0]
+    case = gen.gen_dense_case("nvfp4", K, I, 3, seed=330)
+    mlp = q.QuantMLP.from_case(case)
+    if mlp.decode_ctas() == 0:
+        pytest.skip("no I partition for this shape on this device")
+    dev, _ = run_forward(torch, mlp, case.x)
+    xh = torch.from_numpy(case.x.view(np.int16).copy())
+    oh = torch.zeros((3, K), dtype=torch.int16)
+    if pinned:
+        xh, oh = xh.pin_memory(), oh.pin_memory()
+    mlp.forward_host(xh, oh)
+    assert np.array_equal(oh.numpy().view(np.uint16), dev)
+    mlp.close()

@@ -332,7 +332,7 @@ static bool use_gemm(qmlp_t* h, qmlp_path path, int M) {
 
 // stage bit 0: gate/up + SwiGLU (x -> workspace act); bit 1: down (act -> out)
 static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void* x, int M, void* out,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool host_io = false) {
     if (fault("launch")) return QMLP_ERR_CUDA;
     const bool gemm = use_gemm(h, path, M);
     if (gemm && !h->has_gemm) return QMLP_ERR_SHAPE;
@@ -397,6 +397,7 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
             S.chsd = h->gv[2].chs;
             S.invd = h->gv[2].inv_g;
             S.x = xb;
+            S.x_in_host = host_io;
             S.act_out = ab;  // the workspace act (qmlp_forward_debug returns it)
             S.out = ob;
             S.part = h->spart;
@@ -450,8 +451,20 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
     return QMLP_OK;
 }
 
-static qmlp_status run_forward(qmlp_t* h, qmlp_path path, const void* x, int M, void* out, cudaStream_t s) {
-    return run_stages(h, path, 3, x, M, out, s);
+static qmlp_status run_forward(qmlp_t* h, qmlp_path path, const void* x, int M, void* out, cudaStream_t s,
+                               bool host_io = false) {
+    return run_stages(h, path, 3, x, M, out, s, host_io);
+}
+
+// Device address of a host buffer the GPU can read and write in place
+// (pinned, mapped into the device address space), else nullptr.
+static void* device_alias(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
 qmlp_status qmlp_forward_path(qmlp_t* h, qmlp_path path, const void* x, int M, void* out,
@@ -509,6 +522,15 @@ qmlp_status qmlp_forward_host(qmlp_t* h, const void* x_host, int M, void* out_ho
     if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t bytes = (size_t)M * h->K * 2;
+    // pinned buffers: the kernels read x and write out in host memory over the
+    // coherent CPU-GPU link, with no copy-engine round trips
+    void* xd = device_alias(x_host);
+    void* od = device_alias(out_host);
+    if (xd && od && aligned16(xd) && aligned16(od) && !overlaps(x_host, bytes, out_host, bytes)) {
+        qmlp_status st = run_forward(h, QMLP_PATH_AUTO, xd, M, od, s, true);
+        if (st != QMLP_OK) return st;
+        return cudaStreamSynchronize(s) == cudaSuccess ? QMLP_OK : QMLP_ERR_CUDA;
+    }
     if (cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return QMLP_ERR_CUDA;
     qmlp_status st = run_forward(h, QMLP_PATH_AUTO, h->x_stage, M, h->out_stage, s);
     if (st != QMLP_OK) return st;

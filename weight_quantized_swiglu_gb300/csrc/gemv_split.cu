@@ -712,7 +712,8 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
     a.depth = lay.depth;
     a.SA = lay.sa;
     a.xraw_off = lay.xraw;
-    a.xraw_bytes = lay.xraw_bytes;
+    // the bulk copy of x needs device memory; host-resident x is staged by loads
+    a.xraw_bytes = L.x_in_host ? 0 : lay.xraw_bytes;
     const int nt = L.M <= 8 ? 1 : 2;
     const bool m1 = L.M == 1;
     if (L.fmt == kNVFP4) {

@@ -119,6 +119,7 @@ struct SplitLaunch {
     const float* chsd = nullptr;     // FP8 down per-channel scales
     float invd = 1.0f;               // NVFP4 down 1/global
     const void* x = nullptr;         // bf16 [M, K]
+    bool x_in_host = false;          // x is device-mapped host memory: staged with plain loads
     void* act_out = nullptr;         // optional bf16 [M, I]
     void* out = nullptr;             // bf16 [M, K]
     float* part = nullptr;           // >= split_part_elems
