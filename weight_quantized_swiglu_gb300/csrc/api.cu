@@ -198,7 +198,7 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
     h->max_M = d->max_M;
     h->device = dev;
     h->num_sms = sms;
-    h->sp = plan_split(d->K, d->I, sms);
+    h->sp = plan_split(d->fmt, d->K, d->I, sms);
     h->layout_warps = h->sp.G ? h->sp.G * 16 : gemv_layout_warps(sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* tmp[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
@@ -206,7 +206,7 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
     const int Ns[3] = {d->I, d->I, d->K}, Ks[3] = {d->K, d->K, d->I};
     cudaError_t e = cudaSuccess;
     for (int p = 0; p < 3 && st == QMLP_OK; ++p)
-        st = load_proj(h, *srcs[p], Ns[p], Ks[p], p < 2 ? kGemvRecsPerStepPair : kGemvRecsPerStepSingle, h->gv[p],
+        st = load_proj(h, *srcs[p], Ns[p], Ks[p], p < 2 ? gemv_recs_pair(d->fmt) : gemv_recs_single(d->fmt), h->gv[p],
                        &tmp[2 * p], &tmp[2 * p + 1], s);
 
     // the CTA-sliced copy of the down projection for the I-partitioned kernel

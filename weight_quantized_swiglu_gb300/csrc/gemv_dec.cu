@@ -380,15 +380,14 @@ cudaError_t repack_nvfp4_split(const uint8_t* w, const uint8_t* scale, int N, in
                                uint8_t* wc, cudaStream_t s) {
     if (!P.G || (K / kChunkK) != P.G * P.Cb || K % kChunkK) return cudaErrorInvalidValue;
     repack_nvfp4_gemv_kernel<<<1024, 256, 0, s>>>(w, scale, N, K,
-                                                  RecPos{P.LB, P.G * 16, kGemvRecsPerStepSingle, true, P.Cb, P.LB},
-                                                  wc);
+                                                  RecPos{P.LB, P.G * 16, P.RB, true, P.Cb, P.LB}, wc);
     return cudaPeekAtLastError();
 }
 
 cudaError_t repack_fp8_split(const uint8_t* w, int N, int K, const SplitPlan& P, uint8_t* wc, cudaStream_t s) {
     if (!P.G || (K / kChunkK) != P.G * P.Cb || K % kChunkK) return cudaErrorInvalidValue;
     repack_fp8_gemv_kernel<<<1024, 256, 0, s>>>(w, N, K,
-                                                RecPos{P.LB, P.G * 16, kGemvRecsPerStepSingle, true, P.Cb, P.LB}, wc);
+                                                RecPos{P.LB, P.G * 16, P.RB, true, P.Cb, P.LB}, wc);
     return cudaPeekAtLastError();
 }
 

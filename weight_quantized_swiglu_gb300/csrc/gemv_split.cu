@@ -41,7 +41,6 @@ constexpr int kThr = kCT + 32;        // + one producer warp
 constexpr int kDepthMax = 16;
 constexpr int kBudget = 220 * 1024;
 constexpr int kBars = 2 * kDepthMax * 8 + 16;  // full, empty, x
-constexpr int kRA = kGemvRecsPerStepPair;  // gate/up records per warp per step
 constexpr uint64_t kLimit = 2000000000ull;  // 2 s
 
 struct Args {
@@ -283,7 +282,7 @@ template <int FMT, int NT, bool M1, int CB>
 QMLP_DEV bool phase_b_fixed(const Args& a, const Ring& r, int q, int steps, const uint4* xs, const int* s_sigb,
                             int M, int warp) {
     constexpr int rec = rec_bytes<FMT>();
-    constexpr int R = kGemvRecsPerStepSingle;
+    constexpr int R = gemv_recs_single(FMT);
     static_assert(R % CB == 0, "whole tiles per step");
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     uint4 xb[CB][NT][2];
@@ -357,7 +356,8 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     r.full0 = smem_u32(r.base + (size_t)a.depth * a.slot_bytes);
     r.empty0 = r.full0 + 8u * kDepthMax;
     r.xbar = r.empty0 + 8u * kDepthMax;
-    const int stepsA = a.LA / kRA, stepsB = a.LB / kGemvRecsPerStepSingle;
+    constexpr int kRA = gemv_recs_pair(FMT), kRB = gemv_recs_single(FMT);
+    const int stepsA = a.LA / kRA, stepsB = a.LB / kRB;
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.depth; ++i) {
             mbar_init(r.full0 + 8u * i, 1);
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
             Steps st;
             const uint32_t rec = rec_bytes<FMT>();
             st.bytes_a = kW * kRA * rec;
-            st.bytes_b = kW * kGemvRecsPerStepSingle * rec;
+            st.bytes_b = kW * kRB * rec;
             st.stride_a = (size_t)a.G * st.bytes_a;
             st.stride_b = (size_t)a.G * st.bytes_b;
             st.a0 = a.wa0 + (size_t)blockIdx.x * st.bytes_a;
@@ -514,10 +514,11 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     }
 
     // ---------------- phase B: down over this CTA's act slice ----------------
-    if (s_fail == 0 && (a.Cb == 1 || a.Cb == 2 || a.Cb == 4)) {
+    constexpr int kCB4 = kRB % 4 == 0 ? 4 : 1;  // CB = 4 has a fixed path when a step holds whole tiles
+    if (s_fail == 0 && (a.Cb == 1 || a.Cb == 2 || (a.Cb == 4 && kRB % 4 == 0))) {
         ok = a.Cb == 1   ? phase_b_fixed<FMT, NT, M1, 1>(a, r, q, stepsB, xs, s_sigb, M, warp)
              : a.Cb == 2 ? phase_b_fixed<FMT, NT, M1, 2>(a, r, q, stepsB, xs, s_sigb, M, warp)
-                         : phase_b_fixed<FMT, NT, M1, 4>(a, r, q, stepsB, xs, s_sigb, M, warp);
+                         : phase_b_fixed<FMT, NT, M1, kCB4>(a, r, q, stepsB, xs, s_sigb, M, warp);
     } else if (s_fail == 0) {
         const int slots = 4 * M;
         const int pb_floats = M * 16;
@@ -537,8 +538,8 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                 break;
             }
             const uint8_t* sb = r.base + (uint32_t)slot * (uint32_t)r.slot_bytes +
-                                (uint32_t)warp * kGemvRecsPerStepSingle * rec;
-            const int kend = min(k + kGemvRecsPerStepSingle, n);
+                                (uint32_t)warp * kRB * rec;
+            const int kend = min(k + kRB, n);
             for (; k < kend; ++k, sb += rec) {
                 ChunkW w[1];
                 w[0] = lds_chunk<FMT>(sb, lane);
@@ -561,7 +562,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                     cs = 0;
                 }
             }
-            k = max(k, (j + 1) * kGemvRecsPerStepSingle);
+            k = max(k, (j + 1) * kRB);
             __syncwarp();
             if (lane == 0) mbar_arrive(r.empty0 + 8u * slot);
             if (++slot == r.depth) {
@@ -664,14 +665,18 @@ Layout layout_for(int fmt, int M, int K, const SplitPlan& P) {
     const int rec = fmt == kNVFP4 ? kRecNVFP4 : kRecFP8;
     auto al = [](size_t v) { return (int)((v + 127) & ~(size_t)127); };
     L.xs = al((size_t)std::max(kca, P.Cb) * 128 * M);
-    L.sa = (kca + P.LA - 1) / P.LA + 1;  // contributors per gate/up tile (upper bound)
+    L.sa = P.SA;
     L.pa = L.xs;
     L.act = L.pa + al((size_t)P.T * L.sa * 2 * M * 16 * 4);
     L.pb = L.act + al((size_t)M * P.T * 16 * 4);
-    L.xraw = L.pb + al((size_t)kW * 2 * M * 16 * 4);
+    // split down tiles (two contributors per warp boundary) only on the
+    // generic down path: Cb not 1, 2 or 4, or a step not whole tiles
+    const int rb = gemv_recs_single(fmt);
+    const bool fixed_b = (P.Cb == 1 || P.Cb == 2 || P.Cb == 4) && rb % P.Cb == 0;
+    L.xraw = L.pb + (fixed_b ? 0 : al((size_t)kW * 2 * M * 16 * 4));
     L.xraw_bytes = (size_t)M * K * 2 <= (size_t)kXRawMax ? M * K * 2 : 0;
     L.ring = L.xraw + al((size_t)L.xraw_bytes);
-    L.slot = std::max(2 * kW * kRA * rec, kW * kGemvRecsPerStepSingle * rec);
+    L.slot = std::max(2 * kW * gemv_recs_pair(fmt) * rec, kW * rb * rec);
     const long avail = (long)kBudget - L.ring - kBars - 1024;
     L.depth = avail > 0 ? (int)std::min<long>(kDepthMax, avail / L.slot) : 0;
     L.total = (size_t)L.ring + (size_t)L.depth * L.slot + kBars;
@@ -680,9 +685,10 @@ Layout layout_for(int fmt, int M, int K, const SplitPlan& P) {
 
 }  // namespace
 
-SplitPlan plan_split(int K, int I, int num_sms) {
+SplitPlan plan_split(int fmt, int K, int I, int num_sms) {
     SplitPlan P;
     if (K % 16 || I % 16 || num_sms < 1) return P;
+    const int ra = gemv_recs_pair(fmt), rb = gemv_recs_single(fmt);
     const int nta = I / 16, kca = (K + kChunkK - 1) / kChunkK, ntd = K / 16;
     for (int T = 4; T <= nta; T += 4) {
         if (nta % T) continue;
@@ -691,14 +697,19 @@ SplitPlan plan_split(int K, int I, int num_sms) {
         // the smallest T with G <= SMs: the most CTAs; too few CTAs cannot
         // pull the bandwidth (each SM's consumers decode ~1.4x the HBM rate)
         if (4 * G < 3 * num_sms) return P;
-        if ((T * kca) % (16 * kRA) != 0) return P;  // gate/up: whole steps, no padding
+        if ((T * kca) % (16 * ra) != 0) return P;  // gate/up: whole steps, no padding
         if (ntd < 16 || T > 64) return P;
         P.G = G;
         P.T = T;
         P.Cb = T / 4;
         P.LA = T * kca / 16;
         const int lb = (ntd * P.Cb + 15) / 16;
-        P.LB = (lb + kGemvRecsPerStepSingle - 1) / kGemvRecsPerStepSingle * kGemvRecsPerStepSingle;
+        P.LB = (lb + rb - 1) / rb * rb;
+        P.RA = ra;
+        P.RB = rb;
+        P.SA = 1;
+        for (int lt = 0; lt < T; ++lt)
+            P.SA = std::max(P.SA, ((lt + 1) * kca - 1) / P.LA - (lt * kca) / P.LA + 1);
         return P;
     }
     return P;
@@ -721,7 +732,8 @@ size_t split_codes_bytes(int fmt, const SplitPlan& P) {
 
 cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t s) {
     if (!split_fits(L.fmt, L.M, L.K, P)) return cudaErrorInvalidValue;
-    if (L.gate.TWr != P.G * kW || L.gate.Lr != P.LA || L.gate.Rr != kRA || L.up.TWr != P.G * kW)
+    if (L.gate.TWr != P.G * kW || L.gate.Lr != P.LA || L.gate.Rr != P.RA || L.up.TWr != P.G * kW ||
+        P.RA != gemv_recs_pair(L.fmt) || P.RB != gemv_recs_single(L.fmt))
         return cudaErrorInvalidValue;
     const Layout lay = layout_for(L.fmt, L.M, L.K, P);
     if (P.T > 64) return cudaErrorInvalidValue;

@@ -83,10 +83,11 @@ cudaError_t repack_nvfp4_gemv(const uint8_t* w, const uint8_t* scale, int N, int
 cudaError_t repack_fp8_gemv(const uint8_t* w, int N, int K, int Lr, int TWr, int Rr, uint8_t* wc, cudaStream_t s);
 size_t gemv_codes_bytes(int fmt, int N, int K, int Lr, int TWr);
 // Records per warp per step of the layout: gate/up (streamed in pairs) take
-// 2, a projection streamed alone takes 4, so one step fills the same number
-// of bytes in both cases.
-constexpr int kGemvRecsPerStepPair = 2;
-constexpr int kGemvRecsPerStepSingle = 4;
+// half as many as a projection streamed alone, so one step fills the same
+// number of bytes in both cases; FP8 records (1024 B) take half as many as
+// NVFP4 ones (576 B), so a step is 32-37 KB for both formats.
+__host__ __device__ constexpr int gemv_recs_pair(int fmt) { return fmt == kFP8 ? 1 : 2; }
+__host__ __device__ constexpr int gemv_recs_single(int fmt) { return fmt == kFP8 ? 2 : 4; }
 // Largest split-K partial buffer (fp32 elements) any GEMV launch of a handle
 // with these sizes can need for M <= 16.
 size_t gemv_part_elems(int K, int I, int num_sms);
@@ -100,15 +101,17 @@ struct SplitPlan {
     int T = 0;        // gate/up row tiles per CTA
     int Cb = 0;       // down 64-k chunks per CTA
     int LA = 0;       // gate/up records per warp (= T*Kc/16; the gate/up layout uses Lr = LA, TWr = 16G)
-    int LB = 0;       // down records per warp in the CTA-sliced layout (multiple of 4)
+    int LB = 0;       // down records per warp in the CTA-sliced layout (multiple of RB)
+    int RA = 0, RB = 0;  // records per warp per step: gate/up pairs, down
+    int SA = 0;       // most warps sharing one gate/up tile
 };
-SplitPlan plan_split(int K, int I, int num_sms);
+SplitPlan plan_split(int fmt, int K, int I, int num_sms);
 bool split_fits(int fmt, int M, int K, const SplitPlan& P);
 size_t split_part_elems(int K, const SplitPlan& P);       // fp32 partials for M <= 16
 size_t split_codes_bytes(int fmt, const SplitPlan& P);     // down records, CTA-sliced
 // Down projection [K, I] into the CTA-sliced layout: local record u = w*LB + k
 // of CTA b (u < Nt*Cb) is (row tile u / Cb, chunk Cb*b + u % Cb), stored at
-// ((k / 4) * 16G + 16b + w) * 4 + k % 4; records past Nt*Cb are zero.
+// ((k / RB) * 16G + 16b + w) * RB + k % RB; records past Nt*Cb are zero.
 cudaError_t repack_nvfp4_split(const uint8_t* w, const uint8_t* scale, int N, int K, const SplitPlan& P,
                                uint8_t* wc, cudaStream_t s);
 cudaError_t repack_fp8_split(const uint8_t* w, int N, int K, const SplitPlan& P, uint8_t* wc, cudaStream_t s);
