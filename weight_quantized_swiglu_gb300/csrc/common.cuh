@@ -154,6 +154,12 @@ QMLP_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t b
         : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel of the stream start
+// its CTAs / wait until the previous kernel has completed and its memory is
+// visible (both are no-ops for kernels launched without the attribute).
+QMLP_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+QMLP_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over `nthreads` threads (a multiple of 32) of the CTA.
 QMLP_DEV void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -1,5 +1,9 @@
 // gemv_split.cu -- the whole decode MLP (M <= 16) in one persistent launch,
 // with the intermediate dimension partitioned across CTAs.
+// Launched with programmatic dependent launch: a CTA may start while the
+// previous kernel of the stream still holds SMs (its producer waits for that
+// kernel before copying x, its consumers before touching any shared buffer);
+// all G <= SMs CTAs, one per SM, are co-resident once it has finished.
 //
 // Operation (vllm.cpp issue "tp>1 fp8w tail-MLP shard ...", "Proposed fix";
 // Qwen3.8-27B-NVFP4, "NVFP4 numerics as implemented"):
@@ -370,14 +374,12 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     if (threadIdx.x < 64) s_cnta[threadIdx.x] = 0;
     if (threadIdx.x < kW) s_cntb[threadIdx.x] = 0;
     __syncthreads();  // the last CTA-wide barrier: the producer never waits on the consumers
+    // the next kernel's CTAs may start as SMs free up (set-up and launch
+    // latency overlap this call's end); they wait before touching its buffers
+    pdl_launch_dependents();
 
     if (warp == kW) {
         if (lane == 0) {
-            // x first (when it fits the raw buffer), then the weights
-            if (a.xraw_bytes) {
-                mbar_arrive_expect_tx(r.xbar, a.xraw_bytes);
-                bulk_g2s(smem_u32(smem + a.xraw_off), a.x, a.xraw_bytes, r.xbar);
-            }
             Steps st;
             const uint32_t rec = rec_bytes<FMT>();
             st.bytes_a = kW * kRA * rec;
@@ -389,6 +391,14 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
             st.b = a.wb + (size_t)blockIdx.x * st.bytes_b;
             st.steps_a = stepsA;
             st.steps = stepsA + stepsB;
+            // x first, once the previous kernel has completed, then the
+            // weights. (Measured: streaming the first weight steps before the
+            // wait delays the x copy behind them and costs ~1 us at M=1.)
+            pdl_wait();
+            if (a.xraw_bytes) {
+                mbar_arrive_expect_tx(r.xbar, a.xraw_bytes);
+                bulk_g2s(smem_u32(smem + a.xraw_off), a.x, a.xraw_bytes, r.xbar);
+            }
             int q = produce<FMT>(st, r, a.err);
             if (a.xraw_bytes) mbar_wait_bounded(r.xbar, 0, kLimit);  // the x copy is never left in flight
             if (q < 0) {
@@ -407,6 +417,10 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     float* s_pb = reinterpret_cast<float*>(smem + a.pb_off);
     const int g = lane >> 2, t = lane & 3;
     bool ok = true;
+
+    // x, act, the partials and the output belong to the previous kernel until
+    // it has completed
+    pdl_wait();
 
     // ---------------- phase A: gate/up over this CTA's tiles ----------------
     if (a.xraw_bytes) {
@@ -645,9 +659,13 @@ cudaError_t launch_t(const Args& a, size_t smem, cudaStream_t s) {
     cfg.blockDim = dim3(kThr);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
+    // Programmatic dependent launch instead of a cooperative one: a CTA can
+    // start (and stream weights) while the previous kernel still holds SMs.
+    // All G CTAs are co-resident once it has finished (one CTA per SM, G <=
+    // SMs, checked at create); the grid barrier's wait is bounded regardless.
     cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeCooperative;
-    at[0].val.cooperative = 1;
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a);

@@ -68,11 +68,6 @@ struct Args {
     __half* y_dbg;
 };
 
-// Programmatic dependent launch: let the next kernel of the stream start /
-// wait until the previous kernel's memory is visible.
-QMLP_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-QMLP_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // One metadata record (little-endian fp16 scale, then fp16 bias or u8 zero)
 // as its raw bytes, low byte first.
 template <int MB>
