@@ -499,18 +499,19 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     // ---------------- restage act (prescaled fp16 fragments) ----------------
     const int tslice = a.T * 16;
     if (s_fail == 0) {
-        if (threadIdx.x < 16) s_maxbits[threadIdx.x] = 0;
-        named_bar_sync(1, kCT);
+        // every warp finds the slice maxima itself (T*16 values per token)
+        // and converts its share of the items: one barrier
         for (int m = 0; m < M; ++m) {
             float mx = 0.0f;
-            for (int i = threadIdx.x; i < tslice; i += kCT) mx = fmaxf(mx, fabsf(s_act[m * tslice + i]));
+            for (int i = lane; i < tslice; i += 32) mx = fmaxf(mx, fabsf(s_act[m * tslice + i]));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0 && mx > 0.0f) atomicMax(&s_maxbits[m], __float_as_int(mx));
+            if (lane == 0) {
+                s_sigw[warp][m] = prescale_exponent(mx);
+                if (warp == 0) s_sigb[m] = s_sigw[warp][m];
+            }
         }
-        named_bar_sync(1, kCT);
-        if (threadIdx.x < M) s_sigb[threadIdx.x] = prescale_exponent(__int_as_float(s_maxbits[threadIdx.x]));
-        named_bar_sync(1, kCT);
+        __syncwarp();
         const int slots = 4 * M;
         for (int it = threadIdx.x; it < M * (tslice / 8); it += kCT) {
             const int m = it / (tslice / 8), k8 = (it % (tslice / 8)) * 8;
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                 const __nv_bfloat162 b2 = __floats2bfloat162_rn(src[2 * h], src[2 * h + 1]);  // exact: bf16 values
                 vw[h] = *reinterpret_cast<const uint32_t*>(&b2);
             }
-            stage_store8(xs, slots, m, k8, s_sigb[m], v);
+            stage_store8(xs, slots, m, k8, s_sigw[warp][m], v);
         }
         named_bar_sync(1, kCT);
     }
