@@ -589,10 +589,13 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     if (!ok && lane == 0) s_fail = 1;
 
     // ---------------- grid barrier (every CTA arrives exactly once) ----------------
-    __threadfence();
+    // The CTA barrier orders every consumer thread's partial stores before
+    // thread 0's release add (cumulative), and thread 0's acquire poll before
+    // the CTA barrier that precedes the reads of the other CTAs' partials.
     named_bar_sync(1, kCT);
     if (threadIdx.x == 0) {
-        const unsigned long long tk = atomicAdd(a.ticket, 1ull);
+        unsigned long long tk;
+        asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(tk) : "l"(a.ticket) : "memory");
         const unsigned long long target = (tk / (unsigned long long)a.G + 1ull) * (unsigned long long)a.G;
         int pass = 1;
         if (tk + 1ull != target) {
@@ -605,7 +608,6 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                 }
             }
         }
-        __threadfence();
         s_pass = pass;
     }
     named_bar_sync(1, kCT);
