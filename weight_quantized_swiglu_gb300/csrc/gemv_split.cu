@@ -46,6 +46,7 @@ constexpr int kDepthMax = 16;
 constexpr int kBudget = 220 * 1024;
 constexpr int kBars = 2 * kDepthMax * 8 + 16;  // full, empty, x
 constexpr uint64_t kLimit = 2000000000ull;  // 2 s
+constexpr int kRedLoads = 10;                // partials a warp adds per output: G <= 16 * kRedLoads
 
 struct Args {
     // phase A: gate (wc0) and up (wc1), row-tile-major layout over 16*G warps
@@ -623,16 +624,35 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     const int units_n = (a.K + 31) / 32;
     const int units = M * units_n;
     float* red = reinterpret_cast<float*>(smem);
+    const size_t bstride = (size_t)M * a.K;
     int nu = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++nu) {
-        const int m = u / units_n, n = (u % units_n) * 32 + lane;
-        float sum = 0.0f;
-        if (n < a.K) {
-            const float* src = a.part + (size_t)m * a.K + n;
-            const size_t bstride = (size_t)M * a.K;
-            for (int b = warp; b < a.G; b += kW) sum += __ldcg(src + (size_t)b * bstride);
+    // two units per round; every load of a round is issued before the adds
+    // (in the same fixed order), so a round costs one L2 round trip
+    for (int u0 = blockIdx.x; u0 < units; u0 += 2 * gridDim.x) {
+        const int u1 = u0 + gridDim.x;
+        const int n0 = (u0 % units_n) * 32 + lane, n1 = (u1 % units_n) * 32 + lane;
+        const bool ok0 = n0 < a.K, ok1 = u1 < units && n1 < a.K;
+        const float* src0 = a.part + (size_t)(u0 / units_n) * a.K + n0;
+        const float* src1 = a.part + (size_t)(u1 / units_n) * a.K + n1;
+        float v0[kRedLoads], v1[kRedLoads];
+#pragma unroll
+        for (int i = 0; i < kRedLoads; ++i) {
+            const int b = warp + i * kW;
+            v0[i] = (ok0 && b < a.G) ? __ldcg(src0 + (size_t)b * bstride) : 0.0f;
+            v1[i] = (ok1 && b < a.G) ? __ldcg(src1 + (size_t)b * bstride) : 0.0f;
         }
-        red[(nu * kW + warp) * 32 + lane] = sum;
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kRedLoads; ++i) {
+            s0 += v0[i];
+            s1 += v1[i];
+        }
+        red[(nu * kW + warp) * 32 + lane] = s0;
+        ++nu;
+        if (u1 < units) {
+            red[(nu * kW + warp) * 32 + lane] = s1;
+            ++nu;
+        }
     }
     named_bar_sync(1, kCT);
     for (int i = warp; i < nu; i += kW) {
@@ -714,7 +734,7 @@ SplitPlan plan_split(int fmt, int K, int I, int num_sms) {
     for (int T = 4; T <= nta; T += 4) {
         if (nta % T) continue;
         const int G = nta / T;
-        if (G > num_sms) continue;
+        if (G > num_sms || G > kW * kRedLoads) continue;
         // the smallest T with G <= SMs: the most CTAs; too few CTAs cannot
         // pull the bandwidth (each SM's consumers decode ~1.4x the HBM rate)
         if (4 * G < 3 * num_sms) return P;
