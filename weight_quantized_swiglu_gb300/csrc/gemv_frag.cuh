@@ -170,17 +170,28 @@ QMLP_DEV void stage_sync(int nth) {
 // [2^14, 2^15). One pass over memory: each thread keeps its (at most
 // kStageRegs) 16-byte items in registers between the max and the convert;
 // larger slices take a second pass. Ends with a barrier over those threads.
+// REGS bounds the unrolled per-thread items: code that runs once per call is
+// fetched cold, so a caller that knows its slice is small asks for fewer.
 constexpr int kStageRegs = 8;
 
+// 2^e as a float, e in [-126, 127]
+QMLP_DEV float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// x * 2^sig as two multiplies by exact powers of two: for every sig the
+// prescale produces ([-113, 163]) both halves are normal exponents, so the
+// product is exact whenever it is a normal float (as scalbnf) and the fp16
+// rounding is the only one; anything smaller rounds to zero in fp16 either way.
 QMLP_DEV void stage_store8(uint4* xs, int slots, int m, int kl, int sig, const uint4& v) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+    const int s1 = sig / 2;
+    const float f1 = pow2f(s1), f2 = pow2f(sig - s1);
     const int cc = kl / kChunkK, j = (kl % kChunkK) / 16, reg = (kl % 16) / 8;
     const int half = j >> 1, word = (j & 1) * 2 + reg;
     uint32_t* base = reinterpret_cast<uint32_t*>(xs + (size_t)(cc * 2 + half) * slots + m * 4);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         const float2 f = __bfloat1622float2(h[t]);
-        const __half2 hh = __floats2half2_rn(scalbnf(f.x, sig), scalbnf(f.y, sig));
+        const __half2 hh = __floats2half2_rn(f.x * f1 * f2, f.y * f1 * f2);
         base[t * 4 + word] = *reinterpret_cast<const uint32_t*>(&hh);
     }
 }
@@ -202,6 +213,7 @@ QMLP_DEV uint4 ld_x16(const __nv_bfloat16* p, bool smem_src) {
     return smem_src ? *reinterpret_cast<const uint4*>(p) : __ldcg(reinterpret_cast<const uint4*>(p));
 }
 
+template <int REGS = kStageRegs>
 QMLP_DEV void stage_x(const __nv_bfloat16* x, int M, int ld, int kb, int ke, int kpe, uint4* xs, int* s_maxbits,
                       int* s_sig, int nth = -1, bool smem_src = false) {
     if (nth < 0) nth = blockDim.x;
@@ -210,12 +222,12 @@ QMLP_DEV void stage_x(const __nv_bfloat16* x, int M, int ld, int kb, int ke, int
     const int real8 = (ke - kb) / 8;
     const int pad8 = (kpe - kb) / 8;
     const int total = M * real8;
-    const bool in_regs = total <= kStageRegs * nth;
-    uint4 v[kStageRegs];
+    const bool in_regs = total <= REGS * nth;
+    uint4 v[REGS];
     if (tid < 16) s_maxbits[tid] = 0;
     // issue every load first (one memory round trip), then reduce
 #pragma unroll
-    for (int i = 0; i < kStageRegs; ++i) {
+    for (int i = 0; i < REGS; ++i) {
         const int it = tid + i * nth;
         v[i] = make_uint4(0, 0, 0, 0);
         if (in_regs && it < total) {
@@ -230,7 +242,7 @@ QMLP_DEV void stage_x(const __nv_bfloat16* x, int M, int ld, int kb, int ke, int
         float mx = 0.0f;
         if (in_regs) {
 #pragma unroll
-            for (int i = 0; i < kStageRegs; ++i) {
+            for (int i = 0; i < REGS; ++i) {
                 const int it = tid + i * nth;
                 if (it < total && it / real8 == m) mx = fmaxf(mx, absmax8(v[i]));
             }
@@ -247,7 +259,7 @@ QMLP_DEV void stage_x(const __nv_bfloat16* x, int M, int ld, int kb, int ke, int
     stage_sync(nth);
     if (in_regs) {
 #pragma unroll
-        for (int i = 0; i < kStageRegs; ++i) {
+        for (int i = 0; i < REGS; ++i) {
             const int it = tid + i * nth;
             if (it < total) {
                 const int m = it / real8, q = it - m * real8;

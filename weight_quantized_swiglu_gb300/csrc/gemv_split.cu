@@ -46,6 +46,8 @@ constexpr int kDepthMax = 16;
 constexpr int kBudget = 220 * 1024;
 constexpr int kBars = 2 * kDepthMax * 8 + 16;  // full, empty, x
 constexpr uint64_t kLimit = 2000000000ull;  // 2 s
+constexpr int kXRawMax = 16 * 1024;  // raw x copied to shared memory up to this size
+constexpr int kPreSteps = 1;                 // weight steps issued before the wait on the previous kernel
 constexpr int kRedLoads = 10;                // partials a warp adds per output: G <= 16 * kRedLoads
 
 struct Args {
@@ -99,9 +101,9 @@ struct Steps {
 // (Measured: L2 prefetches of later steps, of both phases or of the down
 // steps only, slow the call down by 2-8 us; the bulk copies alone are kept.)
 template <int FMT>
-QMLP_DEV int produce(const Steps& st, const Ring& r, int* err) {
-    int slot = 0, round = 0;
-    for (int q = 0; q < st.steps; ++q) {
+QMLP_DEV int produce(const Steps& st, const Ring& r, int* err, int q0, int q1) {
+    int slot = q0 % r.depth, round = q0 / r.depth;
+    for (int q = q0; q < q1; ++q) {
         if (round > 0 && !mbar_wait_bounded(r.empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kLimit)) {
             atomicExch(err, 24);
             return -(q + 1);
@@ -121,7 +123,7 @@ QMLP_DEV int produce(const Steps& st, const Ring& r, int* err) {
             ++round;
         }
     }
-    return st.steps;
+    return q1;
 }
 
 // 2^-s as a float (exact for every exponent the prescale produces); the
@@ -278,6 +280,53 @@ QMLP_DEV void stage_x_local(const uint4* xr, int M, int K, int kpe, uint4* xs, i
     named_bar_sync(1, kCT);
 }
 
+// x (raw bf16 rows of length K in shared memory) -> prescaled fp16 fragments
+// in xs with two barriers over the consumer threads: each warp writes its
+// per-token max|x| to its own word (no shared initialisation, no atomics),
+// then every thread folds the kW words itself (max is order-independent, so
+// every thread finds the same exponent) and converts its items. Thread m < M
+// also writes sig[m] for the epilogue. Needs M * kpe / 8 <= REGS * kCT.
+template <int REGS>
+QMLP_DEV void stage_x_two_bar(const uint4* xr, int M, int K, int kpe, uint4* xs, float (*wmax)[kW], int* sig) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int k8 = K / 8, p8 = kpe / 8, total = M * p8;
+    uint4 v[REGS];
+#pragma unroll
+    for (int i = 0; i < REGS; ++i) {
+        const int it = tid + i * kCT;
+        const int m = it / p8, q = it - m * p8;
+        v[i] = (it < total && q < k8) ? xr[m * k8 + q] : make_uint4(0, 0, 0, 0);
+    }
+    for (int m = 0; m < M; ++m) {
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < REGS; ++i)
+            if ((tid + i * kCT) / p8 == m) mx = fmaxf(mx, absmax8(v[i]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) wmax[m][warp] = mx;
+    }
+    named_bar_sync(1, kCT);
+#pragma unroll
+    for (int i = 0; i < REGS; ++i) {
+        const int it = tid + i * kCT;
+        if (it < total) {
+            const int m = it / p8;
+            float mx = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kW; ++w) mx = fmaxf(mx, wmax[m][w]);
+            stage_store8(xs, 4 * M, m, (it - m * p8) * 8, prescale_exponent(mx), v[i]);
+        }
+    }
+    if (tid < M) {
+        float mx = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) mx = fmaxf(mx, wmax[tid][w]);
+        sig[tid] = prescale_exponent(mx);
+    }
+    named_bar_sync(1, kCT);
+}
+
 // Phase B when the CTA's slice is CB = 1, 2 or 4 down chunks: every warp's
 // range starts on a row-tile boundary (LB is a multiple of 4), a step's 4
 // records are 4/CB whole tiles, and the CB activation fragments are the same
@@ -349,6 +398,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     __shared__ int s_cnta[64];
     __shared__ int s_cntb[kW];
     __shared__ int s_sigw[kW][16];
+    __shared__ float s_wmax[16][kW];
     __shared__ int s_fail;
     __shared__ int s_pass;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -392,15 +442,18 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
             st.b = a.wb + (size_t)blockIdx.x * st.bytes_b;
             st.steps_a = stepsA;
             st.steps = stepsA + stepsB;
-            // x first, once the previous kernel has completed, then the
-            // weights. (Measured: streaming the first weight steps before the
-            // wait delays the x copy behind them and costs ~1 us at M=1.)
+            // The weights do not depend on the previous kernel: the first
+            // kPreSteps steps go out before the wait, x right after it, then
+            // the rest of the weights. (Measured back to back: one step
+            // gains 0.1-0.5 us; two or more delay the x copy behind them.)
+            const int pre = min(min(kPreSteps, a.depth), st.steps);
+            produce<FMT>(st, r, a.err, 0, pre);
             pdl_wait();
             if (a.xraw_bytes) {
                 mbar_arrive_expect_tx(r.xbar, a.xraw_bytes);
                 bulk_g2s(smem_u32(smem + a.xraw_off), a.x, a.xraw_bytes, r.xbar);
             }
-            int q = produce<FMT>(st, r, a.err);
+            int q = produce<FMT>(st, r, a.err, pre, st.steps);
             if (a.xraw_bytes) mbar_wait_bounded(r.xbar, 0, kLimit);  // the x copy is never left in flight
             if (q < 0) {
                 const int issued = -q - 1;
@@ -431,12 +484,15 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         }
         // (after a failed wait x reads as whatever is there; the error word
         // reports the call)
-        // one token: the CTA-wide max with barriers; several: every warp
-        // finds the maxima itself and only one barrier remains (measured:
-        // 33.4 vs 34.4 us at M=1, 53.2 vs 50.6 us at M=4)
+        // one token: warp maxima, two barriers; several: every warp finds
+        // the maxima itself and only one barrier remains (measured: 33.4 vs
+        // 34.4 us at M=1, 53.2 vs 50.6 us at M=4)
+        // a one-token x in shared memory has at most kXRawMax / 2 columns
+        // (padded to a chunk: still <= 2 items of 8 per consumer thread)
+        static_assert(kXRawMax / 16 <= 2 * kCT && kXRawMax % (2 * kChunkK) == 0, "one-token staging: 2 items");
         if (M1)
-            stage_x(reinterpret_cast<const __nv_bfloat16*>(smem + a.xraw_off), M, a.K, 0, a.K, a.KcA * kChunkK, xs,
-                    s_maxbits, s_sig, kCT, true);
+            stage_x_two_bar<2>(reinterpret_cast<const uint4*>(smem + a.xraw_off), M, a.K, a.KcA * kChunkK, xs,
+                               s_wmax, s_sig);
         else
             stage_x_local(reinterpret_cast<const uint4*>(smem + a.xraw_off), M, a.K, a.KcA * kChunkK, xs,
                           s_sigw[warp], s_sig, warp);
@@ -698,7 +754,6 @@ struct Layout {
     int xs, pa, act, pb, xraw, xraw_bytes, ring, slot, depth, sa;
     size_t total;
 };
-constexpr int kXRawMax = 16 * 1024;  // raw x copied to shared memory up to this size
 
 Layout layout_for(int fmt, int M, int K, const SplitPlan& P) {
     Layout L;
