@@ -101,10 +101,14 @@ QMLP_DEV float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 // Exponent that brings max|v| into [2^14, 2^15): fp16 then holds every bf16
 // value within 2^29 of the maximum exactly (bf16 has 8 significant bits,
 // fp16 11). Zero/non-finite maxima get 0.
+// e with maxabs in [2^(e-1), 2^e) read from the IEEE fields: a normal
+// float's biased exponent b gives e = b - 126; a subnormal m * 2^-149 gives
+// e = (bit length of m) - 149.
 QMLP_DEV int prescale_exponent(float maxabs) {
-    if (!(maxabs > 0.0f) || !isfinite(maxabs)) return 0;
-    int e;
-    frexpf(maxabs, &e);  // maxabs in [2^(e-1), 2^e)
+    const int bits = __float_as_int(maxabs);
+    if (bits <= 0 || bits >= 0x7f800000) return 0;  // zero, negative, inf, nan
+    const int b = bits >> 23;
+    const int e = b ? b - 126 : (32 - __clz(bits)) - 149;
     return 15 - e;
 }
 
