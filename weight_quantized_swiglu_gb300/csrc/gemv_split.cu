@@ -280,50 +280,41 @@ QMLP_DEV void stage_x_local(const uint4* xr, int M, int K, int kpe, uint4* xs, i
     named_bar_sync(1, kCT);
 }
 
-// x (raw bf16 rows of length K in shared memory) -> prescaled fp16 fragments
-// in xs with two barriers over the consumer threads: each warp writes its
-// per-token max|x| to its own word (no shared initialisation, no atomics),
+// One token's x (K raw bf16 values in shared memory) -> prescaled fp16
+// fragments in xs with two barriers over the consumer threads: each warp
+// writes its max|x| to its own word (no shared initialisation, no atomics),
 // then every thread folds the kW words itself (max is order-independent, so
-// every thread finds the same exponent) and converts its items. Thread m < M
-// also writes sig[m] for the epilogue. Needs M * kpe / 8 <= REGS * kCT.
+// every thread finds the same exponent) and converts its items (8 values
+// each; k in [K, kpe) is zero). Thread 0 also writes sig[0] for the
+// epilogue. Needs kpe / 8 <= REGS * kCT. (Written for one token: no index
+// division, one fold per thread -- this runs once per call and its
+// instruction count is on the critical path.)
 template <int REGS>
-QMLP_DEV void stage_x_two_bar(const uint4* xr, int M, int K, int kpe, uint4* xs, float (*wmax)[kW], int* sig) {
+QMLP_DEV void stage_x_one_token(const uint4* xr, int K, int kpe, uint4* xs, float* wmax, int* sig) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int k8 = K / 8, p8 = kpe / 8, total = M * p8;
+    const int k8 = K / 8, p8 = kpe / 8;
     uint4 v[REGS];
+    float mx = 0.0f;
 #pragma unroll
     for (int i = 0; i < REGS; ++i) {
         const int it = tid + i * kCT;
-        const int m = it / p8, q = it - m * p8;
-        v[i] = (it < total && q < k8) ? xr[m * k8 + q] : make_uint4(0, 0, 0, 0);
+        v[i] = it < k8 ? xr[it] : make_uint4(0, 0, 0, 0);
+        mx = fmaxf(mx, absmax8(v[i]));
     }
-    for (int m = 0; m < M; ++m) {
-        float mx = 0.0f;
 #pragma unroll
-        for (int i = 0; i < REGS; ++i)
-            if ((tid + i * kCT) / p8 == m) mx = fmaxf(mx, absmax8(v[i]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) wmax[m][warp] = mx;
-    }
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) wmax[warp] = mx;
     named_bar_sync(1, kCT);
+    mx = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) mx = fmaxf(mx, wmax[w]);
+    const int sg = prescale_exponent(mx);
 #pragma unroll
     for (int i = 0; i < REGS; ++i) {
         const int it = tid + i * kCT;
-        if (it < total) {
-            const int m = it / p8;
-            float mx = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kW; ++w) mx = fmaxf(mx, wmax[m][w]);
-            stage_store8(xs, 4 * M, m, (it - m * p8) * 8, prescale_exponent(mx), v[i]);
-        }
+        if (it < p8) stage_store8(xs, 4, 0, it * 8, sg, v[i]);
     }
-    if (tid < M) {
-        float mx = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kW; ++w) mx = fmaxf(mx, wmax[tid][w]);
-        sig[tid] = prescale_exponent(mx);
-    }
+    if (tid == 0) sig[0] = sg;
     named_bar_sync(1, kCT);
 }
 
@@ -398,7 +389,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     __shared__ int s_cnta[64];
     __shared__ int s_cntb[kW];
     __shared__ int s_sigw[kW][16];
-    __shared__ float s_wmax[16][kW];
+    __shared__ float s_wmax[kW];
     __shared__ int s_fail;
     __shared__ int s_pass;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -491,8 +482,8 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         // (padded to a chunk: still <= 2 items of 8 per consumer thread)
         static_assert(kXRawMax / 16 <= 2 * kCT && kXRawMax % (2 * kChunkK) == 0, "one-token staging: 2 items");
         if (M1)
-            stage_x_two_bar<2>(reinterpret_cast<const uint4*>(smem + a.xraw_off), M, a.K, a.KcA * kChunkK, xs,
-                               s_wmax, s_sig);
+            stage_x_one_token<2>(reinterpret_cast<const uint4*>(smem + a.xraw_off), a.K, a.KcA * kChunkK, xs,
+                                 s_wmax, s_sig);
         else
             stage_x_local(reinterpret_cast<const uint4*>(smem + a.xraw_off), M, a.K, a.KcA * kChunkK, xs,
                           s_sigw[warp], s_sig, warp);
