@@ -8,11 +8,11 @@ synthetic seeded weights. One "step" = one MLP call. Inputs are resident in
 HBM; the weights rotate over several independent device copies whose total
 exceeds twice the L2 size, so every call streams its weights from HBM.
 
-Also reported: the HBM roofline fraction of the dominant kernel (gate/up
-GEMV, timed with CUDA events on its stream), the end-to-end time through the
-host-buffer entry point, the CPU oracle timed on this host, and secondary
-workloads (tiny NVFP4, FP8 W8A16 decode, routed-expert AWQ, NVFP4 prefill
-when the tensor-core GEMM is available).
+Also reported: the HBM roofline fraction of the dominant kernel (the
+single-launch decode MLP, timed with CUDA events on its stream), the
+end-to-end time through the host-buffer entry point, the CPU oracle timed on
+this host, and secondary workloads (tiny NVFP4, FP8 W8A16 decode,
+routed-expert AWQ, NVFP4 and FP8 prefill on the tensor-core GEMM).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
 """
@@ -341,10 +341,10 @@ def bench_moe(meta_bytes=4):
     return res
 
 
-def bench_prefill(M, reps, pk):
+def bench_prefill(M, reps, pk, fmt="nvfp4"):
     import torch
     import weight_quantized_swiglu_gb300 as q
-    case = gen.gen_dense_case("nvfp4", K_HID, I_INT, M, gen.seed_for(3, 0 if M == 512 else 1))
+    case = gen.gen_dense_case(fmt, K_HID, I_INT, M, gen.seed_for(3 if fmt == "nvfp4" else 5, 0 if M == 512 else 1))
     mlp = q.QuantMLP.from_case(case)
     x = torch.from_numpy(case.x.view(np.int16)).cuda()
     out = torch.empty((M, K_HID), dtype=torch.int16, device="cuda")
@@ -478,9 +478,10 @@ def run_profile(args):
             moe.forward(x, q.DT_FP16, ids, rw, out)
         torch.cuda.synchronize()
         moe.check()
-    elif args.profile.startswith("prefill"):
-        M = int(args.profile[len("prefill"):] or 512)
-        case = gen.gen_dense_case("nvfp4", K_HID, I_INT, M, gen.seed_for(3, 0))
+    elif args.profile.startswith("prefill") or args.profile.startswith("fp8prefill"):
+        fp8 = args.profile.startswith("fp8")
+        M = int(args.profile[len("fp8prefill" if fp8 else "prefill"):] or 512)
+        case = gen.gen_dense_case("fp8" if fp8 else "nvfp4", K_HID, I_INT, M, gen.seed_for(5 if fp8 else 3, 0))
         mlp = q.QuantMLP.from_case(case)
         x = torch.from_numpy(case.x.view(np.int16)).cuda()
         out = torch.empty((M, K_HID), dtype=torch.int16, device="cuda")
@@ -503,7 +504,7 @@ def main():
                     help="comma list of extra workloads to time (decode,fp8,tiny,moe,prefill) or 'all'")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile", default=None,
-                    help="eager launches of one operation for ncu: fused|stage0|stage1|fp8_fused|moe|prefillM")
+                    help="eager launches of one operation for ncu: fused|stage0|stage1|fp8_fused|moe|prefillM|fp8prefillM")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.profile:
@@ -544,11 +545,12 @@ def main():
             extras["moe_awq_m1_4B"] = bench_moe(4)
             extras["moe_awq_m1_3B"] = bench_moe(3)
         if "prefill" in want:
-            try:
-                extras["nvfp4_prefill_M512"] = bench_prefill(512, 5, pk)
-                extras["nvfp4_prefill_M8192"] = bench_prefill(8192, 3, pk)
-            except q.QmlpError as e:
-                extras["nvfp4_prefill"] = {"unavailable": str(e)}
+            for fmt in ("nvfp4", "fp8"):
+                try:
+                    extras[f"{fmt}_prefill_M512"] = bench_prefill(512, 5, pk, fmt)
+                    extras[f"{fmt}_prefill_M8192"] = bench_prefill(8192, 3, pk, fmt)
+                except q.QmlpError as e:
+                    extras[f"{fmt}_prefill"] = {"unavailable": str(e)}
         torch.cuda.synchronize()
 
     cpu = cpu_baseline(case, args.cpu_budget) if rank == 0 else None

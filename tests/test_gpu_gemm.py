@@ -1,8 +1,8 @@
-"""GPU parity of the tensor-core prefill path (GEMM family: NVFP4, M >= 17)
-against the CPU oracle, through the C ABI: exact single-weight decode, raw
-projections, the tiny shape at ragged token counts, the 27B-class prefill
-shape at its token counts (sampled rows), determinism and the automatic
-path choice."""
+"""GPU parity of the tensor-core prefill path (GEMM family: NVFP4 and FP8
+per-channel, M >= 17) against the CPU oracle, through the C ABI: exact
+single-weight decode, raw projections, the tiny shape at ragged token
+counts, the 27B-class prefill shape at its token counts (sampled rows),
+determinism and the automatic path choice."""
 import numpy as np
 import pytest
 
@@ -37,11 +37,16 @@ def run_forward(torch, mlp, x_bits, path):
     return bits_from_dev(out), bits_from_dev(act)
 
 
-def test_gemm_one_hot_returns_decoded_weights_exactly(torch_cuda):
-    """x = e_k rows: y[r, n] = E2M1 * E4M3 of W[n, k] exactly, for gate, up
-    and down, at k positions on scale-group, k-step and tile boundaries."""
+FMTS = ["nvfp4", "fp8"]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemm_one_hot_returns_decoded_weights_exactly(torch_cuda, fmt):
+    """x = e_k rows: y[r, n] = the decoded W[n, k] exactly (E2M1 * E4M3, or
+    e4m3fn), for gate, up and down, at k positions on scale-group, k-step
+    and tile boundaries."""
     torch = torch_cuda
-    case = gen.gen_dense_case("nvfp4", TK, TI, 1, seed=201)
+    case = gen.gen_dense_case(fmt, TK, TI, 1, seed=201)
     mlp = q.QuantMLP.from_case(case, max_M=64)
     for which, proj in ((0, case.gate), (1, case.up), (2, case.down)):
         Kp = proj.K
@@ -60,12 +65,13 @@ def test_gemm_one_hot_returns_decoded_weights_exactly(torch_cuda):
     mlp.close()
 
 
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("M", [17, 200])
-def test_gemm_raw_projection_matches_oracle(torch_cuda, M):
+def test_gemm_raw_projection_matches_oracle(torch_cuda, M, fmt):
     """Unscaled projections (fp32 out) on random bf16 x, every projection;
     M = 200 leaves a 72-row ragged second token tile."""
     torch = torch_cuda
-    case = gen.gen_dense_case("nvfp4", TK, TI, 1, seed=202)
+    case = gen.gen_dense_case(fmt, TK, TI, 1, seed=202)
     mlp = q.QuantMLP.from_case(case, max_M=256)
     for which, proj in ((0, case.gate), (1, case.up), (2, case.down)):
         xb = gen.gen_x_only(210 + which + M, M, proj.K)
@@ -79,9 +85,10 @@ def test_gemm_raw_projection_matches_oracle(torch_cuda, M):
     mlp.close()
 
 
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("M", [17, 128, 129, 300])
-def test_gemm_parity_tiny(torch_cuda, M):
-    case = gen.gen_dense_case("nvfp4", TK, TI, M, seed=220 + M)
+def test_gemm_parity_tiny(torch_cuda, M, fmt):
+    case = gen.gen_dense_case(fmt, TK, TI, M, seed=220 + M)
     mlp = q.QuantMLP.from_case(case)
     out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM)
     ref = oracle.dense_forward(case)
@@ -90,8 +97,9 @@ def test_gemm_parity_tiny(torch_cuda, M):
     mlp.close()
 
 
-def test_gemm_is_the_automatic_path_above_16_tokens(torch_cuda):
-    case = gen.gen_dense_case("nvfp4", TK, TI, 40, seed=230)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemm_is_the_automatic_path_above_16_tokens(torch_cuda, fmt):
+    case = gen.gen_dense_case(fmt, TK, TI, 40, seed=230)
     mlp = q.QuantMLP.from_case(case)
     auto, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
     gemm, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM)
@@ -117,12 +125,14 @@ def test_gemm_activation_magnitudes_keep_precision(torch_cuda):
     mlp.close()
 
 
+@pytest.mark.parametrize("name", ["nvfp4_prefill", "fp8_prefill"])
 @pytest.mark.parametrize("variant", [0, 1])
-def test_parity_nvfp4_prefill(torch_cuda, variant):
+def test_parity_prefill(torch_cuda, variant, name):
     """The 27B-class prefill shape (K=5120, I=17408) at M = 512 and 8192 in
-    the launch configuration the bench times; the oracle checks a seeded
-    sample of rows (rows are independent), including tile boundaries."""
-    case = gen.workload_case("nvfp4_prefill", variant)
+    the launch configuration the bench times, NVFP4 and FP8 per-channel; the
+    oracle checks a seeded sample of rows (rows are independent), including
+    tile boundaries."""
+    case = gen.workload_case(name, variant)
     M = case.M
     mlp = q.QuantMLP.from_case(case)
     out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)

@@ -230,28 +230,36 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
         }
     }
 
-    if (st == QMLP_OK && h->fmt == kNVFP4 && d->max_M > kMaxGemvM && gemm_supported(d->K, 2 * d->I) &&
-        gemm_supported(d->I, d->K)) {
+    if (st == QMLP_OK && d->max_M > kMaxGemvM && gemm_supported(d->K, 2 * d->I) && gemm_supported(d->I, d->K)) {
         void *gu = nullptr, *dn = nullptr;
-        if ((e = h->mem.alloc(&gu, gemm_tiles_bytes(2 * d->I, d->K))) != cudaSuccess) st = from_cuda(e);
-        else if ((e = h->mem.alloc(&dn, gemm_tiles_bytes(d->K, d->I))) != cudaSuccess) st = from_cuda(e);
-        else if (repack_nvfp4_gemm(tmp[0], tmp[1], tmp[2], tmp[3], 2 * d->I, d->K, true,
-                                   static_cast<uint8_t*>(gu), s) != cudaSuccess ||
-                 repack_nvfp4_gemm(tmp[4], tmp[5], nullptr, nullptr, d->K, d->I, false,
-                                   static_cast<uint8_t*>(dn), s) != cudaSuccess)
+        const bool nv = h->fmt == kNVFP4;
+        if ((e = h->mem.alloc(&gu, gemm_tiles_bytes(h->fmt, 2 * d->I, d->K))) != cudaSuccess) st = from_cuda(e);
+        else if ((e = h->mem.alloc(&dn, gemm_tiles_bytes(h->fmt, d->K, d->I))) != cudaSuccess) st = from_cuda(e);
+        else if (nv ? (repack_nvfp4_gemm(tmp[0], tmp[1], tmp[2], tmp[3], 2 * d->I, d->K, true,
+                                         static_cast<uint8_t*>(gu), s) != cudaSuccess ||
+                       repack_nvfp4_gemm(tmp[4], tmp[5], nullptr, nullptr, d->K, d->I, false,
+                                         static_cast<uint8_t*>(dn), s) != cudaSuccess)
+                    : (repack_fp8_gemm(tmp[0], tmp[2], 2 * d->I, d->K, true, static_cast<uint8_t*>(gu), s) !=
+                           cudaSuccess ||
+                       repack_fp8_gemm(tmp[4], nullptr, d->K, d->I, false, static_cast<uint8_t*>(dn), s) !=
+                           cudaSuccess))
             st = QMLP_ERR_CUDA;
         if (st == QMLP_OK) {
             h->has_gemm = true;
+            h->gm_gu.fmt = h->gm_d.fmt = h->fmt;
             h->gm_gu.tiles = static_cast<uint8_t*>(gu);
             h->gm_gu.N = 2 * d->I;
             h->gm_gu.K = d->K;
             h->gm_gu.inv_g0 = h->gv[0].inv_g;
             h->gm_gu.inv_g1 = h->gv[1].inv_g;
+            h->gm_gu.cs0 = h->gv[0].chs;  // FP8: the per-channel scales (NVFP4: null)
+            h->gm_gu.cs1 = h->gv[1].chs;
             h->gm_gu.interleaved = true;
             h->gm_d.tiles = static_cast<uint8_t*>(dn);
             h->gm_d.N = d->K;
             h->gm_d.K = d->I;
             h->gm_d.inv_g0 = h->gm_d.inv_g1 = h->gv[2].inv_g;
+            h->gm_d.cs0 = h->gm_d.cs1 = h->gv[2].chs;
             // GEMM workspace: prescaled fp16 activations (x, then act) and
             // the per-token exponents
             const size_t cols = (size_t)std::max(d->K, d->I);

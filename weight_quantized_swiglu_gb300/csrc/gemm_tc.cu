@@ -1,27 +1,32 @@
-// gemm_tc.cu -- tensor-core prefill GEMM for NVFP4 projections (M >= 17).
+// gemm_tc.cu -- tensor-core prefill GEMM for NVFP4 and FP8 per-channel
+// projections (M >= 17).
 //
 // Operation (Qwen3.8-27B-NVFP4, "NVFP4 numerics as implemented" and the
 // prefill tile discussion; vllm.cpp issue "tp>1 fp8w tail-MLP shard ...",
 // "Proposed fix" for the fused gate/up epilogue):
-//   y[m, n] = sum_k a[m, k] * W[n, k],  W[n, k] = E2M1(code) * E4M3(scale[n, k/16])
+//   y[m, n] = sum_k a[m, k] * W[n, k],
+//   NVFP4: W[n, k] = E2M1(code) * E4M3(scale[n, k/16]), factor c[n] = 1/global
+//   FP8:   W[n, k] = e4m3fn(byte),                    factor c[n] = scale[n]
 // followed by one of the epilogues
-//   SwiGLU: act[m, i] = bf16( SiLU(y_g[m, i] / g_gate) * (y_u[m, i] / g_up) )
-//   Plain:  out[m, n] = bf16( y[m, n] / g_down )
-//   Raw:    y[m, n] in fp32 (no global factor), debug.
+//   SwiGLU: act[m, i] = bf16( SiLU(c_g[i] y_g[m, i]) * (c_u[i] y_u[m, i]) )
+//   Plain:  out[m, n] = bf16( c[n] y[m, n] )
+//   Raw:    y[m, n] in fp32 (no factor), debug.
 //
 // GB300 design (sm_103a, one CTA per SM, persistent):
 //  * a (bf16 activations) is first rewritten as fp16 x 2^sigma[m] with one
 //    power of two per token (sigma puts the row maximum in [2^14, 2^15)), so
 //    every bf16 value within 2^29 of the row maximum is held exactly; the
 //    epilogue multiplies by 2^-sigma[m]. W = E2M1 x E4M3 has at most six
-//    significant bits and lies in [2^-10, 2688]: exact in fp16. The MMA is
-//    therefore an fp16 x fp16 -> fp32 product of the same values the bf16
-//    formulation multiplies.
+//    significant bits and lies in [2^-10, 2688]; an e4m3fn value has four
+//    and lies in [2^-9, 448]: both exact in fp16. The MMA is therefore an
+//    fp16 x fp16 -> fp32 product of the same values the bf16 formulation
+//    multiplies.
 //  * Tile 128 tokens x 256 weight rows, k-step 64. Warp roles:
 //      warp 0      TMA producer: the activation tile (cp.async.bulk.tensor,
 //                  128-byte swizzle) and the packed weight block of the step
-//                  (one 9 KB cp.async.bulk) into a 6-stage load ring (TMA
-//                  and L2 latency is several MMA steps long);
+//                  (one cp.async.bulk: 9 KB NVFP4, 16 KB FP8) into a 6-stage
+//                  (FP8: 5-stage) load ring (TMA and L2 latency is several
+//                  MMA steps long);
 //      warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma (M128 N256 K16)
 //                  per step into one of two TMEM accumulators (2 x 256 fp32
 //                  columns), tcgen05.commit frees the load stage and the
@@ -29,16 +34,19 @@
 //      warps 2-5   epilogue: tcgen05.ld of the finished accumulator (warp w
 //                  owns TMEM lanes 32*(w%4)..+31 = 32 token rows), scales,
 //                  SwiGLU, bf16 stores; overlaps the next tile's main loop;
-//      warps 6-13  decoders: packed E2M1 codes + E4M3 scales of the stage ->
-//                  fp16 weights (cvt.rn.f16x2.e2m1x2, then an exact f16x2
-//                  multiply by the group scale) written in the 128-byte
-//                  swizzled K-major layout the MMA descriptor reads, into a
-//                  2-stage ring (decoding step i+1 overlaps the MMAs of step i).
+//      warps 6-13  decoders: the stage's weight block -> fp16 weights
+//                  (NVFP4: cvt.rn.f16x2.e2m1x2, then an exact f16x2 multiply
+//                  by the group scale; FP8: cvt.rn.f16x2.e4m3x2) written in
+//                  the 128-byte swizzled K-major layout the MMA descriptor
+//                  reads, into a 2-stage ring (decoding step i+1 overlaps the
+//                  MMAs of step i).
 //  * Weight block layout (create-time repack): for n-tile j and k-step s a
-//    contiguous 9216-byte block: codes [256 rows][32 B] then scales
-//    [256 rows][4 B]. For gate/up the 256 rows of tile j are gate rows
-//    128j..128j+127 followed by up rows 128j..128j+127, so one accumulator
-//    holds both inputs of 128 SwiGLU outputs per token.
+//    contiguous block: NVFP4 codes [256 rows][32 B] then scales [256 rows]
+//    [4 B] (9216 B); FP8 bytes [256 rows][64 B] (16384 B; the per-channel
+//    scales stay a float vector read by the epilogue). For gate/up the 256
+//    rows of tile j are gate rows 128j..128j+127 followed by up rows
+//    128j..128j+127, so one accumulator holds both inputs of 128 SwiGLU
+//    outputs per token.
 //  * Every wait is bounded (globaltimer); on expiry the kernel records the
 //    error, every role leaves its loop, in-flight copies and MMAs are waited
 //    for (bounded) and TMEM is freed.
@@ -56,12 +64,15 @@ namespace {
 constexpr int BM = 128;                 // tokens per tile (TMEM lanes)
 constexpr int BN = 256;                 // weight rows per tile (accumulator columns)
 constexpr int BK = 64;                  // k per step (one 128-byte swizzle row of fp16)
-constexpr int kLStages = 6;             // load ring: activation tile + packed weight block
 constexpr int kBStages = 2;             // decoded-weight ring
 constexpr int kABytes = BM * BK * 2;    // 16 KB
 constexpr int kBBytes = BN * BK * 2;    // 32 KB
-constexpr int kRawCodes = BN * BK / 2;  // 8 KB
-constexpr int kRawBytes = kRawCodes + BN * (BK / 16);  // + 1 KB scales = 9216
+constexpr int kRawCodes = BN * BK / 2;  // NVFP4: 8 KB of codes, then 1 KB of scales
+// per format: weight block bytes and load-ring depth (activation tile + block)
+template <int FMT>
+constexpr int raw_bytes() { return FMT == kNVFP4 ? kRawCodes + BN * (BK / 16) : BN * BK; }
+template <int FMT>
+constexpr int lstages() { return FMT == kNVFP4 ? 6 : 5; }
 constexpr int kEpiWarps = 4;
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
@@ -70,25 +81,31 @@ constexpr int kTmemCols = 2 * BN;                           // two accumulators
 constexpr uint64_t kGemmWaitNs = 2000000000ull;             // 2 s
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kLStages * kABytes;
-constexpr int kOffRaw = kOffB + kBStages * kBBytes;
-constexpr int kOffBar = kOffRaw + kLStages * kRawBytes;
-// barriers: full[L], empty[L], bfull[B], bempty[B], acc_full[2], acc_empty[2], done
-constexpr int kNumBars = 2 * kLStages + 2 * kBStages + 5;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem address, abort flag
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-
-static_assert(kOffB % 1024 == 0 && kOffRaw % 16 == 0 && kOffBar % 8 == 0, "smem layout");
-static_assert(kSmemBytes <= 227 * 1024, "smem budget");
+template <int FMT>
+struct Smem {
+    static constexpr int L = lstages<FMT>();
+    static constexpr int R = raw_bytes<FMT>();
+    static constexpr int A = 0;
+    static constexpr int B = A + L * kABytes;
+    static constexpr int Raw = B + kBStages * kBBytes;
+    static constexpr int Bar = Raw + L * R;
+    // barriers: full[L], empty[L], bfull[B], bempty[B], acc_full[2], acc_empty[2], done
+    static constexpr int NumBars = 2 * L + 2 * kBStages + 5;
+    static constexpr int Misc = Bar + NumBars * 8;  // tmem address, abort flag
+    static constexpr int Bytes = Misc + 16 + 1024;  // + alignment slack
+    static_assert(B % 1024 == 0 && Raw % 16 == 0 && Bar % 8 == 0, "smem layout");
+    static_assert(Bytes <= 227 * 1024, "smem budget");
+};
 
 struct Args {
-    const uint8_t* tiles;  // packed weight blocks [Nt][KS][kRawBytes]
+    const uint8_t* tiles;  // weight blocks [Nt][KS][raw_bytes]
     int M, N, Kd;          // tokens, weight rows (projection outputs), contraction length
     int epi;               // kEpiSwiGLU / kEpiPlain / kEpiRaw
     int raw_sel;           // raw on an interleaved gate/up GEMM: 0 gate rows, 1 up rows
     int interleaved;       // tiles hold gate/up halves
-    float inv0, inv1;      // global factors (gate, up) or (down, down)
+    float inv0, inv1;      // NVFP4 global factors (gate, up) or (down, down)
+    const float* cs0;      // FP8 per-channel scales: gate (interleaved) or the projection's
+    const float* cs1;      // FP8 up scales (interleaved)
     const int* sig;        // [M] per-token prescale exponent
     void* out;             // bf16 [M, N_out] or fp32 [M, N_out]
     int ldo;               // out row length (elements)
@@ -209,13 +226,43 @@ QMLP_DEV void decode_item(const uint8_t* raw, uint8_t* bt, int n, int h) {
     }
 }
 
+// FP8: one (row, 32-k half) item = 32 e4m3fn bytes -> 32 fp16 (exact).
+QMLP_DEV void decode_item_fp8(const uint8_t* raw, uint8_t* bt, int n, int h) {
+    const uint4 c0 = *reinterpret_cast<const uint4*>(raw + n * 64 + h * 32);
+    const uint4 c1 = *reinterpret_cast<const uint4*>(raw + n * 64 + h * 32 + 16);
+    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint8_t* row = bt + n * 128;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 o;
+        e4m3x4_to_f16x2x2(words[2 * j], o.x, o.y);
+        e4m3x4_to_f16x2x2(words[2 * j + 1], o.z, o.w);
+        const int chunk = (h * 4 + j) ^ (n & 7);
+        *reinterpret_cast<uint4*>(row + chunk * 16) = o;
+    }
+}
+
+// The output factors of accumulator columns col..col+3: four consecutive
+// per-channel scales (FP8; the same four for every thread, a broadcast
+// load) or the global factor (NVFP4). col is a multiple of 4.
+template <int FMT>
+QMLP_DEV float4 factor4(const float* cs, float inv, int col) {
+    if (FMT == kNVFP4) return make_float4(inv, inv, inv, inv);
+    return __ldg(reinterpret_cast<const float4*>(cs + col));
+}
+QMLP_DEV float f4_at(const float4& f, int e) { return e == 0 ? f.x : e == 1 ? f.y : e == 2 ? f.z : f.w; }
+
 QMLP_DEV uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&p);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap amap,
-                                                                   const Args a) {
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap amap, const Args a) {
+    using S = Smem<FMT>;
+    constexpr int kLStages = S::L;
+    constexpr int kRawBytes = S::R;
+    constexpr int kOffA = S::A, kOffB = S::B, kOffRaw = S::Raw, kOffBar = S::Bar, kOffMisc = S::Misc;
     extern __shared__ uint8_t dyn_smem_raw[];
     const uint32_t base_s = (smem_u32(dyn_smem_raw) + 1023u) & ~1023u;
     uint8_t* base = dyn_smem_raw + (base_s - smem_u32(dyn_smem_raw));
@@ -355,15 +402,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
                     if (live) {
                         uint32_t pk[16];
 #pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            float r2[2];
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 fg = factor4<FMT>(a.cs0, a.inv0, nt * (BN / 2) + c0 + j);
+                            const float4 fu = factor4<FMT>(a.cs1, a.inv1, nt * (BN / 2) + c0 + j);
+                            float r4[4];
 #pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const float gv = scalbnf(g[j + e], -sg) * a.inv0;
-                                const float uv = scalbnf(u[j + e], -sg) * a.inv1;
-                                r2[e] = silu_f32(gv) * uv;
+                            for (int e = 0; e < 4; ++e) {
+                                const float gv = scalbnf(g[j + e], -sg) * f4_at(fg, e);
+                                const float uv = scalbnf(u[j + e], -sg) * f4_at(fu, e);
+                                r4[e] = silu_f32(gv) * uv;
                             }
-                            pk[j / 2] = pack_bf16x2(r2[0], r2[1]);
+                            pk[j / 2] = pack_bf16x2(r4[0], r4[1]);
+                            pk[j / 2 + 1] = pack_bf16x2(r4[2], r4[3]);
                         }
                         uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * (BN / 2) + c0);
 #pragma unroll
@@ -380,8 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
                     if (live) {
                         uint32_t pk[16];
 #pragma unroll
-                        for (int j = 0; j < 32; j += 2)
-                            pk[j / 2] = pack_bf16x2(scalbnf(y[j], -sg) * a.inv0, scalbnf(y[j + 1], -sg) * a.inv0);
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 f = factor4<FMT>(a.cs0, a.inv0, nt * BN + c0 + j);
+                            pk[j / 2] = pack_bf16x2(scalbnf(y[j], -sg) * f.x, scalbnf(y[j + 1], -sg) * f.y);
+                            pk[j / 2 + 1] = pack_bf16x2(scalbnf(y[j + 2], -sg) * f.z, scalbnf(y[j + 3], -sg) * f.w);
+                        }
                         uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * BN + c0);
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
@@ -428,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_nvfp4_kernel(const __grid_co
 #pragma unroll
                 for (int j = 0; j < (BN * 2) / kDecThreads; ++j) {
                     const int item = d + j * kDecThreads;
-                    decode_item(raw, bt, item >> 1, item & 1);
+                    if (FMT == kNVFP4) decode_item(raw, bt, item >> 1, item & 1);
+                    else decode_item_fp8(raw, bt, item >> 1, item & 1);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(bfull(b));
@@ -511,13 +565,38 @@ __global__ void repack_gemm_kernel(const uint8_t* __restrict__ w0, const uint8_t
             s = s0;
             row = j * BN + r;
         }
-        uint8_t* dst = tiles + blk * kRawBytes;
+        uint8_t* dst = tiles + blk * raw_bytes<kNVFP4>();
         const uint4* src = reinterpret_cast<const uint4*>(w + (size_t)row * (K / 2) + ks * (BK / 2));
         uint4* dc = reinterpret_cast<uint4*>(dst + r * 32);
         dc[0] = src[0];
         dc[1] = src[1];
         *reinterpret_cast<uint32_t*>(dst + kRawCodes + r * 4) =
             *reinterpret_cast<const uint32_t*>(s + (size_t)row * (K / 16) + ks * (BK / 16));
+    }
+}
+
+// FP8: block row r of (n-tile j, k-step ks) = the 64 e4m3fn bytes of weight
+// row `row` at k = 64 ks .. 64 ks + 63 (same row mapping as NVFP4).
+__global__ void repack_fp8_gemm_kernel(const uint8_t* __restrict__ w0, const uint8_t* __restrict__ w1, int N, int K,
+                                       int interleave, uint8_t* __restrict__ tiles) {
+    const int KS = K / BK;
+    const long total = (long)(N / BN) * KS * BN;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const int r = (int)(idx % BN);
+        const long blk = idx / BN;  // = j * KS + ks
+        const int ks = (int)(blk % KS);
+        const int j = (int)(blk / KS);
+        const uint8_t* w = w0;
+        int row = j * BN + r;
+        if (interleave) {
+            const bool up = r >= BN / 2;
+            w = up ? w1 : w0;
+            row = j * (BN / 2) + (r - (up ? BN / 2 : 0));
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(w + (size_t)row * K + ks * BK);
+        uint4* dst = reinterpret_cast<uint4*>(tiles + blk * raw_bytes<kFP8>() + r * BK);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) dst[v] = src[v];
     }
 }
 
@@ -539,9 +618,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+template <int FMT>
+cudaError_t launch_fmt(const CUtensorMap& map, const Args& a, int grid, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::Bytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    gemm_kernel<FMT><<<grid, kThreads, Smem<FMT>::Bytes, s>>>(map, a);
+    return cudaPeekAtLastError();
+}
+
 bool gemm_supported(int K, int N) { return K >= BK && K % BK == 0 && N >= BN && N % BN == 0; }
 
-size_t gemm_tiles_bytes(int N, int K) { return (size_t)(N / BN) * (K / BK) * kRawBytes; }
+size_t gemm_tiles_bytes(int fmt, int N, int K) {
+    return (size_t)(N / BN) * (K / BK) * (fmt == kNVFP4 ? raw_bytes<kNVFP4>() : raw_bytes<kFP8>());
+}
 
 cudaError_t repack_nvfp4_gemm(const uint8_t* w0, const uint8_t* s0, const uint8_t* w1, const uint8_t* s1, int N,
                               int K, bool interleave, uint8_t* tiles, cudaStream_t s) {
@@ -549,6 +643,15 @@ cudaError_t repack_nvfp4_gemm(const uint8_t* w0, const uint8_t* s0, const uint8_
     const long total = (long)(N / BN) * (K / BK) * BN;
     const int grid = (int)std::min<long>((total + 255) / 256, 65535);
     repack_gemm_kernel<<<grid, 256, 0, s>>>(w0, s0, w1, s1, N, K, interleave ? 1 : 0, tiles);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t repack_fp8_gemm(const uint8_t* w0, const uint8_t* w1, int N, int K, bool interleave, uint8_t* tiles,
+                            cudaStream_t s) {
+    if (!gemm_supported(K, N) || (interleave && !w1)) return cudaErrorInvalidValue;
+    const long total = (long)(N / BN) * (K / BK) * BN;
+    const int grid = (int)std::min<long>((total + 255) / 256, 65535);
+    repack_fp8_gemm_kernel<<<grid, 256, 0, s>>>(w0, w1, N, K, interleave ? 1 : 0, tiles);
     return cudaPeekAtLastError();
 }
 
@@ -587,20 +690,16 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     a.interleaved = P.interleaved ? 1 : 0;
     a.inv0 = P.inv_g0;
     a.inv1 = P.inv_g1;
+    a.cs0 = P.cs0;
+    a.cs1 = P.cs1;
+    if (P.fmt == kFP8 && (!P.cs0 || (P.interleaved && !P.cs1))) return cudaErrorInvalidValue;
     a.sig = L.sig;
     a.out = L.out;
     a.ldo = L.epi == kEpiSwiGLU ? P.N / 2 : (L.epi == kEpiRaw && P.interleaved ? P.N / 2 : P.N);
     a.err = L.err;
-    static bool attr = false;
-    if (!attr) {
-        e = cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
     const int tiles = ((L.M + BM - 1) / BM) * (P.N / BN);
     const int grid = std::min(tiles, std::max(num_sms, 1));
-    gemm_nvfp4_kernel<<<grid, kThreads, kSmemBytes, s>>>(map, a);
-    return cudaPeekAtLastError();
+    return P.fmt == kFP8 ? launch_fmt<kFP8>(map, a, grid, s) : launch_fmt<kNVFP4>(map, a, grid, s);
 }
 
 }  // namespace qmlp

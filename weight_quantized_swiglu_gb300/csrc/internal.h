@@ -135,12 +135,17 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
 // Tensor-core prefill GEMM (NVFP4, tcgen05)
 // ---------------------------------------------------------------------------
 struct GemmProj {
-    const uint8_t* tiles = nullptr;  // packed weight blocks [N/256][K/64][9216 B], see gemm_tc.cu
-    float inv_g0 = 1.0f, inv_g1 = 1.0f;  // global factors: (gate, up) when interleaved, else both = down
+    int fmt = kNVFP4;                    // kNVFP4 or kFP8
+    const uint8_t* tiles = nullptr;      // weight blocks [N/256][K/64][9216 B NVFP4 | 16384 B FP8], see gemm_tc.cu
+    float inv_g0 = 1.0f, inv_g1 = 1.0f;  // NVFP4 global factors: (gate, up) when interleaved, else both = down
+    const float* cs0 = nullptr;          // FP8 per-channel scales: gate when interleaved, else the projection's
+    const float* cs1 = nullptr;          // FP8 up scales when interleaved
     int N = 0, K = 0;                    // N weight rows (2I when interleaved), K contraction length
     bool interleaved = false;            // tile rows = 128 gate rows then the same 128 up rows
 };
-size_t gemm_tiles_bytes(int N, int K);
+size_t gemm_tiles_bytes(int fmt, int N, int K);
+cudaError_t repack_fp8_gemm(const uint8_t* w0, const uint8_t* w1, int N, int K, bool interleave, uint8_t* tiles,
+                            cudaStream_t s);
 cudaError_t repack_nvfp4_gemm(const uint8_t* w0, const uint8_t* s0, const uint8_t* w1,
                               const uint8_t* s1, int N, int K, bool interleave, uint8_t* tiles,
                               cudaStream_t s);

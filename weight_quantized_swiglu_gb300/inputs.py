@@ -225,6 +225,8 @@ WORKLOADS = {
     "dense_nvfp4_decode": (1, "nvfp4", DENSE_K, DENSE_I, (1, 4)),
     "dense_fp8_decode": (2, "fp8", DENSE_K, DENSE_I, (1, 16)),
     "nvfp4_prefill": (3, "nvfp4", DENSE_K, DENSE_I, (512, 8192)),
+    # config 4 is the routed-expert workload (gen_moe_case)
+    "fp8_prefill": (5, "fp8", DENSE_K, DENSE_I, (512, 8192)),
 }
 
 
