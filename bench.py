@@ -341,6 +341,53 @@ def bench_moe(meta_bytes=4):
     return res
 
 
+def bench_moe_tokens(Ms=(16, 512), meta_bytes=4):
+    """Routed experts for M tokens (grouped by expert on the device), E=512
+    K=2560 I=160 top-10: CUDA-graph replay of 20 calls, 7 samples, median.
+    Bytes = the unique valid experts' codes + metadata (each read once when
+    the grouping shares them)."""
+    import torch
+    import weight_quantized_swiglu_gb300 as q
+    tok = gen.gen_moe_tokens(gen.seed_for(6, 0), max(Ms))
+    c = tok.case
+    moe = q.MoeAWQ.from_case(c, meta_bytes)
+    moe.reserve(max(Ms))
+    per_exp = 2 * c.I * c.K // 2 + 2 * c.I * (c.K // 32) * meta_bytes + c.K * c.I // 2 + c.K * (c.I // 32) * meta_bytes
+    s = torch.cuda.Stream()
+    res = {}
+    for M in Ms:
+        x = torch.from_numpy(tok.x16[:M].view(np.int16).copy()).cuda()
+        ids = torch.from_numpy(tok.ids[:M].copy()).cuda()
+        rw = torch.from_numpy(tok.rw[:M].copy()).cuda()
+        out = torch.empty((M, c.K), dtype=torch.int16, device="cuda")
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                moe.forward_tokens(x, q.DT_FP16, ids, rw, out, stream=s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(20):
+                moe.forward_tokens(x, q.DT_FP16, ids, rw, out, stream=s)
+        g.replay()
+        torch.cuda.synchronize()
+        samples = []
+        for _ in range(7):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            samples.append(e0.elapsed_time(e1))
+        us = statistics.median(samples) * 1e3 / 20
+        uniq = len({int(i) for i in tok.ids[:M].ravel() if 0 <= i < c.E})
+        res[f"M{M}"] = {"us_per_call": us, "tokens_per_s": M / (us * 1e-6), "unique_experts": uniq,
+                        "gbs_unique_bytes": uniq * per_exp / (us * 1e-6) / 1e9}
+        del g
+    moe.check()
+    moe.close()
+    return res
+
+
 def bench_prefill(M, reps, pk, fmt="nvfp4"):
     import torch
     import weight_quantized_swiglu_gb300 as q
@@ -544,6 +591,7 @@ def main():
         if "moe" in want:
             extras["moe_awq_m1_4B"] = bench_moe(4)
             extras["moe_awq_m1_3B"] = bench_moe(3)
+            extras["moe_awq_tokens_4B"] = bench_moe_tokens()
         if "prefill" in want:
             for fmt in ("nvfp4", "fp8"):
                 try:

@@ -222,6 +222,33 @@ qmlp_status qmlp_moe_debug_stages(qmlp_moe_t* h, const void* x, qmlp_dtype xdt,
                                   const int32_t* expert_ids, const float* router_w, int topk,
                                   void* out, void* gu, void* act, void* y, qmlp_stream_t stream);
 
+/* Reserve the workspace of multi-token calls: after this, qmlp_moe_forward
+ * accepts 1 <= M <= max_tokens (routes = M * topk <= max_tokens * 16). Sizes
+ * the handle-owned fp16 intermediates for max_tokens * 16 routes (act [.., I],
+ * y [.., K]) plus the route and group lists; a larger later reservation adds
+ * a larger workspace (the old one is freed by destroy). Allocates and
+ * synchronizes the stream: call it before capturing graphs. A handle starts
+ * with max_tokens = 1. Limits: K <= 8192 and E <= 8192 for M > 1.
+ * Errors: INVALID_ARG, SHAPE, OOM, CUDA. */
+qmlp_status qmlp_moe_reserve(qmlp_moe_t* h, int max_tokens, qmlp_stream_t stream);
+
+/* The routed-expert step for M tokens, every token independently exactly as
+ * qmlp_moe_m1_forward computes it (the source PR defines the one-token
+ * operator; tokens do not interact):
+ *  x          = device [M, K], bf16 or fp16 per xdt (row-major)
+ *  expert_ids = device int32 [M, topk] (token t's routes in router order)
+ *  router_w   = device fp32 [M, topk]
+ *  out        = device fp16 [M, K]
+ * M == 1 runs the one-token kernels. For M > 1 the valid routes of all tokens
+ * are sorted by expert on the device and tokens that share an expert share
+ * its weight reads (groups of up to 8 routes); results do not depend on the
+ * grouping and are the same bytes every call. 1 <= topk <= 16,
+ * 1 <= M <= the reserved max_tokens. Allocates nothing; graph-capturable.
+ * Errors: INVALID_ARG, ALIGNMENT, ALIAS (out overlaps x, ids or router_w),
+ * SHAPE, CUDA. */
+qmlp_status qmlp_moe_forward(qmlp_moe_t* h, const void* x, qmlp_dtype xdt, const int32_t* expert_ids,
+                             const float* router_w, int topk, int M, void* out, qmlp_stream_t stream);
+
 qmlp_status qmlp_moe_check(qmlp_moe_t* h, qmlp_stream_t stream);
 
 /* The routed-expert step of qmlp_moe_m1_forward without a handle, for callers
@@ -250,7 +277,7 @@ qmlp_status qmlp_moe_m1_forward_noalloc(const qmlp_moe_desc* banks, const void* 
 /* Human-readable name of a status ("QMLP_OK", ...). Never NULL. */
 const char* qmlp_status_str(qmlp_status s);
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor): 101 (multi-token routed experts). */
 int qmlp_abi_version(void);
 
 #ifdef __cplusplus

@@ -74,6 +74,8 @@ _SIGS = {
     "qmlp_moe_m1_forward": ([_VP, _VP, _I, _VP, _VP, _I, _VP, _VP], _I),
     "qmlp_moe_debug_stages": ([_VP, _VP, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _VP], _I),
     "qmlp_moe_check": ([_VP, _VP], _I),
+    "qmlp_moe_reserve": ([_VP, _I, _VP], _I),
+    "qmlp_moe_forward": ([_VP, _VP, _I, _VP, _VP, _I, _I, _VP, _VP], _I),
     "qmlp_moe_m1_forward_noalloc": ([ctypes.POINTER(qmlp_moe_desc), _VP, _I, _VP, _VP, _I, _VP, _VP], _I),
     "qmlp_status_str": ([_I], ctypes.c_char_p),
     "qmlp_abi_version": ([], _I),
@@ -193,6 +195,14 @@ def qmlp_moe_debug_stages(h, x, xdt, ids, rw, topk, out, gu, act, y, stream=None
                                        _ptr(act), _ptr(y), _stream(stream))
 
 
+def qmlp_moe_reserve(h, max_tokens, stream=None) -> int:
+    return lib().qmlp_moe_reserve(h, max_tokens, _stream(stream))
+
+
+def qmlp_moe_forward(h, x, xdt, ids, rw, topk, M, out, stream=None) -> int:
+    return lib().qmlp_moe_forward(h, _ptr(x), xdt, _ptr(ids), _ptr(rw), topk, M, _ptr(out), _stream(stream))
+
+
 def qmlp_moe_check(h, stream=None) -> int:
     return lib().qmlp_moe_check(h, _stream(stream))
 
@@ -278,7 +288,7 @@ class QuantMLP:
 
 
 class MoeAWQ:
-    """Routed-expert AWQ int4 g32 handle (M = 1)."""
+    """Routed-expert AWQ int4 g32 handle (one token; M tokens after reserve())."""
 
     def __init__(self, E, K, I, meta_bytes, w13, w13_meta, w2, w2_meta, stream=None):
         self.E, self.K, self.I, self.meta = E, K, I, meta_bytes
@@ -295,6 +305,15 @@ class MoeAWQ:
     def forward(self, x, xdt, ids, rw, out, topk=None, stream=None):
         topk = ids.shape[0] if topk is None else topk
         _chk(qmlp_moe_m1_forward(self.h, x, xdt, ids, rw, topk, out, stream), "qmlp_moe_m1_forward")
+        return out
+
+    def reserve(self, max_tokens, stream=None):
+        _chk(qmlp_moe_reserve(self.h, max_tokens, stream), "qmlp_moe_reserve")
+
+    def forward_tokens(self, x, xdt, ids, rw, out, stream=None):
+        """M tokens: x [M, K], ids / rw [M, topk], out [M, K]."""
+        M, topk = ids.shape
+        _chk(qmlp_moe_forward(self.h, x, xdt, ids, rw, topk, M, out, stream), "qmlp_moe_forward")
         return out
 
     def debug_stages(self, x, xdt, ids, rw, out, gu=None, act=None, y=None, topk=None, stream=None):

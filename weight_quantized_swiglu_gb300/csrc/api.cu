@@ -103,6 +103,13 @@ struct qmlp_moe_s {
     uint8_t *w13 = nullptr, *w13_meta = nullptr, *w2 = nullptr, *w2_meta = nullptr;
     __half* act_ws = nullptr;
     int* err = nullptr;
+    // multi-token workspace (qmlp_moe_reserve): routes = max_tokens * 16
+    int max_tokens = 1;
+    __half* g_act = nullptr;   // [routes, I]
+    __half* g_y = nullptr;     // [routes, K]
+    int* g_route = nullptr;    // [routes]
+    int4* g_groups = nullptr;  // [moe_grouped_max_groups(routes, E)]
+    int* g_ngroups = nullptr;
     Owner mem;
 };
 
@@ -123,7 +130,7 @@ const char* qmlp_status_str(qmlp_status s) {
     return "QMLP_ERR_UNKNOWN";
 }
 
-int qmlp_abi_version(void) { return 100; }
+int qmlp_abi_version(void) { return 101; }
 
 // ---------------------------------------------------------------------------
 // dense MLP
@@ -743,6 +750,75 @@ qmlp_status qmlp_moe_debug_stages(qmlp_moe_t* h, const void* x, qmlp_dtype xdt, 
                                   const float* rw, int topk, void* out, void* gu, void* act, void* y,
                                   qmlp_stream_t stream) {
     return moe_run(h, x, xdt, ids, rw, topk, out, gu, act, y, stream);
+}
+
+qmlp_status qmlp_moe_reserve(qmlp_moe_t* h, int max_tokens, qmlp_stream_t stream) {
+    if (!h) return QMLP_ERR_INVALID_ARG;
+    if (max_tokens < 1 || max_tokens > (1 << 20)) return QMLP_ERR_SHAPE;
+    if (max_tokens <= h->max_tokens) return QMLP_OK;
+    if (h->K > kMoeGroupedMaxK || h->E > kMoeGroupedMaxE) return QMLP_ERR_SHAPE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QMLP_ERR_CUDA;
+    const size_t routes = (size_t)max_tokens * 16;
+    void *act = nullptr, *y = nullptr, *rl = nullptr, *gr = nullptr, *ng = nullptr;
+    cudaError_t e;
+    if ((e = h->mem.alloc(&act, routes * h->I * sizeof(__half))) != cudaSuccess ||
+        (e = h->mem.alloc(&y, routes * h->K * sizeof(__half))) != cudaSuccess ||
+        (e = h->mem.alloc(&rl, routes * sizeof(int))) != cudaSuccess ||
+        (e = h->mem.alloc(&gr, moe_grouped_max_groups((int)routes, h->E) * sizeof(int4))) != cudaSuccess ||
+        (e = h->mem.alloc(&ng, 16)) != cudaSuccess) {
+        for (void* p : {act, y, rl, gr, ng}) {
+            auto it = std::find(h->mem.ptrs.begin(), h->mem.ptrs.end(), p);
+            if (p && it != h->mem.ptrs.end()) {
+                cudaFree(p);
+                h->mem.ptrs.erase(it);
+            }
+        }
+        return from_cuda(e);
+    }
+    // the previous (smaller) workspace stays owned by the handle until destroy
+    h->g_act = static_cast<__half*>(act);
+    h->g_y = static_cast<__half*>(y);
+    h->g_route = static_cast<int*>(rl);
+    h->g_groups = static_cast<int4*>(gr);
+    h->g_ngroups = static_cast<int*>(ng);
+    h->max_tokens = max_tokens;
+    return QMLP_OK;
+}
+
+qmlp_status qmlp_moe_forward(qmlp_moe_t* h, const void* x, qmlp_dtype xdt, const int32_t* ids, const float* rw,
+                             int topk, int M, void* out, qmlp_stream_t stream) {
+    if (!h || !x || !ids || !rw || !out) return QMLP_ERR_INVALID_ARG;
+    if (M < 1 || M > h->max_tokens) return QMLP_ERR_SHAPE;
+    if (M == 1) return moe_run(h, x, xdt, ids, rw, topk, out, nullptr, nullptr, nullptr, stream);
+    if (xdt != QMLP_DT_BF16 && xdt != QMLP_DT_FP16) return QMLP_ERR_INVALID_ARG;
+    if (topk < 1 || topk > 16) return QMLP_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(ids) || !aligned16(rw)) return QMLP_ERR_ALIGNMENT;
+    const size_t xb = (size_t)M * h->K * 2, rb = (size_t)M * topk * 4;
+    if (overlaps(out, xb, x, xb) || overlaps(out, xb, ids, rb) || overlaps(out, xb, rw, rb)) return QMLP_ERR_ALIAS;
+    if (fault("launch")) return QMLP_ERR_CUDA;
+    MoeGroupedLaunch L;
+    L.E = h->E;
+    L.K = h->K;
+    L.I = h->I;
+    L.meta_bytes = h->meta;
+    L.M = M;
+    L.topk = topk;
+    L.w13 = h->w13;
+    L.w13_meta = h->w13_meta;
+    L.w2 = h->w2;
+    L.w2_meta = h->w2_meta;
+    L.x = x;
+    L.x_is_bf16 = xdt == QMLP_DT_BF16;
+    L.ids = ids;
+    L.rw = rw;
+    L.out = static_cast<__half*>(out);
+    L.act_ws = h->g_act;
+    L.y_ws = h->g_y;
+    L.route_list = h->g_route;
+    L.groups = h->g_groups;
+    L.n_groups = h->g_ngroups;
+    return launch_moe_grouped(L, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMLP_OK : QMLP_ERR_CUDA;
 }
 
 qmlp_status qmlp_moe_check(qmlp_moe_t* h, qmlp_stream_t stream) {

@@ -184,6 +184,29 @@ struct MoeLaunch {
     __half* y_dbg;            // optional [topk][K]
 };
 cudaError_t launch_moe(const MoeLaunch& L, int num_sms, cudaStream_t s);
+
+// M tokens, routes grouped by expert (see moe_grouped.cu).
+constexpr int kMoeGroupedMaxK = 8192;  // x of a group's 8 tokens is staged in shared memory
+constexpr int kMoeGroupedMaxE = 8192;  // the routing CTA keeps 4 ints per expert in shared memory
+struct MoeGroupedLaunch {
+    int E, K, I, meta_bytes, M, topk;
+    const uint8_t* w13;
+    const uint8_t* w13_meta;
+    const uint8_t* w2;
+    const uint8_t* w2_meta;
+    const void* x;                 // [M, K]
+    int x_is_bf16;
+    const int32_t* ids;            // [M, topk]
+    const float* rw;               // [M, topk]
+    __half* out;                   // [M, K]
+    __half* act_ws;                // [>= M*topk, I]
+    __half* y_ws;                  // [>= M*topk, K]
+    int* route_list;               // [>= M*topk]
+    int4* groups;                  // [>= moe_grouped_max_groups(M*topk, E)]
+    int* n_groups;                 // one int
+};
+size_t moe_grouped_max_groups(int routes, int E);
+cudaError_t launch_moe_grouped(const MoeGroupedLaunch& L, cudaStream_t s);
 cudaError_t repack_moe(const uint8_t* w, const uint8_t* meta, int meta_bytes, int E, int N,
                        int Kr, uint8_t* w_out, uint8_t* meta_out, cudaStream_t s);
 

@@ -1,0 +1,555 @@
+// moe_grouped.cu -- routed-expert AWQ int4 group-32 MLP for M tokens.
+//
+// Operation: every token t independently computes the one-token routed
+// expert step (1Cat-vLLM PR "[Kernel][SM70] Add native-g32 AWQ QPN M1
+// operator", "What it does"; the PR leaves grouped decode and prefill out):
+//   for each route r of t in router order with 0 <= ids[t, r] < E:
+//     h       = x[t] . W13[id]^T in fp32; g, u = fp16(h[:I]), fp16(h[I:])
+//     act     = fp16(SiLU(g) * u)
+//     y[t, r] = fp16(act . W2[id]^T) in fp32
+//   out[t] = fp16( sum over valid r, in router order, of rw[t, r] * y[t, r] )
+// with the same half_fma weight decode as the one-token kernels.
+//
+// GB300 design: tokens that share an expert share its weight reads.
+//  * moe_route_kernel (one CTA): counting sort of the valid routes by
+//    expert (shared-memory histogram, scan, scatter) and a list of groups of
+//    at most 8 routes with one expert. The order of the routes inside an
+//    expert's bucket is whatever the atomics give: it does not matter,
+//    because every route is one column of the MMAs below and a column's
+//    result depends on nothing else in the group.
+//  * moe_w13_grouped_kernel: kW13Ctas CTAs per group, each looping over its
+//    share of the 16-row gate/up tile pairs (x staged once per CTA);
+//    the group's tokens are the 8 columns of the m16n8k16 MMAs (A fragments
+//    decoded from the checkpoint layout as in the one-token kernel), each
+//    token prescaled by its own power of two; the K split over 10 warps is
+//    added in a fixed order.
+//  * moe_w2_grouped_kernel: kW2Ctas CTAs per group, each looping over its
+//    share of the 256-row blocks, a warp per 16 rows, the group's act rows
+//    as the MMA columns; y is stored as fp16.
+//  * moe_combine_kernel: one thread per (token, output element) adds the
+//    token's valid routes in router order (fmaf, fp32), like the one-token
+//    W2 stage.
+//  * All four are chained with programmatic dependent launch; a grid sized
+//    for the worst-case group count exits early past the real count.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace qmlp {
+namespace {
+
+constexpr int kGW13 = 10;  // W13 K splits: 2 x kGW13 warps per CTA (gate and up tiles)
+constexpr int kGC13 = 2;   // 64-k chunks a W13 warp loads at once
+constexpr int kGG2 = 10;   // k16 groups a W2 warp loads at once
+constexpr int kCols = 8;   // routes per group (MMA n8)
+constexpr int kRouteThreads = 1024;
+constexpr int kW13Ctas = 2;  // CTAs per group in W13 (each loops over its share of the I/16 tile pairs)
+constexpr int kW2Ctas = 2;   // CTAs per group in W2 (each loops over its share of the 256-row blocks)
+constexpr int kXB = 8;     // x items a thread has in flight while staging a group's tokens
+
+struct GArgs {
+    int E, K, I, M, topk;
+    const uint8_t* w13;
+    const uint8_t* w13_meta;
+    const uint8_t* w2;
+    const uint8_t* w2_meta;
+    const void* x;  // [M, K]
+    int x_is_bf16;
+    int meta_al4;
+    const int32_t* ids;  // [M, topk]
+    const float* rw;     // [M, topk]
+    __half* out;         // [M, K]
+    __half* act_ws;      // [M * topk, I]
+    __half* y_ws;        // [M * topk, K]
+    int* route_list;     // [M * topk]: route indices sorted by expert
+    int4* groups;        // {expert, first position in route_list, count, 0}
+    int* n_groups;
+};
+
+template <int MB>
+QMLP_DEV uint32_t gload_meta(const uint8_t* p, bool al4) {
+    if (MB == 4 && al4) return __ldg(reinterpret_cast<const unsigned int*>(p));
+    uint32_t v = 0;
+#pragma unroll
+    for (int i = 0; i < MB; ++i) v |= (uint32_t)__ldg(p + i) << (8 * i);
+    return v;
+}
+
+// {scale, scale}, {bias, bias} of one record (bias stored, or half(-zero*scale))
+template <int MB>
+QMLP_DEV void gmeta_sb2(uint32_t m, uint32_t& s2, uint32_t& b2) {
+    const uint32_t s = m & 0xFFFFu;
+    uint32_t b;
+    if (MB == 4) {
+        b = m >> 16;
+    } else {
+        const float bf = -(float)((m >> 16) & 0xFFu) * __half2float(__ushort_as_half((unsigned short)s));
+        b = __half_as_ushort(__float2half_rn(bf));
+    }
+    s2 = s | (s << 16);
+    b2 = b | (b << 16);
+}
+
+QMLP_DEV uint32_t ghfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// The byte of w that `sel` picks (two u4 codes, low nibble = earlier k) ->
+// f16x2 {half_fma(q_lo, s, b), half_fma(q_hi, s, b)}: the byte goes to both
+// halves, 0x6400 | q is 1024 + q exactly, one exact HFMA2 gives (q_lo, q_hi),
+// one HFMA2 the single-rounding half_fma.
+QMLP_DEV uint32_t gawq_pair(uint32_t w, uint32_t sel, uint32_t s2, uint32_t b2) {
+    const uint32_t m = __byte_perm(w, 0u, sel);
+    const uint32_t h = (m & 0x00F0000Fu) | 0x64006400u;
+    const uint32_t q = ghfma2(h, 0x2C003C00u, 0xD400E400u);
+    return ghfma2(q, s2, b2);
+}
+QMLP_DEV uint32_t gpair_selector(int t) { return (uint32_t)t | (4u << 4) | ((uint32_t)t << 8) | (4u << 12); }
+
+// ---------------------------------------------------------------------------
+// routing: valid routes sorted by expert, groups of <= 8
+// ---------------------------------------------------------------------------
+// Block-wide exclusive scan of one 64-bit value per thread (kRouteThreads).
+QMLP_DEV unsigned long long block_excl_scan(unsigned long long v, unsigned long long* wsum,
+                                            unsigned long long* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long w = wsum[lane];
+        unsigned long long wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        wsum[lane] = wi - w;  // exclusive prefix of the warp totals
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    return wsum[warp] + inc - v;
+}
+
+__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const GArgs a) {
+    extern __shared__ int rsm[];  // cnt[E], off[E], cur[E], goff[E]
+    __shared__ unsigned long long wsum[32];
+    __shared__ unsigned long long total;
+    int* cnt = rsm;
+    int* off = cnt + a.E;
+    int* cur = off + a.E;
+    int* goff = cur + a.E;
+    pdl_wait();  // the ids and the workspace belong to the kernels before
+    pdl_launch_dependents();
+    const int n = a.M * a.topk;
+    for (int e = threadIdx.x; e < a.E; e += kRouteThreads) {
+        cnt[e] = 0;
+        cur[e] = 0;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kRouteThreads) {
+        const int id = a.ids[i];
+        if (id >= 0 && id < a.E) atomicAdd(&cnt[id], 1);
+    }
+    __syncthreads();
+    // a contiguous chunk of experts per thread: routes and groups, scanned
+    // together (routes in the high word, groups in the low word)
+    const int per = (a.E + kRouteThreads - 1) / kRouteThreads;
+    const int e0 = min(a.E, threadIdx.x * per), e1 = min(a.E, e0 + per);
+    unsigned long long mine = 0;
+    for (int e = e0; e < e1; ++e) mine += ((unsigned long long)cnt[e] << 32) + (unsigned)((cnt[e] + kCols - 1) / kCols);
+    unsigned long long pre = block_excl_scan(mine, wsum, &total);
+    for (int e = e0; e < e1; ++e) {
+        off[e] = (int)(pre >> 32);
+        goff[e] = (int)(pre & 0xFFFFFFFFull);
+        pre += ((unsigned long long)cnt[e] << 32) + (unsigned)((cnt[e] + kCols - 1) / kCols);
+    }
+    if (threadIdx.x == 0) *a.n_groups = (int)(total & 0xFFFFFFFFull);
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kRouteThreads) {
+        const int id = a.ids[i];
+        if (id >= 0 && id < a.E) a.route_list[off[id] + atomicAdd(&cur[id], 1)] = i;
+    }
+    for (int e = e0; e < e1; ++e)
+        for (int j = 0; j * kCols < cnt[e]; ++j)
+            a.groups[goff[e] + j] = make_int4(e, off[e] + j * kCols, min(kCols, cnt[e] - j * kCols), 0);
+}
+
+// ---------------------------------------------------------------------------
+// W13 + SwiGLU for a group of routes sharing one expert
+// ---------------------------------------------------------------------------
+template <int MB>
+__global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const GArgs a) {
+    extern __shared__ __align__(16) uint32_t xs[];  // [kCols][K/2 + 4] fp16 pairs (padded: no bank conflicts)
+    __shared__ float part[2 * kGW13][16][kCols];
+    __shared__ int s_route[kCols];
+    __shared__ int s_max[kCols];
+    __shared__ int s_sig[kCols];
+    pdl_wait();
+    pdl_launch_dependents();
+    if ((int)blockIdx.x >= *a.n_groups) return;
+    const int4 grp = a.groups[blockIdx.x];
+    const int e = grp.x, cnt = grp.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int tile = warp / kGW13, ks = warp % kGW13;
+    const int Kc = a.K / 64, gpr = a.K / 32, N = 2 * a.I;
+    const int cpw = (Kc + kGW13 - 1) / kGW13;
+    const int c0 = ks * cpw, c1 = min(Kc, c0 + cpw);
+    const bool al4 = a.meta_al4 != 0;
+    // this CTA's tile pairs: tp = blockIdx.y, blockIdx.y + gridDim.y, ...
+    const int ntp = a.I / 16;
+    size_t rows[2];
+    auto set_rows = [&](int tp) {
+        rows[0] = (size_t)e * N + tile * a.I + 16 * tp + g;
+        rows[1] = rows[0] + 8;
+    };
+    int tp = blockIdx.y;
+    set_rows(tp);
+    uint4 cw[kGC13][2][2];
+    uint32_t mw[kGC13][2][2];
+    auto load_batch = [&](int cb) {
+#pragma unroll
+        for (int i = 0; i < kGC13; ++i) {
+            const int c = cb + i;
+            if (c < c1) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint4* src = reinterpret_cast<const uint4*>(a.w13 + rows[q] * (a.K / 2) + c * 32);
+                    cw[i][q][0] = __ldg(src);
+                    cw[i][q][1] = __ldg(src + 1);
+                    const uint8_t* m = a.w13_meta + (rows[q] * gpr + 2 * c) * MB;
+                    mw[i][q][0] = gload_meta<MB>(m, al4);
+                    mw[i][q][1] = gload_meta<MB>(m + MB, al4);
+                }
+            }
+        }
+    };
+    load_batch(c0);  // the first codes are in flight while x is staged
+
+    // the group's tokens -> fp16 pairs, each token times its own 2^sig.
+    // Items (slot c, pair k2) are spread over the CTA, kXB loads in flight
+    // per thread; bf16 input takes one pass for the per-token maxima and
+    // one to convert.
+    const int xstride = a.K / 2 + 4;
+    if (threadIdx.x < kCols) {
+        s_route[threadIdx.x] = threadIdx.x < cnt ? a.route_list[grp.y + threadIdx.x] : -1;
+        s_max[threadIdx.x] = 0;
+    }
+    __syncthreads();
+    const uint32_t* xin = reinterpret_cast<const uint32_t*>(a.x);
+    const int kh = a.K / 2, items = kCols * kh, nth = blockDim.x;
+    auto load_items = [&](int base, uint32_t (&v)[kXB]) {
+#pragma unroll
+        for (int i = 0; i < kXB; ++i) {
+            const int idx = base + i * nth;
+            const int c = idx / kh;
+            v[i] = (idx < items && c < cnt) ? xin[(size_t)(s_route[c] / a.topk) * kh + (idx - c * kh)] : 0u;
+        }
+    };
+    if (a.x_is_bf16) {
+        float mx[kCols];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) mx[c] = 0.0f;
+        for (int base = threadIdx.x; base < items; base += kXB * nth) {
+            uint32_t v[kXB];
+            load_items(base, v);
+#pragma unroll
+            for (int i = 0; i < kXB; ++i) {
+                const int c = min(kCols - 1, (base + i * nth) / kh);
+                const float m2 = fmaxf(fabsf(__uint_as_float(v[i] << 16)), fabsf(__uint_as_float(v[i] & 0xFFFF0000u)));
+#pragma unroll
+                for (int cc = 0; cc < kCols; ++cc)
+                    if (cc == c) mx[cc] = fmaxf(mx[cc], m2);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+            float m = mx[c];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0 && m > 0.0f) atomicMax(&s_max[c], __float_as_int(m));
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x < kCols) s_sig[threadIdx.x] = a.x_is_bf16 ? prescale_exponent(__int_as_float(s_max[threadIdx.x])) : 0;
+    __syncthreads();
+    for (int base = threadIdx.x; base < items; base += kXB * nth) {
+        uint32_t v[kXB];
+        load_items(base, v);
+#pragma unroll
+        for (int i = 0; i < kXB; ++i) {
+            const int idx = base + i * nth;
+            if (idx < items) {
+                const int c = idx / kh, k2 = idx - c * kh;
+                uint32_t o = v[i];
+                if (a.x_is_bf16 && c < cnt) {
+                    const int sg = s_sig[c];
+                    const __half2 h = __floats2half2_rn(scalbnf(__uint_as_float(o << 16), sg),
+                                                        scalbnf(__uint_as_float(o & 0xFFFF0000u), sg));
+                    o = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                xs[c * xstride + k2] = o;
+            }
+        }
+    }
+    __syncthreads();
+
+    const uint32_t sel = gpair_selector(t);
+    const uint32_t* xcol = xs + g * xstride;  // this lane's MMA column = route slot g
+    for (; tp < ntp; tp += gridDim.y) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int cb = c0; cb < c1; cb += kGC13) {
+            if (cb != c0) load_batch(cb);
+#pragma unroll
+            for (int i = 0; i < kGC13; ++i) {
+                const int c = cb + i;
+                if (c < c1) {
+                    uint32_t s2[2][2], b2[2][2];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        gmeta_sb2<MB>(mw[i][q][0], s2[q][0], b2[q][0]);
+                        gmeta_sb2<MB>(mw[i][q][1], s2[q][1], b2[q][1]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int h = j >> 1;
+                        const uint32_t wa0 = (j & 1) ? cw[i][0][h].z : cw[i][0][h].x;
+                        const uint32_t wb0 = (j & 1) ? cw[i][0][h].w : cw[i][0][h].y;
+                        const uint32_t wa1 = (j & 1) ? cw[i][1][h].z : cw[i][1][h].x;
+                        const uint32_t wb1 = (j & 1) ? cw[i][1][h].w : cw[i][1][h].y;
+                        const int k2 = (c * 64 + 16 * j) / 2 + t;
+                        mma_f16_16816(d, gawq_pair(wa0, sel, s2[0][h], b2[0][h]),
+                                      gawq_pair(wa1, sel, s2[1][h], b2[1][h]), gawq_pair(wb0, sel, s2[0][h], b2[0][h]),
+                                      gawq_pair(wb1, sel, s2[1][h], b2[1][h]), xcol[k2], xcol[k2 + 4]);
+                    }
+                }
+            }
+        }
+        // C fragment: (row g, cols 2t, 2t+1) and (row g+8, the same cols)
+        part[warp][g][2 * t] = d[0];
+        part[warp][g][2 * t + 1] = d[1];
+        part[warp][g + 8][2 * t] = d[2];
+        part[warp][g + 8][2 * t + 1] = d[3];
+        // the next tile pair's first codes go out before the reduction
+        if (tp + (int)gridDim.y < ntp) {
+            set_rows(tp + gridDim.y);
+            load_batch(c0);
+        }
+        __syncthreads();
+        if (threadIdx.x < 16 * kCols) {
+            const int j = threadIdx.x / kCols, c = threadIdx.x % kCols;
+            if (c < cnt) {
+                float hg = 0.0f, hu = 0.0f;
+                for (int w = 0; w < kGW13; ++w) {
+                    hg += part[w][j][c];
+                    hu += part[kGW13 + w][j][c];
+                }
+                const int sg = s_sig[c];
+                const __half gh = __float2half_rn(scalbnf(hg, -sg)), uh = __float2half_rn(scalbnf(hu, -sg));
+                a.act_ws[(size_t)s_route[c] * a.I + 16 * tp + j] =
+                    __float2half_rn(silu_f32(__half2float(gh)) * __half2float(uh));
+            }
+        }
+        __syncthreads();  // part is rewritten by the next tile pair
+    }
+}
+
+// ---------------------------------------------------------------------------
+// W2 for a group of routes sharing one expert -> y (fp16)
+// ---------------------------------------------------------------------------
+template <int MB>
+__global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) {
+    extern __shared__ __align__(16) uint32_t acts[];  // [kCols][I/2 + 4]
+    __shared__ int s_route[kCols];
+    pdl_wait();
+    pdl_launch_dependents();
+    if ((int)blockIdx.x >= *a.n_groups) return;
+    const int4 grp = a.groups[blockIdx.x];
+    const int e = grp.x, cnt = grp.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int astride = a.I / 2 + 4;
+    if (threadIdx.x < kCols) s_route[threadIdx.x] = threadIdx.x < cnt ? a.route_list[grp.y + threadIdx.x] : -1;
+    __syncthreads();
+    {
+        // the group's act rows, all of a thread's loads in flight together
+        const int ih = a.I / 2, items = kCols * ih, nth = blockDim.x;
+        const uint32_t* act32 = reinterpret_cast<const uint32_t*>(a.act_ws);
+        for (int base = threadIdx.x; base < items; base += kXB * nth) {
+            uint32_t v[kXB];
+#pragma unroll
+            for (int i = 0; i < kXB; ++i) {
+                const int idx = base + i * nth, c = idx / ih;
+                v[i] = (idx < items && c < cnt) ? act32[(size_t)s_route[c] * ih + (idx - c * ih)] : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < kXB; ++i) {
+                const int idx = base + i * nth;
+                if (idx < items) acts[(idx / ih) * astride + idx % ih] = v[i];
+            }
+        }
+    }
+    __syncthreads();
+    const int ng = a.I / 16, gpr = a.I / 32;
+    const bool al4 = a.meta_al4 != 0;
+    const uint32_t sel = gpair_selector(t);
+    const uint32_t* xcol = acts + g * astride;
+    // this CTA's 256-row blocks; warps are independent from here (no barrier)
+    for (int nb = blockIdx.y; 256 * nb < a.K; nb += gridDim.y) {
+    const int n0 = 256 * nb + 16 * warp;
+    if (n0 >= a.K) continue;
+    const size_t row0 = (size_t)e * a.K + n0 + g;
+    const uint2* c0p = reinterpret_cast<const uint2*>(a.w2 + row0 * (a.I / 2));
+    const uint2* c8p = reinterpret_cast<const uint2*>(a.w2 + (row0 + 8) * (a.I / 2));
+    const uint8_t* m0p = a.w2_meta + row0 * gpr * MB;
+    const uint8_t* m8p = a.w2_meta + (row0 + 8) * gpr * MB;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int gb = 0; gb < ng; gb += kGG2) {
+        uint2 cw[kGG2][2];
+        uint32_t mw[kGG2 / 2][2];
+#pragma unroll
+        for (int i = 0; i < kGG2; ++i) {
+            if (gb + i < ng) {
+                cw[i][0] = __ldg(c0p + gb + i);
+                cw[i][1] = __ldg(c8p + gb + i);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kGG2 / 2; ++i) {
+            const int ag = gb / 2 + i;
+            if (ag < gpr) {
+                mw[i][0] = gload_meta<MB>(m0p + (size_t)ag * MB, al4);
+                mw[i][1] = gload_meta<MB>(m8p + (size_t)ag * MB, al4);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kGG2; ++i) {
+            const int j = gb + i;
+            if (j < ng) {
+                uint32_t s0, b0, s8, b8;
+                gmeta_sb2<MB>(mw[i / 2][0], s0, b0);
+                gmeta_sb2<MB>(mw[i / 2][1], s8, b8);
+                mma_f16_16816(d, gawq_pair(cw[i][0].x, sel, s0, b0), gawq_pair(cw[i][1].x, sel, s8, b8),
+                              gawq_pair(cw[i][0].y, sel, s0, b0), gawq_pair(cw[i][1].y, sel, s8, b8),
+                              xcol[8 * j + t], xcol[8 * j + 4 + t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int c = 2 * t + (q & 1), row = n0 + g + 8 * (q >> 1);
+        if (c < cnt) a.y_ws[(size_t)s_route[c] * a.K + row] = __float2half_rn(d[q]);
+    }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// ordered router-weighted sum per token
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) moe_combine_kernel(const GArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tok = blockIdx.x, n = 256 * blockIdx.y + threadIdx.x;
+    if (n >= a.K) return;
+    // every load first (an invalid route's y slot is read and ignored),
+    // then the sum in router order
+    int id[16];
+    float w[16];
+    __half y[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        if (r < a.topk) {
+            const int i = tok * a.topk + r;
+            id[r] = a.ids[i];
+            w[r] = a.rw[i];
+            y[r] = a.y_ws[(size_t)i * a.K + n];
+        }
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+        if (r < a.topk && id[r] >= 0 && id[r] < a.E) s = fmaf(w[r], __half2float(y[r]), s);
+    a.out[(size_t)tok * a.K + n] = __float2half_rn(s);
+}
+
+cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* at) {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = grid;
+    c.blockDim = block;
+    c.dynamicSmemBytes = smem;
+    c.stream = s;
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    c.attrs = at;
+    c.numAttrs = 1;
+    return c;
+}
+
+template <int MB>
+cudaError_t launch_grouped_mb(const GArgs& a, int gmax, cudaStream_t s) {
+    const size_t rsmem = (size_t)4 * a.E * sizeof(int);
+    const size_t xsmem = (size_t)kCols * (a.K / 2 + 4) * 4;
+    const size_t asmem = (size_t)kCols * (a.I / 2 + 4) * 4;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kMoeGroupedMaxE * 4 * (int)sizeof(int));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe_w13_grouped_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kCols * (kMoeGroupedMaxK / 2 + 4) * 4);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t c = pdl_cfg(dim3(1), dim3(kRouteThreads), rsmem, s, at);
+    cudaError_t e = cudaLaunchKernelEx(&c, moe_route_kernel, a);
+    if (e != cudaSuccess) return e;
+    c = pdl_cfg(dim3(gmax, std::min(a.I / 16, kW13Ctas)), dim3(2 * kGW13 * 32), xsmem, s, at);
+    if ((e = cudaLaunchKernelEx(&c, moe_w13_grouped_kernel<MB>, a)) != cudaSuccess) return e;
+    c = pdl_cfg(dim3(gmax, std::min((a.K + 255) / 256, kW2Ctas)), dim3(16 * 32), asmem, s, at);
+    if ((e = cudaLaunchKernelEx(&c, moe_w2_grouped_kernel<MB>, a)) != cudaSuccess) return e;
+    c = pdl_cfg(dim3(a.M, (a.K + 255) / 256), dim3(256), 0, s, at);
+    return cudaLaunchKernelEx(&c, moe_combine_kernel, a);
+}
+
+}  // namespace
+
+size_t moe_grouped_max_groups(int routes, int E) { return (size_t)routes / kCols + 1 + (size_t)std::min(E, routes); }
+
+cudaError_t launch_moe_grouped(const MoeGroupedLaunch& L, cudaStream_t s) {
+    if (L.M < 1 || L.topk < 1 || L.topk > 16 || L.K % 64 || L.I % 32 || L.K > kMoeGroupedMaxK ||
+        L.E > kMoeGroupedMaxE || L.E < 1)
+        return cudaErrorInvalidValue;
+    GArgs a;
+    a.E = L.E;
+    a.K = L.K;
+    a.I = L.I;
+    a.M = L.M;
+    a.topk = L.topk;
+    a.w13 = L.w13;
+    a.w13_meta = L.w13_meta;
+    a.w2 = L.w2;
+    a.w2_meta = L.w2_meta;
+    a.x = L.x;
+    a.x_is_bf16 = L.x_is_bf16;
+    a.meta_al4 = ((reinterpret_cast<uintptr_t>(L.w13_meta) | reinterpret_cast<uintptr_t>(L.w2_meta)) & 3u) == 0;
+    a.ids = L.ids;
+    a.rw = L.rw;
+    a.out = L.out;
+    a.act_ws = L.act_ws;
+    a.y_ws = L.y_ws;
+    a.route_list = L.route_list;
+    a.groups = L.groups;
+    a.n_groups = L.n_groups;
+    const int gmax = (int)moe_grouped_max_groups(L.M * L.topk, L.E);
+    return L.meta_bytes == 4 ? launch_grouped_mb<4>(a, gmax, s) : launch_grouped_mb<3>(a, gmax, s);
+}
+
+}  // namespace qmlp

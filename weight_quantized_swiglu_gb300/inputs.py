@@ -210,6 +210,41 @@ def gen_moe_case(seed: int, E: int = MOE_E, K: int = MOE_K, I: int = MOE_I, topk
     return MoeCase(E, K, I, topk, w13, m13_4, m13_3, w2, m2_4, m2_3, x16, xb, ids, rw, seed)
 
 
+@dataclass
+class MoeTokens:
+    """M tokens over one expert bank: `case` holds the weights (its one-token
+    fields are token 0's); x16 / xb [M, K] bits, ids [M, topk] int32,
+    rw [M, topk] fp32."""
+    case: MoeCase
+    x16: np.ndarray
+    xb: np.ndarray
+    ids: np.ndarray
+    rw: np.ndarray
+
+    @property
+    def M(self) -> int:
+        return self.ids.shape[0]
+
+
+def gen_moe_tokens(seed: int, M: int, E: int = MOE_E, K: int = MOE_K, I: int = MOE_I, topk: int = MOE_TOPK,
+                   n_invalid: int = 1, n_dup: int = 1) -> MoeTokens:
+    """x [M, K] first, then the weights, then every token's routes in token
+    order (each token: the one-token recipe -- distinct ids, duplicates and
+    invalid ids at seeded positions, softmax router weights)."""
+    rng = np.random.default_rng(seed)
+    xf = rng.standard_normal((M, K), dtype=np.float32)
+    x16 = f32_to_fp16_bits(xf)
+    xb = f32_to_bf16_bits(xf)
+    w13, m13_4, m13_3, w2, m2_4, m2_3 = gen_awq_weights(rng, E, K, I)
+    ids = np.empty((M, topk), dtype=np.int32)
+    rw = np.empty((M, topk), dtype=np.float32)
+    for t in range(M):
+        ids[t], rw[t] = gen_routes(rng, E, topk, n_invalid, n_dup)
+    case = MoeCase(E, K, I, topk, w13, m13_4, m13_3, w2, m2_4, m2_3, x16[0].copy(), xb[0].copy(),
+                   ids[0].copy(), rw[0].copy(), seed)
+    return MoeTokens(case, x16, xb, ids, rw)
+
+
 def rotating_ids(call: int, topk: int = MOE_TOPK, n_experts: int = 480) -> np.ndarray:
     """Ids of call `call` when cycling `n_experts` experts, topk distinct per call."""
     base = (call * topk) % n_experts
