@@ -116,11 +116,14 @@ def test_parity_dense_nvfp4_decode(torch_cuda, variant):
     mlp.close()
 
 
+@pytest.mark.parametrize("path", [q.PATH_AUTO, q.PATH_GEMV])
 @pytest.mark.parametrize("variant", [0, 1])
-def test_parity_dense_fp8_decode(torch_cuda, variant):
+def test_parity_dense_fp8_decode(torch_cuda, variant, path):
+    """M = 1 and 16; at 16 tokens the automatic path is the tensor-core GEMM,
+    so the decode kernels' 16-token pass is also run explicitly."""
     case = case_of("dense_fp8_decode", variant)
     mlp = q.QuantMLP.from_case(case)
-    out, act = run_forward(torch_cuda, mlp, case.x)
+    out, act = run_forward(torch_cuda, mlp, case.x, path=path)
     ref = oracle.dense_forward(case)
     compare(act, ref["act"], what="act")
     compare(out, ref["out"], what="out")

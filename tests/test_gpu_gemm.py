@@ -98,7 +98,40 @@ def test_gemm_parity_tiny(torch_cuda, M, fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M", [9, 40, 128])
+def test_gemm_split_k_parity(torch_cuda, M, fmt):
+    """K=1024, I=2048: at M <= 128 the gate/up GEMM (16 column tiles) runs 2
+    k-splits and the down GEMM (4 column tiles) 4, each writing fp32 partials
+    that a reduce kernel adds in split order; same bytes on every call."""
+    case = gen.gen_dense_case(fmt, 1024, 2048, M, seed=250 + M)
+    mlp = q.QuantMLP.from_case(case, max_M=128)  # GEMM tiles exist when max_M > 16
+    out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM)
+    ref = oracle.dense_forward(case)
+    compare(act, ref["act"], what="act")
+    compare(out, ref["out"], what="out")
+    out2, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM)
+    assert np.array_equal(out, out2)
+    mlp.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_parity_mid_m_27b(torch_cuda, fmt):
+    """K=5120, I=17408 at M = 40 (between the decode batch and the prefill
+    tile): the automatic path is the GEMM with a 7-way split-K down
+    projection; every row against the oracle."""
+    case = gen.gen_dense_case(fmt, gen.DENSE_K, gen.DENSE_I, 40, seed=260)
+    mlp = q.QuantMLP.from_case(case)
+    out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
+    ref = oracle.dense_forward(case)
+    compare(act, ref["act"], what="act")
+    compare(out, ref["out"], what="out")
+    mlp.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 def test_gemm_is_the_automatic_path_above_16_tokens(torch_cuda, fmt):
+    """(The tiny shape has no I partition: its decode path takes 16 tokens
+    per pass, and the GEMM starts at 17.)"""
     case = gen.gen_dense_case(fmt, TK, TI, 40, seed=230)
     mlp = q.QuantMLP.from_case(case)
     auto, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)

@@ -86,6 +86,7 @@ struct qmlp_s {
     bool has_gemm = false;
     GemmProj gm_gu, gm_d;
     void* a16 = nullptr;       // fp16 [max_M, max(K, I)] (GEMM prescaled activations)
+    float* gemm_ws = nullptr;  // split-K partials of the GEMM (small M)
     int* sig = nullptr;        // [max_M] per-token prescale exponents
     void* act = nullptr;       // bf16 [max_M, I]
     float* part = nullptr;     // split-K partials
@@ -97,6 +98,13 @@ struct qmlp_s {
     void* out_stage = nullptr; // bf16 [max_M, K]
     Owner mem;
 };
+
+// Fewest tokens the automatic path sends to the tensor-core GEMM. Measured on
+// the 27B-class shape (K=5120, I=17408): the single-launch decode kernel
+// takes 59 / 71 us (NVFP4 / FP8) at 8 tokens, but a second 8-token launch
+// for M = 9..16 (106-142 us) loses to the split-K GEMM (87-117 us). Shapes
+// without the I partition decode 16 tokens per stream-K pass.
+static int gemm_min_m(const qmlp_s* h) { return h->sp.G ? kMaxSplitM + 1 : kMaxGemvM + 1; }
 
 struct qmlp_moe_s {
     int E = 0, K = 0, I = 0, meta = 0, device = 0, num_sms = 0;
@@ -237,7 +245,7 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
         }
     }
 
-    if (st == QMLP_OK && d->max_M > kMaxGemvM && gemm_supported(d->K, 2 * d->I) && gemm_supported(d->I, d->K)) {
+    if (st == QMLP_OK && d->max_M >= gemm_min_m(h) && gemm_supported(d->K, 2 * d->I) && gemm_supported(d->I, d->K)) {
         void *gu = nullptr, *dn = nullptr;
         const bool nv = h->fmt == kNVFP4;
         if ((e = h->mem.alloc(&gu, gemm_tiles_bytes(h->fmt, 2 * d->I, d->K))) != cudaSuccess) st = from_cuda(e);
@@ -271,6 +279,9 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
             // the per-token exponents
             const size_t cols = (size_t)std::max(d->K, d->I);
             if ((e = h->mem.alloc(&h->a16, (size_t)d->max_M * cols * 2)) != cudaSuccess) st = from_cuda(e);
+            else if ((e = h->mem.alloc(reinterpret_cast<void**>(&h->gemm_ws),
+                                       gemm_splitk_ws_elems(sms) * sizeof(float))) != cudaSuccess)
+                st = from_cuda(e);
             else if ((e = h->mem.alloc(reinterpret_cast<void**>(&h->sig), (size_t)d->max_M * sizeof(int))) !=
                      cudaSuccess)
                 st = from_cuda(e);
@@ -342,7 +353,7 @@ static qmlp_status validate_fwd(qmlp_t* h, const void* x, int M, const void* out
 static bool use_gemm(qmlp_t* h, qmlp_path path, int M) {
     if (path == QMLP_PATH_GEMV) return false;
     if (path == QMLP_PATH_GEMM) return true;
-    return h->has_gemm && M > kMaxGemvM;
+    return h->has_gemm && M >= gemm_min_m(h);
 }
 
 // stage bit 0: gate/up + SwiGLU (x -> workspace act); bit 1: down (act -> out)
@@ -357,6 +368,7 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
         g.err = h->err;
         g.a16 = h->a16;
         g.sig = h->sig;
+        g.ws = h->gemm_ws;
         if (stages & 1) {
             g.epi = kEpiSwiGLU;
             g.w = h->gm_gu;

@@ -74,6 +74,7 @@ constexpr int raw_bytes() { return FMT == kNVFP4 ? kRawCodes + BN * (BK / 16) : 
 template <int FMT>
 constexpr int lstages() { return FMT == kNVFP4 ? 6 : 5; }
 constexpr int kEpiWarps = 4;
+constexpr int kMaxSplits = 16;          // split-K ways at most (a split keeps >= 8 k-steps)
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kThreads = (2 + kEpiWarps + kDecWarps) * 32;  // 448
@@ -109,6 +110,8 @@ struct Args {
     const int* sig;        // [M] per-token prescale exponent
     void* out;             // bf16 [M, N_out] or fp32 [M, N_out]
     int ldo;               // out row length (elements)
+    int splits;            // k-range splits per tile (1: the epilogue above; > 1: fp32 partials to ws)
+    float* ws;             // [splits][M][N] fp32 partial sums (splits > 1)
     int* err;
 };
 
@@ -282,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int Nt = a.N / BN;
     const int KS = a.Kd / BK;
     const int tiles = Mt * Nt;
+    const int units = tiles * a.splits;  // (tile, k-range) work units, k-range-minor
+    auto ks_begin = [&](int sp) { return (int)(((long)sp * KS) / a.splits); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kLStages; ++s) {
@@ -312,10 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&amap)) : "memory");
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const int t = u / a.splits, sp = u % a.splits;
                 const int nt = t / Mt, mt = t % Mt;
                 const uint8_t* blk = a.tiles + (size_t)nt * KS * kRawBytes;
-                for (int ks = 0; ks < KS; ++ks, ++it) {
+                for (int ks = ks_begin(sp); ks < ks_begin(sp + 1); ++ks, ++it) {
                     const int s = it % kLStages;
                     if (it >= kLStages &&
                         !wait_or_abort(empty(s), (uint32_t)((it / kLStages - 1) & 1), abort_flag, a.err, 11)) {
@@ -339,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (lane == 0) {
             int it = 0, tc = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++tc) {
+                const int sp = u % a.splits;
                 const int buf = tc & 1, use = tc >> 1;
                 if (use > 0 &&
                     !wait_or_abort(acc_empty(buf), (uint32_t)((use - 1) & 1), abort_flag, a.err, 12)) {
@@ -348,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
-                for (int ks = 0; ks < KS; ++ks, ++it) {
+                const int kb = ks_begin(sp);
+                for (int ks = kb; ks < ks_begin(sp + 1); ++ks, ++it) {
                     const int s = it % kLStages, b = it % kBStages;
                     if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 13) ||
                         !wait_or_abort(bfull(b), (uint32_t)((it / kBStages) & 1), abort_flag, a.err, 14)) {
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         umma_f16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), kIdesc,
-                                 (ks | k) != 0 ? 1u : 0u);
+                                 (ks != kb || k != 0) ? 1u : 0u);
                     }
                     issued = true;
                     umma_commit(empty(s));
@@ -381,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int q = warp & 3;  // TMEM lane quarter of this warp
         const int row_in_tile = q * 32 + lane;
         int tc = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++tc) {
+            const int t = u / a.splits, sp = u % a.splits;
             const int nt = t / Mt, mt = t % Mt;
             const int buf = tc & 1, use = tc >> 1;
             // warp-uniform: the TMEM loads below are .sync.aligned
@@ -392,7 +401,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const bool live = m < a.M;
             const int sg = live ? a.sig[m] : 0;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-            if (a.epi == kEpiSwiGLU) {
+            if (a.splits > 1) {
+                // a k-range of the tile: its fp32 partial, unscaled, in the
+                // GEMM's own column order; the reduce kernel adds the splits
+                // in order and applies the epilogue
+                float* ws = a.ws + ((size_t)sp * a.M + m) * a.N + nt * BN;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    float y[32];
+                    tmem_ld32(tbase + c0, y);
+                    if (live) {
+                        float4* dst = reinterpret_cast<float4*>(ws + c0);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) dst[v] = make_float4(y[4 * v], y[4 * v + 1], y[4 * v + 2], y[4 * v + 3]);
+                    }
+                }
+            } else if (a.epi == kEpiSwiGLU) {
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN / 2; c0 += 32) {
@@ -467,8 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int d = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. kDecThreads-1
         int it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-            for (int ks = 0; ks < KS; ++ks, ++it) {
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int sp = u % a.splits;
+            for (int ks = ks_begin(sp); ks < ks_begin(sp + 1); ++ks, ++it) {
                 const int s = it % kLStages, b = it % kBStages;
                 if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 16) ||
                     (it >= kBStages &&
@@ -495,6 +520,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Split-K: out = epilogue( sum over the splits, in split order, of the fp32
+// partials ) with the tile epilogue's arithmetic (2^-sigma[m], the factor,
+// SiLU for gate/up, bf16). One thread per output element.
+template <int FMT>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const Args a) {
+    const bool swiglu = a.epi == kEpiSwiGLU;
+    const int nout = swiglu ? a.N / 2 : a.N;
+    const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long)a.M * nout) return;
+    const int m = (int)(idx / nout), n = (int)(idx % nout);
+    const int sg = a.sig[m];
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)m * a.ldo + n;
+    const size_t plane = (size_t)a.M * a.N;
+    const float* ws = a.ws + (size_t)m * a.N;
+    if (swiglu) {
+        const int col = (n / (BN / 2)) * BN + n % (BN / 2);  // gate column of the interleaved tile
+        float g = 0.0f, u = 0.0f;
+        for (int sp = 0; sp < a.splits; ++sp) {
+            g += ws[sp * plane + col];
+            u += ws[sp * plane + col + BN / 2];
+        }
+        const float fg = FMT == kNVFP4 ? a.inv0 : a.cs0[n], fu = FMT == kNVFP4 ? a.inv1 : a.cs1[n];
+        const float gv = scalbnf(g, -sg) * fg, uv = scalbnf(u, -sg) * fu;
+        *out = __float2bfloat16_rn(silu_f32(gv) * uv);
+    } else {
+        float y = 0.0f;
+        for (int sp = 0; sp < a.splits; ++sp) y += ws[sp * plane + n];
+        const float f = FMT == kNVFP4 ? a.inv0 : a.cs0[n];
+        *out = __float2bfloat16_rn(scalbnf(y, -sg) * f);
     }
 }
 
@@ -628,10 +685,16 @@ cudaError_t launch_fmt(const CUtensorMap& map, const Args& a, int grid, cudaStre
         attr = true;
     }
     gemm_kernel<FMT><<<grid, kThreads, Smem<FMT>::Bytes, s>>>(map, a);
+    cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess || a.splits == 1) return e;
+    const long n = (long)a.M * (a.epi == kEpiSwiGLU ? a.N / 2 : a.N);
+    splitk_reduce_kernel<FMT><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a);
     return cudaPeekAtLastError();
 }
 
 bool gemm_supported(int K, int N) { return K >= BK && K % BK == 0 && N >= BN && N % BN == 0; }
+
+size_t gemm_splitk_ws_elems(int num_sms) { return (size_t)std::max(num_sms, 1) * BM * BN; }
 
 size_t gemm_tiles_bytes(int fmt, int N, int K) {
     return (size_t)(N / BN) * (K / BK) * (fmt == kNVFP4 ? raw_bytes<kNVFP4>() : raw_bytes<kFP8>());
@@ -697,8 +760,17 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     a.out = L.out;
     a.ldo = L.epi == kEpiSwiGLU ? P.N / 2 : (L.epi == kEpiRaw && P.interleaved ? P.N / 2 : P.N);
     a.err = L.err;
-    const int tiles = ((L.M + BM - 1) / BM) * (P.N / BN);
-    const int grid = std::min(tiles, std::max(num_sms, 1));
+    // Split-K when the tiles cannot fill the GPU (small M, or the down
+    // projection's few column tiles): each (tile, k-range) unit writes fp32
+    // partials and a reduce kernel adds them in split order. The partials
+    // never exceed num_sms tiles' worth: splits * tiles <= num_sms.
+    const int tiles0 = ((L.M + BM - 1) / BM) * (P.N / BN);
+    const int KS = P.K / BK;
+    a.splits = 1;
+    a.ws = L.ws;
+    if (L.ws && L.epi != kEpiRaw && 2 * tiles0 <= num_sms)
+        a.splits = std::max(1, std::min(std::min(num_sms / tiles0, KS / 8), kMaxSplits));
+    const int grid = std::min(tiles0 * a.splits, std::max(num_sms, 1));
     return P.fmt == kFP8 ? launch_fmt<kFP8>(map, a, grid, s) : launch_fmt<kNVFP4>(map, a, grid, s);
 }
 

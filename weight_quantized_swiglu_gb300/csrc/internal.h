@@ -159,8 +159,10 @@ struct GemmLaunch {
     void* a16 = nullptr;      // workspace fp16 [M, K]: prescaled activations
     int* sig = nullptr;       // workspace [M]: per-token prescale exponents
     int* err = nullptr;       // device error word
+    float* ws = nullptr;      // split-K partials, >= gemm_splitk_ws_elems (null: no split-K)
 };
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s);
+size_t gemm_splitk_ws_elems(int num_sms);
 bool gemm_supported(int K, int N);
 
 // ---------------------------------------------------------------------------
