@@ -595,6 +595,7 @@ def main():
         if "prefill" in want:
             for fmt in ("nvfp4", "fp8"):
                 try:
+                    extras[f"{fmt}_mid_M64"] = bench_prefill(64, 5, pk, fmt)
                     extras[f"{fmt}_prefill_M512"] = bench_prefill(512, 5, pk, fmt)
                     extras[f"{fmt}_prefill_M8192"] = bench_prefill(8192, 3, pk, fmt)
                 except q.QmlpError as e:
