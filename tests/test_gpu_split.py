@@ -68,9 +68,10 @@ def test_split_parity(torch_cuda, K, I, fmt, M):
     mlp.close()
 
 
-def test_split_many_calls_keep_the_barrier_aligned(torch_cuda):
-    """200 back-to-back launches (the ticket counter keeps counting) give the
-    same bits as the first, with changing inputs in between."""
+def test_split_many_back_to_back_calls(torch_cuda):
+    """200 back-to-back calls (each call's streaming CTAs start while the
+    previous call's reduce kernel runs) give the same bits as the first,
+    with changing inputs in between."""
     torch = torch_cuda
     K, I = SHAPES[0]
     case = gen.gen_dense_case("nvfp4", K, I, 2, seed=320)

@@ -22,9 +22,17 @@
 //  2. restage the slice as prescaled fp16 fragments, stream the down
 //     records of the slice (every output row tile, Cb = T/4 k-chunks) ->
 //     the CTA's partial out[m, n] over its slice, fp32, to global memory;
-//  3. one grid-wide barrier (a 64-bit ticket counter: one atomic per CTA),
-//     then every CTA reduces a share of the outputs over the G partials in
-//     a fixed order and applies the down scale.
+//  3. either (a) one grid-wide barrier (a 64-bit ticket counter: one
+//     atomic per CTA), then every CTA reduces a share of the outputs over
+//     the G partials in a fixed order and applies the down scale; or (b)
+//     the CTA leaves and a small reduce kernel, launched next, does the same
+//     sums once this grid has completed. (b) lets the next call's CTAs
+//     start as soon as these leave and fill their weight rings before they
+//     wait for the reduce kernel: measured faster where the start of a call
+//     is HBM-bound (FP8: 44.05 vs 44.97 us at M=1; NVFP4 M=4: 45.8 vs 47.0),
+//     slower where the consumers bound it (NVFP4 M=1: 31.0-31.4 vs 30.55 us,
+//     the second grid completion is on its critical path), so (a) serves
+//     NVFP4 M=1 and (b) everything else.
 // The producer warp streams the gate/up records and then the down records
 // without a pause (the down weights do not depend on act), one bulk-async
 // copy per projection and step into a shared-memory ring, as in
@@ -47,7 +55,8 @@ constexpr int kBudget = 220 * 1024;
 constexpr int kBars = 2 * kDepthMax * 8 + 16;  // full, empty, x
 constexpr uint64_t kLimit = 2000000000ull;  // 2 s
 constexpr int kXRawMax = 16 * 1024;  // raw x copied to shared memory up to this size
-constexpr int kPreSteps = 1;                 // weight steps issued before the wait on the previous kernel
+constexpr int kPreStepsBarrier = 1;          // weight steps issued before the wait on the previous kernel:
+constexpr int kPreStepsSep = kDepthMax;      //   schedule (a) / schedule (b) (the whole ring)
 constexpr int kRedLoads = 10;                // partials a warp adds per output: G <= 16 * kRedLoads
 
 struct Args {
@@ -380,7 +389,7 @@ QMLP_DEV unsigned long long ld_acquire_u64(const unsigned long long* p) {
     return v;
 }
 
-template <int FMT, int NT, bool M1>
+template <int FMT, int NT, bool M1, bool SEP>
 __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_constant__ Args a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_maxbits[16];
@@ -437,7 +446,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
             // kPreSteps steps go out before the wait, x right after it, then
             // the rest of the weights. (Measured back to back: one step
             // gains 0.1-0.5 us; two or more delay the x copy behind them.)
-            const int pre = min(min(kPreSteps, a.depth), st.steps);
+            const int pre = min(min(SEP ? kPreStepsSep : kPreStepsBarrier, a.depth), st.steps);
             produce<FMT>(st, r, a.err, 0, pre);
             pdl_wait();
             if (a.xraw_bytes) {
@@ -635,6 +644,9 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         }
     }
     if (!ok && lane == 0) s_fail = 1;
+    // schedule (b): the partials are written (a failed wait is in the error
+    // word); the reduce kernel waits for this grid
+    if (SEP) return;
 
     // ---------------- grid barrier (every CTA arrives exactly once) ----------------
     // The CTA barrier orders every consumer thread's partial stores before
@@ -715,9 +727,66 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     }
 }
 
-template <int FMT, int NT, bool M1>
+// ---------------- schedule (b): reduction over the G partials ----------------
+// One CTA per output unit (token m, 32 columns): warp w adds the partials
+// b = w, w + 8, ... (every load of a lane in flight together), then warp 0
+// adds the 8 warp sums in order and applies the down scale: a fixed order.
+// Small (256 threads, few registers, 1 KB of shared memory), so it sits
+// beside a streaming CTA of the next call on the same SM.
+constexpr int kRedThr = 256;
+constexpr int kRedWarps = kRedThr / 32;
+constexpr int kRedPer = 20;  // partials per lane: G <= kRedWarps * kRedPer
+// <= 48 registers a thread: 8 warps x 48 x 32 beside a streaming CTA's
+// 17 warps x 96 x 32 stay within the SM's 65536 registers
+constexpr int kRedMinBlocks = 5;
+static_assert(kW * kRedLoads <= kRedWarps * kRedPer, "every planned G is reducible");
+
+struct RArgs {
+    const float* part;  // [G][M][K]
+    const float* chsd;  // FP8 down per-channel scales
+    float invd;         // NVFP4 down 1/global
+    __nv_bfloat16* out; // [M, K]
+    int G, M, K;
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kRedThr, kRedMinBlocks) gemv_split_reduce_kernel(const __grid_constant__ RArgs a) {
+    __shared__ float red[kRedWarps][32];
+    // the next kernel may start (its streaming CTAs fill their rings) ...
+    pdl_launch_dependents();
+    // ... while this one waits for every partial of the streaming grid
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units_n = (a.K + 31) / 32, units = a.M * units_n;
+    const size_t bstride = (size_t)a.M * a.K;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int m = u / units_n, n = (u % units_n) * 32 + lane;
+        const float* src = a.part + (size_t)m * a.K + n;
+        float v[kRedPer];
+#pragma unroll
+        for (int i = 0; i < kRedPer; ++i) {
+            const int b = warp + i * kRedWarps;
+            v[i] = (n < a.K && b < a.G) ? __ldcg(src + (size_t)b * bstride) : 0.0f;
+        }
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kRedPer; ++i) s += v[i];
+        red[warp][lane] = s;
+        __syncthreads();
+        if (warp == 0 && n < a.K) {
+            float tot = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kRedWarps; ++w) tot += red[w][lane];
+            const float sd = FMT == kNVFP4 ? a.invd : a.chsd[n];
+            a.out[(size_t)m * a.K + n] = __float2bfloat16_rn(tot * sd);
+        }
+        __syncthreads();
+    }
+}
+
+template <int FMT, int NT, bool M1, bool SEP>
 cudaError_t launch_t(const Args& a, size_t smem, cudaStream_t s) {
-    auto kern = gemv_split_kernel<FMT, NT, M1>;
+    auto kern = gemv_split_kernel<FMT, NT, M1, SEP>;
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBudget);
@@ -803,7 +872,7 @@ SplitPlan plan_split(int fmt, int K, int I, int num_sms) {
 }
 
 bool split_fits(int fmt, int M, int K, const SplitPlan& P) {
-    if (!P.G || M < 1 || M > 16) return false;
+    if (!P.G || M < 1 || M > 8) return false;
     const Layout L = layout_for(fmt, M, K, P);
     // reduction scratch (units per CTA x 16 warps x 32 floats) in the x region
     const size_t units = (size_t)M * ((K + 31) / 32);
@@ -861,14 +930,33 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
     a.xraw_off = lay.xraw;
     // the bulk copy of x needs device memory; host-resident x is staged by loads
     a.xraw_bytes = L.x_in_host ? 0 : lay.xraw_bytes;
-    const int nt = L.M <= 8 ? 1 : 2;
+    // M <= 8 (split_fits): one 8-token MMA tile. Schedule (a) for NVFP4 at
+    // one token, (b) otherwise (see the top of the file).
     const bool m1 = L.M == 1;
-    if (L.fmt == kNVFP4) {
-        if (nt == 2) return launch_t<kNVFP4, 2, false>(a, lay.total, s);
-        return m1 ? launch_t<kNVFP4, 1, true>(a, lay.total, s) : launch_t<kNVFP4, 1, false>(a, lay.total, s);
-    }
-    if (nt == 2) return launch_t<kFP8, 2, false>(a, lay.total, s);
-    return m1 ? launch_t<kFP8, 1, true>(a, lay.total, s) : launch_t<kFP8, 1, false>(a, lay.total, s);
+    if (L.fmt == kNVFP4 && m1) return launch_t<kNVFP4, 1, true, false>(a, lay.total, s);
+    cudaError_t e = L.fmt == kNVFP4 ? launch_t<kNVFP4, 1, false, true>(a, lay.total, s)
+                    : m1            ? launch_t<kFP8, 1, true, true>(a, lay.total, s)
+                                    : launch_t<kFP8, 1, false, true>(a, lay.total, s);
+    if (e != cudaSuccess) return e;
+    RArgs r;
+    r.part = L.part;
+    r.chsd = L.chsd;
+    r.invd = L.invd;
+    r.out = static_cast<__nv_bfloat16*>(L.out);
+    r.G = P.G;
+    r.M = L.M;
+    r.K = L.K;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(L.M * ((L.K + 31) / 32)));
+    cfg.blockDim = dim3(kRedThr);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return L.fmt == kNVFP4 ? cudaLaunchKernelEx(&cfg, gemv_split_reduce_kernel<kNVFP4>, r)
+                           : cudaLaunchKernelEx(&cfg, gemv_split_reduce_kernel<kFP8>, r);
 }
 
 }  // namespace qmlp
