@@ -258,8 +258,8 @@ def bench_headline(args, world, rank, local, pk):
         "gu_us": gu_us,
         "down_us": dn_us,
         "hbm_gbs_call": achieved,
-        "roofline": {"bound": "hbm", "kernel": "gemv_split_kernel<NVFP4, M=1> + its reduce kernel (one MLP call, "
-                                               "I partitioned over CTAs; time = the whole call)",
+        "roofline": {"bound": "hbm", "kernel": "gemv_split_kernel<NVFP4, M=1> (whole MLP, I partitioned over CTAs, "
+                                               "in-kernel reduction; time = the whole call)",
                      "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
                      "algorithmic_bytes_per_launch": call_bytes,
@@ -269,7 +269,7 @@ def bench_headline(args, world, rank, local, pk):
         "clocks": clocks,
         "rotating_copies": R,
         "l2_bytes": l2,
-        "gpu_launches": 2 * K,  # per call at M=1: the streaming kernel and its reduce kernel
+        "gpu_launches": K,  # one kernel per call at M=1 (NVFP4: in-kernel reduction)
     }
     return res, case
 
