@@ -201,7 +201,7 @@ QMLP_DEV bool combine_smem(float* slots, int slot_floats, int slot, int nc, int*
 // act slice (and optionally the global act).
 template <int FMT, int NT>
 QMLP_DEV void epilogue_a(const Args& a, int M, int lt, const float (&v)[2][NT][4], const int* s_sig,
-                         float* s_act) {
+                         float* s_act, int* s_actmax) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int tslice = a.T * 16;
 #pragma unroll
@@ -218,7 +218,11 @@ QMLP_DEV void epilogue_a(const Args& a, int M, int lt, const float (&v)[2][NT][4
             const float gv = v[0][n][e] * pw * s0;
             const float uv = v[1][n][e] * pw * s1;
             const __nv_bfloat16 act = __float2bfloat16_rn(silu_f32(gv) * uv);
-            s_act[m * tslice + r] = __bfloat162float(act);
+            const float af = __bfloat162float(act);
+            s_act[m * tslice + r] = af;
+            // running max|act| of the slice (non-negative floats order as
+            // their bits): the restage needs no scan of its own
+            atomicMax(&s_actmax[m], __float_as_int(fabsf(af)));
             if (a.act_out) a.act_out[(size_t)m * a.I + i] = act;
         }
 }
@@ -233,15 +237,16 @@ struct AccA {
 };
 template <int FMT, int NT>
 __device__ __noinline__ void finish_tile_a(const Args& a, int M, int lt, bool whole, int warp, AccA<NT> acc,
-                                           float* s_pa, int pa_floats, int* s_cnta, const int* s_sig, float* s_act) {
+                                           float* s_pa, int pa_floats, int* s_cnta, const int* s_sig, float* s_act,
+                                           int* s_actmax) {
     if (whole) {
-        epilogue_a<FMT, NT>(a, M, lt, acc.v, s_sig, s_act);
+        epilogue_a<FMT, NT>(a, M, lt, acc.v, s_sig, s_act, s_actmax);
         return;
     }
     const int w0 = (lt * a.KcA) / a.LA, w1 = ((lt + 1) * a.KcA - 1) / a.LA;
     if (combine_smem<NT, 2>(s_pa + (size_t)lt * a.SA * pa_floats, pa_floats, warp - w0, w1 - w0 + 1, &s_cnta[lt], M,
                             acc.v))
-        epilogue_a<FMT, NT>(a, M, lt, acc.v, s_sig, s_act);
+        epilogue_a<FMT, NT>(a, M, lt, acc.v, s_sig, s_act, s_actmax);
 }
 
 // Phase-B result of down row tile rt over this CTA's slice -> global partial.
@@ -310,8 +315,9 @@ QMLP_DEV void stage_x_one_token(const uint4* xr, int K, int kpe, uint4* xs, floa
         v[i] = it < k8 ? xr[it] : make_uint4(0, 0, 0, 0);
         mx = fmaxf(mx, absmax8(v[i]));
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // one warp reduction: mx is a non-negative float (fmaxf drops NaN), so
+    // its bits order as unsigned integers
+    mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
     if (lane == 0) wmax[warp] = mx;
     named_bar_sync(1, kCT);
     mx = 0.0f;
@@ -396,6 +402,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     __shared__ int s_sig[16];
     __shared__ int s_sigb[16];
     __shared__ int s_cnta[64];
+    __shared__ int s_actmax[16];  // per token: max|act| bits over the CTA's slice
     __shared__ int s_cntb[kW];
     __shared__ int s_sigw[kW][16];
     __shared__ float s_wmax[kW];
@@ -423,6 +430,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         s_fail = 0;
     }
     if (threadIdx.x < 64) s_cnta[threadIdx.x] = 0;
+    if (threadIdx.x < 16) s_actmax[threadIdx.x] = 0;
     if (threadIdx.x < kW) s_cntb[threadIdx.x] = 0;
     __syncthreads();  // the last CTA-wide barrier: the producer never waits on the consumers
     // the next kernel's CTAs may start as SMs free up (set-up and launch
@@ -534,7 +542,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
 #pragma unroll
                             for (int e = 0; e < 4; ++e) av.v[p][n][e] = acc[p][n][e];
                     finish_tile_a<FMT, NT>(a, M, lt, cs == 0 && c == a.KcA, warp, av, s_pa, pa_floats, s_cnta, s_sig,
-                                           s_act);
+                                           s_act, s_actmax);
                     zero_acc<NT, 2>(acc);
                     ++lt;
                     c = 0;
@@ -556,19 +564,9 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     // ---------------- restage act (prescaled fp16 fragments) ----------------
     const int tslice = a.T * 16;
     if (s_fail == 0) {
-        // every warp finds the slice maxima itself (T*16 values per token)
-        // and converts its share of the items: one barrier
-        for (int m = 0; m < M; ++m) {
-            float mx = 0.0f;
-            for (int i = lane; i < tslice; i += 32) mx = fmaxf(mx, fabsf(s_act[m * tslice + i]));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) {
-                s_sigw[warp][m] = prescale_exponent(mx);
-                if (warp == 0) s_sigb[m] = s_sigw[warp][m];
-            }
-        }
-        __syncwarp();
+        // the slice maxima were kept by the epilogues: the items (8 act
+        // values each) convert straight away; one barrier
+        if (threadIdx.x < M) s_sigb[threadIdx.x] = prescale_exponent(__int_as_float(s_actmax[threadIdx.x]));
         const int slots = 4 * M;
         for (int it = threadIdx.x; it < M * (tslice / 8); it += kCT) {
             const int m = it / (tslice / 8), k8 = (it % (tslice / 8)) * 8;
@@ -580,7 +578,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                 const __nv_bfloat162 b2 = __floats2bfloat162_rn(src[2 * h], src[2 * h + 1]);  // exact: bf16 values
                 vw[h] = *reinterpret_cast<const uint32_t*>(&b2);
             }
-            stage_store8(xs, slots, m, k8, s_sigw[warp][m], v);
+            stage_store8(xs, slots, m, k8, prescale_exponent(__int_as_float(s_actmax[m])), v);
         }
         named_bar_sync(1, kCT);
     }
