@@ -92,19 +92,21 @@ def test_split_many_back_to_back_calls(torch_cuda):
 
 
 @pytest.mark.parametrize("pinned", [True, False])
-def test_split_host_buffers_match_device(torch_cuda, pinned):
+@pytest.mark.parametrize("M", [1, 3])
+def test_split_host_buffers_match_device(torch_cuda, pinned, M):
     """qmlp_forward_host on the I-partitioned kernel: pinned buffers are read
-    and written in place by the kernel, pageable ones go through the staging
-    copies; both give the device-buffer result bit for bit."""
+    and written in place by the kernel (one token: the compact staging reads
+    x in host memory), pageable ones go through the staging copies; both give
+    the device-buffer result bit for bit."""
     torch = torch_cuda
     K, I = SHAPES[0]
-    case = gen.gen_dense_case("nvfp4", K, I, 3, seed=330)
+    case = gen.gen_dense_case("nvfp4", K, I, M, seed=330 + M)
     mlp = q.QuantMLP.from_case(case)
     if mlp.decode_ctas() == 0:
         pytest.skip("no I partition for this shape on this device")
     dev, _ = run_forward(torch, mlp, case.x)
     xh = torch.from_numpy(case.x.view(np.int16).copy())
-    oh = torch.zeros((3, K), dtype=torch.int16)
+    oh = torch.zeros((M, K), dtype=torch.int16)
     if pinned:
         xh, oh = xh.pin_memory(), oh.pin_memory()
     mlp.forward_host(xh, oh)

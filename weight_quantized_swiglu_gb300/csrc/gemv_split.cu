@@ -504,6 +504,10 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         else
             stage_x_local(reinterpret_cast<const uint4*>(smem + a.xraw_off), M, a.K, a.KcA * kChunkK, xs,
                           s_sigw[warp], s_sig, warp);
+    } else if (M1 && a.KcA * kChunkK <= 16 * kCT) {
+        // one token read in place (host-mapped memory): the same compact
+        // staging, its loads in flight together
+        stage_x_one_token<2>(reinterpret_cast<const uint4*>(a.x), a.K, a.KcA * kChunkK, xs, s_wmax, s_sig);
     } else {
         stage_x(a.x, M, a.K, 0, a.K, a.KcA * kChunkK, xs, s_maxbits, s_sig, kCT);
     }
