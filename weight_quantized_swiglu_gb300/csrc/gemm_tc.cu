@@ -260,7 +260,7 @@ QMLP_DEV uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&p);
 }
 
-template <int FMT>
+template <int FMT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap amap, const Args a) {
     using S = Smem<FMT>;
     constexpr int kLStages = S::L;
@@ -285,8 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int Nt = a.N / BN;
     const int KS = a.Kd / BK;
     const int tiles = Mt * Nt;
-    const int units = tiles * a.splits;  // (tile, k-range) work units, k-range-minor
-    auto ks_begin = [&](int sp) { return (int)(((long)sp * KS) / a.splits); };
+    // (tile, k-range) work units, k-range-minor; the unsplit instance folds
+    // to one unit per tile over the whole k range
+    const int nsp = SPLIT ? a.splits : 1;
+    const int units = tiles * nsp;
+    auto ks_begin = [&](int sp) { return SPLIT ? (int)(((long)sp * KS) / nsp) : (sp == 0 ? 0 : KS); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kLStages; ++s) {
@@ -318,10 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const int t = u / a.splits, sp = u % a.splits;
+                const int t = SPLIT ? u / nsp : u, sp = SPLIT ? u % nsp : 0;
                 const int nt = t / Mt, mt = t % Mt;
                 const uint8_t* blk = a.tiles + (size_t)nt * KS * kRawBytes;
-                for (int ks = ks_begin(sp); ks < ks_begin(sp + 1); ++ks, ++it) {
+                const int ks1 = ks_begin(sp + 1);
+                for (int ks = ks_begin(sp); ks < ks1; ++ks, ++it) {
                     const int s = it % kLStages;
                     if (it >= kLStages &&
                         !wait_or_abort(empty(s), (uint32_t)((it / kLStages - 1) & 1), abort_flag, a.err, 11)) {
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             int it = 0, tc = 0;
             bool ok = true, issued = false;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++tc) {
-                const int sp = u % a.splits;
+                const int sp = SPLIT ? u % nsp : 0;
                 const int buf = tc & 1, use = tc >> 1;
                 if (use > 0 &&
                     !wait_or_abort(acc_empty(buf), (uint32_t)((use - 1) & 1), abort_flag, a.err, 12)) {
@@ -355,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
-                const int kb = ks_begin(sp);
-                for (int ks = kb; ks < ks_begin(sp + 1); ++ks, ++it) {
+                const int kb = ks_begin(sp), ke = ks_begin(sp + 1);
+                for (int ks = kb; ks < ke; ++ks, ++it) {
                     const int s = it % kLStages, b = it % kBStages;
                     if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 13) ||
                         !wait_or_abort(bfull(b), (uint32_t)((it / kBStages) & 1), abort_flag, a.err, 14)) {
@@ -390,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int row_in_tile = q * 32 + lane;
         int tc = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++tc) {
-            const int t = u / a.splits, sp = u % a.splits;
+            const int t = SPLIT ? u / nsp : u, sp = SPLIT ? u % nsp : 0;
             const int nt = t / Mt, mt = t % Mt;
             const int buf = tc & 1, use = tc >> 1;
             // warp-uniform: the TMEM loads below are .sync.aligned
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const bool live = m < a.M;
             const int sg = live ? a.sig[m] : 0;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-            if (a.splits > 1) {
+            if (SPLIT) {
                 // a k-range of the tile: its fp32 partial, unscaled, in the
                 // GEMM's own column order; the reduce kernel adds the splits
                 // in order and applies the epilogue
@@ -492,8 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const int sp = u % a.splits;
-            for (int ks = ks_begin(sp); ks < ks_begin(sp + 1); ++ks, ++it) {
+            const int sp = SPLIT ? u % nsp : 0;
+            const int ks1 = ks_begin(sp + 1);
+            for (int ks = ks_begin(sp); ks < ks1; ++ks, ++it) {
                 const int s = it % kLStages, b = it % kBStages;
                 if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 16) ||
                     (it >= kBStages &&
@@ -679,12 +684,16 @@ template <int FMT>
 cudaError_t launch_fmt(const CUtensorMap& map, const Args& a, int grid, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::Bytes);
+        cudaError_t e =
+            cudaFuncSetAttribute(gemm_kernel<FMT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::Bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_kernel<FMT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Smem<FMT>::Bytes);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    gemm_kernel<FMT><<<grid, kThreads, Smem<FMT>::Bytes, s>>>(map, a);
+    if (a.splits > 1) gemm_kernel<FMT, true><<<grid, kThreads, Smem<FMT>::Bytes, s>>>(map, a);
+    else gemm_kernel<FMT, false><<<grid, kThreads, Smem<FMT>::Bytes, s>>>(map, a);
     cudaError_t e = cudaPeekAtLastError();
     if (e != cudaSuccess || a.splits == 1) return e;
     const long n = (long)a.M * (a.epi == kEpiSwiGLU ? a.N / 2 : a.N);
