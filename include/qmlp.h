@@ -154,11 +154,13 @@ qmlp_status qmlp_forward_debug(qmlp_t* h, qmlp_path path, const void* x, int M, 
 qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void* x, int M,
                                float* y, qmlp_stream_t stream);
 
-/* CTAs of the single-launch decode kernel that partitions the intermediate
- * dimension (each CTA computes gate/up for its slice of I and the down
- * projection over that slice; the partial outputs are reduced in a fixed
- * order after one grid barrier). 0 when the shape has no such partition on
- * this device (the stream-K kernel is used instead). Used for M <= 8. */
+/* CTAs of the decode kernel that partitions the intermediate dimension (each
+ * CTA computes gate/up for its slice of I and the down projection over that
+ * slice; the partial outputs are added in a fixed order -- after a grid
+ * barrier inside the kernel for one NVFP4 token, else by a small reduce
+ * kernel launched after it). 0 when the shape has no such partition on this
+ * device (the stream-K kernel is used instead). Used for M <= 8; the tensor-
+ * core GEMM takes M >= 9 when this partition exists. */
 int qmlp_decode_ctas(qmlp_t* h);
 
 /* Synchronize `stream` and report (then clear) a bounded-wait give-up
