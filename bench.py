@@ -134,14 +134,19 @@ class ClockSampler:
 # distributed plumbing (replicas only: no data-path collective)
 # ----------------------------------------------------------------------------
 def dist_setup(n_gpus):
+    """Rank layout from the torchrun environment; one process per GPU over
+    NCCL (gloo when there is no GPU: the host logic alone, as in the tests)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
@@ -152,11 +157,14 @@ def barrier(world):
 
 
 def max_over_ranks(world, v):
+    """The largest v over the ranks (timings: the job is as slow as its
+    slowest replica)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
