@@ -57,6 +57,7 @@ constexpr uint64_t kLimit = 2000000000ull;  // 2 s
 constexpr int kXRawMax = 16 * 1024;  // raw x copied to shared memory up to this size
 constexpr int kPreStepsBarrier = 1;          // weight steps issued before the wait on the previous kernel:
 constexpr int kPreStepsSep = kDepthMax;      //   schedule (a) / schedule (b) (the whole ring)
+constexpr double kSmallCtaBytes = 256.0 * 1024;  // weight bytes a CTA streams in a "small" MLP
 constexpr int kRedLoads = 10;                // partials a warp adds per output: G <= 16 * kRedLoads
 
 struct Args {
@@ -681,10 +682,11 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     // The CTA's units (token m, 32 output columns): every warp adds its
     // share of the partials of all of them first (the loads of all units in
     // flight together), one barrier, then a warp per unit adds the 16 warp
-    // sums in order. Scratch: the x staging region, idle after phase B.
+    // sums in order. Scratch: the weight ring, idle after phase B (every
+    // step issued was consumed, so no copy is in flight).
     const int units_n = (a.K + 31) / 32;
     const int units = M * units_n;
-    float* red = reinterpret_cast<float*>(smem);
+    float* red = reinterpret_cast<float*>(r.base);
     const size_t bstride = (size_t)M * a.K;
     int nu = 0;
     // two units per round; every load of a round is issued before the adds
@@ -848,14 +850,21 @@ SplitPlan plan_split(int fmt, int K, int I, int num_sms) {
     if (K % 16 || I % 16 || num_sms < 1) return P;
     const int ra = gemv_recs_pair(fmt), rb = gemv_recs_single(fmt);
     const int nta = I / 16, kca = (K + kChunkK - 1) / kChunkK, ntd = K / 16;
+    // a small MLP (every CTA streams at most kSmallCtaBytes) is bound by
+    // fixed costs, not bandwidth: a few CTAs serve it
+    const double wbytes = (double)3 * K * I * (fmt == kNVFP4 ? 9.0 / 16.0 : 1.0);
     for (int T = 4; T <= nta; T += 4) {
         if (nta % T) continue;
         const int G = nta / T;
         if (G > num_sms || G > kW * kRedLoads) continue;
+        const bool small = wbytes / G <= kSmallCtaBytes;
         // the smallest T with G <= SMs: the most CTAs; too few CTAs cannot
         // pull the bandwidth (each SM's consumers decode ~1.4x the HBM rate)
-        if (4 * G < 3 * num_sms) return P;
-        if ((T * kca) % (16 * ra) != 0) return P;  // gate/up: whole steps, no padding
+        if (4 * G < 3 * num_sms && !small) return P;
+        if ((T * kca) % (16 * ra) != 0) {  // gate/up: whole steps, no padding
+            if (small) continue;
+            return P;
+        }
         if (ntd < 16 || T > 64) return P;
         P.G = G;
         P.T = T;
@@ -876,10 +885,11 @@ SplitPlan plan_split(int fmt, int K, int I, int num_sms) {
 bool split_fits(int fmt, int M, int K, const SplitPlan& P) {
     if (!P.G || M < 1 || M > 8) return false;
     const Layout L = layout_for(fmt, M, K, P);
-    // reduction scratch (units per CTA x 16 warps x 32 floats) in the x region
+    // the in-kernel reduction's scratch (units per CTA x 16 warps x 32
+    // floats) lives in the ring
     const size_t units = (size_t)M * ((K + 31) / 32);
     const size_t per_cta = (units + P.G - 1) / P.G;
-    return L.depth >= 2 && per_cta * kW * 32 * 4 <= (size_t)L.xs;
+    return L.depth >= 2 && per_cta * kW * 32 * 4 <= (size_t)L.depth * L.slot;
 }
 
 size_t split_part_elems(int K, const SplitPlan& P) { return (size_t)P.G * 16 * K; }
