@@ -1,7 +1,8 @@
-"""GPU parity of the single-launch decode kernel that partitions the
-intermediate dimension across CTAs (each CTA: gate/up for its slice of I,
-then the down projection over that slice; partial outputs reduced in a
-fixed order after one grid barrier), against the CPU oracle."""
+"""GPU parity of the decode kernel that partitions the intermediate
+dimension across CTAs (each CTA: gate/up for its slice of I, then the down
+projection over that slice; partial outputs added in a fixed order, after a
+grid barrier inside the kernel for one NVFP4 token, else by a reduce kernel
+launched after it), against the CPU oracle."""
 import numpy as np
 import pytest
 
@@ -50,6 +51,21 @@ def test_plan_of_the_27b_shape(torch_cuda):
 # 7680 -> 120 CTAs); down tiles split at warp boundaries with padding records
 # (1536, 23040 -> 120 CTAs, 3 down chunks per CTA, 20 records per warp).
 SHAPES = [(1024, 7680), (1536, 23040)]
+
+
+@pytest.mark.parametrize("fmt,M", [("nvfp4", 1), ("nvfp4", 4), ("fp8", 1), ("fp8", 8)])
+def test_small_mlp_runs_on_a_few_ctas(torch_cuda, fmt, M):
+    """K=256, I=512 (~0.2 MB of weights): fixed costs bound the call, so the
+    partition uses a few CTAs (NVFP4: 4 of 8 gate/up row tiles each, FP8: 8
+    of 4); both reduction schedules against the oracle."""
+    case = gen.gen_dense_case(fmt, 256, 512, M, seed=340 + M)
+    mlp = q.QuantMLP.from_case(case)
+    assert mlp.decode_ctas() == (4 if fmt == "nvfp4" else 8)
+    out, act = run_forward(torch_cuda, mlp, case.x)
+    ref = oracle.dense_forward(case)
+    compare(act, ref["act"], what="act")
+    compare(out, ref["out"], what="out")
+    mlp.close()
 
 
 @pytest.mark.parametrize("K,I", SHAPES)
