@@ -24,8 +24,8 @@
 //  * Tile 128 tokens x 256 weight rows, k-step 64. Warp roles:
 //      warp 0      TMA producer: the activation tile (cp.async.bulk.tensor,
 //                  128-byte swizzle) and the packed weight block of the step
-//                  (one cp.async.bulk: 9 KB NVFP4, 16 KB FP8) into a 6-stage
-//                  (FP8: 5-stage) load ring (TMA and L2 latency is several
+//                  (one cp.async.bulk: 9 KB NVFP4, 16 KB FP8) into a 5-stage
+//                  load ring (TMA and L2 latency is several
 //                  MMA steps long);
 //      warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma (M128 N256 K16)
 //                  per step into one of two TMEM accumulators (2 x 256 fp32
@@ -38,8 +38,8 @@
 //                  (NVFP4: cvt.rn.f16x2.e2m1x2, then an exact f16x2 multiply
 //                  by the group scale; FP8: cvt.rn.f16x2.e4m3x2) written in
 //                  the 128-byte swizzled K-major layout the MMA descriptor
-//                  reads, into a 2-stage ring (decoding step i+1 overlaps the
-//                  MMAs of step i).
+//                  reads, into a 3-stage (FP8: 2-stage) ring, so decoding
+//                  runs ahead of the MMAs.
 //  * Weight block layout (create-time repack): for n-tile j and k-step s a
 //    contiguous block: NVFP4 codes [256 rows][32 B] then scales [256 rows]
 //    [4 B] (9216 B); FP8 bytes [256 rows][64 B] (16384 B; the per-channel
@@ -64,15 +64,18 @@ namespace {
 constexpr int BM = 128;                 // tokens per tile (TMEM lanes)
 constexpr int BN = 256;                 // weight rows per tile (accumulator columns)
 constexpr int BK = 64;                  // k per step (one 128-byte swizzle row of fp16)
-constexpr int kBStages = 2;             // decoded-weight ring
 constexpr int kABytes = BM * BK * 2;    // 16 KB
 constexpr int kBBytes = BN * BK * 2;    // 32 KB
 constexpr int kRawCodes = BN * BK / 2;  // NVFP4: 8 KB of codes, then 1 KB of scales
 // per format: weight block bytes and load-ring depth (activation tile + block)
 template <int FMT>
 constexpr int raw_bytes() { return FMT == kNVFP4 ? kRawCodes + BN * (BK / 16) : BN * BK; }
+// Ring depths (measured at M=8192: NVFP4 3.51 -> 3.39 ms with a third decoded
+// stage for a sixth load stage; FP8, whose blocks are 16 KB, keeps 5 + 2).
 template <int FMT>
-constexpr int lstages() { return FMT == kNVFP4 ? 6 : 5; }
+constexpr int lstages() { return 5; }
+template <int FMT>
+constexpr int bstages() { return FMT == kNVFP4 ? 3 : 2; }
 constexpr int kEpiWarps = 4;
 constexpr int kMaxSplits = 16;          // split-K ways at most (a split keeps >= 8 k-steps)
 constexpr int kDecWarps = 8;
@@ -85,13 +88,14 @@ constexpr uint64_t kGemmWaitNs = 2000000000ull;             // 2 s
 template <int FMT>
 struct Smem {
     static constexpr int L = lstages<FMT>();
+    static constexpr int BS = bstages<FMT>();
     static constexpr int R = raw_bytes<FMT>();
     static constexpr int A = 0;
     static constexpr int B = A + L * kABytes;
-    static constexpr int Raw = B + kBStages * kBBytes;
+    static constexpr int Raw = B + BS * kBBytes;
     static constexpr int Bar = Raw + L * R;
     // barriers: full[L], empty[L], bfull[B], bempty[B], acc_full[2], acc_empty[2], done
-    static constexpr int NumBars = 2 * L + 2 * kBStages + 5;
+    static constexpr int NumBars = 2 * L + 2 * BS + 5;
     static constexpr int Misc = Bar + NumBars * 8;  // tmem address, abort flag
     static constexpr int Bytes = Misc + 16 + 1024;  // + alignment slack
     static_assert(B % 1024 == 0 && Raw % 16 == 0 && Bar % 8 == 0, "smem layout");
@@ -264,6 +268,7 @@ template <int FMT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap amap, const Args a) {
     using S = Smem<FMT>;
     constexpr int kLStages = S::L;
+    constexpr int kBStages = S::BS;
     constexpr int kRawBytes = S::R;
     constexpr int kOffA = S::A, kOffB = S::B, kOffRaw = S::Raw, kOffBar = S::Bar, kOffMisc = S::Misc;
     extern __shared__ uint8_t dyn_smem_raw[];
