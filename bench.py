@@ -534,6 +534,19 @@ def run_profile(args):
             moe.forward(x, q.DT_FP16, ids, rw, out)
         torch.cuda.synchronize()
         moe.check()
+    elif args.profile.startswith("moetokens"):
+        M = int(args.profile[len("moetokens"):] or 16)
+        tok = gen.gen_moe_tokens(gen.seed_for(6, 0), M)
+        moe = q.MoeAWQ.from_case(tok.case, 4)
+        moe.reserve(M)
+        x = torch.from_numpy(tok.x16.view(np.int16).copy()).cuda()
+        ids = torch.from_numpy(tok.ids.copy()).cuda()
+        rw = torch.from_numpy(tok.rw.copy()).cuda()
+        out = torch.empty((M, tok.case.K), dtype=torch.int16, device="cuda")
+        for _ in range(n):
+            moe.forward_tokens(x, q.DT_FP16, ids, rw, out)
+        torch.cuda.synchronize()
+        moe.check()
     elif args.profile.startswith("prefill") or args.profile.startswith("fp8prefill"):
         fp8 = args.profile.startswith("fp8")
         M = int(args.profile[len("fp8prefill" if fp8 else "prefill"):] or 512)
@@ -560,7 +573,7 @@ def main():
                     help="comma list of extra workloads to time (decode,fp8,tiny,moe,prefill) or 'all'")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile", default=None,
-                    help="eager launches of one operation for ncu: fused|stage0|stage1|fp8_fused|moe|prefillM|fp8prefillM")
+                    help="eager launches of one operation for ncu: fused|stage0|stage1|fp8_fused|moe|moetokensM|prefillM|fp8prefillM")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.profile:
