@@ -735,6 +735,7 @@ static qmlp_status moe_run(qmlp_moe_t* h, const void* x, qmlp_dtype xdt, const i
     L.K = h->K;
     L.I = h->I;
     L.meta_bytes = h->meta;
+    L.sliced = 1;  // the handle's banks (repack_moe)
     L.w13 = h->w13;
     L.w13_meta = h->w13_meta;
     L.w2 = h->w2;

@@ -170,7 +170,8 @@ bool gemm_supported(int K, int N);
 // ---------------------------------------------------------------------------
 struct MoeLaunch {
     int E, K, I, meta_bytes;
-    const uint8_t* w13;       // repacked, see moe_awq.cu
+    int sliced = 0;           // 1: the banks are lane-sliced (the handle's copy), 0: checkpoint layout
+    const uint8_t* w13;       // see moe_awq.cu
     const uint8_t* w13_meta;
     const uint8_t* w2;
     const uint8_t* w2_meta;

@@ -39,6 +39,15 @@
 //  * Programmatic dependent launch: the W2 grid starts while W13 runs, reads
 //    the ids and loads its codes and metadata into registers, and only then
 //    waits (griddepcontrol.wait) for the intermediate.
+//  * Lane-sliced banks (the handle's copy, made at create): every 16-byte
+//    unit of a row (4 words, 32 k) is byte-transposed so that byte t of its
+//    four words is one aligned 32-bit word at offset 4t -- exactly what lane
+//    t's PRMT picks. A lane then loads 4 bytes per unit instead of the whole
+//    unit: 4x less register space per chunk, so W13 keeps a warp's 4 chunks
+//    in flight at once. The allocation-free entry point reads the banks in
+//    the checkpoint layout and uses the same kernels in that layout.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -46,7 +55,8 @@ namespace qmlp {
 namespace {
 
 constexpr int kK13 = 10;  // W13 K splits: a CTA has 2 x kK13 warps (gate and up tiles)
-constexpr int kC13 = 2;   // 64-k chunks a W13 warp loads at once
+constexpr int kC13 = 2;   // 64-k chunks a W13 warp loads at once (checkpoint layout)
+constexpr int kC13S = 4;  // the same with lane-sliced banks (a fifth of the registers per chunk)
 constexpr int kG2 = 10;   // k16 groups a W2 warp loads at once
 
 struct Args {
@@ -119,7 +129,7 @@ QMLP_DEV uint32_t pair_selector(int t) {
 // ---------------------------------------------------------------------------
 // W13 + SwiGLU
 // ---------------------------------------------------------------------------
-template <int MB>
+template <int MB, bool SL>
 __global__ void __launch_bounds__(2 * kK13 * 32) moe_w13_kernel(const Args a) {
     extern __shared__ __align__(16) uint32_t x16[];  // [K/2] fp16 pairs
     __shared__ float part[2 * kK13][16];            // [warp][row of its tile]
@@ -140,18 +150,25 @@ __global__ void __launch_bounds__(2 * kK13 * 32) moe_w13_kernel(const Args a) {
     const bool al4 = a.meta_al4 != 0;
     const size_t row0 = (size_t)id * N + tile * a.I + 16 * blockIdx.x + g;
     const size_t rows[2] = {row0, row0 + 8};
-    uint4 cw[kC13][2][2];  // two 16-byte halves of each row's 32-byte chunk
-    uint32_t mw[kC13][2][2];
+    constexpr int kC = SL ? kC13S : kC13;
+    uint4 cw[kC][2][2];      // checkpoint layout: the two 16-byte units of each row's 32-byte chunk
+    uint32_t cs[kC][2][2];   // lane-sliced layout: this lane's 4 bytes of each unit
+    uint32_t mw[kC][2][2];
     auto load_batch = [&](int cb) {
 #pragma unroll
-        for (int i = 0; i < kC13; ++i) {
+        for (int i = 0; i < kC; ++i) {
             const int c = cb + i;
             if (c < c1) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const uint4* src = reinterpret_cast<const uint4*>(a.w13 + rows[q] * (a.K / 2) + c * 32);
-                    cw[i][q][0] = __ldg(src);
-                    cw[i][q][1] = __ldg(src + 1);
+                    const uint8_t* rowc = a.w13 + rows[q] * (a.K / 2) + c * 32;
+                    if (SL) {
+                        cs[i][q][0] = __ldg(reinterpret_cast<const unsigned int*>(rowc + 4 * t));
+                        cs[i][q][1] = __ldg(reinterpret_cast<const unsigned int*>(rowc + 16 + 4 * t));
+                    } else {
+                        cw[i][q][0] = __ldg(reinterpret_cast<const uint4*>(rowc));
+                        cw[i][q][1] = __ldg(reinterpret_cast<const uint4*>(rowc) + 1);
+                    }
                     const uint8_t* m = a.w13_meta + (rows[q] * gpr + 2 * c) * MB;
                     mw[i][q][0] = load_meta<MB>(m, al4);
                     mw[i][q][1] = load_meta<MB>(m + MB, al4);
@@ -190,10 +207,10 @@ __global__ void __launch_bounds__(2 * kK13 * 32) moe_w13_kernel(const Args a) {
 
     const uint32_t sel = pair_selector(t);
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int cb = c0; cb < c1; cb += kC13) {
+    for (int cb = c0; cb < c1; cb += kC) {
         if (cb != c0) load_batch(cb);
 #pragma unroll
-        for (int i = 0; i < kC13; ++i) {
+        for (int i = 0; i < kC; ++i) {
             const int c = cb + i;
             if (c < c1) {
                 uint32_t s2[2][2], b2[2][2];
@@ -205,19 +222,30 @@ __global__ void __launch_bounds__(2 * kK13 * 32) moe_w13_kernel(const Args a) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {  // k16 group j: AWQ group j/2, words 2j, 2j+1 of the chunk
                     const int h = j >> 1;
-                    const uint32_t wa0 = (j & 1) ? cw[i][0][h].z : cw[i][0][h].x;
-                    const uint32_t wb0 = (j & 1) ? cw[i][0][h].w : cw[i][0][h].y;
-                    const uint32_t wa1 = (j & 1) ? cw[i][1][h].z : cw[i][1][h].x;
-                    const uint32_t wb1 = (j & 1) ? cw[i][1][h].w : cw[i][1][h].y;
                     uint32_t x0 = 0, x1 = 0;
                     if (g == 0) {
                         const int k2 = (c * 64 + 16 * j) / 2 + t;
                         x0 = x16[k2];
                         x1 = x16[k2 + 4];
                     }
-                    mma_f16_16816(d, awq_pair(wa0, sel, s2[0][h], b2[0][h]), awq_pair(wa1, sel, s2[1][h], b2[1][h]),
-                                  awq_pair(wb0, sel, s2[0][h], b2[0][h]), awq_pair(wb1, sel, s2[1][h], b2[1][h]), x0,
-                                  x1);
+                    uint32_t f0, f1, f2, f3;  // rows g, g+8 at k 2t.. (words 2j), then at 8+2t.. (words 2j+1)
+                    if (SL) {
+                        const uint32_t sa = pair_selector(2 * (j & 1)), sb = pair_selector(2 * (j & 1) + 1);
+                        f0 = awq_pair(cs[i][0][h], sa, s2[0][h], b2[0][h]);
+                        f1 = awq_pair(cs[i][1][h], sa, s2[1][h], b2[1][h]);
+                        f2 = awq_pair(cs[i][0][h], sb, s2[0][h], b2[0][h]);
+                        f3 = awq_pair(cs[i][1][h], sb, s2[1][h], b2[1][h]);
+                    } else {
+                        const uint32_t wa0 = (j & 1) ? cw[i][0][h].z : cw[i][0][h].x;
+                        const uint32_t wb0 = (j & 1) ? cw[i][0][h].w : cw[i][0][h].y;
+                        const uint32_t wa1 = (j & 1) ? cw[i][1][h].z : cw[i][1][h].x;
+                        const uint32_t wb1 = (j & 1) ? cw[i][1][h].w : cw[i][1][h].y;
+                        f0 = awq_pair(wa0, sel, s2[0][h], b2[0][h]);
+                        f1 = awq_pair(wa1, sel, s2[1][h], b2[1][h]);
+                        f2 = awq_pair(wb0, sel, s2[0][h], b2[0][h]);
+                        f3 = awq_pair(wb1, sel, s2[1][h], b2[1][h]);
+                    }
+                    mma_f16_16816(d, f0, f1, f2, f3, x0, x1);
                 }
             }
         }
@@ -250,7 +278,7 @@ __global__ void __launch_bounds__(2 * kK13 * 32) moe_w13_kernel(const Args a) {
 // ---------------------------------------------------------------------------
 // W2 + ordered router-weighted sum
 // ---------------------------------------------------------------------------
-template <int MB>
+template <int MB, bool SL>
 __global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
     __shared__ float ys[16][16];
     const int r = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -266,14 +294,25 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
     const uint8_t* m0p = a.w2_meta + row0 * gpr * MB;
     const uint8_t* m8p = a.w2_meta + (row0 + 8) * gpr * MB;
     const bool al4 = a.meta_al4 != 0;
-    uint2 cw[kG2][2];         // words 2j, 2j+1 of rows g and g+8 for k16 group j
+    uint2 cw[kG2][2];         // checkpoint layout: words 2j, 2j+1 of rows g and g+8 for k16 group j
+    uint32_t cs[kG2 / 2][2];  // lane-sliced layout: this lane's 4 bytes of unit j/2 (groups j, j+1)
     uint32_t mw[kG2 / 2][2];  // the AWQ records of the batch
     auto load_batch = [&](int gb) {  // gb is a multiple of kG2 (even)
+        if (SL) {
 #pragma unroll
-        for (int i = 0; i < kG2; ++i) {
-            if (valid && gb + i < ng) {
-                cw[i][0] = __ldg(c0p + gb + i);
-                cw[i][1] = __ldg(c8p + gb + i);
+            for (int i = 0; i < kG2 / 2; ++i) {
+                if (valid && gb + 2 * i < ng) {
+                    cs[i][0] = __ldg(reinterpret_cast<const unsigned int*>(c0p + gb + 2 * i) + t);
+                    cs[i][1] = __ldg(reinterpret_cast<const unsigned int*>(c8p + gb + 2 * i) + t);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kG2; ++i) {
+                if (valid && gb + i < ng) {
+                    cw[i][0] = __ldg(c0p + gb + i);
+                    cw[i][1] = __ldg(c8p + gb + i);
+                }
             }
         }
 #pragma unroll
@@ -306,8 +345,14 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
                         x0 = act[8 * j + t];
                         x1 = act[8 * j + 4 + t];
                     }
-                    mma_f16_16816(d, awq_pair(cw[i][0].x, sel, s0, b0), awq_pair(cw[i][1].x, sel, s8, b8),
-                                  awq_pair(cw[i][0].y, sel, s0, b0), awq_pair(cw[i][1].y, sel, s8, b8), x0, x1);
+                    if (SL) {
+                        const uint32_t sa = pair_selector(2 * (i & 1)), sb = pair_selector(2 * (i & 1) + 1);
+                        mma_f16_16816(d, awq_pair(cs[i / 2][0], sa, s0, b0), awq_pair(cs[i / 2][1], sa, s8, b8),
+                                      awq_pair(cs[i / 2][0], sb, s0, b0), awq_pair(cs[i / 2][1], sb, s8, b8), x0, x1);
+                    } else {
+                        mma_f16_16816(d, awq_pair(cw[i][0].x, sel, s0, b0), awq_pair(cw[i][1].x, sel, s8, b8),
+                                      awq_pair(cw[i][0].y, sel, s0, b0), awq_pair(cw[i][1].y, sel, s8, b8), x0, x1);
+                    }
                 }
             }
         }
@@ -332,11 +377,11 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
     }
 }
 
-template <int MB>
+template <int MB, bool SL>
 cudaError_t launch_mb(const Args& a, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(moe_w13_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(moe_w13_kernel<MB, SL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              16384 * 2);
         if (e != cudaSuccess) return e;
         attr = true;
@@ -351,7 +396,7 @@ cudaError_t launch_mb(const Args& a, cudaStream_t s) {
     c13.stream = s;
     c13.attrs = pdl;
     c13.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&c13, moe_w13_kernel<MB>, a);
+    cudaError_t e = cudaLaunchKernelEx(&c13, moe_w13_kernel<MB, SL>, a);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t c2 = {};
     c2.gridDim = dim3(a.K / 16);
@@ -359,7 +404,7 @@ cudaError_t launch_mb(const Args& a, cudaStream_t s) {
     c2.stream = s;
     c2.attrs = pdl;
     c2.numAttrs = 1;
-    return cudaLaunchKernelEx(&c2, moe_w2_kernel<MB>, a);
+    return cudaLaunchKernelEx(&c2, moe_w2_kernel<MB, SL>, a);
 }
 
 }  // namespace
@@ -386,14 +431,41 @@ cudaError_t launch_moe(const MoeLaunch& L, int num_sms, cudaStream_t s) {
     a.gu_dbg = L.gu_dbg;
     a.act_dbg = L.act_dbg;
     a.y_dbg = L.y_dbg;
-    return L.meta_bytes == 4 ? launch_mb<4>(a, s) : launch_mb<3>(a, s);
+    if (L.sliced) return L.meta_bytes == 4 ? launch_mb<4, true>(a, s) : launch_mb<3, true>(a, s);
+    return L.meta_bytes == 4 ? launch_mb<4, false>(a, s) : launch_mb<3, false>(a, s);
 }
 
-// The banks are consumed in the checkpoint layout ([E, N, Kr/2] codes,
-// [E, N, Kr/32] records): a device copy.
+namespace {
+// Lane-sliced codes: within every 16-byte unit, output word t holds byte t
+// of input words 0..3 (a 4x4 byte transpose; units stay in place, so rows
+// keep their offsets and every unit its alignment).
+__global__ void slice_units_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, size_t units) {
+    for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (size_t)gridDim.x * blockDim.x) {
+        const uint4 v = in[u];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            o[t] = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[t] |= ((w[j] >> (8 * t)) & 0xFFu) << (8 * j);
+        }
+        out[u] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+}  // namespace
+
+// The handle's banks: codes lane-sliced ([E, N, Kr/2] bytes, every 16-byte
+// unit transposed), records as in the checkpoint ([E, N, Kr/32] records).
 cudaError_t repack_moe(const uint8_t* w, const uint8_t* meta, int meta_bytes, int E, int N, int Kr,
                        uint8_t* w_out, uint8_t* meta_out, cudaStream_t s) {
-    cudaError_t e = cudaMemcpyAsync(w_out, w, (size_t)E * N * (Kr / 2), cudaMemcpyDeviceToDevice, s);
+    const size_t bytes = (size_t)E * N * (Kr / 2);
+    if (bytes % 16) return cudaErrorInvalidValue;
+    const size_t units = bytes / 16;
+    const int grid = (int)std::min<size_t>((units + 255) / 256, 65535);
+    slice_units_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(w), reinterpret_cast<uint4*>(w_out), units);
+    cudaError_t e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
     return cudaMemcpyAsync(meta_out, meta, (size_t)E * N * (Kr / 32) * meta_bytes, cudaMemcpyDeviceToDevice, s);
 }

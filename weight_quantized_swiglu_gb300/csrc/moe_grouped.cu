@@ -8,7 +8,9 @@
 //     act     = fp16(SiLU(g) * u)
 //     y[t, r] = fp16(act . W2[id]^T) in fp32
 //   out[t] = fp16( sum over valid r, in router order, of rw[t, r] * y[t, r] )
-// with the same half_fma weight decode as the one-token kernels.
+// with the same half_fma weight decode as the one-token kernels, on the
+// handle's lane-sliced banks (byte t of every 4 words is lane t's 32-bit
+// word, see moe_awq.cu).
 //
 // GB300 design: tokens that share an expert share its weight reads.
 //  * moe_route_kernel (one CTA): counting sort of the valid routes by
@@ -40,7 +42,7 @@ namespace qmlp {
 namespace {
 
 constexpr int kGW13 = 10;  // W13 K splits: 2 x kGW13 warps per CTA (gate and up tiles)
-constexpr int kGC13 = 2;   // 64-k chunks a W13 warp loads at once
+constexpr int kGC13 = 4;   // 64-k chunks a W13 warp loads at once (lane-sliced banks: 4 bytes per unit and lane)
 constexpr int kGG2 = 10;   // k16 groups a W2 warp loads at once
 constexpr int kCols = 8;   // routes per group (MMA n8)
 constexpr int kRouteThreads = 1024;
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
     };
     int tp = blockIdx.y;
     set_rows(tp);
-    uint4 cw[kGC13][2][2];
+    uint32_t cs[kGC13][2][2];  // this lane's 4 bytes of the two 16-byte units of each row's chunk
     uint32_t mw[kGC13][2][2];
     auto load_batch = [&](int cb) {
 #pragma unroll
@@ -222,9 +224,9 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
             if (c < c1) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const uint4* src = reinterpret_cast<const uint4*>(a.w13 + rows[q] * (a.K / 2) + c * 32);
-                    cw[i][q][0] = __ldg(src);
-                    cw[i][q][1] = __ldg(src + 1);
+                    const uint8_t* rowc = a.w13 + rows[q] * (a.K / 2) + c * 32;
+                    cs[i][q][0] = __ldg(reinterpret_cast<const unsigned int*>(rowc + 4 * t));
+                    cs[i][q][1] = __ldg(reinterpret_cast<const unsigned int*>(rowc + 16 + 4 * t));
                     const uint8_t* m = a.w13_meta + (rows[q] * gpr + 2 * c) * MB;
                     mw[i][q][0] = gload_meta<MB>(m, al4);
                     mw[i][q][1] = gload_meta<MB>(m + MB, al4);
@@ -302,7 +304,6 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
     }
     __syncthreads();
 
-    const uint32_t sel = gpair_selector(t);
     const uint32_t* xcol = xs + g * xstride;  // this lane's MMA column = route slot g
     for (; tp < ntp; tp += gridDim.y) {
         float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -320,15 +321,14 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
+                        // group j: unit j/2, its words 2(j&1) (k 2t..) and 2(j&1)+1 (k 8+2t..)
                         const int h = j >> 1;
-                        const uint32_t wa0 = (j & 1) ? cw[i][0][h].z : cw[i][0][h].x;
-                        const uint32_t wb0 = (j & 1) ? cw[i][0][h].w : cw[i][0][h].y;
-                        const uint32_t wa1 = (j & 1) ? cw[i][1][h].z : cw[i][1][h].x;
-                        const uint32_t wb1 = (j & 1) ? cw[i][1][h].w : cw[i][1][h].y;
+                        const uint32_t sa = gpair_selector(2 * (j & 1)), sb = gpair_selector(2 * (j & 1) + 1);
                         const int k2 = (c * 64 + 16 * j) / 2 + t;
-                        mma_f16_16816(d, gawq_pair(wa0, sel, s2[0][h], b2[0][h]),
-                                      gawq_pair(wa1, sel, s2[1][h], b2[1][h]), gawq_pair(wb0, sel, s2[0][h], b2[0][h]),
-                                      gawq_pair(wb1, sel, s2[1][h], b2[1][h]), xcol[k2], xcol[k2 + 4]);
+                        mma_f16_16816(d, gawq_pair(cs[i][0][h], sa, s2[0][h], b2[0][h]),
+                                      gawq_pair(cs[i][1][h], sa, s2[1][h], b2[1][h]),
+                                      gawq_pair(cs[i][0][h], sb, s2[0][h], b2[0][h]),
+                                      gawq_pair(cs[i][1][h], sb, s2[1][h], b2[1][h]), xcol[k2], xcol[k2 + 4]);
                     }
                 }
             }
@@ -399,7 +399,6 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
     __syncthreads();
     const int ng = a.I / 16, gpr = a.I / 32;
     const bool al4 = a.meta_al4 != 0;
-    const uint32_t sel = gpair_selector(t);
     const uint32_t* xcol = acts + g * astride;
     // this CTA's 256-row blocks; warps are independent from here (no barrier)
     for (int nb = blockIdx.y; 256 * nb < a.K; nb += gridDim.y) {
@@ -412,13 +411,13 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
     const uint8_t* m8p = a.w2_meta + (row0 + 8) * gpr * MB;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     for (int gb = 0; gb < ng; gb += kGG2) {
-        uint2 cw[kGG2][2];
+        uint32_t cs[kGG2 / 2][2];  // this lane's 4 bytes of unit (gb/2 + i): k16 groups gb+2i, gb+2i+1
         uint32_t mw[kGG2 / 2][2];
 #pragma unroll
-        for (int i = 0; i < kGG2; ++i) {
-            if (gb + i < ng) {
-                cw[i][0] = __ldg(c0p + gb + i);
-                cw[i][1] = __ldg(c8p + gb + i);
+        for (int i = 0; i < kGG2 / 2; ++i) {
+            if (gb + 2 * i < ng) {
+                cs[i][0] = __ldg(reinterpret_cast<const unsigned int*>(c0p + gb + 2 * i) + t);
+                cs[i][1] = __ldg(reinterpret_cast<const unsigned int*>(c8p + gb + 2 * i) + t);
             }
         }
 #pragma unroll
@@ -436,8 +435,9 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
                 uint32_t s0, b0, s8, b8;
                 gmeta_sb2<MB>(mw[i / 2][0], s0, b0);
                 gmeta_sb2<MB>(mw[i / 2][1], s8, b8);
-                mma_f16_16816(d, gawq_pair(cw[i][0].x, sel, s0, b0), gawq_pair(cw[i][1].x, sel, s8, b8),
-                              gawq_pair(cw[i][0].y, sel, s0, b0), gawq_pair(cw[i][1].y, sel, s8, b8),
+                const uint32_t sa = gpair_selector(2 * (i & 1)), sb = gpair_selector(2 * (i & 1) + 1);
+                mma_f16_16816(d, gawq_pair(cs[i / 2][0], sa, s0, b0), gawq_pair(cs[i / 2][1], sa, s8, b8),
+                              gawq_pair(cs[i / 2][0], sb, s0, b0), gawq_pair(cs[i / 2][1], sb, s8, b8),
                               xcol[8 * j + t], xcol[8 * j + 4 + t]);
             }
         }
