@@ -811,6 +811,7 @@ qmlp_status qmlp_moe_forward(qmlp_moe_t* h, const void* x, qmlp_dtype xdt, const
     if (overlaps(out, xb, x, xb) || overlaps(out, xb, ids, rb) || overlaps(out, xb, rw, rb)) return QMLP_ERR_ALIAS;
     if (fault("launch")) return QMLP_ERR_CUDA;
     MoeGroupedLaunch L;
+    L.num_sms = h->num_sms;
     L.E = h->E;
     L.K = h->K;
     L.I = h->I;

@@ -193,6 +193,7 @@ constexpr int kMoeGroupedMaxK = 8192;  // x of a group's 8 tokens is staged in s
 constexpr int kMoeGroupedMaxE = 8192;  // the routing CTA keeps 4 ints per expert in shared memory
 struct MoeGroupedLaunch {
     int E, K, I, meta_bytes, M, topk;
+    int num_sms = 0;
     const uint8_t* w13;
     const uint8_t* w13_meta;
     const uint8_t* w2;

@@ -19,13 +19,14 @@
 //    expert's bucket is whatever the atomics give: it does not matter,
 //    because every route is one column of the MMAs below and a column's
 //    result depends on nothing else in the group.
-//  * moe_w13_grouped_kernel: kW13Ctas CTAs per group, each looping over its
-//    share of the 16-row gate/up tile pairs (x staged once per CTA);
+//  * moe_w13_grouped_kernel: 1-5 CTAs per group (fewer when there are many
+//    groups), each looping over its share of the 16-row gate/up tile pairs
+//    (x staged once per CTA);
 //    the group's tokens are the 8 columns of the m16n8k16 MMAs (A fragments
 //    decoded from the checkpoint layout as in the one-token kernel), each
 //    token prescaled by its own power of two; the K split over 10 warps is
 //    added in a fixed order.
-//  * moe_w2_grouped_kernel: kW2Ctas CTAs per group, each looping over its
+//  * moe_w2_grouped_kernel: as many CTAs per group, each looping over its
 //    share of the 256-row blocks, a warp per 16 rows, the group's act rows
 //    as the MMA columns; y is stored as fp16.
 //  * moe_combine_kernel: one thread per (token, output element) adds the
@@ -46,8 +47,7 @@ constexpr int kGC13 = 4;   // 64-k chunks a W13 warp loads at once (lane-sliced 
 constexpr int kGG2 = 10;   // k16 groups a W2 warp loads at once
 constexpr int kCols = 8;   // routes per group (MMA n8)
 constexpr int kRouteThreads = 1024;
-constexpr int kW13Ctas = 2;  // CTAs per group in W13 (each loops over its share of the I/16 tile pairs)
-constexpr int kW2Ctas = 2;   // CTAs per group in W2 (each loops over its share of the 256-row blocks)
+constexpr int kMaxCtasPerGroup = 5;  // CTAs per group (each loops over its share of the tile pairs / 256-row blocks)
 constexpr int kXB = 8;     // x items a thread has in flight while staging a group's tokens
 
 struct GArgs {
@@ -493,7 +493,7 @@ cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, c
 }
 
 template <int MB>
-cudaError_t launch_grouped_mb(const GArgs& a, int gmax, cudaStream_t s) {
+cudaError_t launch_grouped_mb(const GArgs& a, int gmax, int cpg, cudaStream_t s) {
     const size_t rsmem = (size_t)4 * a.E * sizeof(int);
     const size_t xsmem = (size_t)kCols * (a.K / 2 + 4) * 4;
     const size_t asmem = (size_t)kCols * (a.I / 2 + 4) * 4;
@@ -511,9 +511,9 @@ cudaError_t launch_grouped_mb(const GArgs& a, int gmax, cudaStream_t s) {
     cudaLaunchConfig_t c = pdl_cfg(dim3(1), dim3(kRouteThreads), rsmem, s, at);
     cudaError_t e = cudaLaunchKernelEx(&c, moe_route_kernel, a);
     if (e != cudaSuccess) return e;
-    c = pdl_cfg(dim3(gmax, std::min(a.I / 16, kW13Ctas)), dim3(2 * kGW13 * 32), xsmem, s, at);
+    c = pdl_cfg(dim3(gmax, std::min(a.I / 16, cpg)), dim3(2 * kGW13 * 32), xsmem, s, at);
     if ((e = cudaLaunchKernelEx(&c, moe_w13_grouped_kernel<MB>, a)) != cudaSuccess) return e;
-    c = pdl_cfg(dim3(gmax, std::min((a.K + 255) / 256, kW2Ctas)), dim3(16 * 32), asmem, s, at);
+    c = pdl_cfg(dim3(gmax, std::min((a.K + 255) / 256, cpg)), dim3(16 * 32), asmem, s, at);
     if ((e = cudaLaunchKernelEx(&c, moe_w2_grouped_kernel<MB>, a)) != cudaSuccess) return e;
     c = pdl_cfg(dim3(a.M, (a.K + 255) / 256), dim3(256), 0, s, at);
     return cudaLaunchKernelEx(&c, moe_combine_kernel, a);
@@ -549,7 +549,12 @@ cudaError_t launch_moe_grouped(const MoeGroupedLaunch& L, cudaStream_t s) {
     a.groups = L.groups;
     a.n_groups = L.n_groups;
     const int gmax = (int)moe_grouped_max_groups(L.M * L.topk, L.E);
-    return L.meta_bytes == 4 ? launch_grouped_mb<4>(a, gmax, s) : launch_grouped_mb<3>(a, gmax, s);
+    // CTAs per group: about four waves' worth of CTAs in all (measured at
+    // E=512 top-10: M=16 85.5 -> ~82 us with 4-5 per group; M=512 best with
+    // 1-2 -- 466 us -- and 562 us with 5)
+    const int sms = std::max(1, L.num_sms);
+    const int cpg = std::max(1, std::min(kMaxCtasPerGroup, (4 * sms + gmax - 1) / gmax));
+    return L.meta_bytes == 4 ? launch_grouped_mb<4>(a, gmax, cpg, s) : launch_grouped_mb<3>(a, gmax, cpg, s);
 }
 
 }  // namespace qmlp
