@@ -63,11 +63,13 @@ def oracle_tokens(tok, meta, xdt, rows, ids=None):
 
 @pytest.mark.parametrize("meta", [4, 3])
 @pytest.mark.parametrize("xdt", ["fp16", "bf16"])
-@pytest.mark.parametrize("M", [2, 9, 37])
+@pytest.mark.parametrize("M", [2, 9, 13, 37])
 def test_tokens_small_bank_heavy_sharing(torch_cuda, meta, xdt, M):
-    """E = 16: most experts carry many routes, so groups fill (8 routes),
-    experts spread over several groups and a token's duplicate shares a
-    group with its original; every token also has one invalid id."""
+    """E = 16: most experts carry many routes, so groups fill, experts spread
+    over several groups and a token's duplicate shares a group with its
+    original; every token also has one invalid id. Groups hold 8 routes up
+    to M = 12 and 16 routes (two MMA column sets) from M = 13, where the
+    M x 10 routes reach 8 per expert."""
     tok = gen.gen_moe_tokens(400 + M, M, E=16, K=512, I=160)
     moe = q.MoeAWQ.from_case(tok.case, meta)
     moe.reserve(M)

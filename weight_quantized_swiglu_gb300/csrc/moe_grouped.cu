@@ -15,15 +15,17 @@
 // GB300 design: tokens that share an expert share its weight reads.
 //  * moe_route_kernel (one CTA): counting sort of the valid routes by
 //    expert (shared-memory histogram, scan, scatter) and a list of groups of
-//    at most 8 routes with one expert. The order of the routes inside an
-//    expert's bucket is whatever the atomics give: it does not matter,
-//    because every route is one column of the MMAs below and a column's
-//    result depends on nothing else in the group.
+//    at most 8 routes with one expert -- 16 once the routes average 8 or
+//    more per expert (and K <= 4096), a group then being two sets of MMA
+//    columns that share every decoded weight fragment. The order of the
+//    routes inside an expert's bucket is whatever the atomics give: it does
+//    not matter, because every route is one column of the MMAs below and a
+//    column's result depends on nothing else in the group.
 //  * moe_w13_grouped_kernel: 1-5 CTAs per group (fewer when there are many
 //    groups), each looping over its share of the 16-row gate/up tile pairs
 //    (x staged once per CTA);
-//    the group's tokens are the 8 columns of the m16n8k16 MMAs (A fragments
-//    decoded from the checkpoint layout as in the one-token kernel), each
+//    the group's tokens are the 8 (or 2 x 8) columns of the m16n8k16 MMAs
+//    (A fragments decoded as in the one-token kernel), each
 //    token prescaled by its own power of two; the K split over 10 warps is
 //    added in a fixed order.
 //  * moe_w2_grouped_kernel: as many CTAs per group, each looping over its
@@ -45,13 +47,15 @@ namespace {
 constexpr int kGW13 = 10;  // W13 K splits: 2 x kGW13 warps per CTA (gate and up tiles)
 constexpr int kGC13 = 4;   // 64-k chunks a W13 warp loads at once (lane-sliced banks: 4 bytes per unit and lane)
 constexpr int kGG2 = 10;   // k16 groups a W2 warp loads at once
-constexpr int kCols = 8;   // routes per group (MMA n8)
+constexpr int kCols = 8;   // routes per MMA (n8); a group holds 8 or 16 routes (NC), 16 as two MMAs per A fragment
+constexpr int kWideMaxK = 4096;  // 16-route groups: x of 16 tokens staged in shared memory
 constexpr int kRouteThreads = 1024;
 constexpr int kMaxCtasPerGroup = 5;  // CTAs per group (each loops over its share of the tile pairs / 256-row blocks)
 constexpr int kXB = 8;     // x items a thread has in flight while staging a group's tokens
 
 struct GArgs {
     int E, K, I, M, topk;
+    int gcap;  // routes per group: 8 or 16
     const uint8_t* w13;
     const uint8_t* w13_meta;
     const uint8_t* w2;
@@ -167,12 +171,13 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const GArgs a)
     const int per = (a.E + kRouteThreads - 1) / kRouteThreads;
     const int e0 = min(a.E, threadIdx.x * per), e1 = min(a.E, e0 + per);
     unsigned long long mine = 0;
-    for (int e = e0; e < e1; ++e) mine += ((unsigned long long)cnt[e] << 32) + (unsigned)((cnt[e] + kCols - 1) / kCols);
+    const int gc = a.gcap;
+    for (int e = e0; e < e1; ++e) mine += ((unsigned long long)cnt[e] << 32) + (unsigned)((cnt[e] + gc - 1) / gc);
     unsigned long long pre = block_excl_scan(mine, wsum, &total);
     for (int e = e0; e < e1; ++e) {
         off[e] = (int)(pre >> 32);
         goff[e] = (int)(pre & 0xFFFFFFFFull);
-        pre += ((unsigned long long)cnt[e] << 32) + (unsigned)((cnt[e] + kCols - 1) / kCols);
+        pre += ((unsigned long long)cnt[e] << 32) + (unsigned)((cnt[e] + gc - 1) / gc);
     }
     if (threadIdx.x == 0) *a.n_groups = (int)(total & 0xFFFFFFFFull);
     __syncthreads();
@@ -181,25 +186,28 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const GArgs a)
         if (id >= 0 && id < a.E) a.route_list[off[id] + atomicAdd(&cur[id], 1)] = i;
     }
     for (int e = e0; e < e1; ++e)
-        for (int j = 0; j * kCols < cnt[e]; ++j)
-            a.groups[goff[e] + j] = make_int4(e, off[e] + j * kCols, min(kCols, cnt[e] - j * kCols), 0);
+        for (int j = 0; j * gc < cnt[e]; ++j)
+            a.groups[goff[e] + j] = make_int4(e, off[e] + j * gc, min(gc, cnt[e] - j * gc), 0);
 }
 
 // ---------------------------------------------------------------------------
 // W13 + SwiGLU for a group of routes sharing one expert
 // ---------------------------------------------------------------------------
-template <int MB>
+template <int MB, int NC>
 __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const GArgs a) {
-    extern __shared__ __align__(16) uint32_t xs[];  // [kCols][K/2 + 4] fp16 pairs (padded: no bank conflicts)
-    __shared__ float part[2 * kGW13][16][kCols];
-    __shared__ int s_route[kCols];
-    __shared__ int s_max[kCols];
-    __shared__ int s_sig[kCols];
+    extern __shared__ __align__(16) uint32_t xs[];  // [NC][K/2 + 4] fp16 pairs (padded: no bank conflicts)
+    __shared__ float part[2 * kGW13][16][NC];
+    __shared__ int s_route[NC];
+    __shared__ int s_max[NC];
+    __shared__ int s_sig[NC];
     pdl_wait();
     pdl_launch_dependents();
     if ((int)blockIdx.x >= *a.n_groups) return;
     const int4 grp = a.groups[blockIdx.x];
     const int e = grp.x, cnt = grp.z;
+    // a group of more than 8 routes is two MMA column sets on the same A fragments
+    const bool two = NC == 16 && cnt > kCols;
+    const int ns = two ? 2 * kCols : kCols;  // slots staged
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int tile = warp / kGW13, ks = warp % kGW13;
     const int Kc = a.K / 64, gpr = a.K / 32, N = 2 * a.I;
@@ -241,13 +249,13 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
     // per thread; bf16 input takes one pass for the per-token maxima and
     // one to convert.
     const int xstride = a.K / 2 + 4;
-    if (threadIdx.x < kCols) {
+    if (threadIdx.x < NC) {
         s_route[threadIdx.x] = threadIdx.x < cnt ? a.route_list[grp.y + threadIdx.x] : -1;
         s_max[threadIdx.x] = 0;
     }
     __syncthreads();
     const uint32_t* xin = reinterpret_cast<const uint32_t*>(a.x);
-    const int kh = a.K / 2, items = kCols * kh, nth = blockDim.x;
+    const int kh = a.K / 2, items = ns * kh, nth = blockDim.x;
     auto load_items = [&](int base, uint32_t (&v)[kXB]) {
 #pragma unroll
         for (int i = 0; i < kXB; ++i) {
@@ -257,23 +265,23 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
         }
     };
     if (a.x_is_bf16) {
-        float mx[kCols];
+        float mx[NC];
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) mx[c] = 0.0f;
+        for (int c = 0; c < NC; ++c) mx[c] = 0.0f;
         for (int base = threadIdx.x; base < items; base += kXB * nth) {
             uint32_t v[kXB];
             load_items(base, v);
 #pragma unroll
             for (int i = 0; i < kXB; ++i) {
-                const int c = min(kCols - 1, (base + i * nth) / kh);
+                const int c = min(NC - 1, (base + i * nth) / kh);
                 const float m2 = fmaxf(fabsf(__uint_as_float(v[i] << 16)), fabsf(__uint_as_float(v[i] & 0xFFFF0000u)));
 #pragma unroll
-                for (int cc = 0; cc < kCols; ++cc)
+                for (int cc = 0; cc < NC; ++cc)
                     if (cc == c) mx[cc] = fmaxf(mx[cc], m2);
             }
         }
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) {
+        for (int c = 0; c < NC; ++c) {
             float m = mx[c];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
         }
         __syncthreads();
     }
-    if (threadIdx.x < kCols) s_sig[threadIdx.x] = a.x_is_bf16 ? prescale_exponent(__int_as_float(s_max[threadIdx.x])) : 0;
+    if (threadIdx.x < NC) s_sig[threadIdx.x] = a.x_is_bf16 ? prescale_exponent(__int_as_float(s_max[threadIdx.x])) : 0;
     __syncthreads();
     for (int base = threadIdx.x; base < items; base += kXB * nth) {
         uint32_t v[kXB];
@@ -304,9 +312,11 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
     }
     __syncthreads();
 
-    const uint32_t* xcol = xs + g * xstride;  // this lane's MMA column = route slot g
+    const uint32_t* xcol = xs + g * xstride;  // this lane's MMA columns = route slots g and 8 + g
+    const uint32_t* xcol1 = xcol + kCols * xstride;
     for (; tp < ntp; tp += gridDim.y) {
         float d[4] = {0.f, 0.f, 0.f, 0.f};
+        float d1[4] = {0.f, 0.f, 0.f, 0.f};
         for (int cb = c0; cb < c1; cb += kGC13) {
             if (cb != c0) load_batch(cb);
 #pragma unroll
@@ -325,10 +335,12 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
                         const int h = j >> 1;
                         const uint32_t sa = gpair_selector(2 * (j & 1)), sb = gpair_selector(2 * (j & 1) + 1);
                         const int k2 = (c * 64 + 16 * j) / 2 + t;
-                        mma_f16_16816(d, gawq_pair(cs[i][0][h], sa, s2[0][h], b2[0][h]),
-                                      gawq_pair(cs[i][1][h], sa, s2[1][h], b2[1][h]),
-                                      gawq_pair(cs[i][0][h], sb, s2[0][h], b2[0][h]),
-                                      gawq_pair(cs[i][1][h], sb, s2[1][h], b2[1][h]), xcol[k2], xcol[k2 + 4]);
+                        const uint32_t a0 = gawq_pair(cs[i][0][h], sa, s2[0][h], b2[0][h]);
+                        const uint32_t a1 = gawq_pair(cs[i][1][h], sa, s2[1][h], b2[1][h]);
+                        const uint32_t a2 = gawq_pair(cs[i][0][h], sb, s2[0][h], b2[0][h]);
+                        const uint32_t a3 = gawq_pair(cs[i][1][h], sb, s2[1][h], b2[1][h]);
+                        mma_f16_16816(d, a0, a1, a2, a3, xcol[k2], xcol[k2 + 4]);
+                        if (two) mma_f16_16816(d1, a0, a1, a2, a3, xcol1[k2], xcol1[k2 + 4]);
                     }
                 }
             }
@@ -338,14 +350,20 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
         part[warp][g][2 * t + 1] = d[1];
         part[warp][g + 8][2 * t] = d[2];
         part[warp][g + 8][2 * t + 1] = d[3];
+        if (two) {
+            part[warp][g][kCols + 2 * t] = d1[0];
+            part[warp][g][kCols + 2 * t + 1] = d1[1];
+            part[warp][g + 8][kCols + 2 * t] = d1[2];
+            part[warp][g + 8][kCols + 2 * t + 1] = d1[3];
+        }
         // the next tile pair's first codes go out before the reduction
         if (tp + (int)gridDim.y < ntp) {
             set_rows(tp + gridDim.y);
             load_batch(c0);
         }
         __syncthreads();
-        if (threadIdx.x < 16 * kCols) {
-            const int j = threadIdx.x / kCols, c = threadIdx.x % kCols;
+        if (threadIdx.x < 16 * NC) {
+            const int j = threadIdx.x / NC, c = threadIdx.x % NC;
             if (c < cnt) {
                 float hg = 0.0f, hu = 0.0f;
                 for (int w = 0; w < kGW13; ++w) {
@@ -365,10 +383,10 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
 // ---------------------------------------------------------------------------
 // W2 for a group of routes sharing one expert -> y (fp16)
 // ---------------------------------------------------------------------------
-template <int MB>
+template <int MB, int NC>
 __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) {
-    extern __shared__ __align__(16) uint32_t acts[];  // [kCols][I/2 + 4]
-    __shared__ int s_route[kCols];
+    extern __shared__ __align__(16) uint32_t acts[];  // [NC][I/2 + 4]
+    __shared__ int s_route[NC];
     pdl_wait();
     pdl_launch_dependents();
     if ((int)blockIdx.x >= *a.n_groups) return;
@@ -376,11 +394,12 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
     const int e = grp.x, cnt = grp.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int astride = a.I / 2 + 4;
-    if (threadIdx.x < kCols) s_route[threadIdx.x] = threadIdx.x < cnt ? a.route_list[grp.y + threadIdx.x] : -1;
+    const bool two = NC == 16 && cnt > kCols;  // two MMA column sets on the same A fragments
+    if (threadIdx.x < NC) s_route[threadIdx.x] = threadIdx.x < cnt ? a.route_list[grp.y + threadIdx.x] : -1;
     __syncthreads();
     {
         // the group's act rows, all of a thread's loads in flight together
-        const int ih = a.I / 2, items = kCols * ih, nth = blockDim.x;
+        const int ih = a.I / 2, items = (two ? 2 * kCols : kCols) * ih, nth = blockDim.x;
         const uint32_t* act32 = reinterpret_cast<const uint32_t*>(a.act_ws);
         for (int base = threadIdx.x; base < items; base += kXB * nth) {
             uint32_t v[kXB];
@@ -400,6 +419,7 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
     const int ng = a.I / 16, gpr = a.I / 32;
     const bool al4 = a.meta_al4 != 0;
     const uint32_t* xcol = acts + g * astride;
+    const uint32_t* xcol1 = xcol + kCols * astride;
     // this CTA's 256-row blocks; warps are independent from here (no barrier)
     for (int nb = blockIdx.y; 256 * nb < a.K; nb += gridDim.y) {
     const int n0 = 256 * nb + 16 * warp;
@@ -410,6 +430,7 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
     const uint8_t* m0p = a.w2_meta + row0 * gpr * MB;
     const uint8_t* m8p = a.w2_meta + (row0 + 8) * gpr * MB;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
+    float d1[4] = {0.f, 0.f, 0.f, 0.f};
     for (int gb = 0; gb < ng; gb += kGG2) {
         uint32_t cs[kGG2 / 2][2];  // this lane's 4 bytes of unit (gb/2 + i): k16 groups gb+2i, gb+2i+1
         uint32_t mw[kGG2 / 2][2];
@@ -436,9 +457,10 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
                 gmeta_sb2<MB>(mw[i / 2][0], s0, b0);
                 gmeta_sb2<MB>(mw[i / 2][1], s8, b8);
                 const uint32_t sa = gpair_selector(2 * (i & 1)), sb = gpair_selector(2 * (i & 1) + 1);
-                mma_f16_16816(d, gawq_pair(cs[i / 2][0], sa, s0, b0), gawq_pair(cs[i / 2][1], sa, s8, b8),
-                              gawq_pair(cs[i / 2][0], sb, s0, b0), gawq_pair(cs[i / 2][1], sb, s8, b8),
-                              xcol[8 * j + t], xcol[8 * j + 4 + t]);
+                const uint32_t a0 = gawq_pair(cs[i / 2][0], sa, s0, b0), a1 = gawq_pair(cs[i / 2][1], sa, s8, b8);
+                const uint32_t a2 = gawq_pair(cs[i / 2][0], sb, s0, b0), a3 = gawq_pair(cs[i / 2][1], sb, s8, b8);
+                mma_f16_16816(d, a0, a1, a2, a3, xcol[8 * j + t], xcol[8 * j + 4 + t]);
+                if (two) mma_f16_16816(d1, a0, a1, a2, a3, xcol1[8 * j + t], xcol1[8 * j + 4 + t]);
             }
         }
     }
@@ -446,6 +468,7 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
     for (int q = 0; q < 4; ++q) {
         const int c = 2 * t + (q & 1), row = n0 + g + 8 * (q >> 1);
         if (c < cnt) a.y_ws[(size_t)s_route[c] * a.K + row] = __float2half_rn(d[q]);
+        if (two && kCols + c < cnt) a.y_ws[(size_t)s_route[kCols + c] * a.K + row] = __float2half_rn(d1[q]);
     }
     }
 }
@@ -492,18 +515,18 @@ cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, c
     return c;
 }
 
-template <int MB>
+template <int MB, int NC>
 cudaError_t launch_grouped_mb(const GArgs& a, int gmax, int cpg, cudaStream_t s) {
     const size_t rsmem = (size_t)4 * a.E * sizeof(int);
-    const size_t xsmem = (size_t)kCols * (a.K / 2 + 4) * 4;
-    const size_t asmem = (size_t)kCols * (a.I / 2 + 4) * 4;
+    const size_t xsmem = (size_t)NC * (a.K / 2 + 4) * 4;
+    const size_t asmem = (size_t)NC * (a.I / 2 + 4) * 4;
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kMoeGroupedMaxE * 4 * (int)sizeof(int));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(moe_w13_grouped_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kCols * (kMoeGroupedMaxK / 2 + 4) * 4);
+            e = cudaFuncSetAttribute(moe_w13_grouped_kernel<MB, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     NC * ((NC == kCols ? kMoeGroupedMaxK : kWideMaxK) / 2 + 4) * 4);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -512,9 +535,9 @@ cudaError_t launch_grouped_mb(const GArgs& a, int gmax, int cpg, cudaStream_t s)
     cudaError_t e = cudaLaunchKernelEx(&c, moe_route_kernel, a);
     if (e != cudaSuccess) return e;
     c = pdl_cfg(dim3(gmax, std::min(a.I / 16, cpg)), dim3(2 * kGW13 * 32), xsmem, s, at);
-    if ((e = cudaLaunchKernelEx(&c, moe_w13_grouped_kernel<MB>, a)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&c, moe_w13_grouped_kernel<MB, NC>, a)) != cudaSuccess) return e;
     c = pdl_cfg(dim3(gmax, std::min((a.K + 255) / 256, cpg)), dim3(16 * 32), asmem, s, at);
-    if ((e = cudaLaunchKernelEx(&c, moe_w2_grouped_kernel<MB>, a)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&c, moe_w2_grouped_kernel<MB, NC>, a)) != cudaSuccess) return e;
     c = pdl_cfg(dim3(a.M, (a.K + 255) / 256), dim3(256), 0, s, at);
     return cudaLaunchKernelEx(&c, moe_combine_kernel, a);
 }
@@ -548,13 +571,20 @@ cudaError_t launch_moe_grouped(const MoeGroupedLaunch& L, cudaStream_t s) {
     a.route_list = L.route_list;
     a.groups = L.groups;
     a.n_groups = L.n_groups;
-    const int gmax = (int)moe_grouped_max_groups(L.M * L.topk, L.E);
+    const int routes = L.M * L.topk;
+    const int gmax = (int)moe_grouped_max_groups(routes, L.E);
+    // 16-route groups once experts average 8 routes or more: each decoded
+    // weight fragment then feeds two MMAs
+    const bool wide = L.K <= kWideMaxK && routes >= kCols * L.E;
+    a.gcap = wide ? 2 * kCols : kCols;
     // CTAs per group: about four waves' worth of CTAs in all (measured at
     // E=512 top-10: M=16 85.5 -> ~82 us with 4-5 per group; M=512 best with
     // 1-2 -- 466 us -- and 562 us with 5)
     const int sms = std::max(1, L.num_sms);
     const int cpg = std::max(1, std::min(kMaxCtasPerGroup, (4 * sms + gmax - 1) / gmax));
-    return L.meta_bytes == 4 ? launch_grouped_mb<4>(a, gmax, cpg, s) : launch_grouped_mb<3>(a, gmax, cpg, s);
+    if (L.meta_bytes == 4)
+        return wide ? launch_grouped_mb<4, 2 * kCols>(a, gmax, cpg, s) : launch_grouped_mb<4, kCols>(a, gmax, cpg, s);
+    return wide ? launch_grouped_mb<3, 2 * kCols>(a, gmax, cpg, s) : launch_grouped_mb<3, kCols>(a, gmax, cpg, s);
 }
 
 }  // namespace qmlp
