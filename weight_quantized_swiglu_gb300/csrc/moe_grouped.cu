@@ -51,7 +51,7 @@ constexpr int kCols = 8;   // routes per MMA (n8); a group holds 8 or 16 routes 
 constexpr int kWideMaxK = 4096;  // 16-route groups: x of 16 tokens staged in shared memory
 constexpr int kRouteThreads = 1024;
 constexpr int kMaxCtasPerGroup = 5;  // CTAs per group (each loops over its share of the tile pairs / 256-row blocks)
-constexpr int kXB = 8;     // x items a thread has in flight while staging a group's tokens
+constexpr int kXB = 8;     // act items a thread has in flight while staging a group's routes (W2)
 
 struct GArgs {
     int E, K, I, M, topk;
@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
     __shared__ int s_route[NC];
     __shared__ int s_max[NC];
     __shared__ int s_sig[NC];
+    __shared__ int s_tok[NC];  // slot's token, -1 past the group's routes
     pdl_wait();
     pdl_launch_dependents();
     if ((int)blockIdx.x >= *a.n_groups) return;
@@ -244,69 +245,69 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
     };
     load_batch(c0);  // the first codes are in flight while x is staged
 
-    // the group's tokens -> fp16 pairs, each token times its own 2^sig.
-    // Items (slot c, pair k2) are spread over the CTA, kXB loads in flight
-    // per thread; bf16 input takes one pass for the per-token maxima and
-    // one to convert.
+    // the group's tokens -> fp16 pairs, each token times its own 2^sig. A
+    // thread takes pairs k2 = threadIdx.x + n * blockDim.x of every slot,
+    // eight slots' loads in flight together; bf16 input takes one pass for
+    // the per-token maxima and one to convert.
     const int xstride = a.K / 2 + 4;
     if (threadIdx.x < NC) {
-        s_route[threadIdx.x] = threadIdx.x < cnt ? a.route_list[grp.y + threadIdx.x] : -1;
+        const int r = threadIdx.x < cnt ? a.route_list[grp.y + threadIdx.x] : -1;
+        s_route[threadIdx.x] = r;
+        s_tok[threadIdx.x] = r >= 0 ? r / a.topk : -1;
         s_max[threadIdx.x] = 0;
     }
     __syncthreads();
     const uint32_t* xin = reinterpret_cast<const uint32_t*>(a.x);
-    const int kh = a.K / 2, items = ns * kh, nth = blockDim.x;
-    auto load_items = [&](int base, uint32_t (&v)[kXB]) {
+    const int kh = a.K / 2;
+    // slots [c0, c0 + 8) at pair k2 (zeros past the group's routes)
+    auto load_slots = [&](int c0, int k2, uint32_t (&v)[kCols]) {
 #pragma unroll
-        for (int i = 0; i < kXB; ++i) {
-            const int idx = base + i * nth;
-            const int c = idx / kh;
-            v[i] = (idx < items && c < cnt) ? xin[(size_t)(s_route[c] / a.topk) * kh + (idx - c * kh)] : 0u;
+        for (int c = 0; c < kCols; ++c) {
+            const int tk = s_tok[c0 + c];
+            v[c] = tk >= 0 ? xin[(size_t)tk * kh + k2] : 0u;
         }
     };
     if (a.x_is_bf16) {
-        float mx[NC];
+#pragma unroll 1
+        for (int c0 = 0; c0 < ns; c0 += kCols) {
+            float mx[kCols];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) mx[c] = 0.0f;
-        for (int base = threadIdx.x; base < items; base += kXB * nth) {
-            uint32_t v[kXB];
-            load_items(base, v);
+            for (int c = 0; c < kCols; ++c) mx[c] = 0.0f;
+            for (int k2 = threadIdx.x; k2 < kh; k2 += blockDim.x) {
+                uint32_t v[kCols];
+                load_slots(c0, k2, v);
 #pragma unroll
-            for (int i = 0; i < kXB; ++i) {
-                const int c = min(NC - 1, (base + i * nth) / kh);
-                const float m2 = fmaxf(fabsf(__uint_as_float(v[i] << 16)), fabsf(__uint_as_float(v[i] & 0xFFFF0000u)));
-#pragma unroll
-                for (int cc = 0; cc < NC; ++cc)
-                    if (cc == c) mx[cc] = fmaxf(mx[cc], m2);
+                for (int c = 0; c < kCols; ++c)
+                    mx[c] = fmaxf(mx[c], fmaxf(fabsf(__uint_as_float(v[c] << 16)),
+                                               fabsf(__uint_as_float(v[c] & 0xFFFF0000u))));
             }
-        }
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            float m = mx[c];
+            for (int c = 0; c < kCols; ++c) {
+                float m = mx[c];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0 && m > 0.0f) atomicMax(&s_max[c], __float_as_int(m));
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                if (lane == 0 && m > 0.0f) atomicMax(&s_max[c0 + c], __float_as_int(m));
+            }
         }
         __syncthreads();
     }
     if (threadIdx.x < NC) s_sig[threadIdx.x] = a.x_is_bf16 ? prescale_exponent(__int_as_float(s_max[threadIdx.x])) : 0;
     __syncthreads();
-    for (int base = threadIdx.x; base < items; base += kXB * nth) {
-        uint32_t v[kXB];
-        load_items(base, v);
+    for (int k2 = threadIdx.x; k2 < kh; k2 += blockDim.x) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < ns; c0 += kCols) {
+            uint32_t v[kCols];
+            load_slots(c0, k2, v);
 #pragma unroll
-        for (int i = 0; i < kXB; ++i) {
-            const int idx = base + i * nth;
-            if (idx < items) {
-                const int c = idx / kh, k2 = idx - c * kh;
-                uint32_t o = v[i];
-                if (a.x_is_bf16 && c < cnt) {
-                    const int sg = s_sig[c];
+            for (int c = 0; c < kCols; ++c) {
+                uint32_t o = v[c];
+                if (a.x_is_bf16) {
+                    const int sg = s_sig[c0 + c];
                     const __half2 h = __floats2half2_rn(scalbnf(__uint_as_float(o << 16), sg),
                                                         scalbnf(__uint_as_float(o & 0xFFFF0000u), sg));
                     o = *reinterpret_cast<const uint32_t*>(&h);
                 }
-                xs[c * xstride + k2] = o;
+                xs[(c0 + c) * xstride + k2] = o;
             }
         }
     }
