@@ -51,7 +51,6 @@ constexpr int kCols = 8;   // routes per MMA (n8); a group holds 8 or 16 routes 
 constexpr int kWideMaxK = 4096;  // 16-route groups: x of 16 tokens staged in shared memory
 constexpr int kRouteThreads = 1024;
 constexpr int kMaxCtasPerGroup = 5;  // CTAs per group (each loops over its share of the tile pairs / 256-row blocks)
-constexpr int kXB = 8;     // act items a thread has in flight while staging a group's routes (W2)
 
 struct GArgs {
     int E, K, I, M, topk;
@@ -399,20 +398,22 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
     if (threadIdx.x < NC) s_route[threadIdx.x] = threadIdx.x < cnt ? a.route_list[grp.y + threadIdx.x] : -1;
     __syncthreads();
     {
-        // the group's act rows, all of a thread's loads in flight together
-        const int ih = a.I / 2, items = (two ? 2 * kCols : kCols) * ih, nth = blockDim.x;
+        // the group's act rows: a thread takes pairs k2 = threadIdx.x + n * blockDim.x
+        // of every slot, eight slots' loads in flight together
+        const int ih = a.I / 2;
         const uint32_t* act32 = reinterpret_cast<const uint32_t*>(a.act_ws);
-        for (int base = threadIdx.x; base < items; base += kXB * nth) {
-            uint32_t v[kXB];
+        const int ns = two ? 2 * kCols : kCols;
+        for (int k2 = threadIdx.x; k2 < ih; k2 += blockDim.x) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < ns; c0 += kCols) {
+                uint32_t v[kCols];
 #pragma unroll
-            for (int i = 0; i < kXB; ++i) {
-                const int idx = base + i * nth, c = idx / ih;
-                v[i] = (idx < items && c < cnt) ? act32[(size_t)s_route[c] * ih + (idx - c * ih)] : 0u;
-            }
+                for (int c = 0; c < kCols; ++c) {
+                    const int r = s_route[c0 + c];
+                    v[c] = r >= 0 ? act32[(size_t)r * ih + k2] : 0u;
+                }
 #pragma unroll
-            for (int i = 0; i < kXB; ++i) {
-                const int idx = base + i * nth;
-                if (idx < items) acts[(idx / ih) * astride + idx % ih] = v[i];
+                for (int c = 0; c < kCols; ++c) acts[(c0 + c) * astride + k2] = v[c];
             }
         }
     }
