@@ -22,8 +22,9 @@
 //    not matter, because every route is one column of the MMAs below and a
 //    column's result depends on nothing else in the group.
 //  * moe_w13_grouped_kernel: 1-5 CTAs per group (fewer when there are many
-//    groups), each looping over its share of the 16-row gate/up tile pairs
-//    (x staged once per CTA);
+//    groups), each looping over its share of the row octets -- 8 gate rows
+//    and the matching 8 up rows as one 16-row MMA tile, so a CTA is only the
+//    10 K-split warps and two fit on an SM (x staged once per CTA);
 //    the group's tokens are the 8 (or 2 x 8) columns of the m16n8k16 MMAs
 //    (A fragments decoded as in the one-token kernel), each
 //    token prescaled by its own power of two; the K split over 10 warps is
@@ -44,13 +45,13 @@
 namespace qmlp {
 namespace {
 
-constexpr int kGW13 = 10;  // W13 K splits: 2 x kGW13 warps per CTA (gate and up tiles)
-constexpr int kGC13 = 4;   // 64-k chunks a W13 warp loads at once (lane-sliced banks: 4 bytes per unit and lane)
+constexpr int kGW13 = 10;  // W13 K splits: kGW13 warps per CTA, each on 8 gate + 8 up rows
+constexpr int kGC13 = 1;   // 64-k chunks a W13 warp loads at once (lane-sliced banks: 4 bytes per unit and lane)
 constexpr int kGG2 = 10;   // k16 groups a W2 warp loads at once
 constexpr int kCols = 8;   // routes per MMA (n8); a group holds 8 or 16 routes (NC), 16 as two MMAs per A fragment
 constexpr int kWideMaxK = 4096;  // 16-route groups: x of 16 tokens staged in shared memory
 constexpr int kRouteThreads = 1024;
-constexpr int kMaxCtasPerGroup = 5;  // CTAs per group (each loops over its share of the tile pairs / 256-row blocks)
+constexpr int kMaxCtasPerGroup = 5;  // CTAs per group (each loops over its share of the row octets / 256-row blocks)
 
 struct GArgs {
     int E, K, I, M, topk;
@@ -193,9 +194,9 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const GArgs a)
 // W13 + SwiGLU for a group of routes sharing one expert
 // ---------------------------------------------------------------------------
 template <int MB, int NC>
-__global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const GArgs a) {
+__global__ void __launch_bounds__(kGW13 * 32, 3) moe_w13_grouped_kernel(const GArgs a) {
     extern __shared__ __align__(16) uint32_t xs[];  // [NC][K/2 + 4] fp16 pairs (padded: no bank conflicts)
-    __shared__ float part[2 * kGW13][16][NC];
+    __shared__ float part[kGW13][16][NC];
     __shared__ int s_route[NC];
     __shared__ int s_max[NC];
     __shared__ int s_sig[NC];
@@ -209,17 +210,19 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
     const bool two = NC == 16 && cnt > kCols;
     const int ns = two ? 2 * kCols : kCols;  // slots staged
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int tile = warp / kGW13, ks = warp % kGW13;
+    const int ks = warp;
     const int Kc = a.K / 64, gpr = a.K / 32, N = 2 * a.I;
     const int cpw = (Kc + kGW13 - 1) / kGW13;
     const int c0 = ks * cpw, c1 = min(Kc, c0 + cpw);
     const bool al4 = a.meta_al4 != 0;
-    // this CTA's tile pairs: tp = blockIdx.y, blockIdx.y + gridDim.y, ...
-    const int ntp = a.I / 16;
+    // this CTA's row octets tp = blockIdx.y, blockIdx.y + gridDim.y, ...:
+    // gate rows 8tp..8tp+7 are MMA rows 0-7 and the matching up rows MMA
+    // rows 8-15, so one warp's tile holds both halves of 8 SwiGLU outputs
+    const int ntp = a.I / 8;
     size_t rows[2];
     auto set_rows = [&](int tp) {
-        rows[0] = (size_t)e * N + tile * a.I + 16 * tp + g;
-        rows[1] = rows[0] + 8;
+        rows[0] = (size_t)e * N + 8 * tp + g;
+        rows[1] = rows[0] + a.I;
     };
     int tp = blockIdx.y;
     set_rows(tp);
@@ -356,27 +359,27 @@ __global__ void __launch_bounds__(2 * kGW13 * 32) moe_w13_grouped_kernel(const G
             part[warp][g + 8][kCols + 2 * t] = d1[2];
             part[warp][g + 8][kCols + 2 * t + 1] = d1[3];
         }
-        // the next tile pair's first codes go out before the reduction
+        // the next octet's first codes go out before the reduction
         if (tp + (int)gridDim.y < ntp) {
             set_rows(tp + gridDim.y);
             load_batch(c0);
         }
         __syncthreads();
-        if (threadIdx.x < 16 * NC) {
+        if (threadIdx.x < 8 * NC) {
             const int j = threadIdx.x / NC, c = threadIdx.x % NC;
             if (c < cnt) {
                 float hg = 0.0f, hu = 0.0f;
                 for (int w = 0; w < kGW13; ++w) {
                     hg += part[w][j][c];
-                    hu += part[kGW13 + w][j][c];
+                    hu += part[w][8 + j][c];
                 }
                 const int sg = s_sig[c];
                 const __half gh = __float2half_rn(scalbnf(hg, -sg)), uh = __float2half_rn(scalbnf(hu, -sg));
-                a.act_ws[(size_t)s_route[c] * a.I + 16 * tp + j] =
+                a.act_ws[(size_t)s_route[c] * a.I + 8 * tp + j] =
                     __float2half_rn(silu_f32(__half2float(gh)) * __half2float(uh));
             }
         }
-        __syncthreads();  // part is rewritten by the next tile pair
+        __syncthreads();  // part is rewritten by the next octet
     }
 }
 
@@ -536,7 +539,7 @@ cudaError_t launch_grouped_mb(const GArgs& a, int gmax, int cpg, cudaStream_t s)
     cudaLaunchConfig_t c = pdl_cfg(dim3(1), dim3(kRouteThreads), rsmem, s, at);
     cudaError_t e = cudaLaunchKernelEx(&c, moe_route_kernel, a);
     if (e != cudaSuccess) return e;
-    c = pdl_cfg(dim3(gmax, std::min(a.I / 16, cpg)), dim3(2 * kGW13 * 32), xsmem, s, at);
+    c = pdl_cfg(dim3(gmax, std::min(a.I / 8, cpg)), dim3(kGW13 * 32), xsmem, s, at);
     if ((e = cudaLaunchKernelEx(&c, moe_w13_grouped_kernel<MB, NC>, a)) != cudaSuccess) return e;
     c = pdl_cfg(dim3(gmax, std::min((a.K + 255) / 256, cpg)), dim3(16 * 32), asmem, s, at);
     if ((e = cudaLaunchKernelEx(&c, moe_w2_grouped_kernel<MB, NC>, a)) != cudaSuccess) return e;
@@ -579,11 +582,12 @@ cudaError_t launch_moe_grouped(const MoeGroupedLaunch& L, cudaStream_t s) {
     // weight fragment then feeds two MMAs
     const bool wide = L.K <= kWideMaxK && routes >= kCols * L.E;
     a.gcap = wide ? 2 * kCols : kCols;
-    // CTAs per group: about four waves' worth of CTAs in all (measured at
-    // E=512 top-10: M=16 85.5 -> ~82 us with 4-5 per group; M=512 best with
-    // 1-2 -- 466 us -- and 562 us with 5)
+    // CTAs per group: about four waves' worth of CTAs in all, counting the
+    // worst-case group count, and at least 2 (measured at E=512 top-10: M=16
+    // 64.9 us with 4 per group, 72.1 with 5; M=512 302.9 us with 2, 314.7
+    // with 1)
     const int sms = std::max(1, L.num_sms);
-    const int cpg = std::max(1, std::min(kMaxCtasPerGroup, (4 * sms + gmax - 1) / gmax));
+    const int cpg = std::max(2, std::min(kMaxCtasPerGroup, (4 * sms + gmax - 1) / gmax));
     if (L.meta_bytes == 4)
         return wide ? launch_grouped_mb<4, 2 * kCols>(a, gmax, cpg, s) : launch_grouped_mb<4, kCols>(a, gmax, cpg, s);
     return wide ? launch_grouped_mb<3, 2 * kCols>(a, gmax, cpg, s) : launch_grouped_mb<3, kCols>(a, gmax, cpg, s);
