@@ -18,7 +18,7 @@
  * Output rows are independent; they are spread over OpenMP threads without
  * changing any per-output summation order.
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - E2M1 is the OCP MX FP4 element (sign, 2 exponent bits with bias 1,
  *     1 mantissa bit); the pages only name it.
  *   - The NVFP4 global factor is the fp32 value 1.0f/global, applied to the
