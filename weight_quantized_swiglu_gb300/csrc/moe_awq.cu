@@ -31,9 +31,9 @@
 //  * B fragment = the token: x as fp16 (fp16 input as is; bf16 input times a
 //    power of two per call, exact for every value within 2^29 of max|x|),
 //    the intermediate act as fp16 (exact).
-//  * W13: a CTA per (route, 16-row gate/up tile pair); each warp takes one
-//    of the two tiles over a tenth of K, and the partial sums are added in a
-//    fixed order in shared memory.
+//  * W13: a CTA per (route, 8 gate rows and the matching 8 up rows as one
+//    16-row MMA tile); each warp takes the tile over a tenth of K, and the
+//    partial sums are added in a fixed order in shared memory.
 //  * W2: a CTA per 16 output rows with one warp per route; the fp16 route
 //    results are added in router order by one thread per output row.
 //  * Programmatic dependent launch: the W2 grid starts while W13 runs, reads
@@ -54,7 +54,7 @@
 namespace qmlp {
 namespace {
 
-constexpr int kK13 = 10;  // W13 K splits: a CTA has 2 x kK13 warps (gate and up tiles)
+constexpr int kK13 = 10;  // W13 K splits: a CTA has kK13 warps, each on 8 gate + 8 up rows
 constexpr int kC13 = 2;   // 64-k chunks a W13 warp loads at once (checkpoint layout)
 constexpr int kC13S = 4;  // the same with lane-sliced banks (a fifth of the registers per chunk)
 constexpr int kG2 = 10;   // k16 groups a W2 warp loads at once
@@ -130,9 +130,9 @@ QMLP_DEV uint32_t pair_selector(int t) {
 // W13 + SwiGLU
 // ---------------------------------------------------------------------------
 template <int MB, bool SL>
-__global__ void __launch_bounds__(2 * kK13 * 32) moe_w13_kernel(const Args a) {
+__global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
     extern __shared__ __align__(16) uint32_t x16[];  // [K/2] fp16 pairs
-    __shared__ float part[2 * kK13][16];            // [warp][row of its tile]
+    __shared__ float part[kK13][16];                // [warp][row of its tile]
     __shared__ int s_max;
     // the ids, x and (through the intermediate) the previous call's W2
     // stage belong to the kernels before this one
@@ -142,14 +142,15 @@ __global__ void __launch_bounds__(2 * kK13 * 32) moe_w13_kernel(const Args a) {
     const int id = a.ids[r];
     if (id < 0 || id >= a.E) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    // warp = (tile, K split): tile 0 = gate rows 16*bx.., tile 1 = up rows I + 16*bx..
-    const int tile = warp / kK13, ks = warp % kK13;
+    // warp = K split; its 16-row MMA tile is gate rows 8*bx.. (rows 0-7) and
+    // the matching up rows I + 8*bx.. (rows 8-15), both halves of 8 outputs
+    const int ks = warp;
     const int Kc = a.K / 64, gpr = a.K / 32, N = 2 * a.I;
     const int cpw = (Kc + kK13 - 1) / kK13;  // chunks per warp
     const int c0 = ks * cpw, c1 = min(Kc, c0 + cpw);
     const bool al4 = a.meta_al4 != 0;
-    const size_t row0 = (size_t)id * N + tile * a.I + 16 * blockIdx.x + g;
-    const size_t rows[2] = {row0, row0 + 8};
+    const size_t row0 = (size_t)id * N + 8 * blockIdx.x + g;
+    const size_t rows[2] = {row0, row0 + a.I};
     constexpr int kC = SL ? kC13S : kC13;
     uint4 cw[kC][2][2];      // checkpoint layout: the two 16-byte units of each row's 32-byte chunk
     uint32_t cs[kC][2][2];   // lane-sliced layout: this lane's 4 bytes of each unit
@@ -256,14 +257,14 @@ __global__ void __launch_bounds__(2 * kK13 * 32) moe_w13_kernel(const Args a) {
         part[warp][g + 8] = d[2];
     }
     __syncthreads();
-    if (threadIdx.x < 16) {
+    if (threadIdx.x < 8) {
         const int j = threadIdx.x;
         float hg = 0.0f, hu = 0.0f;
         for (int w = 0; w < kK13; ++w) {
             hg += part[w][j];
-            hu += part[kK13 + w][j];
+            hu += part[w][8 + j];
         }
-        const int q = 16 * blockIdx.x + j;
+        const int q = 8 * blockIdx.x + j;
         const __half gh = __float2half_rn(scalbnf(hg, -sig)), uh = __float2half_rn(scalbnf(hu, -sig));
         const __half act = __float2half_rn(silu_f32(__half2float(gh)) * __half2float(uh));
         a.act_ws[(size_t)r * a.I + q] = act;
@@ -390,8 +391,8 @@ cudaError_t launch_mb(const Args& a, cudaStream_t s) {
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t c13 = {};
-    c13.gridDim = dim3(a.I / 16, a.topk);
-    c13.blockDim = dim3(2 * kK13 * 32);
+    c13.gridDim = dim3(a.I / 8, a.topk);
+    c13.blockDim = dim3(kK13 * 32);
     c13.dynamicSmemBytes = (size_t)a.K * 2;
     c13.stream = s;
     c13.attrs = pdl;
