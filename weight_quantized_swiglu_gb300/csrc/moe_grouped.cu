@@ -32,9 +32,9 @@
 //  * moe_w2_grouped_kernel: as many CTAs per group, each looping over its
 //    share of the 256-row blocks, a warp per 16 rows, the group's act rows
 //    as the MMA columns; y is stored as fp16.
-//  * moe_combine_kernel: one thread per (token, output element) adds the
-//    token's valid routes in router order (fmaf, fp32), like the one-token
-//    W2 stage.
+//  * moe_combine_kernel: one thread per (token, 8 output elements, one
+//    16-byte load per route) adds the token's valid routes in router order
+//    (fmaf, fp32), like the one-token W2 stage.
 //  * All four are chained with programmatic dependent launch; a grid sized
 //    for the worst-case group count exits early past the real count.
 #include <algorithm>
@@ -481,30 +481,43 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
 // ---------------------------------------------------------------------------
 // ordered router-weighted sum per token
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) moe_combine_kernel(const GArgs a) {
+constexpr int kCombThr = 128;  // combine: threads per CTA, 8 output elements each
+
+__global__ void __launch_bounds__(kCombThr) moe_combine_kernel(const GArgs a) {
     pdl_wait();
     pdl_launch_dependents();
-    const int tok = blockIdx.x, n = 256 * blockIdx.y + threadIdx.x;
+    const int tok = blockIdx.x, n = 8 * (kCombThr * blockIdx.y + threadIdx.x);
     if (n >= a.K) return;
-    // every load first (an invalid route's y slot is read and ignored),
-    // then the sum in router order
+    // every load first (16 bytes of each route's y row; an invalid route's
+    // slot is read and ignored), then the sum in router order per element
     int id[16];
     float w[16];
-    __half y[16];
+    uint4 y[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
         if (r < a.topk) {
             const int i = tok * a.topk + r;
             id[r] = a.ids[i];
             w[r] = a.rw[i];
-            y[r] = a.y_ws[(size_t)i * a.K + n];
+            y[r] = *reinterpret_cast<const uint4*>(a.y_ws + (size_t)i * a.K + n);
         }
     }
-    float s = 0.0f;
+    float acc[8];
 #pragma unroll
-    for (int r = 0; r < 16; ++r)
-        if (r < a.topk && id[r] >= 0 && id[r] < a.E) s = fmaf(w[r], __half2float(y[r]), s);
-    a.out[(size_t)tok * a.K + n] = __float2half_rn(s);
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        if (r < a.topk && id[r] >= 0 && id[r] < a.E) {
+            const __half* h = reinterpret_cast<const __half*>(&y[r]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(w[r], __half2float(h[e]), acc[e]);
+        }
+    }
+    uint4 o;
+    __half* oh = reinterpret_cast<__half*>(&o);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) oh[e] = __float2half_rn(acc[e]);
+    *reinterpret_cast<uint4*>(a.out + (size_t)tok * a.K + n) = o;
 }
 
 cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* at) {
@@ -543,7 +556,7 @@ cudaError_t launch_grouped_mb(const GArgs& a, int gmax, int cpg, cudaStream_t s)
     if ((e = cudaLaunchKernelEx(&c, moe_w13_grouped_kernel<MB, NC>, a)) != cudaSuccess) return e;
     c = pdl_cfg(dim3(gmax, std::min((a.K + 255) / 256, cpg)), dim3(16 * 32), asmem, s, at);
     if ((e = cudaLaunchKernelEx(&c, moe_w2_grouped_kernel<MB, NC>, a)) != cudaSuccess) return e;
-    c = pdl_cfg(dim3(a.M, (a.K + 255) / 256), dim3(256), 0, s, at);
+    c = pdl_cfg(dim3(a.M, (a.K / 8 + kCombThr - 1) / kCombThr), dim3(kCombThr), 0, s, at);
     return cudaLaunchKernelEx(&c, moe_combine_kernel, a);
 }
 
