@@ -26,6 +26,11 @@
  *    stream. Forward calls only enqueue work (except *_host, which waits).
  *  - One handle serves one stream at a time: its workspace is shared by all
  *    calls on it.
+ *  - One GPU per process: the kernels' shared-memory attributes are set on
+ *    the first launch of each kernel in the process, for the device current
+ *    then; handles on a second device of the same process get QMLP_ERR_CUDA
+ *    from the launches that need a large shared-memory window. Run one
+ *    process per GPU.
  *  - Validation happens before any launch; a rejected call launches nothing.
  *  - Launch failures return QMLP_ERR_CUDA. Errors raised asynchronously by a
  *    kernel surface on a later call or on the caller's synchronization; a
