@@ -21,14 +21,14 @@
 //    routes inside an expert's bucket is whatever the atomics give: it does
 //    not matter, because every route is one column of the MMAs below and a
 //    column's result depends on nothing else in the group.
-//  * moe_w13_grouped_kernel: 1-5 CTAs per group (fewer when there are many
+//  * moe_w13_grouped_kernel: 2-5 CTAs per group (fewer when there are many
 //    groups), each looping over its share of the row octets -- 8 gate rows
 //    and the matching 8 up rows as one 16-row MMA tile, so a CTA is only the
-//    10 K-split warps and two fit on an SM (x staged once per CTA);
-//    the group's tokens are the 8 (or 2 x 8) columns of the m16n8k16 MMAs
-//    (A fragments decoded as in the one-token kernel), each
-//    token prescaled by its own power of two; the K split over 10 warps is
-//    added in a fixed order.
+//    10 K-split warps, each with one 64-k chunk in flight (64 registers:
+//    three CTAs per SM; x staged once per CTA); the group's tokens are the
+//    8 (or 2 x 8) columns of the m16n8k16 MMAs (A fragments decoded as in
+//    the one-token kernel), each token prescaled by its own power of two;
+//    the K split over 10 warps is added in a fixed order.
 //  * moe_w2_grouped_kernel: as many CTAs per group, each looping over its
 //    share of the 256-row blocks, a warp per 16 rows, the group's act rows
 //    as the MMA columns; y is stored as fp16.
