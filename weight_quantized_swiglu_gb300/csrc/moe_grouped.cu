@@ -598,7 +598,8 @@ cudaError_t launch_moe_grouped(const MoeGroupedLaunch& L, cudaStream_t s) {
     // CTAs per group: about four waves' worth of CTAs in all, counting the
     // worst-case group count, and at least 2 (measured at E=512 top-10: M=16
     // 64.9 us with 4 per group, 72.1 with 5; M=512 302.9 us with 2, 314.7
-    // with 1)
+    // with 1; with three W13 CTAs per SM, M=512 258 us with 2, 267 with 3,
+    // 269 with 4)
     const int sms = std::max(1, L.num_sms);
     const int cpg = std::max(2, std::min(kMaxCtasPerGroup, (4 * sms + gmax - 1) / gmax));
     if (L.meta_bytes == 4)
