@@ -4,7 +4,8 @@ Every step of the computation runs in the CUDA kernels of ``libqmlp.so``
 (built in-tree by ``weight_quantized_swiglu_gb300.build``); this module only
 marshals arguments through the C ABI declared in ``include/qmlp.h``. There is
 no CPU fallback: if the library is missing or fails to load, every call
-raises ``QmlpError``.
+raises ``RuntimeError``, and a failed call raises ``QmlpError`` (a
+``RuntimeError``) carrying the library's status.
 
 Module-level functions carry the C names (``qmlp_create``, ``qmlp_forward``,
 ...); ``QuantMLP`` and ``MoeAWQ`` wrap the handles for convenience. Device
