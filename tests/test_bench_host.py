@@ -30,3 +30,21 @@ def test_unparsable_lines_are_skipped_and_empty_output_is_none():
     assert r["samples"] == 1 and r["sm_mhz"] == 1500.0
     assert bench.parse_clock_samples("") is None
     assert bench.parse_clock_samples("0, [N/A], [N/A], 0, 0x0, a, b, c, d") is None
+
+
+def test_headline_traffic_record_is_used_only_for_the_captured_source(monkeypatch):
+    """The DRAM bytes the bench reports for its dominant kernel come from the
+    committed ncu record only while the kernel's sources hash to the value
+    recorded with the capture; otherwise the bench reports null."""
+    import json
+    rec = json.load(open(f"{bench.ROOT}/profiles/traffic.json"))["gemv_split_nvfp4_m1"]
+    t = bench.ncu_traffic("gemv_split_nvfp4_m1")
+    if t is not None:
+        # the capture moved at most a few percent more than the algorithmic
+        # bytes of one call (150,405,132 B: no re-reads)
+        assert 150_405_132 <= t <= 1.05 * 150_405_132
+    monkeypatch.setattr(bench, "kernel_src_sha", lambda files: "0" * 16)
+    assert bench.ncu_traffic("gemv_split_nvfp4_m1") is None
+    monkeypatch.setattr(bench, "kernel_src_sha", lambda files: rec["src_sha"])
+    assert bench.ncu_traffic("gemv_split_nvfp4_m1") == rec["dram_bytes_per_launch"]
+    assert bench.ncu_traffic("no_such_kernel") is None
