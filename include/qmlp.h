@@ -165,8 +165,66 @@ qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void*
  * barrier inside the kernel for one NVFP4 token, else by a small reduce
  * kernel launched after it). 0 when the shape has no such partition on this
  * device (the stream-K kernel is used instead). Used for M <= 8; the tensor-
- * core GEMM takes M >= 9 when this partition exists. */
+ * core GEMM takes M >= 9 when this partition exists.
+ * The one-token NVFP4 schedule waits (bounded, 2 s) at that grid barrier for
+ * all its CTAs, one per SM: if kernels of other streams hold SMs for longer,
+ * the call gives up, its output is not valid and qmlp_check returns
+ * QMLP_ERR_DEVICE_TIMEOUT. */
 int qmlp_decode_ctas(qmlp_t* h);
+
+/* The I-partitioned decode kernel (see qmlp_decode_ctas) with its raw
+ * epilogues, for tests that check its own weight layouts bit for bit:
+ *  x      = device bf16 [M, K]; act_in = device bf16 [M, I] (the down
+ *           projection consumes act_in instead of the SwiGLU of x)
+ *  g, u   = device fp32 [M, I]: sum_k x[m,k] W[i,k] of gate / up, no factor
+ *  out_f32= device fp32 [M, K]: sum_i act_in[m,i] Wd[o,i], no factor
+ * With one-hot x (act_in) every value is a single decoded weight exactly.
+ * 1 <= M <= 8. Errors: INVALID_ARG, ALIGNMENT, ALIAS, SHAPE (no partition for
+ * this shape, or M out of range), CUDA. */
+qmlp_status qmlp_debug_split(qmlp_t* h, const void* x, const void* act_in, int M, float* g, float* u,
+                             float* out_f32, qmlp_stream_t stream);
+
+/* Error-path tests only: every later launch of this handle's decode
+ * (I-partitioned) and tensor-core GEMM kernels gives up a wait on another
+ * role or CTA after limit_ns (0: the default of 2 s), and, when
+ * withhold_last_step is non-zero, their producers never issue their last
+ * weight step, so those waits run out: the kernels record it, leave without
+ * a fault, and qmlp_check returns QMLP_ERR_DEVICE_TIMEOUT. Errors: INVALID_ARG. */
+qmlp_status qmlp_debug_set_wait(qmlp_t* h, uint64_t limit_ns, int withhold_last_step);
+
+/*
+ * Tensor-parallel shard over the intermediate dimension (vllm.cpp issue "tp>1
+ * fp8w tail-MLP shard host-dequantizes every layer", "Proposed fix"): rank r
+ * of n keeps gate/up rows [r I/n, (r+1) I/n) and the same columns of down, and
+ * one sum over the ranks' [M, K] partials gives the layer's output.
+ */
+/* Create rank `rank`'s shard from the description of the WHOLE layer (the
+ * same pointers and sizes qmlp_create takes; only the shard's rows and columns
+ * are read). The handle's intermediate size is I / nranks; forward on it
+ * returns bf16(sigma_d x its own partial). Limits: as qmlp_create, plus
+ * 0 <= rank < nranks, I % nranks == 0, (I / nranks) % 16 == 0.
+ * Errors: as qmlp_create (INVALID_ARG for a bad rank). */
+qmlp_status qmlp_create_shard(qmlp_t** out, const qmlp_desc* desc, int rank, int nranks, qmlp_stream_t stream);
+
+/* This shard's partial: partial[m, o] = sum over the shard's i of act[m,i]
+ * Wd[o,i] in fp32 with no down factor (act = bf16 SwiGLU, as qmlp_forward).
+ *  x = device bf16 [M, K]; partial = device fp32 [M, K].
+ * Errors: as qmlp_forward. */
+qmlp_status qmlp_forward_partial(qmlp_t* h, const void* x, int M, float* partial, qmlp_stream_t stream);
+
+/* The exchange step after the partials are gathered (an all-gather of the
+ * [M, K] fp32 partials, rank-major): out[m, o] = bf16( sigma_d[o] * sum over
+ * r = 0..nranks-1 in rank order of partials[r][m][o] ). The order is fixed,
+ * so every rank computes the same bytes.
+ *  partials = device fp32 [nranks][M][K]; out = device bf16 [M, K]
+ * nranks must equal the handle's. Errors: INVALID_ARG, SHAPE, ALIGNMENT,
+ * ALIAS, CUDA. */
+qmlp_status qmlp_shard_combine(qmlp_t* h, const float* partials, int nranks, int M, void* out,
+                               qmlp_stream_t stream);
+
+/* Rank, rank count and intermediate size of a handle (0, 1 and I for a
+ * whole-layer handle). Returns 0 for a NULL handle, else 1. */
+int qmlp_shard_info(qmlp_t* h, int* rank, int* nranks, int* I_shard);
 
 /* Synchronize `stream` and report (then clear) a bounded-wait give-up
  * recorded by this handle's kernels: OK or DEVICE_TIMEOUT (CUDA on a sticky
@@ -248,7 +306,7 @@ qmlp_status qmlp_moe_reserve(qmlp_moe_t* h, int max_tokens, qmlp_stream_t stream
  *  out        = device fp16 [M, K]
  * M == 1 runs the one-token kernels. For M > 1 the valid routes of all tokens
  * are sorted by expert on the device and tokens that share an expert share
- * its weight reads (groups of up to 8 routes); results do not depend on the
+ * its weight reads (groups of up to 16 routes); results do not depend on the
  * grouping and are the same bytes every call. 1 <= topk <= 16,
  * 1 <= M <= the reserved max_tokens. Allocates nothing; graph-capturable.
  * Errors: INVALID_ARG, ALIGNMENT, ALIAS (out overlaps x, ids or router_w),
@@ -275,8 +333,12 @@ qmlp_status qmlp_moe_check(qmlp_moe_t* h, qmlp_stream_t stream);
  * capture. All calls share the array, which keeps the last call's contents
  * (no call needs it cleared: each route's row is written before it is read);
  * calls whose kernels overlap on the GPU (other streams, or other threads)
- * race on it and must be serialized by the caller.
- * Errors: INVALID_ARG, ALIGNMENT, ALIAS, SHAPE, UNSUPPORTED_ARCH, CUDA. */
+ * race on it and must be serialized by the caller. The looked-up address is
+ * kept for the life of the process: resetting the device (cudaDeviceReset,
+ * or tearing down and recreating its primary context) while the library
+ * stays loaded is not supported for this entry point.
+ * Errors: INVALID_ARG, ALIGNMENT, ALIAS (out overlaps x, ids, router_w or any
+ * of the four banks), SHAPE, UNSUPPORTED_ARCH, CUDA. */
 qmlp_status qmlp_moe_m1_forward_noalloc(const qmlp_moe_desc* banks, const void* x, qmlp_dtype xdt,
                                         const int32_t* expert_ids, const float* router_w, int topk,
                                         void* out, qmlp_stream_t stream);
@@ -284,7 +346,7 @@ qmlp_status qmlp_moe_m1_forward_noalloc(const qmlp_moe_desc* banks, const void* 
 /* Human-readable name of a status ("QMLP_OK", ...). Never NULL. */
 const char* qmlp_status_str(qmlp_status s);
 
-/* ABI version of this header (major * 100 + minor): 101 (multi-token routed experts). */
+/* ABI version of this header (major * 100 + minor): 102 (tensor-parallel shard). */
 int qmlp_abi_version(void);
 
 #ifdef __cplusplus

@@ -44,7 +44,7 @@ def test_binding_signatures_cover_the_header():
 def test_status_strings(L):
     assert q.qmlp_status_str(0) == "QMLP_OK"
     assert q.qmlp_status_str(8) == "QMLP_ERR_DEVICE_TIMEOUT"
-    assert q.qmlp_abi_version() == 101
+    assert q.qmlp_abi_version() == 102
 
 
 def test_null_arguments_are_rejected_without_a_device(L):
@@ -76,3 +76,25 @@ def test_bad_shapes_are_rejected_before_the_device(L):
 
 def test_library_is_built_for_sm_103a_only():
     assert qbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_noalloc_rejects_out_overlapping_the_banks_without_a_device(L):
+    """The allocation-free routed-expert call reads the caller's banks in
+    place, so an output that overlaps any of them is an alias error; the
+    check is pointer arithmetic only and runs before any device call."""
+    E, K, I, meta = 4, 64, 32, 4
+    sizes = [E * 2 * I * (K // 2), E * 2 * I * (K // 32) * meta, E * K * (I // 2), E * K * (I // 32) * meta]
+    base = 1 << 32
+    addr, pos = [], base
+    for n in sizes:  # four disjoint, 256-byte aligned fake device ranges
+        addr.append(pos)
+        pos += (n + 255) // 256 * 256 + 4096
+    x, ids, rw = pos, pos + 4096, pos + 8192
+    desc = q.qmlp_moe_desc(E, K, I, meta, *addr)
+    for a, n in zip(addr, sizes):
+        for out in (a, a + (n // 32) * 16):  # start of a bank, and inside it
+            assert q.qmlp_moe_m1_forward_noalloc(desc, x, q.DT_FP16, ids, rw, 4, out, 0) == 3, hex(out)
+    # an output just past the last bank passes the alias checks and then
+    # needs the device: anything but ALIAS (no GPU here)
+    out = addr[3] + (sizes[3] + 15) // 16 * 16 + 1024
+    assert q.qmlp_moe_m1_forward_noalloc(desc, x, q.DT_FP16, ids, rw, 4, out, 0) != 3

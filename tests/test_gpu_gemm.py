@@ -158,22 +158,47 @@ def test_gemm_activation_magnitudes_keep_precision(torch_cuda):
     mlp.close()
 
 
+def prefill_rows(M, seed):
+    """Rows the oracle checks at a prefill size: every row up to 512 tokens;
+    above, the first and the last row of every 128-token tile (so every token
+    tile of the persistent schedule is hit, at both ends) plus 128 seeded
+    random rows from the rest."""
+    if M <= 512:
+        return np.arange(M, dtype=np.int32)
+    ends = np.concatenate([np.arange(0, M, 128), np.minimum(np.arange(127, M + 127, 128), M - 1)])
+    rest = np.setdiff1d(np.arange(M), ends)
+    rnd = np.random.default_rng(seed).choice(rest, 128, replace=False)
+    return np.unique(np.concatenate([ends, rnd])).astype(np.int32)
+
+
+def test_prefill_rows_cover_every_tile():
+    rows = prefill_rows(8192, 1)
+    assert rows.size == 64 * 2 + 128
+    assert set(range(0, 8192, 128)) <= set(rows.tolist()) and set(range(127, 8192, 128)) <= set(rows.tolist())
+    assert np.array_equal(prefill_rows(512, 1), np.arange(512))
+
+
 @pytest.mark.parametrize("name", ["nvfp4_prefill", "fp8_prefill"])
 @pytest.mark.parametrize("variant", [0, 1])
 def test_parity_prefill(torch_cuda, variant, name):
     """The 27B-class prefill shape (K=5120, I=17408) at M = 512 and 8192 in
-    the launch configuration the bench times, NVFP4 and FP8 per-channel; the
-    oracle checks a seeded sample of rows (rows are independent), including
-    tile boundaries."""
+    the launch configuration the bench times, NVFP4 and FP8 per-channel. At
+    M = 512 the oracle checks every row; at M = 8192 it checks 256 rows (rows
+    are independent, so each is an exact oracle for its row): both ends of
+    every 128-token tile and 128 seeded random rows."""
     case = gen.workload_case(name, variant)
     M = case.M
     mlp = q.QuantMLP.from_case(case)
     out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
-    rng = np.random.default_rng(240 + variant)
-    rows = np.unique(np.concatenate([[0, 127, 128, M - 1], rng.choice(M, 20, replace=False)])).astype(np.int32)
+    rows = prefill_rows(M, 240 + variant)
     ref = oracle.dense_forward(case, rows=rows)
     compare(act[rows], ref["act"], what="act")
     compare(out[rows], ref["out"], what="out")
+    # every tile, row by row: one row that went wrong (a mis-assigned tile)
+    # must not hide inside the whole-sample norm
+    for i, r in enumerate(rows):
+        if r % 128 in (0, 127) or r == M - 1:
+            compare(out[r:r + 1], ref["out"][i:i + 1], what=f"out row {r}")
     out2, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
     assert np.array_equal(out, out2)
     mlp.close()

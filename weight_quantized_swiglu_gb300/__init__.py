@@ -69,6 +69,12 @@ _SIGS = {
     "qmlp_forward_debug": ([_VP, _I, _VP, _I, _VP, _VP, _VP], _I),
     "qmlp_debug_project": ([_VP, _I, _I, _VP, _I, _VP, _VP], _I),
     "qmlp_check": ([_VP, _VP], _I),
+    "qmlp_debug_split": ([_VP, _VP, _VP, _I, _VP, _VP, _VP, _VP], _I),
+    "qmlp_debug_set_wait": ([_VP, ctypes.c_uint64, _I], _I),
+    "qmlp_create_shard": ([ctypes.POINTER(_VP), ctypes.POINTER(qmlp_desc), _I, _I, _VP], _I),
+    "qmlp_forward_partial": ([_VP, _VP, _I, _VP, _VP], _I),
+    "qmlp_shard_combine": ([_VP, _VP, _I, _I, _VP, _VP], _I),
+    "qmlp_shard_info": ([_VP, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
     "qmlp_decode_ctas": ([_VP], _I),
     "qmlp_moe_create": ([ctypes.POINTER(_VP), ctypes.POINTER(qmlp_moe_desc), _VP], _I),
     "qmlp_moe_destroy": ([_VP], None),
@@ -172,6 +178,37 @@ def qmlp_check(h, stream=None) -> int:
     return lib().qmlp_check(h, _stream(stream))
 
 
+def qmlp_debug_split(h, x, act_in, M, g, u, out_f32, stream=None) -> int:
+    return lib().qmlp_debug_split(h, _ptr(x), _ptr(act_in), M, _ptr(g), _ptr(u), _ptr(out_f32), _stream(stream))
+
+
+def qmlp_debug_set_wait(h, limit_ns: int, withhold_last_step: bool) -> int:
+    return lib().qmlp_debug_set_wait(h, limit_ns, 1 if withhold_last_step else 0)
+
+
+def qmlp_create_shard(desc: qmlp_desc, rank: int, nranks: int, stream=None) -> int:
+    h = ctypes.c_void_p()
+    st = lib().qmlp_create_shard(ctypes.byref(h), ctypes.byref(desc), rank, nranks, _stream(stream))
+    _chk(st, "qmlp_create_shard")
+    return h.value
+
+
+def qmlp_forward_partial(h, x, M, partial, stream=None) -> int:
+    return lib().qmlp_forward_partial(h, _ptr(x), M, _ptr(partial), _stream(stream))
+
+
+def qmlp_shard_combine(h, partials, nranks, M, out, stream=None) -> int:
+    return lib().qmlp_shard_combine(h, _ptr(partials), nranks, M, _ptr(out), _stream(stream))
+
+
+def qmlp_shard_info(h):
+    """(rank, nranks, I of the handle)"""
+    r, n, i = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    if not lib().qmlp_shard_info(h, ctypes.byref(r), ctypes.byref(n), ctypes.byref(i)):
+        raise QmlpError(1, "qmlp_shard_info")
+    return r.value, n.value, i.value
+
+
 def qmlp_decode_ctas(h) -> int:
     return lib().qmlp_decode_ctas(h)
 
@@ -229,7 +266,9 @@ class QuantMLP:
     Weights may be numpy arrays (host) or torch CUDA tensors; they are copied
     into handle-owned device memory at construction."""
 
-    def __init__(self, fmt: str, K: int, I: int, max_M: int, gate, up, down, stream=None):
+    def __init__(self, fmt: str, K: int, I: int, max_M: int, gate, up, down, stream=None, shard=None):
+        """shard = (rank, nranks): this rank's tensor-parallel shard of the
+        whole layer described by the arguments (qmlp_create_shard)."""
         self.fmt = FMT_NVFP4 if fmt == "nvfp4" else FMT_FP8_PC
         self.K, self.I, self.max_M = K, I, max_M
         keep = []
@@ -240,11 +279,35 @@ class QuantMLP:
             keep += [o1, o2]
             projs.append(qmlp_proj(w, s, float(p.global_scale)))
         d = qmlp_desc(self.fmt, K, I, max_M, *projs)
-        self.h = qmlp_create(d, stream)
+        if shard is None:
+            self.h = qmlp_create(d, stream)
+        else:
+            self.h = qmlp_create_shard(d, shard[0], shard[1], stream)
+            self.I = I // shard[1]
+        self.rank, self.nranks, _ = qmlp_shard_info(self.h)
 
     @classmethod
-    def from_case(cls, case, max_M=None, stream=None):
-        return cls(case.fmt, case.K, case.I, max_M or case.M, case.gate, case.up, case.down, stream)
+    def from_case(cls, case, max_M=None, stream=None, shard=None):
+        return cls(case.fmt, case.K, case.I, max_M or case.M, case.gate, case.up, case.down, stream, shard)
+
+    def forward_partial(self, x, partial, M=None, stream=None):
+        """fp32 [M, K] partial of a tensor-parallel shard (no down factor)."""
+        M = x.shape[0] if M is None else M
+        _chk(qmlp_forward_partial(self.h, x, M, partial, stream), "qmlp_forward_partial")
+        return partial
+
+    def combine(self, partials, out, M=None, stream=None):
+        """out = bf16(sigma_d * rank-ordered sum of partials [nranks, M, K])."""
+        M = partials.shape[1] if M is None else M
+        _chk(qmlp_shard_combine(self.h, partials, self.nranks, M, out, stream), "qmlp_shard_combine")
+        return out
+
+    def debug_split(self, x, act_in, g, u, out_f32, M=None, stream=None):
+        M = x.shape[0] if M is None else M
+        _chk(qmlp_debug_split(self.h, x, act_in, M, g, u, out_f32, stream), "qmlp_debug_split")
+
+    def set_wait(self, limit_ns: int, withhold_last_step: bool = False):
+        _chk(qmlp_debug_set_wait(self.h, limit_ns, withhold_last_step), "qmlp_debug_set_wait")
 
     def forward(self, x, out, M=None, path=PATH_AUTO, stream=None):
         M = x.shape[0] if M is None else M

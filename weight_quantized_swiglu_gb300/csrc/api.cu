@@ -38,18 +38,26 @@ qmlp_status from_cuda(cudaError_t e) {
 }
 
 // Fault injection for host-side tests of the error paths: QMLP_FAULT_INJECT=
-// "alloc" makes device allocations fail, "launch" makes forward calls return
-// QMLP_ERR_CUDA before launching.
+// "alloc" makes every device allocation fail, "alloc:N" the N-th one a handle
+// makes (N >= 1; the earlier ones succeed and must be released), "launch"
+// makes forward calls return QMLP_ERR_CUDA before launching anything.
 bool fault(const char* what) {
     const char* v = getenv("QMLP_FAULT_INJECT");
     return v && strcmp(v, what) == 0;
 }
+long fault_alloc_index() {
+    const char* v = getenv("QMLP_FAULT_INJECT");
+    if (!v || strncmp(v, "alloc:", 6) != 0) return 0;
+    return strtol(v + 6, nullptr, 10);
+}
 
 struct Owner {
     std::vector<void*> ptrs;
+    long count = 0;  // allocations attempted by this owner
     cudaError_t alloc(void** p, size_t bytes) {
         *p = nullptr;
-        if (fault("alloc")) return cudaErrorMemoryAllocation;
+        ++count;
+        if (fault("alloc") || fault_alloc_index() == count) return cudaErrorMemoryAllocation;
         if (bytes == 0) bytes = 16;
         cudaError_t e = cudaMalloc(p, bytes);
         if (e == cudaSuccess) ptrs.push_back(*p);
@@ -96,6 +104,9 @@ struct qmlp_s {
     unsigned* bar = nullptr;   // grid barrier {count, generation}
     void* x_stage = nullptr;   // bf16 [max_M, K] (forward_host)
     void* out_stage = nullptr; // bf16 [max_M, K]
+    int rank = 0, nranks = 1;  // tensor-parallel shard of the intermediate dimension
+    uint64_t wait_ns = 0;      // error-path tests: bounded-wait limit of the kernels (0: default)
+    bool withhold = false;     // error-path tests: the kernels' producers skip their last step
     Owner mem;
 };
 
@@ -138,7 +149,7 @@ const char* qmlp_status_str(qmlp_status s) {
     return "QMLP_ERR_UNKNOWN";
 }
 
-int qmlp_abi_version(void) { return 101; }
+int qmlp_abi_version(void) { return 102; }
 
 // ---------------------------------------------------------------------------
 // dense MLP
@@ -189,9 +200,7 @@ static void free_tmp(qmlp_t* h, void* p) {
     }
 }
 
-qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) {
-    if (!out) return QMLP_ERR_INVALID_ARG;
-    *out = nullptr;
+static qmlp_status validate_desc(const qmlp_desc* d) {
     if (!d) return QMLP_ERR_INVALID_ARG;
     if (d->fmt != QMLP_FMT_NVFP4 && d->fmt != QMLP_FMT_FP8_PC) return QMLP_ERR_INVALID_ARG;
     if (!d->gate.w || !d->gate.scale || !d->up.w || !d->up.scale || !d->down.w || !d->down.scale)
@@ -202,11 +211,85 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
     if (d->fmt == QMLP_FMT_NVFP4 &&
         (!(d->gate.global_scale != 0.0f) || !(d->up.global_scale != 0.0f) || !(d->down.global_scale != 0.0f)))
         return QMLP_ERR_INVALID_ARG;
-    int dev = 0, sms = 0;
-    qmlp_status st = check_device(&dev, &sms);
-    if (st != QMLP_OK) return st;
+    return QMLP_OK;
+}
 
+// Build a handle from a validated description (the whole layer, or one
+// shard's slice of it). `h` is a fresh handle whose Owner may already hold
+// allocations; on error everything it owns is released and h is deleted.
+static qmlp_status create_impl(qmlp_t* h, qmlp_t** out, const qmlp_desc* d, int dev, int sms, cudaStream_t s);
+
+qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) {
+    if (!out) return QMLP_ERR_INVALID_ARG;
+    *out = nullptr;
+    qmlp_status st = validate_desc(d);
+    if (st != QMLP_OK) return st;
+    int dev = 0, sms = 0;
+    st = check_device(&dev, &sms);
+    if (st != QMLP_OK) return st;
+    return create_impl(new qmlp_t(), out, d, dev, sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Tensor-parallel shard over the intermediate dimension (vllm.cpp issue "tp>1
+// fp8w tail-MLP shard ...", "Proposed fix": gate/up row-sliced, down
+// column-sliced, one sum over the hidden output): rank r of n keeps gate/up
+// rows [r I/n, (r+1) I/n) -- contiguous rows of the checkpoint -- and the same
+// columns of down, copied out of each down row into a temporary buffer (a
+// strided copy, host or device source) before the normal create.
+qmlp_status qmlp_create_shard(qmlp_t** out, const qmlp_desc* d, int rank, int nranks, qmlp_stream_t stream) {
+    if (!out) return QMLP_ERR_INVALID_ARG;
+    *out = nullptr;
+    qmlp_status st = validate_desc(d);
+    if (st != QMLP_OK) return st;
+    if (nranks < 1 || rank < 0 || rank >= nranks) return QMLP_ERR_INVALID_ARG;
+    if (d->I % nranks || (d->I / nranks) % 16) return QMLP_ERR_SHAPE;
+    int dev = 0, sms = 0;
+    st = check_device(&dev, &sms);
+    if (st != QMLP_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool nv = d->fmt == QMLP_FMT_NVFP4;
+    const size_t K = (size_t)d->K, I = (size_t)d->I, Is = I / nranks, i0 = Is * rank;
+    qmlp_desc sd = *d;
+    sd.I = (int)Is;
+    const qmlp_proj* src[2] = {&d->gate, &d->up};
+    qmlp_proj* dst[2] = {&sd.gate, &sd.up};
+    for (int p = 0; p < 2; ++p) {
+        dst[p]->w = src[p]->w + i0 * (nv ? K / 2 : K);
+        dst[p]->scale = static_cast<const uint8_t*>(src[p]->scale) + i0 * (nv ? K / 16 : sizeof(float));
+    }
     qmlp_t* h = new qmlp_t();
+    h->rank = rank;
+    h->nranks = nranks;
+    // the down columns [i0, i0 + Is) of every one of its K rows
+    void *dw = nullptr, *ds = nullptr;
+    cudaError_t e;
+    const size_t wrow = nv ? I / 2 : I, wsh = nv ? Is / 2 : Is, woff = nv ? i0 / 2 : i0;
+    if ((e = h->mem.alloc(&dw, K * wsh)) != cudaSuccess) st = from_cuda(e);
+    else if (cudaMemcpy2DAsync(dw, wsh, d->down.w + woff, wrow, wsh, K, cudaMemcpyDefault, s) != cudaSuccess)
+        st = QMLP_ERR_CUDA;
+    if (st == QMLP_OK && nv) {
+        if ((e = h->mem.alloc(&ds, K * (Is / 16))) != cudaSuccess) st = from_cuda(e);
+        else if (cudaMemcpy2DAsync(ds, Is / 16, static_cast<const uint8_t*>(d->down.scale) + i0 / 16, I / 16,
+                                   Is / 16, K, cudaMemcpyDefault, s) != cudaSuccess)
+            st = QMLP_ERR_CUDA;
+    }
+    if (st != QMLP_OK) {
+        cudaStreamSynchronize(s);
+        h->mem.release();
+        delete h;
+        return st;
+    }
+    sd.down.w = static_cast<const uint8_t*>(dw);
+    if (nv) sd.down.scale = ds;  // FP8 keeps the K per-channel scales of down as they are
+    return create_impl(h, out, &sd, dev, sms, s);
+}
+
+
+static qmlp_status create_impl(qmlp_t* h, qmlp_t** out, const qmlp_desc* d, int dev, int sms, cudaStream_t s) {
+    qmlp_status st = QMLP_OK;
+    // allocations made for the shard's down columns before this point are
+    // temporaries: freed once the repack has consumed them
+    std::vector<void*> pre_tmp(h->mem.ptrs);
     h->fmt = d->fmt;
     h->K = d->K;
     h->I = d->I;
@@ -215,7 +298,6 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
     h->num_sms = sms;
     h->sp = plan_split(d->fmt, d->K, d->I, sms);
     h->layout_warps = h->sp.G ? h->sp.G * 16 : gemv_layout_warps(sms);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* tmp[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     const qmlp_proj* srcs[3] = {&d->gate, &d->up, &d->down};
     const int Ns[3] = {d->I, d->I, d->K}, Ks[3] = {d->K, d->K, d->I};
@@ -322,6 +404,7 @@ qmlp_status qmlp_create(qmlp_t** out, const qmlp_desc* d, qmlp_stream_t stream) 
             free_tmp(h, tmp[2 * p]);
             if (h->fmt == kNVFP4) free_tmp(h, tmp[2 * p + 1]);
         }
+        for (void* p : pre_tmp) free_tmp(h, p);
     }
     if (st != QMLP_OK) {
         cudaStreamSynchronize(s);
@@ -356,9 +439,11 @@ static bool use_gemm(qmlp_t* h, qmlp_path path, int M) {
     return h->has_gemm && M >= gemm_min_m(h);
 }
 
-// stage bit 0: gate/up + SwiGLU (x -> workspace act); bit 1: down (act -> out)
+// stage bit 0: gate/up + SwiGLU (x -> workspace act); bit 1: down (act ->
+// out). With out_f32 the down stage writes its fp32 sums without the down
+// factor there (a tensor-parallel shard's partial) instead of bf16 to out.
 static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void* x, int M, void* out,
-                              cudaStream_t s, bool host_io = false) {
+                              cudaStream_t s, bool host_io = false, float* out_f32 = nullptr) {
     if (fault("launch")) return QMLP_ERR_CUDA;
     const bool gemm = use_gemm(h, path, M);
     if (gemm && !h->has_gemm) return QMLP_ERR_SHAPE;
@@ -369,6 +454,8 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
         g.a16 = h->a16;
         g.sig = h->sig;
         g.ws = h->gemm_ws;
+        g.wait_ns = h->wait_ns;
+        g.withhold = h->withhold;
         if (stages & 1) {
             g.epi = kEpiSwiGLU;
             g.w = h->gm_gu;
@@ -377,10 +464,11 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
             if (launch_gemm(g, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
         }
         if (stages & 2) {
-            g.epi = kEpiPlain;
+            g.epi = out_f32 ? kEpiRaw : kEpiPlain;
+            g.raw_sel = 0;
             g.w = h->gm_d;
             g.a = h->act;
-            g.out = out;
+            g.out = out_f32 ? static_cast<void*>(out_f32) : out;
             if (launch_gemm(g, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
         }
         return QMLP_OK;
@@ -395,7 +483,8 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
         const int mb = std::min(block, M - m0);
         const void* xb = static_cast<const uint8_t*>(x) + (size_t)m0 * h->K * 2;
         void* ab = static_cast<uint8_t*>(h->act) + (size_t)m0 * h->I * 2;
-        void* ob = static_cast<uint8_t*>(out) + (size_t)m0 * h->K * 2;
+        void* ob = out_f32 ? static_cast<void*>(out_f32 + (size_t)m0 * h->K)
+                           : static_cast<void*>(static_cast<uint8_t*>(out) + (size_t)m0 * h->K * 2);
         GemvStreamPhase A, B;
         A.epi = kEpiSwiGLU;
         A.p0 = h->gv[0];
@@ -403,7 +492,7 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
         A.x = xb;
         A.out = ab;
         A.counters = h->counters;
-        B.epi = kEpiPlain;
+        B.epi = out_f32 ? kEpiRaw : kEpiPlain;
         B.p0 = h->gv[2];
         B.x = ab;
         B.out = ob;
@@ -426,14 +515,17 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
             S.x = xb;
             S.x_in_host = host_io;
             S.act_out = ab;  // the workspace act (qmlp_forward_debug returns it)
-            S.out = ob;
+            S.out = out_f32 ? nullptr : ob;
+            S.out_f32 = out_f32 ? static_cast<float*>(ob) : nullptr;
             S.part = h->spart;
             S.ticket = h->ticket;
             S.err = h->err;
+            S.wait_ns = h->wait_ns;
+            S.withhold = h->withhold;
             if (launch_split(S, h->sp, s) != cudaSuccess) return QMLP_ERR_CUDA;
             continue;
         }
-        if (stages == 3 && fitAB) {
+        if (stages == 3 && fitAB && !out_f32) {
             if (launch_gemv_stream(h->fmt, mb, A, &B, h->part, h->part_cap, h->bar, h->err, h->num_sms, s) !=
                 cudaSuccess)
                 return QMLP_ERR_CUDA;
@@ -465,7 +557,7 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
                                        s) != cudaSuccess)
                     return QMLP_ERR_CUDA;
             } else {
-                L.epi = kEpiPlain;
+                L.epi = out_f32 ? kEpiRaw : kEpiPlain;
                 L.p0 = h->gv[2];
                 L.p1 = GemvProj();
                 L.x = ab;
@@ -636,6 +728,87 @@ qmlp_status qmlp_check(qmlp_t* h, qmlp_stream_t stream) {
 }
 
 int qmlp_decode_ctas(qmlp_t* h) { return h ? h->sp.G : 0; }
+
+qmlp_status qmlp_debug_set_wait(qmlp_t* h, uint64_t limit_ns, int withhold_last_step) {
+    if (!h) return QMLP_ERR_INVALID_ARG;
+    h->wait_ns = limit_ns;
+    h->withhold = withhold_last_step != 0;
+    return QMLP_OK;
+}
+
+qmlp_status qmlp_debug_split(qmlp_t* h, const void* x, const void* act_in, int M, float* g, float* u,
+                             float* out_f32, qmlp_stream_t stream) {
+    if (!h || !x || !act_in || !g || !u || !out_f32) return QMLP_ERR_INVALID_ARG;
+    if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
+    if (!h->sp.G || M > kMaxSplitM || !split_fits(h->fmt, M, h->K, h->sp)) return QMLP_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(act_in) || !aligned16(g) || !aligned16(u) || !aligned16(out_f32))
+        return QMLP_ERR_ALIGNMENT;
+    const size_t xb = (size_t)M * h->K * 2, ab = (size_t)M * h->I * 2, gb = (size_t)M * h->I * 4,
+                 ob = (size_t)M * h->K * 4;
+    const void* outs[3] = {g, u, out_f32};
+    const size_t osz[3] = {gb, gb, ob};
+    for (int i = 0; i < 3; ++i) {
+        if (overlaps(outs[i], osz[i], x, xb) || overlaps(outs[i], osz[i], act_in, ab)) return QMLP_ERR_ALIAS;
+        for (int j = 0; j < i; ++j)
+            if (overlaps(outs[i], osz[i], outs[j], osz[j])) return QMLP_ERR_ALIAS;
+    }
+    if (fault("launch")) return QMLP_ERR_CUDA;
+    SplitLaunch S;
+    S.fmt = h->fmt;
+    S.M = M;
+    S.K = h->K;
+    S.I = h->I;
+    S.gate = h->gv[0];
+    S.up = h->gv[1];
+    S.wdown = h->wsplit;
+    S.chsd = h->gv[2].chs;
+    S.invd = h->gv[2].inv_g;
+    S.x = x;
+    S.act_out = h->act;
+    S.out_f32 = out_f32;
+    S.act_in = act_in;
+    S.dbg_g = g;
+    S.dbg_u = u;
+    S.part = h->spart;
+    S.ticket = h->ticket;
+    S.err = h->err;
+    S.wait_ns = h->wait_ns;
+    S.withhold = h->withhold;
+    return launch_split(S, h->sp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMLP_OK
+                                                                                          : QMLP_ERR_CUDA;
+}
+
+qmlp_status qmlp_forward_partial(qmlp_t* h, const void* x, int M, float* partial, qmlp_stream_t stream) {
+    if (!h || !x || !partial) return QMLP_ERR_INVALID_ARG;
+    if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(partial)) return QMLP_ERR_ALIGNMENT;
+    const size_t pb = (size_t)M * h->K * 4;
+    if (overlaps(partial, pb, x, (size_t)M * h->K * 2) || overlaps(partial, pb, h->act, (size_t)h->max_M * h->I * 2))
+        return QMLP_ERR_ALIAS;
+    return run_stages(h, QMLP_PATH_AUTO, 3, x, M, nullptr, reinterpret_cast<cudaStream_t>(stream), false, partial);
+}
+
+qmlp_status qmlp_shard_combine(qmlp_t* h, const float* partials, int nranks, int M, void* out,
+                               qmlp_stream_t stream) {
+    if (!h || !partials || !out) return QMLP_ERR_INVALID_ARG;
+    if (nranks != h->nranks) return QMLP_ERR_INVALID_ARG;
+    if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
+    if (!aligned16(partials) || !aligned16(out)) return QMLP_ERR_ALIGNMENT;
+    if (overlaps(out, (size_t)M * h->K * 2, partials, (size_t)nranks * M * h->K * 4)) return QMLP_ERR_ALIAS;
+    if (fault("launch")) return QMLP_ERR_CUDA;
+    return launch_shard_combine(h->fmt, partials, nranks, M, h->K, h->gv[2].inv_g, h->gv[2].chs,
+                                out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QMLP_OK
+               : QMLP_ERR_CUDA;
+}
+
+int qmlp_shard_info(qmlp_t* h, int* rank, int* nranks, int* I_shard) {
+    if (!h) return 0;
+    if (rank) *rank = h->rank;
+    if (nranks) *nranks = h->nranks;
+    if (I_shard) *I_shard = h->I;
+    return 1;
+}
 
 // ---------------------------------------------------------------------------
 // routed-expert AWQ

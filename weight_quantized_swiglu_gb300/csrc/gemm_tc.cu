@@ -117,6 +117,8 @@ struct Args {
     int splits;            // k-range splits per tile (1: the epilogue above; > 1: fp32 partials to ws)
     float* ws;             // [splits][M][N] fp32 partial sums (splits > 1)
     int* err;
+    uint64_t limit;        // ns a wait on another role may take before the CTA aborts
+    int withhold;          // error-path tests: the producer never loads its last k-step
 };
 
 // ---------------------------------------------------------------------------
@@ -194,12 +196,13 @@ constexpr uint32_t kIdesc = (1u << 4)                    // D format fp32
 
 // Wait for phase `parity` of `bar`; false if the CTA's abort flag is raised
 // or the wait ran out (which raises it and records `code`).
-QMLP_DEV bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, int code) {
+QMLP_DEV bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, int code,
+                             uint64_t limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kGemmWaitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             *abort_flag = 1;
             atomicExch(err, code);
             return false;
@@ -330,10 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const int nt = t / Mt, mt = t % Mt;
                 const uint8_t* blk = a.tiles + (size_t)nt * KS * kRawBytes;
                 const int ks1 = ks_begin(sp + 1);
-                for (int ks = ks_begin(sp); ks < ks1; ++ks, ++it) {
+                // error-path tests: the CTA's very last k-step is never loaded
+                const int ks_stop = (a.withhold && u + (int)gridDim.x >= units) ? ks1 - 1 : ks1;
+                for (int ks = ks_begin(sp); ks < ks_stop; ++ks, ++it) {
                     const int s = it % kLStages;
                     if (it >= kLStages &&
-                        !wait_or_abort(empty(s), (uint32_t)((it / kLStages - 1) & 1), abort_flag, a.err, 11)) {
+                        !wait_or_abort(empty(s), (uint32_t)((it / kLStages - 1) & 1), abort_flag, a.err, 11, a.limit)) {
                         ok = false;
                         break;
                     }
@@ -358,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const int sp = SPLIT ? u % nsp : 0;
                 const int buf = tc & 1, use = tc >> 1;
                 if (use > 0 &&
-                    !wait_or_abort(acc_empty(buf), (uint32_t)((use - 1) & 1), abort_flag, a.err, 12)) {
+                    !wait_or_abort(acc_empty(buf), (uint32_t)((use - 1) & 1), abort_flag, a.err, 12, a.limit)) {
                     ok = false;
                     break;
                 }
@@ -367,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const int kb = ks_begin(sp), ke = ks_begin(sp + 1);
                 for (int ks = kb; ks < ke; ++ks, ++it) {
                     const int s = it % kLStages, b = it % kBStages;
-                    if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 13) ||
-                        !wait_or_abort(bfull(b), (uint32_t)((it / kBStages) & 1), abort_flag, a.err, 14)) {
+                    if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 13, a.limit) ||
+                        !wait_or_abort(bfull(b), (uint32_t)((it / kBStages) & 1), abort_flag, a.err, 14, a.limit)) {
                         ok = false;
                         break;
                     }
@@ -403,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const int nt = t / Mt, mt = t % Mt;
             const int buf = tc & 1, use = tc >> 1;
             // warp-uniform: the TMEM loads below are .sync.aligned
-            const bool ready = wait_or_abort(acc_full(buf), (uint32_t)(use & 1), abort_flag, a.err, 15);
+            const bool ready = wait_or_abort(acc_full(buf), (uint32_t)(use & 1), abort_flag, a.err, 15, a.limit);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
             const int m = mt * BM + row_in_tile;
@@ -505,9 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const int ks1 = ks_begin(sp + 1);
             for (int ks = ks_begin(sp); ks < ks1; ++ks, ++it) {
                 const int s = it % kLStages, b = it % kBStages;
-                if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 16) ||
+                if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 16, a.limit) ||
                     (it >= kBStages &&
-                     !wait_or_abort(bempty(b), (uint32_t)((it / kBStages - 1) & 1), abort_flag, a.err, 17))) {
+                     !wait_or_abort(bempty(b), (uint32_t)((it / kBStages - 1) & 1), abort_flag, a.err, 17, a.limit))) {
                     ok = false;
                     break;
                 }
@@ -774,6 +779,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     a.out = L.out;
     a.ldo = L.epi == kEpiSwiGLU ? P.N / 2 : (L.epi == kEpiRaw && P.interleaved ? P.N / 2 : P.N);
     a.err = L.err;
+    a.limit = L.wait_ns ? L.wait_ns : kGemmWaitNs;
+    a.withhold = L.withhold ? 1 : 0;
     // Split-K when the tiles cannot fill the GPU (small M, or the down
     // projection's few column tiles): each (tile, k-range) unit writes fp32
     // partials and a reduce kernel adds them in split order. The partials

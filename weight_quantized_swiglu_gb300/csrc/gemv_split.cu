@@ -53,7 +53,7 @@ constexpr int kThr = kCT + 32;        // + one producer warp
 constexpr int kDepthMax = 16;
 constexpr int kBudget = 220 * 1024;
 constexpr int kBars = 2 * kDepthMax * 8 + 16;  // full, empty, x
-constexpr uint64_t kLimit = 2000000000ull;  // 2 s
+constexpr uint64_t kLimit = 2000000000ull;  // 2 s: waits for copies known to be in flight
 constexpr int kXRawMax = 16 * 1024;  // raw x copied to shared memory up to this size
 constexpr int kPreStepsBarrier = 1;          // weight steps issued before the wait on the previous kernel:
 constexpr int kPreStepsSep = kDepthMax;      //   schedule (a) / schedule (b) (the whole ring)
@@ -74,6 +74,10 @@ struct Args {
     const __nv_bfloat16* x;    // [M, K]
     __nv_bfloat16* act_out;    // optional [M, I]
     __nv_bfloat16* out;        // [M, K]
+    float* out_f32;            // optional [M, K]: the sums in fp32 without the down factor, instead of out
+    const __nv_bfloat16* act_in;  // optional [M, I]: phase B consumes these act values (debug)
+    float* dbg_g;              // optional [M, I]: gate dot products, fp32, no factor (debug)
+    float* dbg_u;              // optional [M, I]: up dot products, likewise
     float* part;               // [G][M][K]
     unsigned long long* ticket;
     int* err;
@@ -84,6 +88,8 @@ struct Args {
     int ring_off, slot_bytes, depth;
     int SA;                    // partial slots per gate/up tile
     int xraw_off, xraw_bytes;  // raw bf16 x copied to shared memory (0: staged from global)
+    uint64_t limit;            // ns a wait on another role or CTA may take before it gives up
+    int withhold;              // error-path tests: the producer never issues the last step
 };
 
 struct Ring {
@@ -91,6 +97,7 @@ struct Ring {
     uint32_t base_s, full0, empty0;
     uint32_t xbar;  // completion of the x copy
     int slot_bytes, depth;
+    uint64_t limit;  // Args::limit
 };
 
 // The producer's view of the two phases: step q < steps_a is the gate and up
@@ -114,7 +121,7 @@ template <int FMT>
 QMLP_DEV int produce(const Steps& st, const Ring& r, int* err, int q0, int q1) {
     int slot = q0 % r.depth, round = q0 / r.depth;
     for (int q = q0; q < q1; ++q) {
-        if (round > 0 && !mbar_wait_bounded(r.empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kLimit)) {
+        if (round > 0 && !mbar_wait_bounded(r.empty0 + 8u * slot, (uint32_t)((round - 1) & 1), r.limit)) {
             atomicExch(err, 24);
             return -(q + 1);
         }
@@ -216,9 +223,15 @@ QMLP_DEV void epilogue_a(const Args& a, int M, int lt, const float (&v)[2][NT][4
             const float s0 = FMT == kNVFP4 ? a.inv0 : a.chs0[i];
             const float s1 = FMT == kNVFP4 ? a.inv1 : a.chs1[i];
             const float pw = pow2_neg(s_sig[m]);
-            const float gv = v[0][n][e] * pw * s0;
-            const float uv = v[1][n][e] * pw * s1;
-            const __nv_bfloat16 act = __float2bfloat16_rn(silu_f32(gv) * uv);
+            const float graw = v[0][n][e] * pw, uraw = v[1][n][e] * pw;
+            const float gv = graw * s0;
+            const float uv = uraw * s1;
+            __nv_bfloat16 act = __float2bfloat16_rn(silu_f32(gv) * uv);
+            if (a.dbg_g) {
+                a.dbg_g[(size_t)m * a.I + i] = graw;
+                a.dbg_u[(size_t)m * a.I + i] = uraw;
+            }
+            if (a.act_in) act = a.act_in[(size_t)m * a.I + i];
             const float af = __bfloat162float(act);
             s_act[m * tslice + r] = af;
             // running max|act| of the slice (non-negative floats order as
@@ -353,7 +366,7 @@ QMLP_DEV bool phase_b_fixed(const Args& a, const Ring& r, int q, int steps, cons
     int slot = q % r.depth;
     uint32_t parity = (uint32_t)((q / r.depth) & 1);
     for (int j = 0; j < steps; ++j) {
-        if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, kLimit)) {
+        if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, a.limit)) {
             if (lane == 0) atomicExch(a.err, 22);
             return false;
         }
@@ -416,6 +429,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     r.base_s = smem_u32(r.base);
     r.slot_bytes = a.slot_bytes;
     r.depth = a.depth;
+    r.limit = a.limit;
     r.full0 = smem_u32(r.base + (size_t)a.depth * a.slot_bytes);
     r.empty0 = r.full0 + 8u * kDepthMax;
     r.xbar = r.empty0 + 8u * kDepthMax;
@@ -450,7 +464,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
             st.a1 = a.wa1 + (size_t)blockIdx.x * st.bytes_a;
             st.b = a.wb + (size_t)blockIdx.x * st.bytes_b;
             st.steps_a = stepsA;
-            st.steps = stepsA + stepsB;
+            st.steps = stepsA + stepsB - (a.withhold ? 1 : 0);
             // The weights do not depend on the previous kernel: the first
             // kPreSteps steps go out before the wait, x right after it, then
             // the rest of the weights. (Measured back to back: one step
@@ -487,7 +501,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
 
     // ---------------- phase A: gate/up over this CTA's tiles ----------------
     if (a.xraw_bytes) {
-        if (!mbar_wait_bounded(r.xbar, 0, kLimit)) {
+        if (!mbar_wait_bounded(r.xbar, 0, a.limit)) {
             if (lane == 0) atomicExch(a.err, 25);
             ok = false;
         }
@@ -525,7 +539,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         uint32_t parity = 0;
         int k = 0;
         for (int j = 0; j < stepsA && ok; ++j) {
-            if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, kLimit)) {
+            if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, a.limit)) {
                 if (lane == 0) atomicExch(a.err, 21);
                 ok = false;
                 break;
@@ -607,7 +621,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         uint32_t parity = (uint32_t)((q / r.depth) & 1);
         int k = 0;
         for (int j = 0; j < stepsB && ok; ++j) {
-            if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, kLimit)) {
+            if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, a.limit)) {
                 if (lane == 0) atomicExch(a.err, 22);
                 ok = false;
                 break;
@@ -664,7 +678,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         if (tk + 1ull != target) {
             const uint64_t t0 = globaltimer_ns();
             while (ld_acquire_u64(a.ticket) < target) {
-                if (globaltimer_ns() - t0 > kLimit) {
+                if (globaltimer_ns() - t0 > a.limit) {
                     atomicExch(a.err, 23);
                     pass = 0;
                     break;
@@ -725,8 +739,12 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
             float tot = 0.0f;
 #pragma unroll
             for (int w = 0; w < kW; ++w) tot += red[(i * kW + w) * 32 + lane];
-            const float sd = FMT == kNVFP4 ? a.invd : a.chsd[n];
-            a.out[(size_t)m * a.K + n] = __float2bfloat16_rn(tot * sd);
+            if (a.out_f32) {
+                a.out_f32[(size_t)m * a.K + n] = tot;
+            } else {
+                const float sd = FMT == kNVFP4 ? a.invd : a.chsd[n];
+                a.out[(size_t)m * a.K + n] = __float2bfloat16_rn(tot * sd);
+            }
         }
     }
 }
@@ -750,6 +768,7 @@ struct RArgs {
     const float* chsd;  // FP8 down per-channel scales
     float invd;         // NVFP4 down 1/global
     __nv_bfloat16* out; // [M, K]
+    float* out_f32;     // optional [M, K]: fp32 sums without the factor, instead of out
     int G, M, K;
 };
 
@@ -781,8 +800,12 @@ __global__ void __launch_bounds__(kRedThr, kRedMinBlocks) gemv_split_reduce_kern
             float tot = 0.0f;
 #pragma unroll
             for (int w = 0; w < kRedWarps; ++w) tot += red[w][lane];
-            const float sd = FMT == kNVFP4 ? a.invd : a.chsd[n];
-            a.out[(size_t)m * a.K + n] = __float2bfloat16_rn(tot * sd);
+            if (a.out_f32) {
+                a.out_f32[(size_t)m * a.K + n] = tot;
+            } else {
+                const float sd = FMT == kNVFP4 ? a.invd : a.chsd[n];
+                a.out[(size_t)m * a.K + n] = __float2bfloat16_rn(tot * sd);
+            }
         }
         __syncthreads();
     }
@@ -918,6 +941,10 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
     a.x = static_cast<const __nv_bfloat16*>(L.x);
     a.act_out = static_cast<__nv_bfloat16*>(L.act_out);
     a.out = static_cast<__nv_bfloat16*>(L.out);
+    a.out_f32 = L.out_f32;
+    a.act_in = static_cast<const __nv_bfloat16*>(L.act_in);
+    a.dbg_g = L.dbg_g;
+    a.dbg_u = L.dbg_u;
     a.part = L.part;
     a.ticket = L.ticket;
     a.err = L.err;
@@ -940,6 +967,8 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
     a.depth = lay.depth;
     a.SA = lay.sa;
     a.xraw_off = lay.xraw;
+    a.limit = L.wait_ns ? L.wait_ns : kLimit;
+    a.withhold = L.withhold ? 1 : 0;
     // the bulk copy of x needs device memory; host-resident x is staged by loads
     a.xraw_bytes = L.x_in_host ? 0 : lay.xraw_bytes;
     // M <= 8 (split_fits): one 8-token MMA tile. Schedule (a) for NVFP4 at
@@ -955,6 +984,7 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
     r.chsd = L.chsd;
     r.invd = L.invd;
     r.out = static_cast<__nv_bfloat16*>(L.out);
+    r.out_f32 = L.out_f32;
     r.G = P.G;
     r.M = L.M;
     r.K = L.K;

@@ -125,11 +125,23 @@ struct SplitLaunch {
     bool x_in_host = false;          // x is device-mapped host memory: staged with plain loads
     void* act_out = nullptr;         // optional bf16 [M, I]
     void* out = nullptr;             // bf16 [M, K]
+    float* out_f32 = nullptr;        // optional fp32 [M, K]: sums without the down factor, written instead of out
+    const void* act_in = nullptr;    // optional bf16 [M, I]: the down projection consumes these (debug)
+    float* dbg_g = nullptr;          // optional fp32 [M, I]: raw gate dot products (debug; with dbg_u)
+    float* dbg_u = nullptr;          // optional fp32 [M, I]: raw up dot products (debug)
     float* part = nullptr;           // >= split_part_elems
     unsigned long long* ticket = nullptr;  // grid-barrier ticket counter (zeroed at create)
     int* err = nullptr;
+    uint64_t wait_ns = 0;            // bounded-wait limit (0: the kernel's default of 2 s)
+    bool withhold = false;           // error-path tests: the last weight step is never issued
 };
 cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t s);
+
+// Tensor-parallel combine (tp_shard.cu): out[m, o] = bf16( sigma_d[o] * sum
+// over r = 0..nranks-1, in rank order, of partials[r][m][o] ), sigma_d = invd
+// (NVFP4) or chsd[o] (FP8).
+cudaError_t launch_shard_combine(int fmt, const float* partials, int nranks, int M, int K, float invd,
+                                 const float* chsd, void* out, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Tensor-core prefill GEMM (NVFP4, tcgen05)
@@ -160,6 +172,8 @@ struct GemmLaunch {
     int* sig = nullptr;       // workspace [M]: per-token prescale exponents
     int* err = nullptr;       // device error word
     float* ws = nullptr;      // split-K partials, >= gemm_splitk_ws_elems (null: no split-K)
+    uint64_t wait_ns = 0;     // bounded-wait limit (0: the kernel's default of 2 s)
+    bool withhold = false;    // error-path tests: the last k-step of each CTA is never loaded
 };
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s);
 size_t gemm_splitk_ws_elems(int num_sms);

@@ -29,7 +29,10 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once
-// per device (host code cannot use the symbol itself as an address).
+// per device (host code cannot use the symbol itself as an address). The
+// cached address is never refreshed: a device reset (or a primary-context
+// teardown) while the library stays loaded is not supported for this entry
+// point.
 cudaError_t scratch_address(int dev, void** out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -66,9 +69,14 @@ extern "C" qmlp_status qmlp_moe_m1_forward_noalloc(const qmlp_moe_desc* banks, c
     if (!aligned16(banks->w13) || !aligned16(banks->w2) || !aligned16(x) || !aligned16(out) ||
         !aligned16(expert_ids) || !aligned16(router_w))
         return QMLP_ERR_ALIGNMENT;
-    const size_t ob = (size_t)banks->K * 2;
+    // out is written while other CTAs still read the inputs and the caller's
+    // banks (read in place, never copied): it may overlap none of them
+    const size_t ob = (size_t)banks->K * 2, mb = (size_t)banks->meta;
+    const size_t E = (size_t)banks->E, K = (size_t)banks->K, I = (size_t)banks->I;
     if (overlaps(out, ob, x, (size_t)banks->K * 2) || overlaps(out, ob, expert_ids, (size_t)topk * 4) ||
-        overlaps(out, ob, router_w, (size_t)topk * 4))
+        overlaps(out, ob, router_w, (size_t)topk * 4) || overlaps(out, ob, banks->w13, E * 2 * I * (K / 2)) ||
+        overlaps(out, ob, banks->w13_meta, E * 2 * I * (K / 32) * mb) ||
+        overlaps(out, ob, banks->w2, E * K * (I / 2)) || overlaps(out, ob, banks->w2_meta, E * K * (I / 32) * mb))
         return QMLP_ERR_ALIAS;
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
