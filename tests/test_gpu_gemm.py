@@ -194,11 +194,19 @@ def test_parity_prefill(torch_cuda, variant, name):
     ref = oracle.dense_forward(case, rows=rows)
     compare(act[rows], ref["act"], what="act")
     compare(out[rows], ref["out"], what="out")
-    # every tile, row by row: one row that went wrong (a mis-assigned tile)
-    # must not hide inside the whole-sample norm
+    # every tile, row by row: one row that went wrong (a mis-assigned or
+    # skipped tile) must not hide inside the whole-sample norm. The contract's
+    # rel-L2 bound is for whole outputs (a single row of a correct result can
+    # sit just above it: act values that round the other way in fp32 and fp64
+    # move ~1 % of a row's outputs by one bf16 ulp); per row the check is the
+    # contract's max|delta| bound against the row's own max, and rel-L2 within
+    # 5e-3 -- a wrong tile is off by ~1.
+    g_all, r_all = oracle.bf16_bits_to_f64(out[rows]), oracle.bf16_bits_to_f64(ref["out"])
     for i, r in enumerate(rows):
         if r % 128 in (0, 127) or r == M - 1:
-            compare(out[r:r + 1], ref["out"][i:i + 1], what=f"out row {r}")
+            d = np.abs(g_all[i] - r_all[i])
+            assert d.max() <= 2e-2 * np.abs(r_all[i]).max(), f"row {r}"
+            assert np.linalg.norm(d) <= 5e-3 * np.linalg.norm(r_all[i]), f"row {r}"
     out2, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
     assert np.array_equal(out, out2)
     mlp.close()
