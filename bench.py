@@ -212,6 +212,28 @@ def time_graph(g, reps, stream):
     return e0.elapsed_time(e1)
 
 
+def time_graph_samples(g, stream, min_samples=7, min_seconds=1.0):
+    """Replays of `g` on `stream`, each timed by its own pair of CUDA events
+    on that stream, back to back: at least `min_samples` of them and at least
+    `min_seconds` of device time (so the clock sampler sees the timed region).
+    Returns the per-replay times in ms."""
+    import torch
+    times, total = [], 0.0
+    while len(times) < min_samples or total < min_seconds * 1e3:
+        n = max(min_samples, 64)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(n):
+                g.replay()
+                ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        batch = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+        times += batch
+        total += sum(batch)
+    return times
+
+
 def bench_headline(args, world, rank, local, pk):
     import torch
     import weight_quantized_swiglu_gb300 as q
@@ -221,32 +243,32 @@ def bench_headline(args, world, rank, local, pk):
     x = torch.from_numpy(case.x.view(np.int16)).cuda()
     out = torch.empty((1, K_HID), dtype=torch.int16, device="cuda")
     s = torch.cuda.Stream()
-    per_graph = R * max(1, 24 // R)
-    g = capture([(lambda m=mlps[i % R]: m.forward(x, out, stream=s)) for i in range(per_graph)], s)
-    reps = max(1, math.ceil(args.steps / per_graph))
-    K = reps * per_graph
+    # one graph of exactly K = --steps calls (the weights rotate over the R
+    # copies), replayed back to back; every replay is one timed sample
+    K = max(1, args.steps)
+    g = capture([(lambda m=mlps[i % R]: m.forward(x, out, stream=s)) for i in range(K)], s)
     with torch.cuda.stream(s):
-        for _ in range(max(1, math.ceil(args.warmup / per_graph))):
+        for _ in range(max(1, math.ceil(args.warmup / K))):
             g.replay()
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     time.sleep(0.25)
     barrier(world)
     torch.cuda.synchronize()
-    total_ms = time_graph(g, reps, s)
+    samples = time_graph_samples(g, s)
     barrier(world)
     clocks = sampler.stop()
-    total_ms = max_over_ranks(world, total_ms)
-    us_per_call = total_ms * 1e3 / K
+    med_ms = max_over_ranks(world, statistics.median(samples))
+    us_per_call = med_ms * 1e3 / K
     mlps[0].check()
     del g
 
     # per-projection kernels (stage launches) for diagnostics
+    per_graph = R * max(1, 24 // R)
     g0 = capture([(lambda m=mlps[i % R]: m.forward_stage(0, x, None, 1, stream=s)) for i in range(per_graph)], s)
     g1 = capture([(lambda m=mlps[i % R]: m.forward_stage(1, None, out, 1, stream=s)) for i in range(per_graph)], s)
-    r2 = max(1, reps // 4)
-    gu_us = time_graph(g0, r2, s) * 1e3 / (r2 * per_graph)
-    dn_us = time_graph(g1, r2, s) * 1e3 / (r2 * per_graph)
+    gu_us = statistics.median(time_graph_samples(g0, s, min_seconds=0.2)) * 1e3 / per_graph
+    dn_us = statistics.median(time_graph_samples(g1, s, min_seconds=0.2)) * 1e3 / per_graph
     del g0, g1
 
     # end-to-end through the host-buffer entry point (pinned buffers; the
@@ -255,7 +277,7 @@ def bench_headline(args, world, rank, local, pk):
     oh = torch.empty((1, K_HID), dtype=torch.int16).pin_memory()
     for i in range(3):
         mlps[i % R].forward_host(xh, oh, stream=s)
-    n_e2e = max(10, min(K, 2000))
+    n_e2e = max(200, min(K, 2000))
     barrier(world)
     t0 = time.perf_counter()
     for i in range(n_e2e):
@@ -269,7 +291,9 @@ def bench_headline(args, world, rank, local, pk):
     res = {
         "us_per_call": us_per_call,
         "steps": K,
-        "ms_per_step": total_ms / K,
+        "samples": len(samples),
+        "sample_spread_us": [min(samples) * 1e3 / K, max(samples) * 1e3 / K],
+        "ms_per_step": med_ms / K,
         "gu_us": gu_us,
         "down_us": dn_us,
         "hbm_gbs_call": achieved,
@@ -284,13 +308,48 @@ def bench_headline(args, world, rank, local, pk):
         "clocks": clocks,
         "rotating_copies": R,
         "l2_bytes": l2,
-        "gpu_launches": K,  # one kernel per call at M=1 (NVFP4: in-kernel reduction)
+        # one kernel per call at M=1 (NVFP4: in-kernel reduction), K calls per
+        # timed replay
+        "gpu_launches": K * len(samples),
     }
     return res, case
 
 
-def bench_dense_secondary(name, variant, reps, fmt_bytes):
-    """us/call of another dense workload (rotating copies, CUDA-graph replay)."""
+def oracle_time(fn, budget_s=2.0):
+    """Wall time of one call of an oracle function on this host's cores:
+    repeated until `budget_s` has passed (at least once). Returns (seconds
+    per call, calls)."""
+    if budget_s > 0:
+        fn()  # tables, page-in (skipped for the long, single-call timings)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return el / n, n
+
+
+def oracle_baseline(fn, unit_scale, unit, what, budget_s=2.0, extrapolate=None):
+    """cpu_baseline object of one workload: the oracle as it stands, timed on
+    the host cores. extrapolate = (factor, how) scales a timed sample to the
+    whole workload and says so."""
+    import oracle
+    oracle.build()
+    sec, n = oracle_time(fn, budget_s)
+    value = sec * unit_scale
+    sample = f"{n} oracle call(s) of {what}, {sec:.3f} s each"
+    kind = "oracle"
+    if extrapolate:
+        value *= extrapolate[0]
+        sample += f"; extrapolated to the whole workload: {extrapolate[1]}"
+        kind = "oracle (extrapolated)"
+    return {"value": value, "unit": unit, "cores": oracle.num_threads(), "kind": kind, "sample": sample}
+
+
+def bench_dense_secondary(name, variant, fmt_bytes):
+    """us/call of another dense workload (rotating copies, CUDA-graph replay,
+    median of >= 7 timed replays), with the oracle timed beside it."""
     import torch
     import weight_quantized_swiglu_gb300 as q
     case = gen.workload_case(name, variant)
@@ -302,13 +361,16 @@ def bench_dense_secondary(name, variant, reps, fmt_bytes):
     per_graph = R * max(1, 24 // R)
     g = capture([(lambda m=mlps[i % R]: m.forward(x, out, stream=s)) for i in range(per_graph)], s)
     time_graph(g, 1, s)
-    n = max(1, reps // per_graph)
-    us = time_graph(g, n, s) * 1e3 / (n * per_graph)
+    samples = time_graph_samples(g, s, min_seconds=0.3)
+    us = statistics.median(samples) * 1e3 / per_graph
     del g
     for m in mlps:
         m.close()
-    return {"M": case.M, "us_per_call": us, "gbs": fmt_bytes / (us * 1e-6) / 1e9,
-            "tokens_per_s": case.M / (us * 1e-6)}
+    import oracle
+    cpu = oracle_baseline(lambda: oracle.dense_forward(case), 1e6, UNIT,
+                          f"the full MLP (K={case.K}, I={case.I}, M={case.M}, fp64)")
+    return {"M": case.M, "us_per_call": us, "samples": len(samples), "gbs": fmt_bytes / (us * 1e-6) / 1e9,
+            "tokens_per_s": case.M / (us * 1e-6), "cpu_baseline": cpu}
 
 
 def bench_moe(meta_bytes=4):
@@ -354,6 +416,10 @@ def bench_moe(meta_bytes=4):
         res[mode] = {"ms_per_48_calls": ms48, "us_per_call": ms48 * 1e3 / 48,
                      "gbs": uniq * per_exp / (ms48 * 1e-3 / 48) / 1e9}
     moe.close()
+    import oracle
+    res["cpu_baseline"] = oracle_baseline(lambda: oracle.moe_m1_forward(c, meta_bytes, "fp16"), 1e6, "us/call",
+                                          f"the routed-expert step (E={c.E}, top-{c.topk}, {meta_bytes}-byte "
+                                          f"metadata, the hot id set)")
     return res
 
 
@@ -396,8 +462,18 @@ def bench_moe_tokens(Ms=(16, 512), meta_bytes=4):
             samples.append(e0.elapsed_time(e1))
         us = statistics.median(samples) * 1e3 / 20
         uniq = len({int(i) for i in tok.ids[:M].ravel() if 0 <= i < c.E})
+        import oracle
+        from dataclasses import replace
+        nt = min(M, 32)  # tokens are independent: a sample of them, scaled by M / nt
+
+        def run_tokens(nt=nt):
+            for t in range(nt):
+                oracle.moe_m1_forward(replace(c, x_fp16=tok.x16[t]), meta_bytes, "fp16", ids=tok.ids[t],
+                                      rw=tok.rw[t])
+        cpu = oracle_baseline(run_tokens, 1e6, "us/call", f"{nt} tokens' routed-expert steps",
+                              extrapolate=None if nt == M else (M / nt, f"x {M}/{nt} tokens"))
         res[f"M{M}"] = {"us_per_call": us, "tokens_per_s": M / (us * 1e-6), "unique_experts": uniq,
-                        "gbs_unique_bytes": uniq * per_exp / (us * 1e-6) / 1e9}
+                        "gbs_unique_bytes": uniq * per_exp / (us * 1e-6) / 1e9, "cpu_baseline": cpu}
         del g
     moe.check()
     moe.close()
@@ -429,8 +505,20 @@ def bench_prefill(M, reps, pk, fmt="nvfp4"):
     ms = statistics.median(times)
     flops = 2.0 * M * 3 * I_INT * K_HID
     tf = flops / (ms * 1e-3) / 1e12
-    return {"M": M, "ms_per_call": ms, "tflops": tf, "frac_bf16_peak": tf / pk["bf16_tflops_sustained"],
-            "tokens_per_s": M / (ms * 1e-3), "l2": "512 MB buffer written between calls"}
+    import oracle
+    if M <= 512:
+        cpu = oracle_baseline(lambda: oracle.dense_forward(case), 1e3, "ms/call",
+                              f"the full MLP (K={K_HID}, I={I_INT}, M={M}, fp64)", budget_s=0.0)
+    else:
+        rows = np.arange(0, M, M // 64, dtype=np.int32)[:64]
+        cpu = oracle_baseline(lambda: oracle.dense_forward(case, rows=rows), 1e3, "ms/call",
+                              f"64 token rows of the M={M} MLP (fp64; every call decodes all weights once)",
+                              budget_s=0.0, extrapolate=(M / 64, f"x {M}/64 rows (an upper bound: the weight "
+                                                                 f"decode is counted once per 64 rows)"))
+    # each call is timed alone (L2 flushed between calls): the burst peak applies
+    return {"M": M, "ms_per_call": ms, "tflops": tf, "frac_bf16_peak": tf / pk["bf16_tflops"],
+            "peak_tflops": pk["bf16_tflops"], "peak_kind": "bf16 burst (cuBLAS, isolated calls), " + pk["source"],
+            "tokens_per_s": M / (ms * 1e-3), "l2": "512 MB buffer written between calls", "cpu_baseline": cpu}
 
 
 def cpu_baseline(case, budget_s=10.0):
@@ -609,14 +697,13 @@ def main():
         import weight_quantized_swiglu_gb300 as q
         want = set(args.extras.split(",")) if args.extras != "all" else {"decode", "fp8", "tiny", "moe", "prefill"}
         if "decode" in want:
-            extras["dense_nvfp4_decode_M4"] = bench_dense_secondary("dense_nvfp4_decode", 1, 2400,
+            extras["dense_nvfp4_decode_M4"] = bench_dense_secondary("dense_nvfp4_decode", 1,
                                                                     nvfp4_bytes(K_HID, I_INT))
         if "fp8" in want:
-            extras["dense_fp8_decode_M1"] = bench_dense_secondary("dense_fp8_decode", 0, 2400, fp8_bytes(K_HID, I_INT))
-            extras["dense_fp8_decode_M16"] = bench_dense_secondary("dense_fp8_decode", 1, 1200,
-                                                                   fp8_bytes(K_HID, I_INT))
+            extras["dense_fp8_decode_M1"] = bench_dense_secondary("dense_fp8_decode", 0, fp8_bytes(K_HID, I_INT))
+            extras["dense_fp8_decode_M16"] = bench_dense_secondary("dense_fp8_decode", 1, fp8_bytes(K_HID, I_INT))
         if "tiny" in want:
-            extras["tiny_nvfp4_M1"] = bench_dense_secondary("tiny_nvfp4", 0, 4800, nvfp4_bytes(gen.TINY_K, gen.TINY_I))
+            extras["tiny_nvfp4_M1"] = bench_dense_secondary("tiny_nvfp4", 0, nvfp4_bytes(gen.TINY_K, gen.TINY_I))
         if "moe" in want:
             extras["moe_awq_m1_4B"] = bench_moe(4)
             extras["moe_awq_m1_3B"] = bench_moe(3)
