@@ -58,6 +58,7 @@ constexpr int kK13 = 10;  // W13 K splits: a CTA has kK13 warps, each on 8 gate 
 constexpr int kC13 = 2;   // 64-k chunks a W13 warp loads at once (checkpoint layout)
 constexpr int kC13S = 4;  // the same with lane-sliced banks (a fifth of the registers per chunk)
 constexpr int kG2 = 10;   // k16 groups a W2 warp loads at once
+constexpr int kXRegs = 4; // x pairs a W13 thread loads before the ids (K <= 2 * 4 * 320 = 2560 in one go)
 
 struct Args {
     int E, K, I;
@@ -129,18 +130,22 @@ QMLP_DEV uint32_t pair_selector(int t) {
 // ---------------------------------------------------------------------------
 // W13 + SwiGLU
 // ---------------------------------------------------------------------------
+// One W13 CTA: route r, gate rows 8 bx.. and the matching up rows. Returns
+// false (the whole CTA, uniformly) for an invalid route, which writes nothing.
 template <int MB, bool SL>
-__global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
-    extern __shared__ __align__(16) uint32_t x16[];  // [K/2] fp16 pairs
-    __shared__ float part[kK13][16];                // [warp][row of its tile]
-    __shared__ int s_max;
-    // the ids, x and (through the intermediate) the previous call's W2
-    // stage belong to the kernels before this one
-    pdl_wait();
-    pdl_launch_dependents();
-    const int r = blockIdx.y;
+QMLP_DEV bool w13_cta(const Args& a, int bx, int r, uint32_t* x16, float (*part)[16], int& s_max) {
+    // x does not depend on the route: its loads go out first, all at once
+    // (then the ids -> weights round trips run while they are in flight)
+    const uint32_t* xin32 = reinterpret_cast<const uint32_t*>(a.x);
+    const int K2 = a.K / 2;
+    uint32_t xv[kXRegs];
+#pragma unroll
+    for (int i = 0; i < kXRegs; ++i) {
+        const int k2 = threadIdx.x + i * (int)blockDim.x;
+        xv[i] = k2 < K2 ? xin32[k2] : 0u;
+    }
     const int id = a.ids[r];
-    if (id < 0 || id >= a.E) return;
+    if (id < 0 || id >= a.E) return false;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     // warp = K split; its 16-row MMA tile is gate rows 8*bx.. (rows 0-7) and
     // the matching up rows I + 8*bx.. (rows 8-15), both halves of 8 outputs
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
     const int cpw = (Kc + kK13 - 1) / kK13;  // chunks per warp
     const int c0 = ks * cpw, c1 = min(Kc, c0 + cpw);
     const bool al4 = a.meta_al4 != 0;
-    const size_t row0 = (size_t)id * N + 8 * blockIdx.x + g;
+    const size_t row0 = (size_t)id * N + 8 * bx + g;
     const size_t rows[2] = {row0, row0 + a.I};
     constexpr int kC = SL ? kC13S : kC13;
     uint4 cw[kC][2][2];      // checkpoint layout: the two 16-byte units of each row's 32-byte chunk
@@ -179,31 +184,39 @@ __global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
     };
     load_batch(c0);  // issued before x is staged: the two round trips overlap
 
-    // x -> fp16 pairs (bf16: times 2^sig so that max|x| lies in [2^14, 2^15))
-    const unsigned short* xin = reinterpret_cast<const unsigned short*>(a.x);
+    // x -> fp16 pairs (bf16: times 2^sig so that max|x| lies in [2^14, 2^15));
+    // pairs past kXRegs per thread (K > 2 kXRegs blockDim) are loaded here
     if (threadIdx.x == 0) s_max = 0;
     __syncthreads();
+    const int kreg = kXRegs * (int)blockDim.x;
     if (a.x_is_bf16) {
         float mx = 0.0f;
-        for (int k = threadIdx.x; k < a.K; k += blockDim.x)
-            mx = fmaxf(mx, fabsf(__bfloat162float(__ushort_as_bfloat16(xin[k]))));
+#pragma unroll
+        for (int i = 0; i < kXRegs; ++i)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(xv[i] << 16)), fabsf(__uint_as_float(xv[i] & 0xFFFF0000u))));
+        for (int k2 = kreg + threadIdx.x; k2 < K2; k2 += blockDim.x) {
+            const uint32_t v = xin32[k2];
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(v << 16)), fabsf(__uint_as_float(v & 0xFFFF0000u))));
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (lane == 0 && mx > 0.0f) atomicMax(&s_max, __float_as_int(mx));
         __syncthreads();
     }
     const int sig = a.x_is_bf16 ? prescale_exponent(__int_as_float(s_max)) : 0;
-    for (int k2 = threadIdx.x; k2 < a.K / 2; k2 += blockDim.x) {
-        const uint32_t v = reinterpret_cast<const uint32_t*>(xin)[k2];
-        if (a.x_is_bf16) {
-            const float lo = scalbnf(__uint_as_float(v << 16), sig);
-            const float hi = scalbnf(__uint_as_float(v & 0xFFFF0000u), sig);
-            const __half2 h = __floats2half2_rn(lo, hi);
-            x16[k2] = *reinterpret_cast<const uint32_t*>(&h);
-        } else {
-            x16[k2] = v;
-        }
+    auto to16 = [&](uint32_t v) -> uint32_t {
+        if (!a.x_is_bf16) return v;
+        const float lo = scalbnf(__uint_as_float(v << 16), sig);
+        const float hi = scalbnf(__uint_as_float(v & 0xFFFF0000u), sig);
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    };
+#pragma unroll
+    for (int i = 0; i < kXRegs; ++i) {
+        const int k2 = threadIdx.x + i * (int)blockDim.x;
+        if (k2 < K2) x16[k2] = to16(xv[i]);
     }
+    for (int k2 = kreg + threadIdx.x; k2 < K2; k2 += blockDim.x) x16[k2] = to16(xin32[k2]);
     __syncthreads();
 
     const uint32_t sel = pair_selector(t);
@@ -223,12 +236,11 @@ __global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {  // k16 group j: AWQ group j/2, words 2j, 2j+1 of the chunk
                     const int h = j >> 1;
-                    uint32_t x0 = 0, x1 = 0;
-                    if (g == 0) {
-                        const int k2 = (c * 64 + 16 * j) / 2 + t;
-                        x0 = x16[k2];
-                        x1 = x16[k2 + 4];
-                    }
+                    // B fragment: lanes with g == 0 hold column 0, the token;
+                    // the other lanes load the same words (a broadcast, no
+                    // branch) into columns 1-7, whose results are never read
+                    const int k2 = (c * 64 + 16 * j) / 2 + t;
+                    const uint32_t x0 = x16[k2], x1 = x16[k2 + 4];
                     uint32_t f0, f1, f2, f3;  // rows g, g+8 at k 2t.. (words 2j), then at 8+2t.. (words 2j+1)
                     if (SL) {
                         const uint32_t sa = pair_selector(2 * (j & 1)), sb = pair_selector(2 * (j & 1) + 1);
@@ -264,7 +276,7 @@ __global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
             hg += part[w][j];
             hu += part[w][8 + j];
         }
-        const int q = 8 * blockIdx.x + j;
+        const int q = 8 * bx + j;
         const __half gh = __float2half_rn(scalbnf(hg, -sig)), uh = __float2half_rn(scalbnf(hu, -sig));
         const __half act = __float2half_rn(silu_f32(__half2float(gh)) * __half2float(uh));
         a.act_ws[(size_t)r * a.I + q] = act;
@@ -274,20 +286,40 @@ __global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
         }
         if (a.act_dbg) a.act_dbg[(size_t)r * a.I + q] = act;
     }
+    return true;
+}
+
+template <int MB, bool SL>
+__global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
+    extern __shared__ __align__(16) uint32_t x16[];  // [K/2] fp16 pairs
+    __shared__ float part[kK13][16];                // [warp][row of its tile]
+    __shared__ int s_max;
+    // the ids, x and (through the intermediate) the previous call's W2
+    // stage belong to the kernels before this one
+    pdl_wait();
+    pdl_launch_dependents();
+    w13_cta<MB, SL>(a, blockIdx.x, blockIdx.y, x16, part, s_max);
 }
 
 // ---------------------------------------------------------------------------
 // W2 + ordered router-weighted sum
 // ---------------------------------------------------------------------------
+// One W2 CTA: output rows 16 bx.., warp r = route r. Launched with
+// programmatic dependent launch: the prologue (ids, codes, metadata) overlaps
+// the W13 grid, then griddepcontrol.wait makes the intermediate visible.
 template <int MB, bool SL>
-__global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
-    __shared__ float ys[16][16];
+QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s_ok) {
     const int r = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int n0 = 16 * blockIdx.x;
-    // prologue, overlapping the W13 stage: the ids (final before W13
-    // released this grid) and the first batch of codes and metadata
-    const int id = a.ids[r];
+    const int n0 = 16 * bx;
+    // prologue, overlapping the W13 stage: the ids and router weights (final
+    // before W13 released this grid), kept in shared memory for the final
+    // sum, and the first batch of codes and metadata
+    const int id = r < a.topk ? a.ids[r] : -1;
     const bool valid = id >= 0 && id < a.E;
+    if (lane == 0) {
+        s_ok[r] = valid ? 1 : 0;
+        s_rw[r] = valid ? a.rw[r] : 0.0f;
+    }
     const int ng = a.I / 16, gpr = a.I / 32;
     const size_t row0 = (size_t)(valid ? id : 0) * a.K + n0 + g;
     const uint2* c0p = reinterpret_cast<const uint2*>(a.w2 + row0 * (a.I / 2));
@@ -334,6 +366,16 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
     if (valid) {
         for (int gb = 0; gb < ng; gb += kG2) {
             if (gb > 0) load_batch(gb);
+            // the batch's act words, all loads at once; B fragment column 0
+            // (lanes g == 0) is the token, the other lanes load the same words
+            // into columns 1-7, whose results are never read (no branch)
+            uint32_t av[kG2][2];
+#pragma unroll
+            for (int i = 0; i < kG2; ++i) {
+                const int j = gb + i;
+                av[i][0] = j < ng ? act[8 * j + t] : 0u;
+                av[i][1] = j < ng ? act[8 * j + 4 + t] : 0u;
+            }
 #pragma unroll
             for (int i = 0; i < kG2; ++i) {
                 const int j = gb + i;
@@ -341,11 +383,7 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
                     uint32_t s0, b0, s8, b8;
                     meta_sb2<MB>(mw[i / 2][0], s0, b0);
                     meta_sb2<MB>(mw[i / 2][1], s8, b8);
-                    uint32_t x0 = 0, x1 = 0;
-                    if (g == 0) {
-                        x0 = act[8 * j + t];
-                        x1 = act[8 * j + 4 + t];
-                    }
+                    const uint32_t x0 = av[i][0], x1 = av[i][1];
                     if (SL) {
                         const uint32_t sa = pair_selector(2 * (i & 1)), sb = pair_selector(2 * (i & 1) + 1);
                         mma_f16_16816(d, awq_pair(cs[i / 2][0], sa, s0, b0), awq_pair(cs[i / 2][1], sa, s8, b8),
@@ -370,12 +408,18 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
     __syncthreads();
     if (threadIdx.x < 16) {
         float s = 0.0f;
-        for (int rr = 0; rr < a.topk; ++rr) {
-            const int idr = a.ids[rr];
-            if (idr >= 0 && idr < a.E) s = fmaf(a.rw[rr], ys[rr][threadIdx.x], s);
-        }
+        for (int rr = 0; rr < a.topk; ++rr)
+            if (s_ok[rr]) s = fmaf(s_rw[rr], ys[rr][threadIdx.x], s);
         a.out[n0 + threadIdx.x] = __float2half_rn(s);
     }
+}
+
+template <int MB, bool SL>
+__global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
+    __shared__ float ys[16][16];
+    __shared__ float s_rw[16];
+    __shared__ int s_ok[16];
+    w2_cta<MB, SL>(a, blockIdx.x, ys, s_rw, s_ok);
 }
 
 template <int MB, bool SL>
