@@ -836,17 +836,22 @@ qmlp_status qmlp_moe_create(qmlp_moe_t** out, const qmlp_moe_desc* d, qmlp_strea
     const size_t w2b = (size_t)d->E * d->K * (d->I / 2), m2b = (size_t)d->E * d->K * (d->I / 32) * mb;
     void *t0 = nullptr, *t1 = nullptr, *p = nullptr;
     cudaError_t e = cudaSuccess;
+    // W13: the warp-block bank of the K-split W13 kernels; W2: lane-sliced codes
     auto stage = [&](const void* src, size_t wbytes, const void* msrc, size_t mbytes, int N, int Kr,
-                     uint8_t** wdst, uint8_t** mdst) -> qmlp_status {
+                     uint8_t** wdst, uint8_t** mdst, bool w13) -> qmlp_status {
         if ((e = h->mem.alloc(&t0, wbytes)) != cudaSuccess) return from_cuda(e);
         if ((e = h->mem.alloc(&t1, mbytes)) != cudaSuccess) return from_cuda(e);
         if (cudaMemcpyAsync(t0, src, wbytes, cudaMemcpyDefault, s) != cudaSuccess) return QMLP_ERR_CUDA;
         if (cudaMemcpyAsync(t1, msrc, mbytes, cudaMemcpyDefault, s) != cudaSuccess) return QMLP_ERR_CUDA;
         void *wo = nullptr, *mo = nullptr;
-        if ((e = h->mem.alloc(&wo, wbytes)) != cudaSuccess) return from_cuda(e);
-        if ((e = h->mem.alloc(&mo, mbytes)) != cudaSuccess) return from_cuda(e);
-        if (repack_moe(static_cast<uint8_t*>(t0), static_cast<uint8_t*>(t1), d->meta, d->E, N, Kr,
-                       static_cast<uint8_t*>(wo), static_cast<uint8_t*>(mo), s) != cudaSuccess)
+        const size_t wob = w13 ? moe_w13_bank_bytes(d->E, d->I, d->K) : wbytes;
+        const size_t mob = w13 ? moe_w13_meta_bank_bytes(d->E, d->I, d->K, d->meta) : mbytes;
+        if ((e = h->mem.alloc(&wo, wob)) != cudaSuccess) return from_cuda(e);
+        if ((e = h->mem.alloc(&mo, mob)) != cudaSuccess) return from_cuda(e);
+        if ((w13 ? repack_moe_w13_blocks(static_cast<uint8_t*>(t0), static_cast<uint8_t*>(t1), d->meta, d->E, d->I,
+                                         d->K, static_cast<uint8_t*>(wo), static_cast<uint8_t*>(mo), s)
+                 : repack_moe(static_cast<uint8_t*>(t0), static_cast<uint8_t*>(t1), d->meta, d->E, N, Kr,
+                              static_cast<uint8_t*>(wo), static_cast<uint8_t*>(mo), s)) != cudaSuccess)
             return QMLP_ERR_CUDA;
         if (cudaStreamSynchronize(s) != cudaSuccess) return QMLP_ERR_CUDA;
         for (void* q : {t0, t1}) {
@@ -860,8 +865,8 @@ qmlp_status qmlp_moe_create(qmlp_moe_t** out, const qmlp_moe_desc* d, qmlp_strea
         *mdst = static_cast<uint8_t*>(mo);
         return QMLP_OK;
     };
-    st = stage(d->w13, w13b, d->w13_meta, m13b, 2 * d->I, d->K, &h->w13, &h->w13_meta);
-    if (st == QMLP_OK) st = stage(d->w2, w2b, d->w2_meta, m2b, d->K, d->I, &h->w2, &h->w2_meta);
+    st = stage(d->w13, w13b, d->w13_meta, m13b, 2 * d->I, d->K, &h->w13, &h->w13_meta, true);
+    if (st == QMLP_OK) st = stage(d->w2, w2b, d->w2_meta, m2b, d->K, d->I, &h->w2, &h->w2_meta, false);
     if (st == QMLP_OK) {
         if ((e = h->mem.alloc(&p, (size_t)16 * d->I * sizeof(__half))) != cudaSuccess) st = from_cuda(e);
         else h->act_ws = static_cast<__half*>(p);

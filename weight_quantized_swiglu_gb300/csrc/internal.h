@@ -225,6 +225,32 @@ struct MoeGroupedLaunch {
 };
 size_t moe_grouped_max_groups(int routes, int E);
 cudaError_t launch_moe_grouped(const MoeGroupedLaunch& L, cudaStream_t s);
+// W13 bank of a handle in warp blocks: the one-token and grouped W13 kernels
+// split K over kMoeKSplit warps, and warp ks of row octet o (gate rows
+// 8o..8o+7 and the matching up rows) reads one contiguous block per expert.
+// Block (e, o, ks) = [q (gate 0 / up 1)][pair p][lane l = 4g + t][16 B]: the
+// 16 bytes are chunks c = ks*cpw + 2p and +1 (64 k each, zero past the warp's
+// range), 8 bytes per chunk = the 32-bit words lane t picks from the chunk's
+// two 16-byte units of row g (byte t of each word of the unit). Metadata:
+// block (e, o, ks) = [q][g][the 2*cpw records of those chunks, padded to a
+// multiple of 16 bytes, sized for whole batches of 4 chunks: the one-token
+// kernel loads a batch's records at once]. Byte counts per block below.
+constexpr int kMoeKSplit = 10;
+__host__ __device__ inline int moe_w13_cpw(int K) { return (K / 64 + kMoeKSplit - 1) / kMoeKSplit; }
+__host__ __device__ inline int moe_w13_pairs(int K) { return (moe_w13_cpw(K) + 1) / 2; }
+__host__ __device__ inline size_t moe_w13_block_bytes(int K) { return (size_t)2 * moe_w13_pairs(K) * 512; }
+__host__ __device__ inline int moe_w13_meta_stride(int K, int MB) {
+    return (2 * ((moe_w13_cpw(K) + 3) / 4 * 4) * MB + 15) / 16 * 16;
+}
+__host__ __device__ inline size_t moe_w13_meta_block_bytes(int K, int MB) { return (size_t)2 * 8 * moe_w13_meta_stride(K, MB); }
+inline size_t moe_w13_bank_bytes(int E, int I, int K) { return (size_t)E * (I / 8) * kMoeKSplit * moe_w13_block_bytes(K); }
+inline size_t moe_w13_meta_bank_bytes(int E, int I, int K, int MB) {
+    return (size_t)E * (I / 8) * kMoeKSplit * moe_w13_meta_block_bytes(K, MB);
+}
+// checkpoint W13 codes [E, 2I, K/2] and records [E, 2I, K/32] x MB -> the
+// warp-block bank above
+cudaError_t repack_moe_w13_blocks(const uint8_t* w, const uint8_t* meta, int meta_bytes, int E, int I, int K,
+                                  uint8_t* w_out, uint8_t* meta_out, cudaStream_t s);
 cudaError_t repack_moe(const uint8_t* w, const uint8_t* meta, int meta_bytes, int E, int N,
                        int Kr, uint8_t* w_out, uint8_t* meta_out, cudaStream_t s);
 

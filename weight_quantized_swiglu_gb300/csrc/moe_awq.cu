@@ -151,16 +151,74 @@ QMLP_DEV bool w13_cta(const Args& a, int bx, int r, uint32_t* x16, float (*part)
     // the matching up rows I + 8*bx.. (rows 8-15), both halves of 8 outputs
     const int ks = warp;
     const int Kc = a.K / 64, gpr = a.K / 32, N = 2 * a.I;
-    const int cpw = (Kc + kK13 - 1) / kK13;  // chunks per warp
+    const int cpw = moe_w13_cpw(a.K);  // chunks per warp
+    static_assert(kK13 == kMoeKSplit, "the bank's warp blocks follow the K split");
     const int c0 = ks * cpw, c1 = min(Kc, c0 + cpw);
     const bool al4 = a.meta_al4 != 0;
     const size_t row0 = (size_t)id * N + 8 * bx + g;
     const size_t rows[2] = {row0, row0 + a.I};
     constexpr int kC = SL ? kC13S : kC13;
+    static_assert(!SL || kC == 4, "batches of 4 chunks: the bank's metadata slots are sized for them");
     uint4 cw[kC][2][2];      // checkpoint layout: the two 16-byte units of each row's 32-byte chunk
-    uint32_t cs[kC][2][2];   // lane-sliced layout: this lane's 4 bytes of each unit
+    uint32_t cs[kC][2][2];   // handle's bank: this lane's word of each unit
     uint32_t mw[kC][2][2];
+    // the handle's bank: this warp's block (e, octet, split) of codes and
+    // its metadata slots (internal.h): per row half, one 16-byte load per
+    // chunk pair and two (three for 3-byte records) for a batch's records
+    const size_t blk = ((size_t)id * (a.I / 8) + bx) * kMoeKSplit + ks;
+    const uint8_t* bcodes = a.w13 + blk * moe_w13_block_bytes(a.K);
+    const int np = moe_w13_pairs(a.K);
+    const int ms = moe_w13_meta_stride(a.K, MB);
     auto load_batch = [&](int cb) {
+        if (SL) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+#pragma unroll
+                for (int pi = 0; pi < kC / 2; ++pi) {
+                    const int pp = (cb - c0) / 2 + pi;
+                    if (pp < np) {
+                        const uint4 u = __ldg(reinterpret_cast<const uint4*>(bcodes + (size_t)(q * np + pp) * 512) +
+                                              lane);
+                        cs[2 * pi][q][0] = u.x;
+                        cs[2 * pi][q][1] = u.y;
+                        cs[2 * pi + 1][q][0] = u.z;
+                        cs[2 * pi + 1][q][1] = u.w;
+                    }
+                }
+                // records 2(cb - c0) .. 2(cb - c0) + 2kC - 1 of the (q, g) slot
+                const uint8_t* slot = a.w13_meta + blk * moe_w13_meta_block_bytes(a.K, MB) + (q * 8 + g) * ms +
+                                      (size_t)(cb - c0) * 2 * MB;
+                {
+                    if (MB == 4) {
+                        const uint4 m0 = __ldg(reinterpret_cast<const uint4*>(slot));
+                        const uint4 m1 = __ldg(reinterpret_cast<const uint4*>(slot) + 1);
+                        const uint32_t mr[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+                        for (int i = 0; i < kC; ++i) {
+                            mw[i][q][0] = mr[2 * i];
+                            mw[i][q][1] = mr[2 * i + 1];
+                        }
+                    } else {
+                        uint32_t mr[3 * kC / 2 + 1];
+#pragma unroll
+                        for (int j = 0; j < 3 * kC / 4; ++j) {
+                            const uint2 v = __ldg(reinterpret_cast<const uint2*>(slot) + j);
+                            mr[2 * j] = v.x;
+                            mr[2 * j + 1] = v.y;
+                        }
+                        mr[3 * kC / 2] = 0u;
+#pragma unroll
+                        for (int i = 0; i < kC; ++i)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int b = 3 * (2 * i + h);  // record 2i + h starts at byte b
+                                mw[i][q][h] = __funnelshift_r(mr[b / 4], mr[b / 4 + 1], 8 * (b % 4)) & 0xFFFFFFu;
+                            }
+                    }
+                }
+            }
+            return;
+        }
 #pragma unroll
         for (int i = 0; i < kC; ++i) {
             const int c = cb + i;
@@ -168,13 +226,8 @@ QMLP_DEV bool w13_cta(const Args& a, int bx, int r, uint32_t* x16, float (*part)
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const uint8_t* rowc = a.w13 + rows[q] * (a.K / 2) + c * 32;
-                    if (SL) {
-                        cs[i][q][0] = __ldg(reinterpret_cast<const unsigned int*>(rowc + 4 * t));
-                        cs[i][q][1] = __ldg(reinterpret_cast<const unsigned int*>(rowc + 16 + 4 * t));
-                    } else {
-                        cw[i][q][0] = __ldg(reinterpret_cast<const uint4*>(rowc));
-                        cw[i][q][1] = __ldg(reinterpret_cast<const uint4*>(rowc) + 1);
-                    }
+                    cw[i][q][0] = __ldg(reinterpret_cast<const uint4*>(rowc));
+                    cw[i][q][1] = __ldg(reinterpret_cast<const uint4*>(rowc) + 1);
                     const uint8_t* m = a.w13_meta + (rows[q] * gpr + 2 * c) * MB;
                     mw[i][q][0] = load_meta<MB>(m, al4);
                     mw[i][q][1] = load_meta<MB>(m + MB, al4);
@@ -500,6 +553,87 @@ __global__ void slice_units_kernel(const uint4* __restrict__ in, uint4* __restri
 }
 
 }  // namespace
+
+namespace {
+// One 16-byte item of the W13 warp-block bank (see internal.h) per thread:
+// (block, q, pair, lane) -> 4 words, chunk c = c0 + 2p + hh, unit h, word =
+// byte t of each of the unit's four checkpoint words.
+__global__ void w13_blocks_kernel(const uint8_t* __restrict__ w, int E, int I, int K, uint4* __restrict__ out) {
+    const int Kc = K / 64, cpw = moe_w13_cpw(K), np = moe_w13_pairs(K), no = I / 8;
+    const size_t items = (size_t)E * no * kMoeKSplit * 2 * np * 32;
+    for (size_t it = (size_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += (size_t)gridDim.x * blockDim.x) {
+        const int l = (int)(it % 32);
+        size_t rest = it / 32;
+        const int p = (int)(rest % np);
+        rest /= np;
+        const int q = (int)(rest % 2);
+        rest /= 2;
+        const int ks = (int)(rest % kMoeKSplit);
+        rest /= kMoeKSplit;
+        const int o = (int)(rest % no);
+        const size_t e = rest / no;
+        const int g = l >> 2, t = l & 3;
+        const int c0 = ks * cpw, c1 = min(Kc, c0 + cpw);
+        const size_t R = (size_t)(q == 0 ? 8 * o + g : I + 8 * o + g);
+        const uint8_t* row = w + (e * 2 * I + R) * (K / 2);
+        uint32_t o4[4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int c = c0 + 2 * p + hh;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v = 0;
+                if (c < c1) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(row + c * 32 + h * 16);
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v |= ((wd[j] >> (8 * t)) & 0xFFu) << (8 * j);
+                }
+                o4[hh * 2 + h] = v;
+            }
+        }
+        out[it] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    }
+}
+
+// One (block, q, g) metadata slot per thread: the 2 cpw records of row R's
+// chunks of the warp's range, zero past it and in the padding.
+__global__ void w13_meta_blocks_kernel(const uint8_t* __restrict__ meta, int MB, int E, int I, int K,
+                                       uint8_t* __restrict__ out) {
+    const int Kc = K / 64, cpw = moe_w13_cpw(K), gpr = K / 32, no = I / 8, ms = moe_w13_meta_stride(K, MB);
+    const size_t slots = (size_t)E * no * kMoeKSplit * 2 * 8;
+    for (size_t it = (size_t)blockIdx.x * blockDim.x + threadIdx.x; it < slots; it += (size_t)gridDim.x * blockDim.x) {
+        const int g = (int)(it % 8);
+        size_t rest = it / 8;
+        const int q = (int)(rest % 2);
+        rest /= 2;
+        const int ks = (int)(rest % kMoeKSplit);
+        rest /= kMoeKSplit;
+        const int o = (int)(rest % no);
+        const size_t e = rest / no;
+        const int c0 = ks * cpw, c1 = min(Kc, c0 + cpw);
+        const size_t R = (size_t)(q == 0 ? 8 * o + g : I + 8 * o + g);
+        const uint8_t* src = meta + ((e * 2 * I + R) * gpr + 2 * (size_t)c0) * MB;
+        uint8_t* dst = out + it * ms;
+        const int nb = 2 * max(0, c1 - c0) * MB;
+        for (int b = 0; b < ms; ++b) dst[b] = b < nb ? src[b] : 0;
+    }
+}
+}  // namespace
+
+cudaError_t repack_moe_w13_blocks(const uint8_t* w, const uint8_t* meta, int meta_bytes, int E, int I, int K,
+                                  uint8_t* w_out, uint8_t* meta_out, cudaStream_t s) {
+    if (K % 64 || I % 8 || E < 1) return cudaErrorInvalidValue;
+    const size_t items = moe_w13_bank_bytes(E, I, K) / 16;
+    w13_blocks_kernel<<<(unsigned)std::min<size_t>((items + 255) / 256, 65535), 256, 0, s>>>(
+        w, E, I, K, reinterpret_cast<uint4*>(w_out));
+    cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+    const size_t slots = (size_t)E * (I / 8) * kMoeKSplit * 16;
+    w13_meta_blocks_kernel<<<(unsigned)std::min<size_t>((slots + 255) / 256, 65535), 256, 0, s>>>(
+        meta, meta_bytes, E, I, K, meta_out);
+    return cudaPeekAtLastError();
+}
 
 // The handle's banks: codes lane-sliced ([E, N, Kr/2] bytes, every 16-byte
 // unit transposed), records as in the checkpoint ([E, N, Kr/32] records).

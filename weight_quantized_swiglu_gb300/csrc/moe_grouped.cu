@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(kGW13 * 32, 3) moe_w13_grouped_kernel(const GA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int ks = warp;
     const int Kc = a.K / 64, gpr = a.K / 32, N = 2 * a.I;
-    const int cpw = (Kc + kGW13 - 1) / kGW13;
+    const int cpw = moe_w13_cpw(a.K);
+    static_assert(kGW13 == kMoeKSplit, "the bank's warp blocks follow the K split");
     const int c0 = ks * cpw, c1 = min(Kc, c0 + cpw);
     const bool al4 = a.meta_al4 != 0;
     // this CTA's row octets tp = blockIdx.y, blockIdx.y + gridDim.y, ...:
@@ -228,24 +229,32 @@ __global__ void __launch_bounds__(kGW13 * 32, 3) moe_w13_grouped_kernel(const GA
     set_rows(tp);
     uint32_t cs[kGC13][2][2];  // this lane's 4 bytes of the two 16-byte units of each row's chunk
     uint32_t mw[kGC13][2][2];
-    auto load_batch = [&](int cb) {
+    // the handle's W13 bank in warp blocks (internal.h): block (e, octet tp,
+    // split ks); chunk c's two words of a row half are 8 adjacent bytes
+    const int np = moe_w13_pairs(a.K), ms = moe_w13_meta_stride(a.K, MB);
+    auto load_batch = [&](int cb, int octet) {
+        const size_t blk = ((size_t)e * (a.I / 8) + octet) * kMoeKSplit + ks;
+        const uint8_t* bc = a.w13 + blk * moe_w13_block_bytes(a.K);
+        const uint8_t* bm = a.w13_meta + blk * moe_w13_meta_block_bytes(a.K, MB);
 #pragma unroll
         for (int i = 0; i < kGC13; ++i) {
             const int c = cb + i;
             if (c < c1) {
+                const int cc = c - c0;
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const uint8_t* rowc = a.w13 + rows[q] * (a.K / 2) + c * 32;
-                    cs[i][q][0] = __ldg(reinterpret_cast<const unsigned int*>(rowc + 4 * t));
-                    cs[i][q][1] = __ldg(reinterpret_cast<const unsigned int*>(rowc + 16 + 4 * t));
-                    const uint8_t* m = a.w13_meta + (rows[q] * gpr + 2 * c) * MB;
+                    const uint2 u = __ldg(reinterpret_cast<const uint2*>(bc + (size_t)(q * np + cc / 2) * 512 +
+                                                                         lane * 16 + (cc % 2) * 8));
+                    cs[i][q][0] = u.x;
+                    cs[i][q][1] = u.y;
+                    const uint8_t* m = bm + (q * 8 + g) * ms + cc * 2 * MB;
                     mw[i][q][0] = gload_meta<MB>(m, al4);
                     mw[i][q][1] = gload_meta<MB>(m + MB, al4);
                 }
             }
         }
     };
-    load_batch(c0);  // the first codes are in flight while x is staged
+    load_batch(c0, tp);  // the first codes are in flight while x is staged
 
     // the group's tokens -> fp16 pairs, each token times its own 2^sig. A
     // thread takes pairs k2 = threadIdx.x + n * blockDim.x of every slot,
@@ -321,7 +330,7 @@ __global__ void __launch_bounds__(kGW13 * 32, 3) moe_w13_grouped_kernel(const GA
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         float d1[4] = {0.f, 0.f, 0.f, 0.f};
         for (int cb = c0; cb < c1; cb += kGC13) {
-            if (cb != c0) load_batch(cb);
+            if (cb != c0) load_batch(cb, tp);
 #pragma unroll
             for (int i = 0; i < kGC13; ++i) {
                 const int c = cb + i;
@@ -362,7 +371,7 @@ __global__ void __launch_bounds__(kGW13 * 32, 3) moe_w13_grouped_kernel(const GA
         // the next octet's first codes go out before the reduction
         if (tp + (int)gridDim.y < ntp) {
             set_rows(tp + gridDim.y);
-            load_batch(c0);
+            load_batch(c0, tp + gridDim.y);
         }
         __syncthreads();
         if (threadIdx.x < 8 * NC) {
