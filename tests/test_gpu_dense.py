@@ -116,13 +116,15 @@ def test_parity_dense_nvfp4_decode(torch_cuda, variant):
     mlp.close()
 
 
-@pytest.mark.parametrize("path", [q.PATH_AUTO, q.PATH_GEMV])
+@pytest.mark.parametrize("path", [q.PATH_AUTO, q.PATH_GEMV, q.PATH_GEMM])
 @pytest.mark.parametrize("variant", [0, 1])
 def test_parity_dense_fp8_decode(torch_cuda, variant, path):
-    """M = 1 and 16; at 16 tokens the automatic path is the tensor-core GEMM,
-    so the decode kernels' 16-token pass is also run explicitly."""
+    """M = 1 and 16; at 16 tokens the automatic path is one launch of the
+    I-partitioned decode kernel (two 8-token column tiles, x in two halves);
+    the tensor-core GEMM at the same token counts is run explicitly (a handle
+    with room for 17 tokens, so that it has GEMM tiles)."""
     case = case_of("dense_fp8_decode", variant)
-    mlp = q.QuantMLP.from_case(case)
+    mlp = q.QuantMLP.from_case(case, max_M=17 if path == q.PATH_GEMM else None)
     out, act = run_forward(torch_cuda, mlp, case.x, path=path)
     ref = oracle.dense_forward(case)
     compare(act, ref["act"], what="act")

@@ -23,11 +23,11 @@ def torch_cuda(cuda_available):
     return torch
 
 
-def run_forward(torch, mlp, x_bits):
+def run_forward(torch, mlp, x_bits, path=q.PATH_GEMV):
     M = x_bits.shape[0]
     out = torch.empty((M, mlp.K), dtype=torch.int16, device="cuda")
     act = torch.empty((M, mlp.I), dtype=torch.int16, device="cuda")
-    mlp.forward_debug(to_dev(x_bits), act, out, path=q.PATH_GEMV)
+    mlp.forward_debug(to_dev(x_bits), act, out, path=path)
     torch.cuda.synchronize()
     mlp.check()
     return bits_from_dev(out), bits_from_dev(act)
@@ -127,4 +127,24 @@ def test_split_host_buffers_match_device(torch_cuda, pinned, M):
         xh, oh = xh.pin_memory(), oh.pin_memory()
     mlp.forward_host(xh, oh)
     assert np.array_equal(oh.numpy().view(np.uint16), dev)
+    mlp.close()
+
+
+@pytest.mark.parametrize("M", [9, 13, 16])
+def test_fp8_sixteen_token_launch(torch_cuda, M):
+    """FP8 at 9..16 tokens on the 27B-class shape: one launch of the
+    I-partitioned kernel with two 8-token column tiles and x staged in two
+    halves (the second tile ragged below 16 tokens); every row against the
+    oracle, the same bytes on a second call, and the automatic path is this
+    kernel (not the GEMM)."""
+    case = gen.gen_dense_case("fp8", gen.DENSE_K, gen.DENSE_I, M, seed=330 + M)
+    mlp = q.QuantMLP.from_case(case, max_M=16)
+    out, act = run_forward(torch_cuda, mlp, case.x, path=q.PATH_AUTO)
+    ref = oracle.dense_forward(case)
+    compare(act, ref["act"], what="act")
+    compare(out, ref["out"], what="out")
+    out2, _ = run_forward(torch_cuda, mlp, case.x, path=q.PATH_AUTO)
+    assert np.array_equal(out, out2)
+    gemv, _ = run_forward(torch_cuda, mlp, case.x, path=q.PATH_GEMV)
+    assert np.array_equal(out, gemv)
     mlp.close()

@@ -20,9 +20,6 @@ using namespace qmlp;
 namespace {
 
 constexpr int kMaxGemvM = 16;
-// Largest token block the I-partitioned fused decode kernel takes (its
-// cross-CTA partials grow with M; larger blocks use the stream-K kernel).
-constexpr int kMaxSplitM = 8;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -110,12 +107,24 @@ struct qmlp_s {
     Owner mem;
 };
 
-// Fewest tokens the automatic path sends to the tensor-core GEMM. Measured on
-// the 27B-class shape (K=5120, I=17408): the single-launch decode kernel
-// takes 59 / 71 us (NVFP4 / FP8) at 8 tokens, but a second 8-token launch
-// for M = 9..16 (106-142 us) loses to the split-K GEMM (87-117 us). Shapes
-// without the I partition decode 16 tokens per stream-K pass.
-static int gemm_min_m(const qmlp_s* h) { return h->sp.G ? kMaxSplitM + 1 : kMaxGemvM + 1; }
+// Largest token block one launch of the I-partitioned decode kernel takes: 16
+// for FP8 (two 8-token column tiles, x staged in two halves) where the
+// partition allows it, else 8. Measured on the 27B-class shape at 16 tokens:
+// FP8 85 us against 96 us on the split-K GEMM; NVFP4 144 us against 87 us
+// (its group scales cost two fp32 FMAs per accumulator element, and every CTA
+// writes and the reduce kernel reads a [16, K] fp32 partial: 2 x 44.6 MB).
+static int split_max_m(const qmlp_s* h) {
+    if (!h->sp.G) return 0;
+    return h->fmt == kFP8 && split_fits(h->fmt, kMaxGemvM, h->K, h->sp) ? kMaxGemvM : 8;
+}
+
+// Fewest tokens the automatic path sends to the tensor-core GEMM: past what
+// one launch of the I-partitioned decode kernel takes (a second launch, which
+// streams the weights again, loses to the split-K GEMM: measured on the
+// 27B-class shape, 106-142 us for 9..16 tokens as two 8-token launches
+// against 87-117 us). Shapes without the I partition decode 16 tokens per
+// stream-K pass.
+static int gemm_min_m(const qmlp_s* h) { return h->sp.G ? split_max_m(h) + 1 : kMaxGemvM + 1; }
 
 struct qmlp_moe_s {
     int E = 0, K = 0, I = 0, meta = 0, device = 0, num_sms = 0;
@@ -478,7 +487,7 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
     // I-partitioned kernel when the shape has a partition (its shared-memory
     // staging of x grows with M), else 16 per stream-K / split-K pass
     const bool split = stages == 3 && h->sp.G && split_fits(h->fmt, 1, h->K, h->sp);
-    const int block = split ? kMaxSplitM : kMaxGemvM;
+    const int block = split ? split_max_m(h) : kMaxGemvM;
     for (int m0 = 0; m0 < M; m0 += block) {
         const int mb = std::min(block, M - m0);
         const void* xb = static_cast<const uint8_t*>(x) + (size_t)m0 * h->K * 2;
@@ -740,7 +749,7 @@ qmlp_status qmlp_debug_split(qmlp_t* h, const void* x, const void* act_in, int M
                              float* out_f32, qmlp_stream_t stream) {
     if (!h || !x || !act_in || !g || !u || !out_f32) return QMLP_ERR_INVALID_ARG;
     if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
-    if (!h->sp.G || M > kMaxSplitM || !split_fits(h->fmt, M, h->K, h->sp)) return QMLP_ERR_SHAPE;
+    if (!h->sp.G || M > split_max_m(h) || !split_fits(h->fmt, M, h->K, h->sp)) return QMLP_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(act_in) || !aligned16(g) || !aligned16(u) || !aligned16(out_f32))
         return QMLP_ERR_ALIGNMENT;
     const size_t xb = (size_t)M * h->K * 2, ab = (size_t)M * h->I * 2, gb = (size_t)M * h->I * 4,

@@ -347,6 +347,54 @@ QMLP_DEV void stage_x_one_token(const uint4* xr, int K, int kpe, uint4* xs, floa
     named_bar_sync(1, kCT);
 }
 
+// 9..16 tokens (see halves_ok): x of pass `pass` as prescaled fp16
+// fragments at half-local chunk positions. Chunk position cp < Kc/2 holds
+// global chunk (cp % q) + (cp / q) * (Kc/2) + pass * q, q = Kc/4 (the same
+// map as half_slot). With find_sig, the per-token exponents are found first
+// from all of x (warp m takes token m; M <= kW). Ends with a barrier over the
+// consumer threads. Loads go out eight per thread at a time.
+QMLP_DEV int half_slot(int c, int kca) { return (c % (kca / 4)) + (kca / 4) * (c / (kca / 2)); }
+
+QMLP_DEV void stage_x_half(const __nv_bfloat16* x, int M, int K, int pass, bool find_sig, uint4* xs, int* s_sig,
+                           int warp) {
+    const int lane = threadIdx.x & 31;
+    const int kca = K / kChunkK, q = kca / 4, h = kca / 2, k8 = K / 8;
+    if (find_sig) {
+        if (warp < M) {
+            const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)warp * K);
+            float mx = 0.0f;
+#pragma unroll 8
+            for (int i = lane; i < k8; i += 32) mx = fmaxf(mx, absmax8(__ldcg(xr + i)));
+            mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
+            if (lane == 0) s_sig[warp] = prescale_exponent(mx);
+        }
+        named_bar_sync(1, kCT);
+    }
+    const int slots = 4 * M, per_tok = h * 8, total = M * per_tok;
+    for (int base = threadIdx.x; base < total; base += 8 * kCT) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int it = base + u * kCT;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (it < total) {
+                const int m = it / per_tok, r = it - m * per_tok, cp = r >> 3, e8 = r & 7;
+                const int c = (cp % q) + (cp / q) * h + pass * q;
+                v[u] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)m * K + c * kChunkK + e8 * 8));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int it = base + u * kCT;
+            if (it < total) {
+                const int m = it / per_tok, r = it - m * per_tok;
+                stage_store8(xs, slots, m, (r >> 3) * kChunkK + (r & 7) * 8, s_sig[m], v[u]);
+            }
+        }
+    }
+    named_bar_sync(1, kCT);
+}
+
 // Phase B when the CTA's slice is CB = 1, 2 or 4 down chunks: every warp's
 // range starts on a row-tile boundary (LB is a multiple of 4), a step's 4
 // records are 4/CB whole tiles, and the CB activation fragments are the same
@@ -500,7 +548,9 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     pdl_wait();
 
     // ---------------- phase A: gate/up over this CTA's tiles ----------------
-    if (a.xraw_bytes) {
+    if (NT == 2) {
+        stage_x_half(a.x, M, a.K, 0, true, xs, s_sig, warp);
+    } else if (a.xraw_bytes) {
         if (!mbar_wait_bounded(r.xbar, 0, a.limit)) {
             if (lane == 0) atomicExch(a.err, 25);
             ok = false;
@@ -538,10 +588,21 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         int slot = 0;
         uint32_t parity = 0;
         int k = 0;
-        for (int j = 0; j < stepsA && ok; ++j) {
+        // 9..16 tokens: the warp's one tile part is combined after the loop
+        // (its slots alias the x halves); a warp whose wait gave up still
+        // reaches both barriers below
+        AccA<NT> pend;
+        int pend_lt = -1, pend_whole = 0;
+        for (int j = 0; j < stepsA && (ok || NT == 2); ++j) {
+            if (NT == 2 && j == stepsA / 2) {
+                named_bar_sync(1, kCT);  // every warp is done with the first half of x
+                stage_x_half(a.x, M, a.K, 1, false, xs, s_sig, warp);
+            }
+            if (!ok) continue;
             if (!mbar_wait_bounded(r.full0 + 8u * slot, parity, a.limit)) {
                 if (lane == 0) atomicExch(a.err, 21);
                 ok = false;
+                if (NT == 2) continue;
                 break;
             }
             const uint8_t* sb = r.base + (uint32_t)slot * (uint32_t)r.slot_bytes + (uint32_t)warp * kRA * rec;
@@ -550,7 +611,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                 w[0] = lds_chunk<FMT>(sb, lane);
                 w[1] = lds_chunk<FMT>(sb + step_bytes, lane);
                 uint4 xb[NT][2];
-                load_xfrag<NT>(xs, c, M, slots, g, t, xb);
+                load_xfrag<NT>(xs, NT == 2 ? half_slot(c, a.KcA) : c, M, slots, g, t, xb);
                 mma_chunk<FMT, NT, 2, M1>(w, xb, acc);
                 if (++c == a.KcA || k == a.LA - 1) {
                     AccA<NT> av;
@@ -560,8 +621,14 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                         for (int n = 0; n < NT; ++n)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) av.v[p][n][e] = acc[p][n][e];
-                    finish_tile_a<FMT, NT>(a, M, lt, cs == 0 && c == a.KcA, warp, av, s_pa, pa_floats, s_cnta, s_sig,
-                                           s_act, s_actmax);
+                    if (NT == 2) {
+                        pend = av;
+                        pend_lt = lt;
+                        pend_whole = cs == 0 && c == a.KcA;
+                    } else {
+                        finish_tile_a<FMT, NT>(a, M, lt, cs == 0 && c == a.KcA, warp, av, s_pa, pa_floats, s_cnta,
+                                               s_sig, s_act, s_actmax);
+                    }
                     zero_acc<NT, 2>(acc);
                     ++lt;
                     c = 0;
@@ -574,6 +641,12 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                 slot = 0;
                 parity ^= 1u;
             }
+        }
+        if (NT == 2) {
+            named_bar_sync(1, kCT);  // x is no longer read: its region takes the combine slots
+            if (pend_lt >= 0)
+                finish_tile_a<FMT, NT>(a, M, pend_lt, pend_whole != 0, warp, pend, s_pa, pa_floats, s_cnta, s_sig,
+                                       s_act, s_actmax);
         }
         q = stepsA;
     }
@@ -842,15 +915,33 @@ struct Layout {
     size_t total;
 };
 
+// 9..16 tokens (two 8-token MMA column tiles): x for all of K no longer
+// fits beside the ring, so phase A stages it in two halves. This works when
+// every gate/up tile is split between exactly two warps at K/2 (LA = Kc/2):
+// the first half of the steps then touches only the chunks [0, Kc/4) and
+// [Kc/2, 3Kc/4) of every tile, the second half the other two quarters.
+bool halves_ok(int fmt, int K, const SplitPlan& P) {
+    const int kca = (K + kChunkK - 1) / kChunkK;
+    return P.G && K % kChunkK == 0 && kca % 4 == 0 && P.LA * 2 == kca && (P.LA / gemv_recs_pair(fmt)) % 2 == 0;
+}
+
 Layout layout_for(int fmt, int M, int K, const SplitPlan& P) {
     Layout L;
     const int kca = (K + kChunkK - 1) / kChunkK;
     const int rec = fmt == kNVFP4 ? kRecNVFP4 : kRecFP8;
     auto al = [](size_t v) { return (int)((v + 127) & ~(size_t)127); };
-    L.xs = al((size_t)std::max(kca, P.Cb) * 128 * M);
     L.sa = P.SA;
-    L.pa = L.xs;
-    L.act = L.pa + al((size_t)P.T * L.sa * 2 * M * 16 * 4);
+    if (M > 8) {
+        // half of x; the tile combine slots alias it (used only once every
+        // warp has finished phase A)
+        L.xs = al(std::max((size_t)std::max(kca / 2, P.Cb) * 128 * M, (size_t)P.T * L.sa * 2 * M * 16 * 4));
+        L.pa = 0;
+        L.act = L.xs;
+    } else {
+        L.xs = al((size_t)std::max(kca, P.Cb) * 128 * M);
+        L.pa = L.xs;
+        L.act = L.pa + al((size_t)P.T * L.sa * 2 * M * 16 * 4);
+    }
     L.pb = L.act + al((size_t)M * P.T * 16 * 4);
     // split down tiles (two contributors per warp boundary) only on the
     // generic down path: Cb not 1, 2 or 4, or a step not whole tiles
@@ -906,7 +997,7 @@ SplitPlan plan_split(int fmt, int K, int I, int num_sms) {
 }
 
 bool split_fits(int fmt, int M, int K, const SplitPlan& P) {
-    if (!P.G || M < 1 || M > 8) return false;
+    if (!P.G || M < 1 || M > 16 || (M > 8 && !halves_ok(fmt, K, P))) return false;
     const Layout L = layout_for(fmt, M, K, P);
     // the in-kernel reduction's scratch (units per CTA x 16 warps x 32
     // floats) lives in the ring
@@ -975,9 +1066,12 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
     // one token, (b) otherwise (see the top of the file).
     const bool m1 = L.M == 1;
     if (L.fmt == kNVFP4 && m1) return launch_t<kNVFP4, 1, true, false>(a, lay.total, s);
-    cudaError_t e = L.fmt == kNVFP4 ? launch_t<kNVFP4, 1, false, true>(a, lay.total, s)
-                    : m1            ? launch_t<kFP8, 1, true, true>(a, lay.total, s)
-                                    : launch_t<kFP8, 1, false, true>(a, lay.total, s);
+    // 9..16 tokens: two 8-token column tiles, x staged in halves
+    cudaError_t e = L.M > 8                ? (L.fmt == kNVFP4 ? launch_t<kNVFP4, 2, false, true>(a, lay.total, s)
+                                                               : launch_t<kFP8, 2, false, true>(a, lay.total, s))
+                    : L.fmt == kNVFP4      ? launch_t<kNVFP4, 1, false, true>(a, lay.total, s)
+                    : m1                   ? launch_t<kFP8, 1, true, true>(a, lay.total, s)
+                                           : launch_t<kFP8, 1, false, true>(a, lay.total, s);
     if (e != cudaSuccess) return e;
     RArgs r;
     r.part = L.part;
