@@ -602,14 +602,14 @@ def run_profile(args):
     from weight_quantized_swiglu_gb300 import build
     build.build()
     n = args.warmup + args.steps
-    if args.profile in ("fused", "fusedM4", "stage0", "stage1", "fp8_fused"):
-        name = "dense_fp8_decode" if args.profile == "fp8_fused" else "dense_nvfp4_decode"
-        case = gen.workload_case(name, 1 if args.profile == "fusedM4" else 0)
+    if args.profile in ("fused", "fusedM4", "stage0", "stage1", "fp8_fused", "fp8_fusedM16"):
+        name = "dense_fp8_decode" if args.profile.startswith("fp8_fused") else "dense_nvfp4_decode"
+        case = gen.workload_case(name, 1 if args.profile in ("fusedM4", "fp8_fusedM16") else 0)
         mlp = q.QuantMLP.from_case(case)
         x = torch.from_numpy(case.x.view(np.int16)).cuda()
         out = torch.empty((case.M, case.K), dtype=torch.int16, device="cuda")
         for _ in range(n):
-            if args.profile in ("fused", "fusedM4", "fp8_fused"):
+            if args.profile in ("fused", "fusedM4", "fp8_fused", "fp8_fusedM16"):
                 mlp.forward(x, out)
             elif args.profile == "stage0":
                 mlp.forward_stage(0, x, None, 1)
@@ -668,7 +668,8 @@ def main():
                     help="comma list of extra workloads to time (decode,fp8,tiny,moe,prefill) or 'all'")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile", default=None,
-                    help="eager launches of one operation for ncu: fused|fusedM4|stage0|stage1|fp8_fused|moe|moetokensM|prefillM|fp8prefillM")
+                    help="eager launches of one operation for ncu: fused|fusedM4|stage0|stage1|fp8_fused|fp8_fusedM16|moe|"
+                         "moetokensM|prefillM|fp8prefillM")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.profile:
