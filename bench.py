@@ -480,7 +480,7 @@ def bench_moe_tokens(Ms=(16, 512), meta_bytes=4):
     return res
 
 
-def bench_prefill(M, reps, pk, fmt="nvfp4"):
+def bench_prefill(M, reps, pk, fmt="nvfp4", pair=False, cpu=True):
     import torch
     import weight_quantized_swiglu_gb300 as q
     case = gen.gen_dense_case(fmt, K_HID, I_INT, M, gen.seed_for(3 if fmt == "nvfp4" else 5, 0 if M == 512 else 1))
@@ -488,15 +488,16 @@ def bench_prefill(M, reps, pk, fmt="nvfp4"):
     x = torch.from_numpy(case.x.view(np.int16)).cuda()
     out = torch.empty((M, K_HID), dtype=torch.int16, device="cuda")
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    path = q.PATH_GEMM_PAIR if pair else q.PATH_GEMM
     for _ in range(3):
-        mlp.forward(x, out, path=q.PATH_GEMM)
+        mlp.forward(x, out, path=path)
     torch.cuda.synchronize()
     times = []
     for _ in range(reps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        mlp.forward(x, out, path=q.PATH_GEMM)
+        mlp.forward(x, out, path=path)
         e1.record()
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
@@ -506,7 +507,9 @@ def bench_prefill(M, reps, pk, fmt="nvfp4"):
     flops = 2.0 * M * 3 * I_INT * K_HID
     tf = flops / (ms * 1e-3) / 1e12
     import oracle
-    if M <= 512:
+    if not cpu:
+        cpu = None
+    elif M <= 512:
         cpu = oracle_baseline(lambda: oracle.dense_forward(case), 1e3, "ms/call",
                               f"the full MLP (K={K_HID}, I={I_INT}, M={M}, fp64)", budget_s=0.0)
     else:
@@ -516,7 +519,7 @@ def bench_prefill(M, reps, pk, fmt="nvfp4"):
                               budget_s=0.0, extrapolate=(M / 64, f"x {M}/64 rows (an upper bound: the weight "
                                                                  f"decode is counted once per 64 rows)"))
     # each call is timed alone (L2 flushed between calls): the burst peak applies
-    return {"M": M, "ms_per_call": ms, "tflops": tf, "frac_bf16_peak": tf / pk["bf16_tflops"],
+    return {"M": M, "path": "gemm_pair" if pair else "gemm", "ms_per_call": ms, "tflops": tf, "frac_bf16_peak": tf / pk["bf16_tflops"],
             "peak_tflops": pk["bf16_tflops"], "peak_kind": "bf16 burst (cuBLAS, isolated calls), " + pk["source"],
             "tokens_per_s": M / (ms * 1e-3), "l2": "512 MB buffer written between calls", "cpu_baseline": cpu}
 
@@ -715,6 +718,8 @@ def main():
                     extras[f"{fmt}_mid_M64"] = bench_prefill(64, 5, pk, fmt)
                     extras[f"{fmt}_prefill_M512"] = bench_prefill(512, 5, pk, fmt)
                     extras[f"{fmt}_prefill_M8192"] = bench_prefill(8192, 3, pk, fmt)
+                    # the CTA-pair GEMM (an explicit path; the automatic one is above)
+                    extras[f"{fmt}_prefill_pair_M8192"] = bench_prefill(8192, 3, pk, fmt, pair=True, cpu=False)
                 except q.QmlpError as e:
                     extras[f"{fmt}_prefill"] = {"unavailable": str(e)}
         torch.cuda.synchronize()

@@ -64,9 +64,13 @@ typedef enum {
 typedef enum { QMLP_FMT_NVFP4 = 1, QMLP_FMT_FP8_PC = 2 } qmlp_format;
 typedef enum { QMLP_DT_BF16 = 1, QMLP_DT_FP16 = 2 } qmlp_dtype;
 typedef enum { QMLP_META_3B = 3, QMLP_META_4B = 4 } qmlp_meta;
-/* Kernel family used by a forward call: AUTO picks the GEMV family for
- * M <= 16 and the tensor-core GEMM family above (NVFP4). */
-typedef enum { QMLP_PATH_AUTO = 0, QMLP_PATH_GEMV = 1, QMLP_PATH_GEMM = 2 } qmlp_path;
+/* Kernel family used by a forward call: AUTO picks the decode (GEMV) family
+ * for small token counts and the tensor-core GEMM above. GEMM_PAIR is the
+ * tensor-core GEMM on CTA pairs (tcgen05.mma.cta_group::2: two SMs share a
+ * 256-token x 256-row tile, each decoding half of its weight rows) for
+ * M >= 256; AUTO does not choose it (the single-CTA GEMM measured faster on
+ * the 27B-class prefill shape). */
+typedef enum { QMLP_PATH_AUTO = 0, QMLP_PATH_GEMV = 1, QMLP_PATH_GEMM = 2, QMLP_PATH_GEMM_PAIR = 3 } qmlp_path;
 
 /* One projection [N, K] as the checkpoint stores it. Pointers may be host or
  * device memory; they are only read during qmlp_create.
@@ -117,8 +121,9 @@ void qmlp_destroy(qmlp_t* h);
  * overlaps x), SHAPE (M < 1 or M > max_M), CUDA. */
 qmlp_status qmlp_forward(qmlp_t* h, const void* x, int M, void* out, qmlp_stream_t stream);
 
-/* As qmlp_forward, forcing a kernel family (tests). GEMM requires NVFP4 and a
- * handle created with max_M > 16; otherwise SHAPE. */
+/* As qmlp_forward, forcing a kernel family. GEMM and GEMM_PAIR require a
+ * handle whose max_M reaches the GEMM threshold (and K % 256, I % 128 ==
+ * 0); GEMM_PAIR also M >= 256. Otherwise SHAPE. */
 qmlp_status qmlp_forward_path(qmlp_t* h, qmlp_path path, const void* x, int M, void* out,
                               qmlp_stream_t stream);
 

@@ -66,6 +66,41 @@ def test_gemm_one_hot_returns_decoded_weights_exactly(torch_cuda, fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+def test_pair_gemm_one_hot_is_bit_exact(torch_cuda, fmt):
+    """The CTA-pair GEMM path (each CTA of a cluster holds half of the 256
+    tokens of a tile and decodes half of its 256 weight rows): x =
+    e_k rows in both halves of the token tile, one per k on scale-group,
+    k-step and tile boundaries, return the decoded weights bit for bit, for
+    gate (rows decoded by the first CTA of each pair), up (the second) and
+    down."""
+    torch = torch_cuda
+    case = gen.gen_dense_case(fmt, TK, TI, 1, seed=205)
+    mlp = q.QuantMLP.from_case(case, max_M=512)
+    for which, proj in ((0, case.gate), (1, case.up), (2, case.down)):
+        Kp = proj.K
+        M = 300  # a full 256-token tile and a ragged second one
+        ks = [(r * 37) % Kp for r in range(M)]
+        ks[:8] = [0, 15, 16, 31, 63, 64, Kp - 1, Kp - 16]
+        ks[128:132] = [1, 17, 65, Kp - 2]  # the second CTA's half of the first tile
+        x = np.zeros((M, Kp), dtype=np.uint16)
+        for r, k in enumerate(ks):
+            x[r, k] = 0x3F80
+        y = torch.empty((M, proj.N), dtype=torch.float32, device="cuda")
+        mlp.debug_project(which, to_dev(x), y, path=q.PATH_GEMM_PAIR)
+        torch.cuda.synchronize()
+        mlp.check()
+        got = y.cpu().numpy().astype(np.float64)
+        ref = oracle.decode_proj(proj)
+        for r, k in enumerate(ks):
+            assert np.array_equal(got[r], ref[:, k]), (which, r, k)
+    # fewer tokens than one pair tile: rejected before any launch
+    y = torch.empty((255, case.gate.N), dtype=torch.float32, device="cuda")
+    x = torch.zeros((255, case.gate.K), dtype=torch.int16, device="cuda")
+    assert q.qmlp_debug_project(mlp.h, 0, q.PATH_GEMM_PAIR, x, 255, y) == 4  # QMLP_ERR_SHAPE
+    mlp.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("M", [17, 200])
 def test_gemm_raw_projection_matches_oracle(torch_cuda, M, fmt):
     """Unscaled projections (fp32 out) on random bf16 x, every projection;
@@ -209,4 +244,8 @@ def test_parity_prefill(torch_cuda, variant, name):
             assert np.linalg.norm(d) <= 5e-3 * np.linalg.norm(r_all[i]), f"row {r}"
     out2, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
     assert np.array_equal(out, out2)
+    # the CTA-pair GEMM on the same inputs, against the same reference rows
+    pout, pact = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM_PAIR)
+    compare(pact[rows], ref["act"], what="pair act")
+    compare(pout[rows], ref["out"], what="pair out")
     mlp.close()

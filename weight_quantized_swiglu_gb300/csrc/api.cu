@@ -442,9 +442,13 @@ static qmlp_status validate_fwd(qmlp_t* h, const void* x, int M, const void* out
     return QMLP_OK;
 }
 
+static bool valid_path(qmlp_path p) {
+    return p == QMLP_PATH_AUTO || p == QMLP_PATH_GEMV || p == QMLP_PATH_GEMM || p == QMLP_PATH_GEMM_PAIR;
+}
+
 static bool use_gemm(qmlp_t* h, qmlp_path path, int M) {
     if (path == QMLP_PATH_GEMV) return false;
-    if (path == QMLP_PATH_GEMM) return true;
+    if (path == QMLP_PATH_GEMM || path == QMLP_PATH_GEMM_PAIR) return true;
     return h->has_gemm && M >= gemm_min_m(h);
 }
 
@@ -456,8 +460,10 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
     if (fault("launch")) return QMLP_ERR_CUDA;
     const bool gemm = use_gemm(h, path, M);
     if (gemm && !h->has_gemm) return QMLP_ERR_SHAPE;
+    if (path == QMLP_PATH_GEMM_PAIR && M < kPairMinM) return QMLP_ERR_SHAPE;
     if (gemm) {
         GemmLaunch g;
+        g.pair = path == QMLP_PATH_GEMM_PAIR;
         g.M = M;
         g.err = h->err;
         g.a16 = h->a16;
@@ -599,7 +605,7 @@ qmlp_status qmlp_forward_path(qmlp_t* h, qmlp_path path, const void* x, int M, v
                               qmlp_stream_t stream) {
     qmlp_status st = validate_fwd(h, x, M, out, 2, 0);
     if (st != QMLP_OK) return st;
-    if (path != QMLP_PATH_AUTO && path != QMLP_PATH_GEMV && path != QMLP_PATH_GEMM) return QMLP_ERR_INVALID_ARG;
+    if (!valid_path(path)) return QMLP_ERR_INVALID_ARG;
     const size_t xb = (size_t)M * h->K * 2;
     if (overlaps(x, xb, out, xb)) return QMLP_ERR_ALIAS;
     if (overlaps(out, xb, h->act, (size_t)h->max_M * h->I * 2)) return QMLP_ERR_ALIAS;
@@ -609,7 +615,7 @@ qmlp_status qmlp_forward_path(qmlp_t* h, qmlp_path path, const void* x, int M, v
 qmlp_status qmlp_forward_stage(qmlp_t* h, int stage, qmlp_path path, const void* x, int M, void* out,
                                qmlp_stream_t stream) {
     if (!h) return QMLP_ERR_INVALID_ARG;
-    if (path != QMLP_PATH_AUTO && path != QMLP_PATH_GEMV && path != QMLP_PATH_GEMM) return QMLP_ERR_INVALID_ARG;
+    if (!valid_path(path)) return QMLP_ERR_INVALID_ARG;
     if (M < 1 || M > h->max_M) return QMLP_ERR_SHAPE;
     if (stage == 0) {
         if (!x || out) return QMLP_ERR_INVALID_ARG;
@@ -678,7 +684,9 @@ qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void*
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (use_gemm(h, path, M)) {
         if (!h->has_gemm) return QMLP_ERR_SHAPE;
+        if (path == QMLP_PATH_GEMM_PAIR && M < kPairMinM) return QMLP_ERR_SHAPE;
         GemmLaunch g;
+        g.pair = path == QMLP_PATH_GEMM_PAIR;
         g.epi = kEpiRaw;
         g.raw_sel = which == 1 ? 1 : 0;
         g.w = which < 2 ? h->gm_gu : h->gm_d;

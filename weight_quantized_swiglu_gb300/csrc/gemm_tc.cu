@@ -214,9 +214,9 @@ QMLP_DEV bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_f
 // Decode one (row, 32-k half) item of a packed block into the swizzled fp16
 // B tile: 16 code bytes (32 weights, low nibble = even k) and two E4M3
 // scales (k 0..15 and 16..31 of the half).
-QMLP_DEV void decode_item(const uint8_t* raw, uint8_t* bt, int n, int h) {
+QMLP_DEV void decode_item(const uint8_t* raw, uint8_t* bt, int n, int h, int soff = kRawCodes) {
     const uint4 c = *reinterpret_cast<const uint4*>(raw + n * 32 + h * 16);
-    const uint32_t s2 = *reinterpret_cast<const uint16_t*>(raw + kRawCodes + n * 4 + h * 2);
+    const uint32_t s2 = *reinterpret_cast<const uint16_t*>(raw + soff + n * 4 + h * 2);
     const uint32_t sf = e4m3x2_to_f16x2(s2);
     const uint32_t sa = dup_lo16(sf), sb = dup_hi16(sf);
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
@@ -265,6 +265,79 @@ QMLP_DEV float f4_at(const float4& f, int e) { return e == 0 ? f.x : e == 1 ? f.
 QMLP_DEV uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// The tile epilogue (no split): accumulator columns of TMEM base `tbase`
+// (this thread's lane = token row m) -> SwiGLU act, plain output or raw fp32.
+template <int FMT>
+QMLP_DEV void store_tile(const Args& a, uint32_t tbase, int m, bool live, int sg, int nt) {
+    if (a.epi == kEpiSwiGLU) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+            float g[32], u[32];
+            tmem_ld32(tbase + c0, g);
+            tmem_ld32(tbase + BN / 2 + c0, u);
+            if (live) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 fg = factor4<FMT>(a.cs0, a.inv0, nt * (BN / 2) + c0 + j);
+                    const float4 fu = factor4<FMT>(a.cs1, a.inv1, nt * (BN / 2) + c0 + j);
+                    float r4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float gv = scalbnf(g[j + e], -sg) * f4_at(fg, e);
+                        const float uv = scalbnf(u[j + e], -sg) * f4_at(fu, e);
+                        r4[e] = silu_f32(gv) * uv;
+                    }
+                    pk[j / 2] = pack_bf16x2(r4[0], r4[1]);
+                    pk[j / 2 + 1] = pack_bf16x2(r4[2], r4[3]);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * (BN / 2) + c0);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+        }
+    } else if (a.epi == kEpiPlain) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            float y[32];
+            tmem_ld32(tbase + c0, y);
+            if (live) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 f = factor4<FMT>(a.cs0, a.inv0, nt * BN + c0 + j);
+                    pk[j / 2] = pack_bf16x2(scalbnf(y[j], -sg) * f.x, scalbnf(y[j + 1], -sg) * f.y);
+                    pk[j / 2 + 1] = pack_bf16x2(scalbnf(y[j + 2], -sg) * f.z, scalbnf(y[j + 3], -sg) * f.w);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * BN + c0);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+        }
+    } else {
+        float* out = reinterpret_cast<float*>(a.out);
+        const int cbeg = a.interleaved ? a.raw_sel * (BN / 2) : 0;
+        const int cend = a.interleaved ? cbeg + BN / 2 : BN;
+        const int ocol = a.interleaved ? nt * (BN / 2) : nt * BN;
+#pragma unroll 1
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
+            float y[32];
+            tmem_ld32(tbase + c0, y);
+            if (live) {
+                float4* dst = reinterpret_cast<float4*>(out + (size_t)m * a.ldo + ocol + (c0 - cbeg));
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    dst[v] = make_float4(scalbnf(y[4 * v], -sg), scalbnf(y[4 * v + 1], -sg),
+                                         scalbnf(y[4 * v + 2], -sg), scalbnf(y[4 * v + 3], -sg));
+            }
+        }
+    }
 }
 
 template <int FMT, bool SPLIT>
@@ -430,72 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         for (int v = 0; v < 8; ++v) dst[v] = make_float4(y[4 * v], y[4 * v + 1], y[4 * v + 2], y[4 * v + 3]);
                     }
                 }
-            } else if (a.epi == kEpiSwiGLU) {
-                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN / 2; c0 += 32) {
-                    float g[32], u[32];
-                    tmem_ld32(tbase + c0, g);
-                    tmem_ld32(tbase + BN / 2 + c0, u);
-                    if (live) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 fg = factor4<FMT>(a.cs0, a.inv0, nt * (BN / 2) + c0 + j);
-                            const float4 fu = factor4<FMT>(a.cs1, a.inv1, nt * (BN / 2) + c0 + j);
-                            float r4[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float gv = scalbnf(g[j + e], -sg) * f4_at(fg, e);
-                                const float uv = scalbnf(u[j + e], -sg) * f4_at(fu, e);
-                                r4[e] = silu_f32(gv) * uv;
-                            }
-                            pk[j / 2] = pack_bf16x2(r4[0], r4[1]);
-                            pk[j / 2 + 1] = pack_bf16x2(r4[2], r4[3]);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * (BN / 2) + c0);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                    }
-                }
-            } else if (a.epi == kEpiPlain) {
-                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    float y[32];
-                    tmem_ld32(tbase + c0, y);
-                    if (live) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 f = factor4<FMT>(a.cs0, a.inv0, nt * BN + c0 + j);
-                            pk[j / 2] = pack_bf16x2(scalbnf(y[j], -sg) * f.x, scalbnf(y[j + 1], -sg) * f.y);
-                            pk[j / 2 + 1] = pack_bf16x2(scalbnf(y[j + 2], -sg) * f.z, scalbnf(y[j + 3], -sg) * f.w);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * BN + c0);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                    }
-                }
             } else {
-                float* out = reinterpret_cast<float*>(a.out);
-                const int cbeg = a.interleaved ? a.raw_sel * (BN / 2) : 0;
-                const int cend = a.interleaved ? cbeg + BN / 2 : BN;
-                const int ocol = a.interleaved ? nt * (BN / 2) : nt * BN;
-#pragma unroll 1
-                for (int c0 = cbeg; c0 < cend; c0 += 32) {
-                    float y[32];
-                    tmem_ld32(tbase + c0, y);
-                    if (live) {
-                        float4* dst = reinterpret_cast<float4*>(out + (size_t)m * a.ldo + ocol + (c0 - cbeg));
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_float4(scalbnf(y[4 * v], -sg), scalbnf(y[4 * v + 1], -sg),
-                                                 scalbnf(y[4 * v + 2], -sg), scalbnf(y[4 * v + 3], -sg));
-                    }
-                }
+                store_tile<FMT>(a, tbase, m, live, sg, nt);
             }
             tc_fence_before();
             mbar_arrive(acc_empty(buf));
@@ -535,6 +544,343 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// CTA-pair GEMM (tcgen05.mma.cta_group::2), prefill M >= 256.
+//
+// A cluster of two CTAs computes a 256-token x 256-row tile: CTA r (its rank
+// in the cluster) holds tokens [128r, 128r + 128) of the activation tile and
+// weight rows [128r, 128r + 128) of the weight tile -- it loads and decodes
+// only that half of every weight block -- and its TMEM holds the 128 x 256
+// accumulator of its tokens. One thread of rank 0 (the leader) issues the
+// MMAs (M = 256, N = 256, K = 16: the tensor cores of both SMs read the A
+// half and the B half of their own CTA, each B half serving both), and its
+// commits arrive on the barriers of both CTAs (multicast). Rank 1's MMA warp
+// forwards to the leader, with one remote mbarrier arrival each, that its A
+// stage has landed and its B stage is decoded, and that its epilogue has
+// drained an accumulator. Per SM and 64-k step this moves half the decoded
+// weight tile through shared memory (decoder stores 16 KB instead of 32 KB,
+// tensor-core reads 16 KB of B instead of 32 KB) and halves the decode work.
+// ---------------------------------------------------------------------------
+constexpr int kBHalf = (BN / 2) * BK * 2;  // 16 KB: 128 decoded weight rows of a 64-k step
+constexpr int kDecGroups = 4;              // decoder groups of the pair kernel (one per B stage)
+
+template <int FMT>
+constexpr int raw_half() { return raw_bytes<FMT>() / 2; }  // NVFP4: 4096 codes + 512 scales; FP8: 8192
+
+template <int FMT>
+struct SmemP {
+    // load stages: A (16 KB) + the weight half-block. A stage is held from its
+    // TMA until the leader's MMA has used it, which now includes the peer's
+    // signal: measured at M=8192 (NVFP4 / FP8), 3.90 / 3.92 ms with 5 stages,
+    // 3.72 / 3.76 with 6.
+    static constexpr int L = 6;
+    static constexpr int BS = 4;  // decoded half-B stages
+    static constexpr int R = raw_half<FMT>();
+    static constexpr int A = 0;
+    static constexpr int B = A + L * kABytes;
+    static constexpr int Raw = B + BS * kBHalf;
+    static constexpr int Bar = Raw + L * R;
+    // full[L], empty[L], bfull[BS], bempty[BS], acc_full[2], acc_empty[2], done,
+    // pbfull[BS] (leader: the peer's decoders have filled B stage b -- so its
+    // A stage of that step has landed too), pacc[2] (leader: the peer's
+    // accumulator is drained)
+    static constexpr int NumBars = 2 * L + 3 * BS + 7;
+    static constexpr int Misc = Bar + NumBars * 8;
+    static constexpr int Bytes = Misc + 16 + 1024;
+    static_assert(B % 1024 == 0 && Raw % 16 == 0 && Bar % 8 == 0 && R % 16 == 0, "smem layout");
+    static_assert(Bytes <= 227 * 1024, "smem budget");
+};
+
+// Instruction descriptor of the pair MMA: fp32 accumulator, fp16 A and B,
+// K-major, N = 256, M = 256 (128 rows in each CTA).
+constexpr uint32_t kIdescPair = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+
+QMLP_DEV uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+QMLP_DEV void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive once on the mbarrier at the same shared-memory offset in CTA `rank`
+// of the cluster.
+QMLP_DEV void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(bar), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+// Wait for phase `parity` of a barrier that the peer CTA arrives on
+// (acquire at cluster scope); false if the abort flag is raised or the wait
+// ran out (which raises it and records `code`).
+QMLP_DEV bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, int code,
+                                    uint64_t limit) {
+    auto try_once = [&]() {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        return ok != 0;
+    };
+    if (try_once()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!try_once()) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit) {
+            *abort_flag = 1;
+            atomicExch(err, code);
+            return false;
+        }
+    }
+    return true;
+}
+
+QMLP_DEV void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+QMLP_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+QMLP_DEV void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on `bar` (same offset) in both CTAs of the pair once every
+// tcgen05 operation this thread issued so far is complete.
+QMLP_DEV void umma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_constant__ CUtensorMap amap, const Args a) {
+    using S = SmemP<FMT>;
+    constexpr int kL = S::L, kBS = S::BS, kR = S::R;
+    extern __shared__ uint8_t dyn_smem_raw[];
+    // the same offsets in both CTAs: the MMA addresses the peer's halves, and
+    // the commits and remote arrivals its barriers, at this CTA's offsets
+    const uint32_t base_s = (smem_u32(dyn_smem_raw) + 1023u) & ~1023u;
+    uint8_t* base = dyn_smem_raw + (base_s - smem_u32(dyn_smem_raw));
+    const uint32_t bar0 = base_s + S::Bar;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (kL + s); };
+    auto bfull = [&](int b) { return bar0 + 8u * (2 * kL + b); };
+    auto bempty = [&](int b) { return bar0 + 8u * (2 * kL + kBS + b); };
+    auto acc_full = [&](int b) { return bar0 + 8u * (2 * kL + 2 * kBS + b); };
+    auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kL + 2 * kBS + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kL + 2 * kBS + 4);
+    auto pbfull = [&](int b) { return bar0 + 8u * (2 * kL + 2 * kBS + 5 + b); };
+    auto pacc = [&](int b) { return bar0 + 8u * (2 * kL + 3 * kBS + 5 + b); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + S::Misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + S::Misc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: the leader, 1: its peer
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int Mt2 = (a.M + 2 * BM - 1) / (2 * BM);  // 256-token tiles
+    const int Nt = a.N / BN;
+    const int KS = a.Kd / BK;
+    const int units = Mt2 * Nt;  // n-tile-major, as the single-CTA kernel
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kL; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < kBS; ++b) {
+            mbar_init(bfull(b), kDecThreads / kDecGroups);
+            mbar_init(bempty(b), 1);
+            mbar_init(pbfull(b), kDecThreads / kDecGroups);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), kEpiWarps * 32);
+            mbar_init(pacc(b), 1);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrival or multicast
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer: this CTA's A half and weight half ----------------
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&amap)) : "memory");
+            int it = 0;
+            bool ok = true;
+            for (int u = pair; u < units && ok; u += npairs) {
+                const int nt = u / Mt2, mt2 = u % Mt2;
+                const uint8_t* blk = a.tiles + (size_t)nt * KS * raw_bytes<FMT>();
+                // error-path tests: the pair's very last k-step is never loaded
+                const int ks_stop = (a.withhold && u + npairs >= units) ? KS - 1 : KS;
+                for (int ks = 0; ks < ks_stop; ++ks, ++it) {
+                    const int s = it % kL;
+                    if (it >= kL &&
+                        !wait_or_abort(empty(s), (uint32_t)((it / kL - 1) & 1), abort_flag, a.err, 41, a.limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full(s), kABytes + kR);
+                    tma_load_2d(base_s + S::A + s * kABytes, &amap, ks * BK, mt2 * 2 * BM + (int)rank * BM, full(s));
+                    const uint8_t* src = blk + (size_t)ks * raw_bytes<FMT>();
+                    const uint32_t dst = base_s + S::Raw + s * kR;
+                    if (FMT == kNVFP4) {
+                        // rows 128 rank.. of the block: their codes, then their scales
+                        bulk_g2s(dst, src + rank * (kRawCodes / 2), kRawCodes / 2, full(s));
+                        bulk_g2s(dst + kRawCodes / 2, src + kRawCodes + rank * (BN / 2) * 4, (BN / 2) * 4, full(s));
+                    } else {
+                        bulk_g2s(dst, src + rank * kR, kR, full(s));
+                    }
+                }
+            }
+            if (!ok) {
+                for (int q = it - 1; q >= 0 && q >= it - kL; --q)
+                    mbar_wait_bounded(full(q % kL), (uint32_t)((q / kL) & 1), kGemmWaitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int it = 0, tc = 0;
+            bool ok = true, issued = false;
+            for (int u = pair; u < units && ok; u += npairs, ++tc) {
+                const int buf = tc & 1, use = tc >> 1;
+                if (rank == 0) {
+                    // ---------------- MMA issuer (leader) ----------------
+                    if (use > 0 &&
+                        (!wait_or_abort(acc_empty(buf), (uint32_t)((use - 1) & 1), abort_flag, a.err, 42, a.limit) ||
+                         !wait_cluster_or_abort(pacc(buf), (uint32_t)((use - 1) & 1), abort_flag, a.err, 43,
+                                                a.limit))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
+                    for (int ks = 0; ks < KS; ++ks, ++it) {
+                        const int s = it % kL, b = it % kBS;
+                        if (!wait_or_abort(full(s), (uint32_t)((it / kL) & 1), abort_flag, a.err, 44, a.limit) ||
+                            !wait_or_abort(bfull(b), (uint32_t)((it / kBS) & 1), abort_flag, a.err, 45, a.limit) ||
+                            !wait_cluster_or_abort(pbfull(b), (uint32_t)((it / kBS) & 1), abort_flag, a.err, 46,
+                                                   a.limit)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = base_s + S::A + s * kABytes;
+                        const uint32_t sb = base_s + S::B + b * kBHalf;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            umma_f16_pair(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), kIdescPair,
+                                          (ks != 0 || k != 0) ? 1u : 0u);
+                        issued = true;
+                        umma_commit_pair(empty(s));
+                        umma_commit_pair(bempty(b));
+                    }
+                    if (!ok) break;
+                    umma_commit_pair(acc_full(buf));
+                } else {
+                    // ---------------- forwarder (peer): accumulator drained ----------------
+                    if (use > 0) {
+                        if (!wait_or_abort(acc_empty(buf), (uint32_t)((use - 1) & 1), abort_flag, a.err, 47, a.limit)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_remote(pacc(buf), 0);
+                    }
+                }
+            }
+            // every MMA that wrote either CTA's TMEM must be finished before
+            // TMEM is freed: the leader's last commit reaches both done barriers
+            if (rank == 0 && issued) umma_commit_pair(done_bar);
+            if (rank != 0 || issued) mbar_wait_bounded(done_bar, 0, kGemmWaitNs);
+        }
+    } else if (warp < 2 + kEpiWarps) {
+        // ---------------- epilogue: this CTA's 128 tokens ----------------
+        const int q = warp & 3;
+        const int row_in_tile = q * 32 + lane;
+        int tc = 0;
+        for (int u = pair; u < units; u += npairs, ++tc) {
+            const int nt = u / Mt2, mt2 = u % Mt2;
+            const int buf = tc & 1, use = tc >> 1;
+            const bool ready = wait_or_abort(acc_full(buf), (uint32_t)(use & 1), abort_flag, a.err, 50, a.limit);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const int m = mt2 * 2 * BM + (int)rank * BM + row_in_tile;
+            const bool live = m < a.M;
+            const int sg = live ? a.sig[m] : 0;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+            store_tile<FMT>(a, tbase, m, live, sg, nt);
+            tc_fence_before();
+            mbar_arrive(acc_empty(buf));
+        }
+    } else {
+        // ---------------- decoders: rows 128 rank.. of each weight block ----------------
+        // kDecGroups groups of warps take turns by step, each decoding a whole
+        // half-B stage: the peer's arrival on the leader's barrier is a
+        // release at cluster scope, and its fence then overlaps the other
+        // groups' decoding instead of gating every step (measured at M=8192,
+        // NVFP4: 6.65 ms with all decoders on each step, 4.67 with two groups).
+        constexpr int kGT = kDecThreads / kDecGroups;  // threads of a group
+        constexpr int kItems = (BN / 2) * 2 / kGT;     // (row, 32-k half) items per thread and step
+        const int dg = (warp - (2 + kEpiWarps)) / (kDecWarps / kDecGroups);
+        const int dt = threadIdx.x - (2 + kEpiWarps) * 32 - dg * kGT;
+        static_assert(kBS % kDecGroups == 0 && (BN / 2) * 2 % kGT == 0, "whole stages per group");
+        int it = 0;
+        bool ok = true;
+        for (int u = pair; u < units && ok; u += npairs) {
+            for (int ks = 0; ks < KS; ++ks, ++it) {
+                if (it % kDecGroups != dg) continue;
+                const int s = it % kL, b = it % kBS;
+                if (!wait_or_abort(full(s), (uint32_t)((it / kL) & 1), abort_flag, a.err, 51, a.limit) ||
+                    (it >= kBS &&
+                     !wait_or_abort(bempty(b), (uint32_t)((it / kBS - 1) & 1), abort_flag, a.err, 52, a.limit))) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* raw = base + S::Raw + s * kR;
+                uint8_t* bt = base + S::B + b * kBHalf;
+#pragma unroll
+                for (int j = 0; j < kItems; ++j) {
+                    const int item = dt + j * kGT;  // (row, 32-k half)
+                    if (FMT == kNVFP4) decode_item(raw, bt, item >> 1, item & 1, kRawCodes / 2);
+                    else decode_item_fp8(raw, bt, item >> 1, item & 1);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                // the leader's MMA thread waits on its own decoders and,
+                // directly, on the peer's (whose A stage landed before they
+                // could read the weight half of the same step)
+                if (rank == 0) mbar_arrive(bfull(b));
+                else mbar_arrive_remote(pbfull(b), 0);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // neither CTA leaves (nor frees TMEM) while the other may still address
+    // its shared memory or its MMAs run
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
 
@@ -690,6 +1036,37 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+// The CTA-pair GEMM over `pairs_wanted` clusters of two (fewer if fewer fit at
+// once: the pairs loop over the tiles).
+template <int FMT>
+cudaError_t launch_pair(const CUtensorMap& map, const Args& a, int pairs_wanted, cudaStream_t s) {
+    static int max_pairs = -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SmemP<FMT>::Bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (max_pairs < 0) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SmemP<FMT>::Bytes);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(2);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<FMT>, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        max_pairs = n;
+    }
+    cfg.gridDim = dim3((unsigned)(2 * std::min(pairs_wanted, max_pairs)));
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<FMT>, map, a);
+}
+
 template <int FMT>
 cudaError_t launch_fmt(const CUtensorMap& map, const Args& a, int grid, cudaStream_t s) {
     static bool attr = false;
@@ -789,8 +1166,15 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     const int KS = P.K / BK;
     a.splits = 1;
     a.ws = L.ws;
-    if (L.ws && L.epi != kEpiRaw && 2 * tiles0 <= num_sms)
+    if (L.ws && L.epi != kEpiRaw && !L.pair && 2 * tiles0 <= num_sms)
         a.splits = std::max(1, std::min(std::min(num_sms / tiles0, KS / 8), kMaxSplits));
+    // 256-token tiles on CTA pairs (every weight row decoded once per 256
+    // tokens), when asked for
+    if (L.pair) {
+        if (L.M < kPairMinM) return cudaErrorInvalidValue;
+        const int pairs = std::min(((L.M + 2 * BM - 1) / (2 * BM)) * (P.N / BN), std::max(num_sms, 2) / 2);
+        return P.fmt == kFP8 ? launch_pair<kFP8>(map, a, pairs, s) : launch_pair<kNVFP4>(map, a, pairs, s);
+    }
     const int grid = std::min(tiles0 * a.splits, std::max(num_sms, 1));
     return P.fmt == kFP8 ? launch_fmt<kFP8>(map, a, grid, s) : launch_fmt<kNVFP4>(map, a, grid, s);
 }

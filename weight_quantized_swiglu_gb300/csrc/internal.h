@@ -174,7 +174,9 @@ struct GemmLaunch {
     float* ws = nullptr;      // split-K partials, >= gemm_splitk_ws_elems (null: no split-K)
     uint64_t wait_ns = 0;     // bounded-wait limit (0: the kernel's default of 2 s)
     bool withhold = false;    // error-path tests: the last k-step of each CTA is never loaded
+    bool pair = false;        // the CTA-pair kernel (M >= kPairMinM; never split-K)
 };
+constexpr int kPairMinM = 256;  // one 256-token tile of a CTA pair
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s);
 size_t gemm_splitk_ws_elems(int num_sms);
 bool gemm_supported(int K, int N);
