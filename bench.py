@@ -645,15 +645,16 @@ def run_profile(args):
             moe.forward_tokens(x, q.DT_FP16, ids, rw, out)
         torch.cuda.synchronize()
         moe.check()
-    elif args.profile.startswith("prefill") or args.profile.startswith("fp8prefill"):
+    elif any(args.profile.startswith(p) for p in ("prefill", "fp8prefill", "pairprefill", "fp8pairprefill")):
         fp8 = args.profile.startswith("fp8")
-        M = int(args.profile[len("fp8prefill" if fp8 else "prefill"):] or 512)
+        pair = "pair" in args.profile
+        M = int(args.profile.split("prefill", 1)[1] or 512)
         case = gen.gen_dense_case("fp8" if fp8 else "nvfp4", K_HID, I_INT, M, gen.seed_for(5 if fp8 else 3, 0))
         mlp = q.QuantMLP.from_case(case)
         x = torch.from_numpy(case.x.view(np.int16)).cuda()
         out = torch.empty((M, K_HID), dtype=torch.int16, device="cuda")
         for _ in range(n):
-            mlp.forward(x, out, path=q.PATH_GEMM)
+            mlp.forward(x, out, path=q.PATH_GEMM_PAIR if pair else q.PATH_GEMM)
         torch.cuda.synchronize()
         mlp.check()
     print(f"profile {args.profile}: {n} calls ok", flush=True)
@@ -672,7 +673,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile", default=None,
                     help="eager launches of one operation for ncu: fused|fusedM4|stage0|stage1|fp8_fused|fp8_fusedM16|moe|"
-                         "moetokensM|prefillM|fp8prefillM")
+                         "moetokensM|prefillM|fp8prefillM|pairprefillM|fp8pairprefillM")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.profile:
@@ -719,7 +720,10 @@ def main():
                     extras[f"{fmt}_prefill_M512"] = bench_prefill(512, 5, pk, fmt)
                     extras[f"{fmt}_prefill_M8192"] = bench_prefill(8192, 3, pk, fmt)
                     # the CTA-pair GEMM (an explicit path; the automatic one is above)
-                    extras[f"{fmt}_prefill_pair_M8192"] = bench_prefill(8192, 3, pk, fmt, pair=True, cpu=False)
+                    pair = bench_prefill(8192, 3, pk, fmt, pair=True, cpu=False)
+                    # same workload and inputs as the line above: its oracle timing applies
+                    pair["cpu_baseline"] = extras[f"{fmt}_prefill_M8192"]["cpu_baseline"]
+                    extras[f"{fmt}_prefill_pair_M8192"] = pair
                 except q.QmlpError as e:
                     extras[f"{fmt}_prefill"] = {"unavailable": str(e)}
         torch.cuda.synchronize()
