@@ -58,7 +58,8 @@ typedef enum {
     QMLP_ERR_UNSUPPORTED_ARCH = 5,/* device is not compute capability 10.3 */
     QMLP_ERR_OOM = 6,             /* device allocation failed at create    */
     QMLP_ERR_CUDA = 7,            /* a CUDA runtime call or launch failed  */
-    QMLP_ERR_DEVICE_TIMEOUT = 8   /* a kernel gave up a bounded wait       */
+    QMLP_ERR_DEVICE_TIMEOUT = 8,  /* a kernel gave up a bounded wait       */
+    QMLP_ERR_DEVICE_BOUNDS = 9    /* an index check failed (checking build) */
 } qmlp_status;
 
 typedef enum { QMLP_FMT_NVFP4 = 1, QMLP_FMT_FP8_PC = 2 } qmlp_format;
@@ -196,6 +197,38 @@ qmlp_status qmlp_debug_split(qmlp_t* h, const void* x, const void* act_in, int M
  * weight step, so those waits run out: the kernels record it, leave without
  * a fault, and qmlp_check returns QMLP_ERR_DEVICE_TIMEOUT. Errors: INVALID_ARG. */
 qmlp_status qmlp_debug_set_wait(qmlp_t* h, uint64_t limit_ns, int withhold_last_step);
+
+/*
+ * Index checks. A library built with -DQMLP_DEBUG_BOUNDS (libqmlp_bounds.so;
+ * the default build compiles the checks away) checks, in every kernel, the
+ * index of each global access whose address comes from layout arithmetic or
+ * runtime data (weight-bank blocks and records, partial buffers, outputs,
+ * route lists) against the size of its buffer. A failed check never traps:
+ * the kernel records the first one and skips the access (a load reads zero,
+ * a store is dropped, a bulk copy is taken from the start of its buffer), so
+ * the call's outputs are then invalid but the device stays usable. This
+ * build stands in for a memory checker where none can run.
+ */
+/* 1 for a checking build, else 0. */
+int qmlp_debug_bounds_enabled(void);
+
+/* Synchronize the device, then report and clear the first failed index
+ * check of any kernel since the last call: *site = the check's number
+ * (per source file: 1-9 decode kernel, 11-19 tensor-core GEMM, 21-29 stream-K
+ * and split-K decode kernels, 31-39 one-token routed experts, 41-49 grouped
+ * routed experts, 51-59 tensor-parallel combine) and *index = the checked
+ * index (low 48 bits), or 0 and 0. Returns OK, DEVICE_BOUNDS (a check
+ * failed), INVALID_ARG (a NULL pointer) or CUDA. A default build always
+ * reports OK. */
+qmlp_status qmlp_debug_bounds(int* site, unsigned long long* index);
+
+/* Checking builds, tests only: from now on the decode kernel's checks allow
+ * only the first gate_up_bank_bytes bytes of each of its gate and up record
+ * banks (0: the whole bank), so its later weight steps fail their check --
+ * the copies are then taken from the bank's start, which exists -- and
+ * qmlp_debug_bounds reports site 1. Errors: INVALID_ARG (NULL handle, or a
+ * default build). */
+qmlp_status qmlp_debug_bounds_limit(qmlp_t* h, size_t gate_up_bank_bytes);
 
 /*
  * Tensor-parallel shard over the intermediate dimension (vllm.cpp issue "tp>1
@@ -351,7 +384,7 @@ qmlp_status qmlp_moe_m1_forward_noalloc(const qmlp_moe_desc* banks, const void* 
 /* Human-readable name of a status ("QMLP_OK", ...). Never NULL. */
 const char* qmlp_status_str(qmlp_status s);
 
-/* ABI version of this header (major * 100 + minor): 102 (tensor-parallel shard). */
+/* ABI version of this header (major * 100 + minor): 103 (index-checking build). */
 int qmlp_abi_version(void);
 
 #ifdef __cplusplus

@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libqmlp.so")
 QMLP_OK = 0
 STATUS = {0: "QMLP_OK", 1: "QMLP_ERR_INVALID_ARG", 2: "QMLP_ERR_ALIGNMENT", 3: "QMLP_ERR_ALIAS",
           4: "QMLP_ERR_SHAPE", 5: "QMLP_ERR_UNSUPPORTED_ARCH", 6: "QMLP_ERR_OOM", 7: "QMLP_ERR_CUDA",
-          8: "QMLP_ERR_DEVICE_TIMEOUT"}
+          8: "QMLP_ERR_DEVICE_TIMEOUT", 9: "QMLP_ERR_DEVICE_BOUNDS"}
 FMT_NVFP4, FMT_FP8_PC = 1, 2
 DT_BF16, DT_FP16 = 1, 2
 META_3B, META_4B = 3, 4
@@ -71,6 +71,9 @@ _SIGS = {
     "qmlp_check": ([_VP, _VP], _I),
     "qmlp_debug_split": ([_VP, _VP, _VP, _I, _VP, _VP, _VP, _VP], _I),
     "qmlp_debug_set_wait": ([_VP, ctypes.c_uint64, _I], _I),
+    "qmlp_debug_bounds_enabled": ([], _I),
+    "qmlp_debug_bounds": ([ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_ulonglong)], _I),
+    "qmlp_debug_bounds_limit": ([_VP, ctypes.c_size_t], _I),
     "qmlp_create_shard": ([ctypes.POINTER(_VP), ctypes.POINTER(qmlp_desc), _I, _I, _VP], _I),
     "qmlp_forward_partial": ([_VP, _VP, _I, _VP, _VP], _I),
     "qmlp_shard_combine": ([_VP, _VP, _I, _I, _VP, _VP], _I),
@@ -90,11 +93,13 @@ _SIGS = {
 
 
 def lib(path: str | None = None):
-    """Load libqmlp.so (raises QmlpError-compatible RuntimeError if absent)."""
+    """Load libqmlp.so (raises QmlpError-compatible RuntimeError if absent).
+    QMLP_LIB in the environment names another build of it to load instead
+    (the index-checking build, lib/libqmlp_bounds.so)."""
     global _lib
     with _lock:
         if _lib is None:
-            p = path or LIB_PATH
+            p = path or os.environ.get("QMLP_LIB") or LIB_PATH
             if not os.path.exists(p):
                 raise RuntimeError(f"libqmlp.so not built ({p}); run weight_quantized_swiglu_gb300.build.build()")
             L = ctypes.CDLL(p)
@@ -184,6 +189,22 @@ def qmlp_debug_split(h, x, act_in, M, g, u, out_f32, stream=None) -> int:
 
 def qmlp_debug_set_wait(h, limit_ns: int, withhold_last_step: bool) -> int:
     return lib().qmlp_debug_set_wait(h, limit_ns, 1 if withhold_last_step else 0)
+
+
+def qmlp_debug_bounds_enabled() -> int:
+    return lib().qmlp_debug_bounds_enabled()
+
+
+def qmlp_debug_bounds():
+    """(status, site, index) of the first failed index check since the last
+    call (a checking build; see include/qmlp.h)."""
+    site, index = ctypes.c_int(0), ctypes.c_ulonglong(0)
+    st = lib().qmlp_debug_bounds(ctypes.byref(site), ctypes.byref(index))
+    return st, site.value, index.value
+
+
+def qmlp_debug_bounds_limit(h, gate_up_bank_bytes: int) -> int:
+    return lib().qmlp_debug_bounds_limit(h, gate_up_bank_bytes)
 
 
 def qmlp_create_shard(desc: qmlp_desc, rank: int, nranks: int, stream=None) -> int:
@@ -308,6 +329,9 @@ class QuantMLP:
 
     def set_wait(self, limit_ns: int, withhold_last_step: bool = False):
         _chk(qmlp_debug_set_wait(self.h, limit_ns, withhold_last_step), "qmlp_debug_set_wait")
+
+    def bounds_limit(self, gate_up_bank_bytes: int):
+        _chk(qmlp_debug_bounds_limit(self.h, gate_up_bank_bytes), "qmlp_debug_bounds_limit")
 
     def forward(self, x, out, M=None, path=PATH_AUTO, stream=None):
         M = x.shape[0] if M is None else M

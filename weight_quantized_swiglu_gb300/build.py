@@ -3,6 +3,11 @@
 Each .cu translation unit is compiled in parallel, then linked into one
 shared library under weight_quantized_swiglu_gb300/lib/. The CUDA runtime is
 linked statically so the library depends only on the driver.
+
+build(bounds=True) builds the same sources with -DQMLP_DEBUG_BOUNDS into
+lib/libqmlp_bounds.so: every kernel then checks the indices of its computed
+global accesses and records the first bad one instead of making it (see
+qmlp_debug_bounds in include/qmlp.h). Tests load it in a process of its own.
 """
 from __future__ import annotations
 
@@ -19,6 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libqmlp.so")
+LIB_BOUNDS = os.path.join(LIBDIR, "libqmlp_bounds.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,25 +44,29 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(os.path.join(LIBDIR, "obj"), exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), bounds: bool = False) -> str:
+    lib = LIB_BOUNDS if bounds else LIB
+    if not force and up_to_date(lib):
+        return lib
+    objdir = os.path.join(LIBDIR, "obj_bounds" if bounds else "obj")
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
                     "--expt-relaxed-constexpr"] + list(extra_flags)
+    if bounds:
+        flags += ["-DQMLP_DEBUG_BOUNDS"]
     if verbose:
         flags += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(LIBDIR, "obj", os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         cmd = [cc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,14 +78,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if verbose:
         for _, err in results:
             sys.stderr.write(err)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results] + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, bounds="--bounds" in sys.argv))

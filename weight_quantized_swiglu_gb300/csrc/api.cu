@@ -88,6 +88,7 @@ struct qmlp_s {
     uint8_t* wsplit = nullptr;  // down records in the CTA-sliced layout
     float* spart = nullptr;     // [G][16][K] fp32 partial outputs
     unsigned long long* ticket = nullptr;  // grid-barrier ticket counter
+    size_t lim_a = 0;  // index-check tests: bytes of the decode kernel's gate/up banks the checks allow (0: all)
     bool has_gemm = false;
     GemmProj gm_gu, gm_d;
     void* a16 = nullptr;       // fp16 [max_M, max(K, I)] (GEMM prescaled activations)
@@ -154,11 +155,12 @@ const char* qmlp_status_str(qmlp_status s) {
         case QMLP_ERR_OOM: return "QMLP_ERR_OOM";
         case QMLP_ERR_CUDA: return "QMLP_ERR_CUDA";
         case QMLP_ERR_DEVICE_TIMEOUT: return "QMLP_ERR_DEVICE_TIMEOUT";
+        case QMLP_ERR_DEVICE_BOUNDS: return "QMLP_ERR_DEVICE_BOUNDS";
     }
     return "QMLP_ERR_UNKNOWN";
 }
 
-int qmlp_abi_version(void) { return 102; }
+int qmlp_abi_version(void) { return 103; }
 
 // ---------------------------------------------------------------------------
 // dense MLP
@@ -537,6 +539,7 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
             S.err = h->err;
             S.wait_ns = h->wait_ns;
             S.withhold = h->withhold;
+            S.lim_a = h->lim_a;
             if (launch_split(S, h->sp, s) != cudaSuccess) return QMLP_ERR_CUDA;
             continue;
         }
@@ -753,6 +756,41 @@ qmlp_status qmlp_debug_set_wait(qmlp_t* h, uint64_t limit_ns, int withhold_last_
     return QMLP_OK;
 }
 
+int qmlp_debug_bounds_enabled(void) {
+#ifdef QMLP_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+qmlp_status qmlp_debug_bounds(int* site, unsigned long long* index) {
+    if (!site || !index) return QMLP_ERR_INVALID_ARG;
+    *site = 0;
+    *index = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QMLP_ERR_CUDA;
+    cudaError_t (*const units[])(unsigned long long*) = {bounds_take_gemv_split, bounds_take_gemm_tc,
+                                                          bounds_take_gemv_stream, bounds_take_gemv_dec,
+                                                          bounds_take_moe_awq, bounds_take_moe_grouped,
+                                                          bounds_take_tp_shard};
+    unsigned long long first = 0;
+    for (auto take : units) {
+        unsigned long long v = 0;
+        if (take(&v) != cudaSuccess) return QMLP_ERR_CUDA;
+        if (!first) first = v;  // every unit's word is read, and so cleared
+    }
+    if (!first) return QMLP_OK;
+    *site = (int)(first >> 48);
+    *index = first & 0xffffffffffffull;
+    return QMLP_ERR_DEVICE_BOUNDS;
+}
+
+qmlp_status qmlp_debug_bounds_limit(qmlp_t* h, size_t gate_up_bank_bytes) {
+    if (!h || !qmlp_debug_bounds_enabled()) return QMLP_ERR_INVALID_ARG;
+    h->lim_a = gate_up_bank_bytes;
+    return QMLP_OK;
+}
+
 qmlp_status qmlp_debug_split(qmlp_t* h, const void* x, const void* act_in, int M, float* g, float* u,
                              float* out_f32, qmlp_stream_t stream) {
     if (!h || !x || !act_in || !g || !u || !out_f32) return QMLP_ERR_INVALID_ARG;
@@ -791,6 +829,7 @@ qmlp_status qmlp_debug_split(qmlp_t* h, const void* x, const void* act_in, int M
     S.err = h->err;
     S.wait_ns = h->wait_ns;
     S.withhold = h->withhold;
+    S.lim_a = h->lim_a;
     return launch_split(S, h->sp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMLP_OK
                                                                                           : QMLP_ERR_CUDA;
 }

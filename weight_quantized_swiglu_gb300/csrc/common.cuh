@@ -172,4 +172,41 @@ QMLP_DEV void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Index checks: a build with -DQMLP_DEBUG_BOUNDS checks the index of every
+// global access whose address the kernels compute from layout arithmetic or
+// runtime data against the size of its buffer (QMLP_INB); the default build
+// compiles the checks away. A failed check records (site << 48 | index) in
+// this translation unit's bounds word -- the first failure wins -- and the
+// caller skips the access: a load reads zero, a store is dropped, a bulk copy
+// is taken from the start of its buffer so that its barrier still completes.
+// No check traps. The host reads and clears the words (qmlp_debug_bounds).
+// Sites are numbered per file (gemv_split 1-9, gemm_tc 11-19, gemv_stream and
+// gemv_dec 21-29, moe_awq 31-39, moe_grouped 41-49, tp_shard 51-59).
+// ---------------------------------------------------------------------------
+#ifdef QMLP_DEBUG_BOUNDS
+static __device__ unsigned long long g_bounds_word;
+QMLP_DEV bool bounds_ok(long long idx, long long lim, int site) {
+    if (idx >= 0 && idx < lim) return true;
+    atomicCAS(&g_bounds_word, 0ull, ((unsigned long long)site << 48) | ((unsigned long long)idx & 0xffffffffffffull));
+    return false;
+}
+#define QMLP_INB(idx, lim, site) (::qmlp::bounds_ok((long long)(idx), (long long)(lim), (site)))
+// The unit's host-side reader: returns the word and clears it.
+#define QMLP_BOUNDS_UNIT(name)                                                        \
+    cudaError_t bounds_take_##name(unsigned long long* v) {                           \
+        cudaError_t e = cudaMemcpyFromSymbol(v, g_bounds_word, sizeof(*v));           \
+        if (e != cudaSuccess) return e;                                               \
+        const unsigned long long z = 0;                                               \
+        return cudaMemcpyToSymbol(g_bounds_word, &z, sizeof(z));                      \
+    }
+#else
+#define QMLP_INB(idx, lim, site) true
+#define QMLP_BOUNDS_UNIT(name)                              \
+    cudaError_t bounds_take_##name(unsigned long long* v) { \
+        *v = 0;                                             \
+        return cudaSuccess;                                 \
+    }
+#endif
+
 }  // namespace qmlp

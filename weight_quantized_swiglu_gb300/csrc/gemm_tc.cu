@@ -119,6 +119,8 @@ struct Args {
     int* err;
     uint64_t limit;        // ns a wait on another role may take before the CTA aborts
     int withhold;          // error-path tests: the producer never loads its last k-step
+    size_t tiles_bytes;    // index checks: bytes of the weight blocks
+    size_t ws_elems;       // index checks: floats of the split-K partial buffer
 };
 
 // ---------------------------------------------------------------------------
@@ -295,9 +297,10 @@ QMLP_DEV void store_tile(const Args& a, uint32_t tbase, int m, bool live, int sg
                     pk[j / 2 + 1] = pack_bf16x2(r4[2], r4[3]);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * (BN / 2) + c0);
+                if (QMLP_INB(nt * (BN / 2) + c0 + 31, a.ldo, 12) && QMLP_INB(m, a.M, 12))
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
         }
     } else if (a.epi == kEpiPlain) {
@@ -315,9 +318,10 @@ QMLP_DEV void store_tile(const Args& a, uint32_t tbase, int m, bool live, int sg
                     pk[j / 2 + 1] = pack_bf16x2(scalbnf(y[j + 2], -sg) * f.z, scalbnf(y[j + 3], -sg) * f.w);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * a.ldo + nt * BN + c0);
+                if (QMLP_INB(nt * BN + c0 + 31, a.ldo, 12) && QMLP_INB(m, a.M, 12))
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
         }
     } else {
@@ -331,6 +335,7 @@ QMLP_DEV void store_tile(const Args& a, uint32_t tbase, int m, bool live, int sg
             tmem_ld32(tbase + c0, y);
             if (live) {
                 float4* dst = reinterpret_cast<float4*>(out + (size_t)m * a.ldo + ocol + (c0 - cbeg));
+                if (QMLP_INB(ocol + (c0 - cbeg) + 31, a.ldo, 12) && QMLP_INB(m, a.M, 12))
 #pragma unroll
                 for (int v = 0; v < 8; ++v)
                     dst[v] = make_float4(scalbnf(y[4 * v], -sg), scalbnf(y[4 * v + 1], -sg),
@@ -415,9 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         ok = false;
                         break;
                     }
+                    const uint8_t* src = blk + (size_t)ks * kRawBytes;
+                    if (!QMLP_INB((size_t)(src - a.tiles) + kRawBytes - 1, a.tiles_bytes, 11)) src = a.tiles;
                     mbar_arrive_expect_tx(full(s), kABytes + kRawBytes);
                     tma_load_2d(base_s + kOffA + s * kABytes, &amap, ks * BK, mt * BM, full(s));
-                    bulk_g2s(base_s + kOffRaw + s * kRawBytes, blk + (size_t)ks * kRawBytes, kRawBytes, full(s));
+                    bulk_g2s(base_s + kOffRaw + s * kRawBytes, src, kRawBytes, full(s));
                 }
             }
             // copies still in flight (only after an abort): wait for the last
@@ -497,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 for (int c0 = 0; c0 < BN; c0 += 32) {
                     float y[32];
                     tmem_ld32(tbase + c0, y);
-                    if (live) {
+                    if (live && QMLP_INB(((size_t)sp * a.M + m) * a.N + nt * BN + c0 + 31, a.ws_elems, 13)) {
                         float4* dst = reinterpret_cast<float4*>(ws + c0);
 #pragma unroll
                         for (int v = 0; v < 8; ++v) dst[v] = make_float4(y[4 * v], y[4 * v + 1], y[4 * v + 2], y[4 * v + 3]);
@@ -742,6 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     mbar_arrive_expect_tx(full(s), kABytes + kR);
                     tma_load_2d(base_s + S::A + s * kABytes, &amap, ks * BK, mt2 * 2 * BM + (int)rank * BM, full(s));
                     const uint8_t* src = blk + (size_t)ks * raw_bytes<FMT>();
+                    if (!QMLP_INB((size_t)(src - a.tiles) + raw_bytes<FMT>() - 1, a.tiles_bytes, 15)) src = a.tiles;
                     const uint32_t dst = base_s + S::Raw + s * kR;
                     if (FMT == kNVFP4) {
                         // rows 128 rank.. of the block: their codes, then their scales
@@ -898,10 +906,12 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const Args a) {
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)m * a.ldo + n;
     const size_t plane = (size_t)a.M * a.N;
     const float* ws = a.ws + (size_t)m * a.N;
+    if (!QMLP_INB((size_t)m * a.ldo + n, (size_t)a.M * a.ldo, 14)) return;
     if (swiglu) {
         const int col = (n / (BN / 2)) * BN + n % (BN / 2);  // gate column of the interleaved tile
         float g = 0.0f, u = 0.0f;
         for (int sp = 0; sp < a.splits; ++sp) {
+            if (!QMLP_INB((size_t)m * a.N + sp * plane + col + BN / 2, a.ws_elems, 14)) break;
             g += ws[sp * plane + col];
             u += ws[sp * plane + col + BN / 2];
         }
@@ -910,7 +920,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const Args a) {
         *out = __float2bfloat16_rn(silu_f32(gv) * uv);
     } else {
         float y = 0.0f;
-        for (int sp = 0; sp < a.splits; ++sp) y += ws[sp * plane + n];
+        for (int sp = 0; sp < a.splits; ++sp)
+            if (QMLP_INB((size_t)m * a.N + sp * plane + n, a.ws_elems, 14)) y += ws[sp * plane + n];
         const float f = FMT == kNVFP4 ? a.inv0 : a.cs0[n];
         *out = __float2bfloat16_rn(scalbnf(y, -sg) * f);
     }
@@ -1158,6 +1169,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     a.err = L.err;
     a.limit = L.wait_ns ? L.wait_ns : kGemmWaitNs;
     a.withhold = L.withhold ? 1 : 0;
+    a.tiles_bytes = gemm_tiles_bytes(P.fmt, P.N, P.K);
+    a.ws_elems = L.ws ? gemm_splitk_ws_elems(num_sms) : 0;
     // Split-K when the tiles cannot fill the GPU (small M, or the down
     // projection's few column tiles): each (tile, k-range) unit writes fp32
     // partials and a reduce kernel adds them in split order. The partials
@@ -1178,5 +1191,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     const int grid = std::min(tiles0 * a.splits, std::max(num_sms, 1));
     return P.fmt == kFP8 ? launch_fmt<kFP8>(map, a, grid, s) : launch_fmt<kNVFP4>(map, a, grid, s);
 }
+
+QMLP_BOUNDS_UNIT(gemm_tc)
 
 }  // namespace qmlp

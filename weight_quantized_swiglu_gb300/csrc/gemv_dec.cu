@@ -55,6 +55,7 @@ struct KArgs {
     void* out;
     float* part;
     int* counters;
+    size_t part_cap;  // index checks: floats of the partial buffer
 };
 
 template <int FMT, int NT, int NP, int EPI>
@@ -93,6 +94,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const KArgs a) {
 
     const size_t tile0 = (size_t)rt * a.Kc + c0;
     ChunkW cur[NP], nxt[NP];
+    // every logical record (row tile, k-chunk) this CTA reads exists
+    if (!QMLP_INB(tile0 + (nch > 0 ? nch - 1 : 0), (size_t)a.Nt * a.Kc, 25)) return;
     if (warp < nch) {
         cur[0] = load_chunk<FMT>(a.wc0, tile0 + warp, a.Lr, a.TWr, a.Rr, lane);
         if (NP == 2) cur[NP - 1] = load_chunk<FMT>(a.wc1, tile0 + warp, a.Lr, a.TWr, a.Rr, lane);
@@ -139,7 +142,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const KArgs a) {
             const int row = rt * kTileRows + r;
 #pragma unroll
             for (int p = 0; p < NP; ++p)
-                a.part[((size_t)(ks * NP + p) * M + m) * a.N + row] = cta_value(p, r, m);
+                if (QMLP_INB(((size_t)(ks * NP + p) * M + m) * a.N + row, a.part_cap, 26))
+                    a.part[((size_t)(ks * NP + p) * M + m) * a.N + row] = cta_value(p, r, m);
         }
         __threadfence();
         __syncthreads();
@@ -153,13 +157,15 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const KArgs a) {
     for (int it = tid; it < items; it += kThreads) {
         const int m = it / kTileRows, r = it - m * kTileRows;
         const int row = rt * kTileRows + r;
+        if (!QMLP_INB(row, a.N, 27)) continue;
         float v[NP];
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             if (a.ksplit > 1) {
                 float s = 0.0f;
                 for (int q = 0; q < a.ksplit; ++q)
-                    s += __ldcg(&a.part[((size_t)(q * NP + p) * M + m) * a.N + row]);
+                    if (QMLP_INB(((size_t)(q * NP + p) * M + m) * a.N + row, a.part_cap, 26))
+                        s += __ldcg(&a.part[((size_t)(q * NP + p) * M + m) * a.N + row]);
                 v[p] = s;
             } else {
                 v[p] = cta_value(p, r, m);
@@ -357,6 +363,7 @@ cudaError_t launch_gemv(const GemvLaunch& L, int num_sms, cudaStream_t s) {
     a.cps = pl.cps;
     a.out = L.out;
     a.part = L.part;
+    a.part_cap = L.part_cap;
     a.counters = L.counters;
     const dim3 grid(P.Nt, pl.ksplit);
     return L.fmt == kNVFP4 ? dispatch<kNVFP4>(a, pl.nt, L.epi, grid, pl.smem, s)
@@ -390,5 +397,7 @@ cudaError_t repack_fp8_split(const uint8_t* w, int N, int K, const SplitPlan& P,
                                                 RecPos{P.LB, P.G * 16, P.RB, true, P.Cb, P.LB}, wc);
     return cudaPeekAtLastError();
 }
+
+QMLP_BOUNDS_UNIT(gemv_dec)
 
 }  // namespace qmlp

@@ -90,6 +90,8 @@ struct Args {
     int xraw_off, xraw_bytes;  // raw bf16 x copied to shared memory (0: staged from global)
     uint64_t limit;            // ns a wait on another role or CTA may take before it gives up
     int withhold;              // error-path tests: the producer never issues the last step
+    size_t wa_bytes, wb_bytes; // index checks: bytes of each gate/up bank and of the down bank
+    size_t part_elems;         // index checks: floats of the partial buffer
 };
 
 struct Ring {
@@ -110,6 +112,11 @@ struct Steps {
     size_t stride_a, stride_b;
     uint32_t bytes_a, bytes_b;  // per block
     int steps_a, steps;
+    size_t off_a, off_b;        // index checks: offset of this CTA's first block in its bank
+    size_t lim_a, lim_b;        // index checks: bank bytes
+    const uint8_t* base_a0;     // index checks: bank starts (a failed check copies from there)
+    const uint8_t* base_a1;
+    const uint8_t* base_b;
 };
 
 // Producer (one thread): every step of both phases into the ring, without a
@@ -128,12 +135,21 @@ QMLP_DEV int produce(const Steps& st, const Ring& r, int* err, int q0, int q1) {
         const uint32_t full = r.full0 + 8u * slot;
         const uint32_t dst = r.base_s + (uint32_t)slot * r.slot_bytes;
         if (q < st.steps_a) {
+            const uint8_t* s0 = st.a0 + (size_t)q * st.stride_a;
+            const uint8_t* s1 = st.a1 + (size_t)q * st.stride_a;
+            if (!QMLP_INB(st.off_a + (size_t)q * st.stride_a + st.bytes_a - 1, st.lim_a, 1)) {
+                s0 = st.base_a0;
+                s1 = st.base_a1;
+            }
             mbar_arrive_expect_tx(full, 2 * st.bytes_a);
-            bulk_g2s(dst, st.a0 + (size_t)q * st.stride_a, st.bytes_a, full);
-            bulk_g2s(dst + st.bytes_a, st.a1 + (size_t)q * st.stride_a, st.bytes_a, full);
+            bulk_g2s(dst, s0, st.bytes_a, full);
+            bulk_g2s(dst + st.bytes_a, s1, st.bytes_a, full);
         } else {
+            const uint8_t* sb = st.b + (size_t)(q - st.steps_a) * st.stride_b;
+            if (!QMLP_INB(st.off_b + (size_t)(q - st.steps_a) * st.stride_b + st.bytes_b - 1, st.lim_b, 2))
+                sb = st.base_b;
             mbar_arrive_expect_tx(full, st.bytes_b);
-            bulk_g2s(dst, st.b + (size_t)(q - st.steps_a) * st.stride_b, st.bytes_b, full);
+            bulk_g2s(dst, sb, st.bytes_b, full);
         }
         if (++slot == r.depth) {
             slot = 0;
@@ -220,6 +236,7 @@ QMLP_DEV void epilogue_a(const Args& a, int M, int lt, const float (&v)[2][NT][4
             if (m >= M) continue;
             const int r = lt * 16 + g + 8 * (e >> 1);  // row within the CTA's slice
             const int i = blockIdx.x * tslice + r;     // intermediate index
+            if (!QMLP_INB((size_t)m * a.I + i, (size_t)a.M * a.I, 4)) continue;
             const float s0 = FMT == kNVFP4 ? a.inv0 : a.chs0[i];
             const float s1 = FMT == kNVFP4 ? a.inv1 : a.chs1[i];
             const float pw = pow2_neg(s_sig[m]);
@@ -273,7 +290,9 @@ QMLP_DEV void store_part_b(const Args& a, int M, int rt, const float (&v)[1][NT]
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int m = n * 8 + 2 * t + (e & 1);
-            if (m < M) dst[(size_t)m * a.K + rt * 16 + g + 8 * (e >> 1)] = v[0][n][e] * pow2_neg(s_sigb[m]);
+            if (m < M && QMLP_INB(rt * 16 + g + 8 * (e >> 1), a.K, 5) &&
+                QMLP_INB((size_t)blockIdx.x * M * a.K + (size_t)m * a.K + rt * 16 + g + 8 * (e >> 1), a.part_elems, 5))
+                dst[(size_t)m * a.K + rt * 16 + g + 8 * (e >> 1)] = v[0][n][e] * pow2_neg(s_sigb[m]);
         }
 }
 
@@ -380,7 +399,8 @@ QMLP_DEV void stage_x_half(const __nv_bfloat16* x, int M, int K, int pass, bool 
             if (it < total) {
                 const int m = it / per_tok, r = it - m * per_tok, cp = r >> 3, e8 = r & 7;
                 const int c = (cp % q) + (cp / q) * h + pass * q;
-                v[u] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)m * K + c * kChunkK + e8 * 8));
+                if (QMLP_INB((size_t)m * K + c * kChunkK + e8 * 8 + 7, (size_t)M * K, 8))
+                    v[u] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)m * K + c * kChunkK + e8 * 8));
             }
         }
 #pragma unroll
@@ -513,6 +533,13 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
             st.b = a.wb + (size_t)blockIdx.x * st.bytes_b;
             st.steps_a = stepsA;
             st.steps = stepsA + stepsB - (a.withhold ? 1 : 0);
+            st.off_a = (size_t)blockIdx.x * st.bytes_a;
+            st.off_b = (size_t)blockIdx.x * st.bytes_b;
+            st.lim_a = a.wa_bytes;
+            st.lim_b = a.wb_bytes;
+            st.base_a0 = a.wa0;
+            st.base_a1 = a.wa1;
+            st.base_b = a.wb;
             // The weights do not depend on the previous kernel: the first
             // kPreSteps steps go out before the wait, x right after it, then
             // the rest of the weights. (Measured back to back: one step
@@ -521,8 +548,12 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
             produce<FMT>(st, r, a.err, 0, pre);
             pdl_wait();
             if (a.xraw_bytes) {
-                mbar_arrive_expect_tx(r.xbar, a.xraw_bytes);
-                bulk_g2s(smem_u32(smem + a.xraw_off), a.x, a.xraw_bytes, r.xbar);
+                if (QMLP_INB(a.xraw_bytes - 1, (size_t)a.M * a.K * 2, 3)) {
+                    mbar_arrive_expect_tx(r.xbar, a.xraw_bytes);
+                    bulk_g2s(smem_u32(smem + a.xraw_off), a.x, a.xraw_bytes, r.xbar);
+                } else {
+                    mbar_arrive(r.xbar);  // no copy: the barrier still completes
+                }
             }
             int q = produce<FMT>(st, r, a.err, pre, st.steps);
             if (a.xraw_bytes) mbar_wait_bounded(r.xbar, 0, kLimit);  // the x copy is never left in flight
@@ -788,8 +819,14 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < kRedLoads; ++i) {
             const int b = warp + i * kW;
-            v0[i] = (ok0 && b < a.G) ? __ldcg(src0 + (size_t)b * bstride) : 0.0f;
-            v1[i] = (ok1 && b < a.G) ? __ldcg(src1 + (size_t)b * bstride) : 0.0f;
+            v0[i] = (ok0 && b < a.G &&
+                     QMLP_INB((size_t)(u0 / units_n) * a.K + n0 + (size_t)b * bstride, a.part_elems, 6))
+                        ? __ldcg(src0 + (size_t)b * bstride)
+                        : 0.0f;
+            v1[i] = (ok1 && b < a.G &&
+                     QMLP_INB((size_t)(u1 / units_n) * a.K + n1 + (size_t)b * bstride, a.part_elems, 6))
+                        ? __ldcg(src1 + (size_t)b * bstride)
+                        : 0.0f;
         }
         float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
@@ -808,7 +845,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
     for (int i = warp; i < nu; i += kW) {
         const int u = blockIdx.x + i * gridDim.x;
         const int m = u / units_n, n = (u % units_n) * 32 + lane;
-        if (n < a.K) {
+        if (n < a.K && QMLP_INB((size_t)m * a.K + n, (size_t)a.M * a.K, 6)) {
             float tot = 0.0f;
 #pragma unroll
             for (int w = 0; w < kW; ++w) tot += red[(i * kW + w) * 32 + lane];
@@ -837,6 +874,7 @@ constexpr int kRedMinBlocks = 5;
 static_assert(kW * kRedLoads <= kRedWarps * kRedPer, "every planned G is reducible");
 
 struct RArgs {
+    size_t part_elems;  // index checks: floats of the partial buffer
     const float* part;  // [G][M][K]
     const float* chsd;  // FP8 down per-channel scales
     float invd;         // NVFP4 down 1/global
@@ -862,14 +900,16 @@ __global__ void __launch_bounds__(kRedThr, kRedMinBlocks) gemv_split_reduce_kern
 #pragma unroll
         for (int i = 0; i < kRedPer; ++i) {
             const int b = warp + i * kRedWarps;
-            v[i] = (n < a.K && b < a.G) ? __ldcg(src + (size_t)b * bstride) : 0.0f;
+            v[i] = (n < a.K && b < a.G && QMLP_INB((size_t)m * a.K + n + (size_t)b * bstride, a.part_elems, 7))
+                       ? __ldcg(src + (size_t)b * bstride)
+                       : 0.0f;
         }
         float s = 0.0f;
 #pragma unroll
         for (int i = 0; i < kRedPer; ++i) s += v[i];
         red[warp][lane] = s;
         __syncthreads();
-        if (warp == 0 && n < a.K) {
+        if (warp == 0 && n < a.K && QMLP_INB((size_t)m * a.K + n, (size_t)a.M * a.K, 7)) {
             float tot = 0.0f;
 #pragma unroll
             for (int w = 0; w < kRedWarps; ++w) tot += red[w][lane];
@@ -1060,6 +1100,10 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
     a.xraw_off = lay.xraw;
     a.limit = L.wait_ns ? L.wait_ns : kLimit;
     a.withhold = L.withhold ? 1 : 0;
+    const size_t rec = L.fmt == kNVFP4 ? kRecNVFP4 : kRecFP8;
+    a.wa_bytes = L.lim_a ? L.lim_a : (size_t)P.G * kW * P.LA * rec;
+    a.wb_bytes = split_codes_bytes(L.fmt, P);
+    a.part_elems = split_part_elems(L.K, P);
     // the bulk copy of x needs device memory; host-resident x is staged by loads
     a.xraw_bytes = L.x_in_host ? 0 : lay.xraw_bytes;
     // M <= 8 (split_fits): one 8-token MMA tile. Schedule (a) for NVFP4 at
@@ -1074,6 +1118,7 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
                                            : launch_t<kFP8, 1, false, true>(a, lay.total, s);
     if (e != cudaSuccess) return e;
     RArgs r;
+    r.part_elems = a.part_elems;
     r.part = L.part;
     r.chsd = L.chsd;
     r.invd = L.invd;
@@ -1094,5 +1139,7 @@ cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t 
     return L.fmt == kNVFP4 ? cudaLaunchKernelEx(&cfg, gemv_split_reduce_kernel<kNVFP4>, r)
                            : cudaLaunchKernelEx(&cfg, gemv_split_reduce_kernel<kFP8>, r);
 }
+
+QMLP_BOUNDS_UNIT(gemv_split)
 
 }  // namespace qmlp

@@ -64,6 +64,7 @@ struct PhaseArgs {
     int L;                   // records per warp
     int smax;                // partial slots per row tile
     int depth;               // ring slots per warp
+    size_t part_floats;      // index checks: floats of the partial buffer
 };
 
 struct StreamArgs {
@@ -89,6 +90,7 @@ __device__ __noinline__ void tile_epilogue(const PhaseArgs* a, int M, int rt, co
             const int m = n * 8 + 2 * t + (e & 1);
             if (m >= M) continue;
             const int row = rt * kTileRows + g + (e >= 2 ? 8 : 0);
+            if (!QMLP_INB(row, a->N, 24)) continue;
             const float y0 = scalbnf(v[(0 * NT + n) * 4 + e], -s_sig[m]);
             if (EPI == kEpiRaw) {
                 reinterpret_cast<float*>(a->out)[(size_t)m * a->N + row] = y0;
@@ -123,6 +125,9 @@ __device__ __noinline__ void write_partial(const PhaseArgs* a, float* part, int 
     int slot, nc;
     tile_contributors(a, rt, gw, &slot, &nc);
     float4* dst = reinterpret_cast<float4*>(part) + ((size_t)rt * a->smax + slot) * (Q * 32);
+    if (!QMLP_INB(slot, a->smax, 22) ||
+        !QMLP_INB((((size_t)rt * a->smax + slot) * (Q * 32) + (Q - 1) * 32 + lane) * 4 + 3, a->part_floats, 22))
+        return;
 #pragma unroll
     for (int q = 0; q < Q; ++q)
         dst[q * 32 + lane] = make_float4(acc[q * 4 + 0], acc[q * 4 + 1], acc[q * 4 + 2], acc[q * 4 + 3]);
@@ -140,7 +145,7 @@ __device__ __noinline__ void finish_partials(const PhaseArgs* a, float* part, in
     int prev = -1;
     if (lane < npend) {
         const int rt = lane == 0 ? pend[0] : pend[1];
-        unsigned* ctr = reinterpret_cast<unsigned*>(&a->counters[rt]);
+        unsigned* ctr = reinterpret_cast<unsigned*>(&a->counters[QMLP_INB(rt, a->Nt, 23) ? rt : 0]);
         asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
     }
     __syncwarp();
@@ -158,6 +163,8 @@ __device__ __noinline__ void finish_partials(const PhaseArgs* a, float* part, in
         for (int e = 0; e < Q * 4; ++e) v[e] = 0.0f;
         const float4* src = reinterpret_cast<const float4*>(part) + (size_t)rt * a->smax * (Q * 32);
         for (int sl = 0; sl < nc; ++sl) {
+            if (!QMLP_INB((((size_t)rt * a->smax + sl) * (Q * 32) + (Q - 1) * 32 + lane) * 4 + 3, a->part_floats, 23))
+                break;
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
                 const float4 f = __ldcg(src + ((size_t)sl * Q + q) * 32 + lane);
@@ -202,9 +209,15 @@ QMLP_DEV int produce_phase(const PhaseArgs& a, const Ring& r, int q, int* err) {
         }
         const uint32_t full = r.full0 + 8u * slot;
         const uint32_t dst = r.base_s + (uint32_t)slot * r.slot_bytes;
+        const uint8_t* s0 = src0 + (size_t)j * stride;
+        const uint8_t* s1 = src1 + (size_t)j * stride;
+        if (!QMLP_INB((size_t)(s0 - a.wc0) + step_bytes - 1, (size_t)a.TWr * a.L * rec, 21)) {
+            s0 = a.wc0;
+            s1 = a.wc1;
+        }
         mbar_arrive_expect_tx(full, NP * step_bytes);
-        bulk_g2s(dst, src0 + (size_t)j * stride, step_bytes, full);
-        if (NP == 2) bulk_g2s(dst + step_bytes, src1 + (size_t)j * stride, step_bytes, full);
+        bulk_g2s(dst, s0, step_bytes, full);
+        if (NP == 2) bulk_g2s(dst + step_bytes, s1, step_bytes, full);
         if (++slot == r.depth) {
             slot = 0;
             ++round;
@@ -549,6 +562,8 @@ cudaError_t launch_gemv_stream(int fmt, int M, const GemvStreamPhase& A, const G
         a.B = a.A;
     }
     if (need > part_cap) return cudaErrorInvalidValue;
+    a.A.part_floats = part_cap;
+    a.B.part_floats = part_cap;
     a.part = part;
     a.bar = bar;
     a.err = err;
@@ -558,5 +573,7 @@ cudaError_t launch_gemv_stream(int fmt, int M, const GemvStreamPhase& A, const G
     a.depth = depth;
     return dispatch(fmt, nt, m1, mode, &a, smem, &blocks, false, s, grid);
 }
+
+QMLP_BOUNDS_UNIT(gemv_stream)
 
 }  // namespace qmlp

@@ -134,6 +134,7 @@ struct SplitLaunch {
     int* err = nullptr;
     uint64_t wait_ns = 0;            // bounded-wait limit (0: the kernel's default of 2 s)
     bool withhold = false;           // error-path tests: the last weight step is never issued
+    size_t lim_a = 0;                // index-check tests: bytes of the gate/up banks the checks allow (0: all)
 };
 cudaError_t launch_split(const SplitLaunch& L, const SplitPlan& P, cudaStream_t s);
 
@@ -255,5 +256,16 @@ cudaError_t repack_moe_w13_blocks(const uint8_t* w, const uint8_t* meta, int met
                                   uint8_t* w_out, uint8_t* meta_out, cudaStream_t s);
 cudaError_t repack_moe(const uint8_t* w, const uint8_t* meta, int meta_bytes, int E, int N,
                        int Kr, uint8_t* w_out, uint8_t* meta_out, cudaStream_t s);
+
+// Index checks of a QMLP_DEBUG_BOUNDS build (common.cuh): each translation
+// unit's first failed check, (site << 48) | index, or 0; reading clears it.
+// The default build returns 0.
+cudaError_t bounds_take_gemv_split(unsigned long long* v);
+cudaError_t bounds_take_gemm_tc(unsigned long long* v);
+cudaError_t bounds_take_gemv_stream(unsigned long long* v);
+cudaError_t bounds_take_gemv_dec(unsigned long long* v);
+cudaError_t bounds_take_moe_awq(unsigned long long* v);
+cudaError_t bounds_take_moe_grouped(unsigned long long* v);
+cudaError_t bounds_take_tp_shard(unsigned long long* v);
 
 }  // namespace qmlp

@@ -83,6 +83,8 @@ struct Args {
     __half* gu_dbg;
     __half* act_dbg;
     __half* y_dbg;
+    // index checks: bytes of the banks, elements of the act workspace
+    size_t w13_bytes, w13_meta_bytes, w2_bytes, w2_meta_bytes, act_elems;
 };
 
 // One metadata record (little-endian fp16 scale, then fp16 bias or u8 zero)
@@ -175,7 +177,14 @@ QMLP_DEV bool w13_cta(const Args& a, int bx, int r, uint32_t* x16, float (*part)
     const uint8_t* bcodes = a.w13 + blk * moe_w13_block_bytes(a.K);
     const int np = moe_w13_pairs(a.K);
     const int ms = moe_w13_meta_stride(a.K, MB);
+    // every byte this lane reads of the banks lies inside them (one check of
+    // the whole range: the offsets inside it are fixed by the layout)
+    const bool inb = SL ? (QMLP_INB((blk + 1) * moe_w13_block_bytes(a.K) - 1, a.w13_bytes, 31) &&
+                           QMLP_INB((blk + 1) * moe_w13_meta_block_bytes(a.K, MB) - 1, a.w13_meta_bytes, 32))
+                        : (QMLP_INB((rows[1] + 1) * (a.K / 2) - 1, a.w13_bytes, 31) &&
+                           QMLP_INB((rows[1] + 1) * gpr * MB - 1, a.w13_meta_bytes, 32));
     auto load_batch = [&](int cb) {
+        if (!inb) return;
         if (SL) {
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
@@ -338,7 +347,7 @@ QMLP_DEV bool w13_cta(const Args& a, int bx, int r, uint32_t* x16, float (*part)
         const int q = 8 * bx + j;
         const __half gh = __float2half_rn(scalbnf(hg, -sig)), uh = __float2half_rn(scalbnf(hu, -sig));
         const __half act = __float2half_rn(silu_f32(__half2float(gh)) * __half2float(uh));
-        a.act_ws[(size_t)r * a.I + q] = act;
+        if (QMLP_INB((size_t)r * a.I + q, a.act_elems, 33)) a.act_ws[(size_t)r * a.I + q] = act;
         if (a.gu_dbg) {
             a.gu_dbg[(size_t)r * 2 * a.I + q] = gh;
             a.gu_dbg[(size_t)r * 2 * a.I + a.I + q] = uh;
@@ -386,10 +395,15 @@ QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s
     const uint8_t* m0p = a.w2_meta + row0 * gpr * MB;
     const uint8_t* m8p = a.w2_meta + (row0 + 8) * gpr * MB;
     const bool al4 = a.meta_al4 != 0;
+    // the lane's rows of the banks and its route's act row lie inside them
+    const bool inb = QMLP_INB((row0 + 9) * (a.I / 2) - 1, a.w2_bytes, 34) &&
+                     QMLP_INB((row0 + 9) * gpr * MB - 1, a.w2_meta_bytes, 34) &&
+                     QMLP_INB((size_t)(r + 1) * a.I - 1, a.act_elems, 35);
     uint2 cw[kG2][2];         // checkpoint layout: words 2j, 2j+1 of rows g and g+8 for k16 group j
     uint32_t cs[kG2 / 2][2];  // lane-sliced layout: this lane's 4 bytes of unit j/2 (groups j, j+1)
     uint32_t mw[kG2 / 2][2];  // the AWQ records of the batch
     auto load_batch = [&](int gb) {  // gb is a multiple of kG2 (even)
+        if (!inb) return;
         if (SL) {
 #pragma unroll
             for (int i = 0; i < kG2 / 2; ++i) {
@@ -432,8 +446,8 @@ QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s
 #pragma unroll
             for (int i = 0; i < kG2; ++i) {
                 const int j = gb + i;
-                av[i][0] = j < ng ? act[8 * j + t] : 0u;
-                av[i][1] = j < ng ? act[8 * j + 4 + t] : 0u;
+                av[i][0] = j < ng && inb ? act[8 * j + t] : 0u;
+                av[i][1] = j < ng && inb ? act[8 * j + 4 + t] : 0u;
             }
 #pragma unroll
             for (int i = 0; i < kG2; ++i) {
@@ -469,7 +483,7 @@ QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s
         float s = 0.0f;
         for (int rr = 0; rr < a.topk; ++rr)
             if (s_ok[rr]) s = fmaf(s_rw[rr], ys[rr][threadIdx.x], s);
-        a.out[n0 + threadIdx.x] = __float2half_rn(s);
+        if (QMLP_INB(n0 + threadIdx.x, a.K, 36)) a.out[n0 + threadIdx.x] = __float2half_rn(s);
     }
 }
 
@@ -535,6 +549,13 @@ cudaError_t launch_moe(const MoeLaunch& L, int num_sms, cudaStream_t s) {
     a.gu_dbg = L.gu_dbg;
     a.act_dbg = L.act_dbg;
     a.y_dbg = L.y_dbg;
+    const int MB = L.meta_bytes;
+    a.w13_bytes = L.sliced ? moe_w13_bank_bytes(L.E, L.I, L.K) : (size_t)L.E * 2 * L.I * (L.K / 2);
+    a.w13_meta_bytes =
+        L.sliced ? moe_w13_meta_bank_bytes(L.E, L.I, L.K, MB) : (size_t)L.E * 2 * L.I * (L.K / 32) * MB;
+    a.w2_bytes = (size_t)L.E * L.K * (L.I / 2);
+    a.w2_meta_bytes = (size_t)L.E * L.K * (L.I / 32) * MB;
+    a.act_elems = (size_t)16 * L.I;
     if (L.sliced) return L.meta_bytes == 4 ? launch_mb<4, true>(a, s) : launch_mb<3, true>(a, s);
     return L.meta_bytes == 4 ? launch_mb<4, false>(a, s) : launch_mb<3, false>(a, s);
 }
@@ -654,5 +675,7 @@ cudaError_t repack_moe(const uint8_t* w, const uint8_t* meta, int meta_bytes, in
     if (e != cudaSuccess) return e;
     return cudaMemcpyAsync(meta_out, meta, (size_t)E * N * (Kr / 32) * meta_bytes, cudaMemcpyDeviceToDevice, s);
 }
+
+QMLP_BOUNDS_UNIT(moe_awq)
 
 }  // namespace qmlp

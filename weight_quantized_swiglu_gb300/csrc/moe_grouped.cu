@@ -71,6 +71,9 @@ struct GArgs {
     int* route_list;     // [M * topk]: route indices sorted by expert
     int4* groups;        // {expert, first position in route_list, count, 0}
     int* n_groups;
+    // index checks: bytes of the banks, the group list's capacity
+    size_t w13_bytes, w13_meta_bytes, w2_bytes, w2_meta_bytes;
+    int gmax;
 };
 
 template <int MB>
@@ -183,11 +186,15 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const GArgs a)
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += kRouteThreads) {
         const int id = a.ids[i];
-        if (id >= 0 && id < a.E) a.route_list[off[id] + atomicAdd(&cur[id], 1)] = i;
+        if (id >= 0 && id < a.E) {
+            const int pos = off[id] + atomicAdd(&cur[id], 1);
+            if (QMLP_INB(pos, n, 41)) a.route_list[pos] = i;
+        }
     }
     for (int e = e0; e < e1; ++e)
         for (int j = 0; j * gc < cnt[e]; ++j)
-            a.groups[goff[e] + j] = make_int4(e, off[e] + j * gc, min(gc, cnt[e] - j * gc), 0);
+            if (QMLP_INB(goff[e] + j, a.gmax, 42))
+                a.groups[goff[e] + j] = make_int4(e, off[e] + j * gc, min(gc, cnt[e] - j * gc), 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -206,6 +213,7 @@ __global__ void __launch_bounds__(kGW13 * 32, 3) moe_w13_grouped_kernel(const GA
     if ((int)blockIdx.x >= *a.n_groups) return;
     const int4 grp = a.groups[blockIdx.x];
     const int e = grp.x, cnt = grp.z;
+    if (!QMLP_INB(e, a.E, 43) || !QMLP_INB(grp.y + cnt - 1, a.M * a.topk, 43) || !QMLP_INB(cnt - 1, NC, 43)) return;
     // a group of more than 8 routes is two MMA column sets on the same A fragments
     const bool two = NC == 16 && cnt > kCols;
     const int ns = two ? 2 * kCols : kCols;  // slots staged
@@ -236,6 +244,9 @@ __global__ void __launch_bounds__(kGW13 * 32, 3) moe_w13_grouped_kernel(const GA
         const size_t blk = ((size_t)e * (a.I / 8) + octet) * kMoeKSplit + ks;
         const uint8_t* bc = a.w13 + blk * moe_w13_block_bytes(a.K);
         const uint8_t* bm = a.w13_meta + blk * moe_w13_meta_block_bytes(a.K, MB);
+        if (!QMLP_INB((blk + 1) * moe_w13_block_bytes(a.K) - 1, a.w13_bytes, 44) ||
+            !QMLP_INB((blk + 1) * moe_w13_meta_block_bytes(a.K, MB) - 1, a.w13_meta_bytes, 44))
+            return;
 #pragma unroll
         for (int i = 0; i < kGC13; ++i) {
             const int c = cb + i;
@@ -384,8 +395,9 @@ __global__ void __launch_bounds__(kGW13 * 32, 3) moe_w13_grouped_kernel(const GA
                 }
                 const int sg = s_sig[c];
                 const __half gh = __float2half_rn(scalbnf(hg, -sg)), uh = __float2half_rn(scalbnf(hu, -sg));
-                a.act_ws[(size_t)s_route[c] * a.I + 8 * tp + j] =
-                    __float2half_rn(silu_f32(__half2float(gh)) * __half2float(uh));
+                if (QMLP_INB((size_t)s_route[c] * a.I + 8 * tp + j, (size_t)a.M * a.topk * a.I, 45))
+                    a.act_ws[(size_t)s_route[c] * a.I + 8 * tp + j] =
+                        __float2half_rn(silu_f32(__half2float(gh)) * __half2float(uh));
             }
         }
         __syncthreads();  // part is rewritten by the next octet
@@ -404,6 +416,7 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
     if ((int)blockIdx.x >= *a.n_groups) return;
     const int4 grp = a.groups[blockIdx.x];
     const int e = grp.x, cnt = grp.z;
+    if (!QMLP_INB(e, a.E, 46) || !QMLP_INB(grp.y + cnt - 1, a.M * a.topk, 46) || !QMLP_INB(cnt - 1, NC, 46)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int astride = a.I / 2 + 4;
     const bool two = NC == 16 && cnt > kCols;  // two MMA column sets on the same A fragments
@@ -422,7 +435,9 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
 #pragma unroll
                 for (int c = 0; c < kCols; ++c) {
                     const int r = s_route[c0 + c];
-                    v[c] = r >= 0 ? act32[(size_t)r * ih + k2] : 0u;
+                    v[c] = r >= 0 && QMLP_INB((size_t)r * ih + k2, (size_t)a.M * a.topk * ih, 46)
+                               ? act32[(size_t)r * ih + k2]
+                               : 0u;
                 }
 #pragma unroll
                 for (int c = 0; c < kCols; ++c) acts[(c0 + c) * astride + k2] = v[c];
@@ -443,6 +458,8 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
     const uint2* c8p = reinterpret_cast<const uint2*>(a.w2 + (row0 + 8) * (a.I / 2));
     const uint8_t* m0p = a.w2_meta + row0 * gpr * MB;
     const uint8_t* m8p = a.w2_meta + (row0 + 8) * gpr * MB;
+    if (!QMLP_INB((row0 + 9) * (a.I / 2) - 1, a.w2_bytes, 47) || !QMLP_INB((row0 + 9) * gpr * MB - 1, a.w2_meta_bytes, 47))
+        continue;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     float d1[4] = {0.f, 0.f, 0.f, 0.f};
     for (int gb = 0; gb < ng; gb += kGG2) {
@@ -481,8 +498,11 @@ __global__ void __launch_bounds__(16 * 32) moe_w2_grouped_kernel(const GArgs a) 
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int c = 2 * t + (q & 1), row = n0 + g + 8 * (q >> 1);
-        if (c < cnt) a.y_ws[(size_t)s_route[c] * a.K + row] = __float2half_rn(d[q]);
-        if (two && kCols + c < cnt) a.y_ws[(size_t)s_route[kCols + c] * a.K + row] = __float2half_rn(d1[q]);
+        const size_t ycap = (size_t)a.M * a.topk * a.K;
+        if (c < cnt && QMLP_INB((size_t)s_route[c] * a.K + row, ycap, 48))
+            a.y_ws[(size_t)s_route[c] * a.K + row] = __float2half_rn(d[q]);
+        if (two && kCols + c < cnt && QMLP_INB((size_t)s_route[kCols + c] * a.K + row, ycap, 48))
+            a.y_ws[(size_t)s_route[kCols + c] * a.K + row] = __float2half_rn(d1[q]);
     }
     }
 }
@@ -508,7 +528,9 @@ __global__ void __launch_bounds__(kCombThr) moe_combine_kernel(const GArgs a) {
             const int i = tok * a.topk + r;
             id[r] = a.ids[i];
             w[r] = a.rw[i];
-            y[r] = *reinterpret_cast<const uint4*>(a.y_ws + (size_t)i * a.K + n);
+            y[r] = QMLP_INB((size_t)i * a.K + n + 7, (size_t)a.M * a.topk * a.K, 49)
+                       ? *reinterpret_cast<const uint4*>(a.y_ws + (size_t)i * a.K + n)
+                       : make_uint4(0, 0, 0, 0);
         }
     }
     float acc[8];
@@ -526,7 +548,8 @@ __global__ void __launch_bounds__(kCombThr) moe_combine_kernel(const GArgs a) {
     __half* oh = reinterpret_cast<__half*>(&o);
 #pragma unroll
     for (int e = 0; e < 8; ++e) oh[e] = __float2half_rn(acc[e]);
-    *reinterpret_cast<uint4*>(a.out + (size_t)tok * a.K + n) = o;
+    if (QMLP_INB((size_t)tok * a.K + n + 7, (size_t)a.M * a.K, 49))
+        *reinterpret_cast<uint4*>(a.out + (size_t)tok * a.K + n) = o;
 }
 
 cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* at) {
@@ -600,6 +623,11 @@ cudaError_t launch_moe_grouped(const MoeGroupedLaunch& L, cudaStream_t s) {
     a.n_groups = L.n_groups;
     const int routes = L.M * L.topk;
     const int gmax = (int)moe_grouped_max_groups(routes, L.E);
+    a.gmax = gmax;
+    a.w13_bytes = moe_w13_bank_bytes(L.E, L.I, L.K);
+    a.w13_meta_bytes = moe_w13_meta_bank_bytes(L.E, L.I, L.K, L.meta_bytes);
+    a.w2_bytes = (size_t)L.E * L.K * (L.I / 2);
+    a.w2_meta_bytes = (size_t)L.E * L.K * (L.I / 32) * L.meta_bytes;
     // 16-route groups once experts average 8 routes or more: each decoded
     // weight fragment then feeds two MMAs
     const bool wide = L.K <= kWideMaxK && routes >= kCols * L.E;
@@ -615,5 +643,7 @@ cudaError_t launch_moe_grouped(const MoeGroupedLaunch& L, cudaStream_t s) {
         return wide ? launch_grouped_mb<4, 2 * kCols>(a, gmax, cpg, s) : launch_grouped_mb<4, kCols>(a, gmax, cpg, s);
     return wide ? launch_grouped_mb<3, 2 * kCols>(a, gmax, cpg, s) : launch_grouped_mb<3, kCols>(a, gmax, cpg, s);
 }
+
+QMLP_BOUNDS_UNIT(moe_grouped)
 
 }  // namespace qmlp

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kCombineThreads) shard_combine_kernel(const fl
             acc.w += v.w;
         }
         const int o = (int)((q * 4) % (size_t)K);  // K % 16 == 0: the four outputs share a row
+        if (!QMLP_INB(o + 3, K, 51)) continue;
         const float4 f = fp8 ? __ldg(reinterpret_cast<const float4*>(chsd + o)) : make_float4(invd, invd, invd, invd);
         const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * f.x, acc.y * f.y);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * f.z, acc.w * f.w);
@@ -58,5 +59,7 @@ cudaError_t launch_shard_combine(int fmt, const float* partials, int nranks, int
                                                            static_cast<__nv_bfloat16*>(out));
     return cudaPeekAtLastError();
 }
+
+QMLP_BOUNDS_UNIT(tp_shard)
 
 }  // namespace qmlp
