@@ -372,7 +372,14 @@ QMLP_DEV void stage_x_one_token(const uint4* xr, int K, int kpe, uint4* xs, floa
 // map as half_slot). With find_sig, the per-token exponents are found first
 // from all of x (warp m takes token m; M <= kW). Ends with a barrier over the
 // consumer threads. Loads go out eight per thread at a time.
-QMLP_DEV int half_slot(int c, int kca) { return (c % (kca / 4)) + (kca / 4) * (c / (kca / 2)); }
+// Chunk c (0 <= c < 4q, q = Kc/4) -> its half-local position c mod q + q
+// [c >= 2q], with compares: the streaming loop evaluates it per record, and
+// a division by the runtime q there cost ~10 instructions per weight group.
+QMLP_DEV int half_slot(int c, int q) {
+    const bool hi = c >= 2 * q;
+    const int cc = hi ? c - 2 * q : c;
+    return (cc >= q ? cc - q : cc) + (hi ? q : 0);
+}
 
 QMLP_DEV void stage_x_half(const __nv_bfloat16* x, int M, int K, int pass, bool find_sig, uint4* xs, int* s_sig,
                            int warp) {
@@ -389,28 +396,35 @@ QMLP_DEV void stage_x_half(const __nv_bfloat16* x, int M, int K, int pass, bool 
         }
         named_bar_sync(1, kCT);
     }
+    // item it = (token m, r < per_tok): kept incrementally from one division
+    // per 8 items (it advances by kCT, r wraps a few times at most); the
+    // chunk position cp < h maps to chunk cp + pass q, plus q for cp >= q
     const int slots = 4 * M, per_tok = h * 8, total = M * per_tok;
     for (int base = threadIdx.x; base < total; base += 8 * kCT) {
         uint4 v[8];
+        int mu[8], ru[8];
+        int m = base / per_tok, r = base - m * per_tok;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int it = base + u * kCT;
+            mu[u] = m;
+            ru[u] = r;
             v[u] = make_uint4(0, 0, 0, 0);
-            if (it < total) {
-                const int m = it / per_tok, r = it - m * per_tok, cp = r >> 3, e8 = r & 7;
-                const int c = (cp % q) + (cp / q) * h + pass * q;
+            if (base + u * kCT < total) {
+                const int cp = r >> 3, e8 = r & 7;
+                const int c = cp + pass * q + (cp >= q ? h - q : 0);
                 if (QMLP_INB((size_t)m * K + c * kChunkK + e8 * 8 + 7, (size_t)M * K, 8))
                     v[u] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)m * K + c * kChunkK + e8 * 8));
             }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int it = base + u * kCT;
-            if (it < total) {
-                const int m = it / per_tok, r = it - m * per_tok;
-                stage_store8(xs, slots, m, (r >> 3) * kChunkK + (r & 7) * 8, s_sig[m], v[u]);
+            r += kCT;
+            while (r >= per_tok) {
+                r -= per_tok;
+                ++m;
             }
         }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (base + u * kCT < total)
+                stage_store8(xs, slots, mu[u], (ru[u] >> 3) * kChunkK + (ru[u] & 7) * 8, s_sig[mu[u]], v[u]);
     }
     named_bar_sync(1, kCT);
 }
@@ -616,6 +630,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
         zero_acc<NT, 2>(acc);
         const int u0 = warp * a.LA;  // local record index of this warp's first record
         int lt = u0 / a.KcA, c = u0 % a.KcA, cs = c;
+        const int qc = a.KcA / 4;    // 9..16 tokens: the x halves' quarter of Kc
         int slot = 0;
         uint32_t parity = 0;
         int k = 0;
@@ -642,7 +657,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_split_kernel(const __grid_consta
                 w[0] = lds_chunk<FMT>(sb, lane);
                 w[1] = lds_chunk<FMT>(sb + step_bytes, lane);
                 uint4 xb[NT][2];
-                load_xfrag<NT>(xs, NT == 2 ? half_slot(c, a.KcA) : c, M, slots, g, t, xb);
+                load_xfrag<NT>(xs, NT == 2 ? half_slot(c, qc) : c, M, slots, g, t, xb);
                 mma_chunk<FMT, NT, 2, M1>(w, xb, acc);
                 if (++c == a.KcA || k == a.LA - 1) {
                     AccA<NT> av;
