@@ -69,8 +69,12 @@ def test_small_mlp_runs_on_a_few_ctas(torch_cuda, fmt, M):
 
 
 @pytest.mark.parametrize("K,I", SHAPES)
-@pytest.mark.parametrize("fmt,M", [("nvfp4", 1), ("nvfp4", 3), ("nvfp4", 8), ("fp8", 1), ("fp8", 5)])
+@pytest.mark.parametrize("fmt,M", [("nvfp4", 1), ("nvfp4", 2), ("nvfp4", 3), ("nvfp4", 8), ("fp8", 1), ("fp8", 2),
+                                   ("fp8", 4), ("fp8", 5)])
 def test_split_parity(torch_cuda, K, I, fmt, M):
+    """Every instance of the decode kernel: one token (each format's
+    schedule), the token counts fixed at compile time (2, 4, 8) and the
+    general one (3, 5)."""
     case = gen.gen_dense_case(fmt, K, I, M, seed=310 + M + K // 512)
     mlp = q.QuantMLP.from_case(case)
     if mlp.decode_ctas() == 0:
