@@ -251,6 +251,7 @@ QMLP_DEV bool w13_cta(const Args& a, int bx, int r, uint32_t* x16, float (*part)
         }
     };
     load_batch(c0);  // issued before x is staged: the two round trips overlap
+    if (MB == 4) pdl_launch_dependents();  // see moe_w13_kernel
 
     // x -> fp16 pairs (bf16: times 2^sig so that max|x| lies in [2^14, 2^15));
     // pairs past kXRegs per thread (K > 2 kXRegs blockDim) are loaded here
@@ -365,8 +366,14 @@ __global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
     // the ids, x and (through the intermediate) the previous call's W2
     // stage belong to the kernels before this one
     pdl_wait();
-    pdl_launch_dependents();
+    // When the W2 grid may launch (its CTAs load their weights while this
+    // grid computes): with 4-byte records once every CTA has issued its own
+    // weight loads (inside w13_cta; a CTA of an invalid route leaves before),
+    // with 3-byte records at once -- measured at E=512 top-10, hot ids:
+    // 7.21 -> 6.77 us (4-byte), 8.00 against 7.80 us had 3-byte records waited.
+    if (MB != 4) pdl_launch_dependents();
     w13_cta<MB, SL>(a, blockIdx.x, blockIdx.y, x16, part, s_max);
+    if (MB == 4) pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -432,7 +439,6 @@ QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s
     };
     load_batch(0);
     pdl_wait();  // the W13 stage (act) is complete and visible
-    pdl_launch_dependents();
     const uint32_t sel = pair_selector(t);
     const uint32_t* act = reinterpret_cast<const uint32_t*>(a.act_ws + (size_t)r * a.I);
     float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -485,6 +491,10 @@ QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s
             if (s_ok[rr]) s = fmaf(s_rw[rr], ys[rr][threadIdx.x], s);
         if (QMLP_INB(n0 + threadIdx.x, a.K, 36)) a.out[n0 + threadIdx.x] = __float2half_rn(s);
     }
+    // only now may the next kernel's CTAs launch: launched while this grid
+    // computes, their set-up slowed the W2 warps on the same SMs (measured,
+    // E=512 top-10: 7.41 -> 7.22 us hot with the trigger here)
+    pdl_launch_dependents();
 }
 
 template <int MB, bool SL>
