@@ -58,6 +58,7 @@ constexpr int kK13 = 10;  // W13 K splits: a CTA has kK13 warps, each on 8 gate 
 constexpr int kC13 = 2;   // 64-k chunks a W13 warp loads at once (checkpoint layout)
 constexpr int kC13S = 4;  // the same with lane-sliced banks (a fifth of the registers per chunk)
 constexpr int kG2 = 10;   // k16 groups a W2 warp loads at once
+constexpr int kW2PreMax = 56 * 1024;  // W2's decoded fragments (w2_pre): up to 11 routes of 10 groups
 constexpr int kXRegs = 4; // x pairs a W13 thread loads before the ids (K <= 2 * 4 * 320 = 2560 in one go)
 // Shared memory of a W13 CTA: x (2K bytes, K <= 16384) needs at most 32 KB;
 // the request is 80 KB so that no SM takes a third W13 CTA. Measured: the
@@ -85,6 +86,7 @@ struct Args {
     __half* y_dbg;
     // index checks: bytes of the banks, elements of the act workspace
     size_t w13_bytes, w13_meta_bytes, w2_bytes, w2_meta_bytes, act_elems;
+    int w2_pre;  // W2 decodes its A fragments into shared memory before the wait (one batch of groups)
 };
 
 // One metadata record (little-endian fp16 scale, then fp16 bias or u8 zero)
@@ -383,7 +385,7 @@ __global__ void __launch_bounds__(kK13 * 32) moe_w13_kernel(const Args a) {
 // programmatic dependent launch: the prologue (ids, codes, metadata) overlaps
 // the W13 grid, then griddepcontrol.wait makes the intermediate visible.
 template <int MB, bool SL>
-QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s_ok) {
+QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s_ok, uint4* frag) {
     const int r = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int n0 = 16 * bx;
     // prologue, overlapping the W13 stage: the ids and router weights (final
@@ -438,11 +440,50 @@ QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s
         }
     };
     load_batch(0);
-    pdl_wait();  // the W13 stage (act) is complete and visible
     const uint32_t sel = pair_selector(t);
+    // With every k16 group in the first batch, the A fragments (which do not
+    // depend on act) are decoded before the wait, into this warp's slice of
+    // shared memory: after the wait only the MMAs remain.
+    const bool pre = a.w2_pre != 0;
+    if (pre && valid) {
+#pragma unroll
+        for (int i = 0; i < kG2; ++i) {
+            if (i < ng) {
+                uint32_t s0, b0, s8, b8;
+                meta_sb2<MB>(mw[i / 2][0], s0, b0);
+                meta_sb2<MB>(mw[i / 2][1], s8, b8);
+                uint4 f;
+                if (SL) {
+                    const uint32_t sa = pair_selector(2 * (i & 1)), sb = pair_selector(2 * (i & 1) + 1);
+                    f = make_uint4(awq_pair(cs[i / 2][0], sa, s0, b0), awq_pair(cs[i / 2][1], sa, s8, b8),
+                                   awq_pair(cs[i / 2][0], sb, s0, b0), awq_pair(cs[i / 2][1], sb, s8, b8));
+                } else {
+                    f = make_uint4(awq_pair(cw[i][0].x, sel, s0, b0), awq_pair(cw[i][1].x, sel, s8, b8),
+                                   awq_pair(cw[i][0].y, sel, s0, b0), awq_pair(cw[i][1].y, sel, s8, b8));
+                }
+                frag[(r * kG2 + i) * 32 + lane] = f;
+            }
+        }
+        __syncwarp();
+    }
+    pdl_wait();  // the W13 stage (act) is complete and visible
     const uint32_t* act = reinterpret_cast<const uint32_t*>(a.act_ws + (size_t)r * a.I);
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    if (valid) {
+    if (valid && pre) {
+        uint32_t av[kG2][2];
+#pragma unroll
+        for (int i = 0; i < kG2; ++i) {
+            av[i][0] = i < ng && inb ? act[8 * i + t] : 0u;
+            av[i][1] = i < ng && inb ? act[8 * i + 4 + t] : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < kG2; ++i) {
+            if (i < ng) {
+                const uint4 f = frag[(r * kG2 + i) * 32 + lane];
+                mma_f16_16816(d, f.x, f.y, f.z, f.w, av[i][0], av[i][1]);
+            }
+        }
+    } else if (valid) {
         for (int gb = 0; gb < ng; gb += kG2) {
             if (gb > 0) load_batch(gb);
             // the batch's act words, all loads at once; B fragment column 0
@@ -499,10 +540,11 @@ QMLP_DEV void w2_cta(const Args& a, int bx, float (*ys)[16], float* s_rw, int* s
 
 template <int MB, bool SL>
 __global__ void __launch_bounds__(16 * 32) moe_w2_kernel(const Args a) {
+    extern __shared__ __align__(16) uint4 w2frag[];  // [topk][kG2][32] decoded A fragments (w2_pre)
     __shared__ float ys[16][16];
     __shared__ float s_rw[16];
     __shared__ int s_ok[16];
-    w2_cta<MB, SL>(a, blockIdx.x, ys, s_rw, s_ok);
+    w2_cta<MB, SL>(a, blockIdx.x, ys, s_rw, s_ok, w2frag);
 }
 
 template <int MB, bool SL>
@@ -511,6 +553,8 @@ cudaError_t launch_mb(const Args& a, cudaStream_t s) {
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(moe_w13_kernel<MB, SL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kW13Smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(moe_w2_kernel<MB, SL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kW2PreMax);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -529,6 +573,7 @@ cudaError_t launch_mb(const Args& a, cudaStream_t s) {
     cudaLaunchConfig_t c2 = {};
     c2.gridDim = dim3(a.K / 16);
     c2.blockDim = dim3(32 * a.topk);
+    c2.dynamicSmemBytes = a.w2_pre ? (size_t)a.topk * kG2 * 32 * sizeof(uint4) : 0;
     c2.stream = s;
     c2.attrs = pdl;
     c2.numAttrs = 1;
@@ -566,6 +611,9 @@ cudaError_t launch_moe(const MoeLaunch& L, int num_sms, cudaStream_t s) {
     a.w2_bytes = (size_t)L.E * L.K * (L.I / 2);
     a.w2_meta_bytes = (size_t)L.E * L.K * (L.I / 32) * MB;
     a.act_elems = (size_t)16 * L.I;
+    // the decoded fragments fit beside two W13 CTAs on an SM (one batch of
+    // groups: I <= 16 kG2)
+    a.w2_pre = L.I / 16 <= kG2 && (size_t)L.topk * kG2 * 32 * sizeof(uint4) <= kW2PreMax;
     if (L.sliced) return L.meta_bytes == 4 ? launch_mb<4, true>(a, s) : launch_mb<3, true>(a, s);
     return L.meta_bytes == 4 ? launch_mb<4, false>(a, s) : launch_mb<3, false>(a, s);
 }
