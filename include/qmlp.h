@@ -141,10 +141,11 @@ qmlp_status qmlp_forward_stage(qmlp_t* h, int stage, qmlp_path path, const void*
 
 /* End-to-end call from host buffers (x: host bf16 [M, K], out: host bf16
  * [M, K]); returns after `stream` has finished. Pinned (device-mapped) host
- * buffers, 16-byte aligned and not overlapping, are read and written in place
- * by the kernels over the coherent CPU-GPU link; otherwise x is copied to
- * the handle's staging buffer and the result copied back (pageable memory
- * works but serializes the copies).
+ * buffers, 16-byte aligned and not overlapping: one small kernel copies x
+ * over the coherent CPU-GPU link into the handle's device stage, and the
+ * kernels write the output in place into the host buffer. Otherwise x is
+ * copied to the staging buffer and the result copied back by the copy engine
+ * (pageable memory works but serializes the copies).
  * Errors: as qmlp_forward. */
 qmlp_status qmlp_forward_host(qmlp_t* h, const void* x_host, int M, void* out_host,
                               qmlp_stream_t stream);

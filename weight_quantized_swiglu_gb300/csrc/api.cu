@@ -21,6 +21,16 @@ namespace {
 
 constexpr int kMaxGemvM = 16;
 
+// x of a host-buffer call, from pinned host memory (over the CPU-GPU link)
+// into device memory, once: the decode kernel's CTAs would otherwise each read
+// all of it over the link. The decode kernel, launched next with programmatic
+// dependent launch, streams its first weights meanwhile.
+__global__ void __launch_bounds__(256) fetch_x_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                      int n16) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x) dst[i] = src[i];
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -664,7 +674,15 @@ qmlp_status qmlp_forward_host(qmlp_t* h, const void* x_host, int M, void* out_ho
     void* xd = device_alias(x_host);
     void* od = device_alias(out_host);
     if (xd && od && aligned16(xd) && aligned16(od) && !overlaps(x_host, bytes, out_host, bytes)) {
-        qmlp_status st = run_forward(h, QMLP_PATH_AUTO, xd, M, od, s, true);
+        // x is fetched once into the handle's device stage (an ordinary
+        // launch: the previous call may still read that stage); the output is
+        // written in place over the link
+        if (fault("launch")) return QMLP_ERR_CUDA;
+        const int n16 = (int)(bytes / 16);
+        fetch_x_kernel<<<std::min(8, (n16 + 255) / 256), 256, 0, s>>>(static_cast<const uint4*>(xd),
+                                                                      static_cast<uint4*>(h->x_stage), n16);
+        if (cudaPeekAtLastError() != cudaSuccess) return QMLP_ERR_CUDA;
+        qmlp_status st = run_forward(h, QMLP_PATH_AUTO, h->x_stage, M, od, s);
         if (st != QMLP_OK) return st;
         return cudaStreamSynchronize(s) == cudaSuccess ? QMLP_OK : QMLP_ERR_CUDA;
     }
