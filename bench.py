@@ -480,7 +480,10 @@ def bench_moe_tokens(Ms=(16, 512), meta_bytes=4):
     return res
 
 
-def bench_prefill(M, reps, pk, fmt="nvfp4", pair=False, cpu=True):
+DQ_MIN_M = 768  # the automatic path decodes the weights once per call from here on
+
+
+def bench_prefill(M, reps, pk, fmt="nvfp4", path=None, cpu=True):
     import torch
     import weight_quantized_swiglu_gb300 as q
     case = gen.gen_dense_case(fmt, K_HID, I_INT, M, gen.seed_for(3 if fmt == "nvfp4" else 5, 0 if M == 512 else 1))
@@ -488,7 +491,11 @@ def bench_prefill(M, reps, pk, fmt="nvfp4", pair=False, cpu=True):
     x = torch.from_numpy(case.x.view(np.int16)).cuda()
     out = torch.empty((M, K_HID), dtype=torch.int16, device="cuda")
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
-    path = q.PATH_GEMM_PAIR if pair else q.PATH_GEMM
+    path = q.PATH_AUTO if path is None else path
+    name = {q.PATH_GEMM: "gemm (decoder warps)", q.PATH_GEMM_PAIR: "gemm_pair (decoder warps, CTA pairs)",
+            q.PATH_GEMM_DQ: "gemm_dq (weights decoded once per call)"}.get(path)
+    if name is None:
+        name = "auto: " + ("gemm_dq (weights decoded once per call)" if M >= DQ_MIN_M else "gemm (decoder warps)")
     for _ in range(3):
         mlp.forward(x, out, path=path)
     torch.cuda.synchronize()
@@ -519,7 +526,7 @@ def bench_prefill(M, reps, pk, fmt="nvfp4", pair=False, cpu=True):
                               budget_s=0.0, extrapolate=(M / 64, f"x {M}/64 rows (an upper bound: the weight "
                                                                  f"decode is counted once per 64 rows)"))
     # each call is timed alone (L2 flushed between calls): the burst peak applies
-    return {"M": M, "path": "gemm_pair" if pair else "gemm", "ms_per_call": ms, "tflops": tf, "frac_bf16_peak": tf / pk["bf16_tflops"],
+    return {"M": M, "path": name, "ms_per_call": ms, "tflops": tf, "frac_bf16_peak": tf / pk["bf16_tflops"],
             "peak_tflops": pk["bf16_tflops"], "peak_kind": "bf16 burst (cuBLAS, isolated calls), " + pk["source"],
             "tokens_per_s": M / (ms * 1e-3), "l2": "512 MB buffer written between calls", "cpu_baseline": cpu}
 
@@ -645,16 +652,18 @@ def run_profile(args):
             moe.forward_tokens(x, q.DT_FP16, ids, rw, out)
         torch.cuda.synchronize()
         moe.check()
-    elif any(args.profile.startswith(p) for p in ("prefill", "fp8prefill", "pairprefill", "fp8pairprefill")):
+    elif any(args.profile.startswith(p) for p in ("prefill", "fp8prefill", "pairprefill", "fp8pairprefill",
+                                                  "dqprefill", "fp8dqprefill")):
         fp8 = args.profile.startswith("fp8")
         pair = "pair" in args.profile
+        path = q.PATH_GEMM_PAIR if pair else q.PATH_GEMM_DQ if "dq" in args.profile else q.PATH_GEMM
         M = int(args.profile.split("prefill", 1)[1] or 512)
         case = gen.gen_dense_case("fp8" if fp8 else "nvfp4", K_HID, I_INT, M, gen.seed_for(5 if fp8 else 3, 0))
         mlp = q.QuantMLP.from_case(case)
         x = torch.from_numpy(case.x.view(np.int16)).cuda()
         out = torch.empty((M, K_HID), dtype=torch.int16, device="cuda")
         for _ in range(n):
-            mlp.forward(x, out, path=q.PATH_GEMM_PAIR if pair else q.PATH_GEMM)
+            mlp.forward(x, out, path=path)
         torch.cuda.synchronize()
         mlp.check()
     print(f"profile {args.profile}: {n} calls ok", flush=True)
@@ -673,7 +682,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile", default=None,
                     help="eager launches of one operation for ncu: fused|fusedM4|stage0|stage1|fp8_fused|fp8_fusedM16|moe|"
-                         "moetokensM|prefillM|fp8prefillM|pairprefillM|fp8pairprefillM")
+                         "moetokensM|prefillM|fp8prefillM|pairprefillM|fp8pairprefillM|dqprefillM|fp8dqprefillM "
+                         "(prefill: the decoder-warp GEMM; dq: weights decoded once per call)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.profile:
@@ -719,11 +729,13 @@ def main():
                     extras[f"{fmt}_mid_M64"] = bench_prefill(64, 5, pk, fmt)
                     extras[f"{fmt}_prefill_M512"] = bench_prefill(512, 5, pk, fmt)
                     extras[f"{fmt}_prefill_M8192"] = bench_prefill(8192, 3, pk, fmt)
-                    # the CTA-pair GEMM (an explicit path; the automatic one is above)
-                    pair = bench_prefill(8192, 3, pk, fmt, pair=True, cpu=False)
-                    # same workload and inputs as the line above: its oracle timing applies
-                    pair["cpu_baseline"] = extras[f"{fmt}_prefill_M8192"]["cpu_baseline"]
-                    extras[f"{fmt}_prefill_pair_M8192"] = pair
+                    # the explicit paths the automatic one (above) does not take at
+                    # this size: the decoder-warp GEMM, single CTAs and CTA pairs
+                    for key, path in (("decwarps", q.PATH_GEMM), ("pair", q.PATH_GEMM_PAIR)):
+                        line = bench_prefill(8192, 3, pk, fmt, path=path, cpu=False)
+                        # same workload and inputs as the automatic line: its oracle timing applies
+                        line["cpu_baseline"] = extras[f"{fmt}_prefill_M8192"]["cpu_baseline"]
+                        extras[f"{fmt}_prefill_{key}_M8192"] = line
                 except q.QmlpError as e:
                     extras[f"{fmt}_prefill"] = {"unavailable": str(e)}
         torch.cuda.synchronize()

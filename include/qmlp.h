@@ -70,8 +70,19 @@ typedef enum { QMLP_META_3B = 3, QMLP_META_4B = 4 } qmlp_meta;
  * tensor-core GEMM on CTA pairs (tcgen05.mma.cta_group::2: two SMs share a
  * 256-token x 256-row tile, each decoding half of its weight rows) for
  * M >= 256; AUTO does not choose it (the single-CTA GEMM measured faster on
- * the 27B-class prefill shape). */
-typedef enum { QMLP_PATH_AUTO = 0, QMLP_PATH_GEMV = 1, QMLP_PATH_GEMM = 2, QMLP_PATH_GEMM_PAIR = 3 } qmlp_path;
+ * the 27B-class prefill shape). GEMM_DQ is the dequantise-once GEMM: each
+ * projection is first decoded, once per call, into fp16 tiles in a buffer
+ * the handle holds (4 I K bytes, allocated by qmlp_create when max_M >=
+ * 768), and the tensor-core GEMM then reads those tiles with no decoding in
+ * its main loop; AUTO takes it from M = 768 on. The products are the same
+ * exact fp16 weight values either way. */
+typedef enum {
+    QMLP_PATH_AUTO = 0,
+    QMLP_PATH_GEMV = 1,
+    QMLP_PATH_GEMM = 2,
+    QMLP_PATH_GEMM_PAIR = 3,
+    QMLP_PATH_GEMM_DQ = 4
+} qmlp_path;
 
 /* One projection [N, K] as the checkpoint stores it. Pointers may be host or
  * device memory; they are only read during qmlp_create.
@@ -122,9 +133,10 @@ void qmlp_destroy(qmlp_t* h);
  * overlaps x), SHAPE (M < 1 or M > max_M), CUDA. */
 qmlp_status qmlp_forward(qmlp_t* h, const void* x, int M, void* out, qmlp_stream_t stream);
 
-/* As qmlp_forward, forcing a kernel family. GEMM and GEMM_PAIR require a
- * handle whose max_M reaches the GEMM threshold (and K % 256, I % 128 ==
- * 0); GEMM_PAIR also M >= 256. Otherwise SHAPE. */
+/* As qmlp_forward, forcing a kernel family. GEMM, GEMM_PAIR and GEMM_DQ
+ * require a handle whose max_M reaches the GEMM threshold (and K % 256,
+ * I % 128 == 0); GEMM_PAIR also M >= 256; GEMM_DQ a handle created with
+ * max_M >= 768 (any M up to max_M). Otherwise SHAPE. */
 qmlp_status qmlp_forward_path(qmlp_t* h, qmlp_path path, const void* x, int M, void* out,
                               qmlp_stream_t stream);
 
@@ -385,7 +397,7 @@ qmlp_status qmlp_moe_m1_forward_noalloc(const qmlp_moe_desc* banks, const void* 
 /* Human-readable name of a status ("QMLP_OK", ...). Never NULL. */
 const char* qmlp_status_str(qmlp_status s);
 
-/* ABI version of this header (major * 100 + minor): 103 (index-checking build). */
+/* ABI version of this header (major * 100 + minor): 104 (dequantise-once GEMM path). */
 int qmlp_abi_version(void);
 
 #ifdef __cplusplus

@@ -3,7 +3,7 @@ default library (in the test process) and once with the checking build
 (libqmlp_bounds.so, in a child process that sets QMLP_LIB). Every kernel
 family runs at least once: the single-launch decode kernel under each of its
 end-of-call schedules, the stream-K stage kernel, the tensor-core GEMM
-(single-CTA, split-K and CTA-pair), the one-token and grouped routed-expert
+(single-CTA, split-K, CTA-pair and dequantise-once), the one-token and grouped routed-expert
 kernels (handle and allocation-free entry points) and the tensor-parallel
 combine. Outputs are returned as raw bytes, so the two builds can be compared
 bit for bit; with the checking build each case also records what
@@ -122,6 +122,8 @@ def cases():
         ("gemm_m1024", lambda t: _dense(t, small("nvfp4", 1024, 503), path=q.PATH_GEMM)),
         ("gemm_fp8_m1024", lambda t: _dense(t, small("fp8", 1024, 504), path=q.PATH_GEMM)),
         ("gemm_pair_m1024", lambda t: _dense(t, small("nvfp4", 1024, 505), path=q.PATH_GEMM_PAIR)),
+        ("gemm_dq_m1600", lambda t: _dense(t, small("nvfp4", 1600, 507), path=q.PATH_GEMM_DQ)),
+        ("gemm_dq_fp8_m100", lambda t: _dense(t, small("fp8", 100, 508), max_M=768, path=q.PATH_GEMM_DQ)),
         ("moe_m1_4b", lambda t: _moe(t, moe_case, 4)),
         ("moe_m1_3b", lambda t: _moe(t, moe_case, 3)),
         ("moe_noalloc", lambda t: _noalloc(t, moe_case)),

@@ -44,7 +44,7 @@ def test_binding_signatures_cover_the_header():
 def test_status_strings(L):
     assert q.qmlp_status_str(0) == "QMLP_OK"
     assert q.qmlp_status_str(8) == "QMLP_ERR_DEVICE_TIMEOUT"
-    assert q.qmlp_abi_version() == 103
+    assert q.qmlp_abi_version() == 104
 
 
 def test_null_arguments_are_rejected_without_a_device(L):

@@ -153,15 +153,15 @@ def test_decode_kernel_wait_runs_out_and_recovers(torch_cuda, fmt, variant):
     mlp.close()
 
 
-@pytest.mark.parametrize("path", [q.PATH_GEMM, q.PATH_GEMM_PAIR])
+@pytest.mark.parametrize("path", [q.PATH_GEMM, q.PATH_GEMM_PAIR, q.PATH_GEMM_DQ])
 @pytest.mark.parametrize("fmt", ["nvfp4", "fp8"])
 def test_gemm_wait_runs_out_and_recovers(torch_cuda, fmt, path):
-    """The tensor-core GEMM (both launches of a forward), single-CTA and on
-    CTA pairs: the MMA and decoder warps give up on the withheld step, raise
-    the CTA's abort flag, the other roles leave their loops, issued MMAs are
-    waited for, both CTAs of a pair meet at the cluster barrier and TMEM is
-    freed."""
+    """The tensor-core GEMM (both launches of a forward), single-CTA, on CTA
+    pairs and dequantise-once: the MMA and decoder warps give up on the
+    withheld step, raise the CTA's abort flag, the other roles leave their
+    loops, issued MMAs are waited for, both CTAs of a pair meet at the
+    cluster barrier and TMEM is freed."""
     case = gen.gen_dense_case(fmt, 1024, 2048, 300, seed=403)
-    mlp = q.QuantMLP.from_case(case)
+    mlp = q.QuantMLP.from_case(case, max_M=768 if path == q.PATH_GEMM_DQ else None)
     _timeout_then_recover(torch_cuda, mlp, case.x, path)
     mlp.close()

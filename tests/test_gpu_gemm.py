@@ -2,6 +2,7 @@
 per-channel, M >= 17) against the CPU oracle, through the C ABI: exact
 single-weight decode, raw projections, the tiny shape at ragged token
 counts, the 27B-class prefill shape at its token counts (sampled rows),
+the dequantise-once GEMM (decoded fp16 weights staged before the GEMM),
 determinism and the automatic path choice."""
 import numpy as np
 import pytest
@@ -97,6 +98,68 @@ def test_pair_gemm_one_hot_is_bit_exact(torch_cuda, fmt):
     y = torch.empty((255, case.gate.N), dtype=torch.float32, device="cuda")
     x = torch.zeros((255, case.gate.K), dtype=torch.int16, device="cuda")
     assert q.qmlp_debug_project(mlp.h, 0, q.PATH_GEMM_PAIR, x, 255, y) == 4  # QMLP_ERR_SHAPE
+    mlp.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_dq_gemm_one_hot_is_bit_exact(torch_cuda, fmt):
+    """The dequantise-once GEMM (each projection decoded into fp16 stage
+    images before the GEMM, which then copies them into shared memory as
+    they are): x = e_k rows return the decoded weights bit for bit, for gate,
+    up and down, at k positions on scale-group, k-step, swizzle-row and tile
+    boundaries -- a misplaced 16-byte chunk of an image moves a weight."""
+    torch = torch_cuda
+    case = gen.gen_dense_case(fmt, TK, TI, 1, seed=207)
+    mlp = q.QuantMLP.from_case(case, max_M=768)  # the decode buffer exists from max_M = 768
+    for which, proj in ((0, case.gate), (1, case.up), (2, case.down)):
+        Kp = proj.K
+        M = 200
+        ks = [(r * 29 + 3) % Kp for r in range(M)]
+        ks[:12] = [0, 7, 8, 15, 16, 31, 32, 63, 64, Kp - 1, Kp - 16, Kp - 64]
+        x = np.zeros((M, Kp), dtype=np.uint16)
+        for r, k in enumerate(ks):
+            x[r, k] = 0x3F80
+        y = torch.empty((M, proj.N), dtype=torch.float32, device="cuda")
+        mlp.debug_project(which, to_dev(x), y, path=q.PATH_GEMM_DQ)
+        torch.cuda.synchronize()
+        mlp.check()
+        got = y.cpu().numpy().astype(np.float64)
+        ref = oracle.decode_proj(proj)
+        for r, k in enumerate(ks):
+            assert np.array_equal(got[r], ref[:, k]), (which, r, k)
+    mlp.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M", [17, 129, 300])
+def test_dq_gemm_parity_and_same_bits_as_decoder_warps(torch_cuda, M, fmt):
+    """The dequantise-once GEMM against the oracle, and bit for bit against
+    the GEMM whose decoder warps decode in the main loop: both feed the same
+    exact fp16 weights to the same MMA sequence (M = 17 also runs split-K)."""
+    case = gen.gen_dense_case(fmt, TK, TI, M, seed=270 + M)
+    mlp = q.QuantMLP.from_case(case, max_M=768)
+    out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM_DQ)
+    ref = oracle.dense_forward(case)
+    compare(act, ref["act"], what="act")
+    compare(out, ref["out"], what="out")
+    gout, gact = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM)
+    assert np.array_equal(act, gact) and np.array_equal(out, gout)
+    mlp.close()
+
+
+def test_dq_gemm_needs_the_decode_buffer(torch_cuda):
+    """A handle created for fewer than 768 tokens holds no decode buffer:
+    the dequantise-once path is refused (SHAPE) before any launch, and the
+    automatic path keeps the decoder-warp GEMM."""
+    torch = torch_cuda
+    case = gen.gen_dense_case("nvfp4", TK, TI, 64, seed=280)
+    mlp = q.QuantMLP.from_case(case, max_M=767)
+    x = to_dev(case.x)
+    out = torch.empty((64, TK), dtype=torch.int16, device="cuda")
+    assert q.qmlp_forward_path(mlp.h, q.PATH_GEMM_DQ, x, 64, out, None) == 4  # QMLP_ERR_SHAPE
+    auto, _ = run_forward(torch, mlp, case.x, q.PATH_AUTO)
+    gemm, _ = run_forward(torch, mlp, case.x, q.PATH_GEMM)
+    assert np.array_equal(auto, gemm)
     mlp.close()
 
 
@@ -244,6 +307,11 @@ def test_parity_prefill(torch_cuda, variant, name):
             assert np.linalg.norm(d) <= 5e-3 * np.linalg.norm(r_all[i]), f"row {r}"
     out2, _ = run_forward(torch_cuda, mlp, case.x, q.PATH_AUTO)
     assert np.array_equal(out, out2)
+    if M >= 768:
+        # the automatic path is the dequantise-once GEMM here; the GEMM with
+        # decoder warps gives the same bits
+        gout, gact = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM)
+        assert np.array_equal(act, gact) and np.array_equal(out, gout)
     # the CTA-pair GEMM on the same inputs, against the same reference rows
     pout, pact = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM_PAIR)
     compare(pact[rows], ref["act"], what="pair act")

@@ -30,7 +30,7 @@ STATUS = {0: "QMLP_OK", 1: "QMLP_ERR_INVALID_ARG", 2: "QMLP_ERR_ALIGNMENT", 3: "
 FMT_NVFP4, FMT_FP8_PC = 1, 2
 DT_BF16, DT_FP16 = 1, 2
 META_3B, META_4B = 3, 4
-PATH_AUTO, PATH_GEMV, PATH_GEMM, PATH_GEMM_PAIR = 0, 1, 2, 3
+PATH_AUTO, PATH_GEMV, PATH_GEMM, PATH_GEMM_PAIR, PATH_GEMM_DQ = 0, 1, 2, 3, 4
 
 
 class QmlpError(RuntimeError):

@@ -102,6 +102,8 @@ struct qmlp_s {
     bool has_gemm = false;
     GemmProj gm_gu, gm_d;
     void* a16 = nullptr;       // fp16 [max_M, max(K, I)] (GEMM prescaled activations)
+    uint8_t* wdec = nullptr;   // dequantise-once GEMM: one projection's decoded fp16 stage images
+    size_t wdec_bytes = 0;
     float* gemm_ws = nullptr;  // split-K partials of the GEMM (small M)
     int* sig = nullptr;        // [max_M] per-token prescale exponents
     void* act = nullptr;       // bf16 [max_M, I]
@@ -137,6 +139,15 @@ static int split_max_m(const qmlp_s* h) {
 // stream-K pass.
 static int gemm_min_m(const qmlp_s* h) { return h->sp.G ? split_max_m(h) + 1 : kMaxGemvM + 1; }
 
+// Fewest tokens the automatic path sends to the dequantise-once GEMM (each
+// projection decoded once per call into fp16 stage images, then a GEMM
+// without decoder warps), and the handle's max_M from which it holds the
+// decode buffer (4 I K bytes: the larger projection). Measured on the
+// 27B-class shape (NVFP4 / FP8, ms, decoder warps against decoded once):
+// M = 512 0.322 / 0.345 against 0.357 / 0.386; M = 1024 0.607 / 0.644
+// against 0.552 / 0.578; M = 8192 3.49 / 3.70 against 2.79 / 2.80.
+constexpr int kDqMinM = 768;
+
 struct qmlp_moe_s {
     int E = 0, K = 0, I = 0, meta = 0, device = 0, num_sms = 0;
     uint8_t *w13 = nullptr, *w13_meta = nullptr, *w2 = nullptr, *w2_meta = nullptr;
@@ -170,7 +181,7 @@ const char* qmlp_status_str(qmlp_status s) {
     return "QMLP_ERR_UNKNOWN";
 }
 
-int qmlp_abi_version(void) { return 103; }
+int qmlp_abi_version(void) { return 104; }
 
 // ---------------------------------------------------------------------------
 // dense MLP
@@ -389,6 +400,13 @@ static qmlp_status create_impl(qmlp_t* h, qmlp_t** out, const qmlp_desc* d, int 
                      cudaSuccess)
                 st = from_cuda(e);
         }
+        if (st == QMLP_OK && d->max_M >= kDqMinM) {
+            const size_t b = std::max(gemm_decoded_bytes(2 * d->I, d->K), gemm_decoded_bytes(d->K, d->I));
+            void* p = nullptr;
+            if ((e = h->mem.alloc(&p, b)) != cudaSuccess) st = from_cuda(e);
+            h->wdec = static_cast<uint8_t*>(p);
+            h->wdec_bytes = b;
+        }
     }
     // workspace
     if (st == QMLP_OK) {
@@ -455,13 +473,20 @@ static qmlp_status validate_fwd(qmlp_t* h, const void* x, int M, const void* out
 }
 
 static bool valid_path(qmlp_path p) {
-    return p == QMLP_PATH_AUTO || p == QMLP_PATH_GEMV || p == QMLP_PATH_GEMM || p == QMLP_PATH_GEMM_PAIR;
+    return p == QMLP_PATH_AUTO || p == QMLP_PATH_GEMV || p == QMLP_PATH_GEMM || p == QMLP_PATH_GEMM_PAIR ||
+           p == QMLP_PATH_GEMM_DQ;
 }
 
 static bool use_gemm(qmlp_t* h, qmlp_path path, int M) {
     if (path == QMLP_PATH_GEMV) return false;
-    if (path == QMLP_PATH_GEMM || path == QMLP_PATH_GEMM_PAIR) return true;
+    if (path == QMLP_PATH_GEMM || path == QMLP_PATH_GEMM_PAIR || path == QMLP_PATH_GEMM_DQ) return true;
     return h->has_gemm && M >= gemm_min_m(h);
+}
+
+// The decode buffer for a GEMM call (null: the decoder warps decode).
+static uint8_t* dq_buffer(const qmlp_t* h, qmlp_path path, int M) {
+    if (path == QMLP_PATH_GEMM_DQ) return h->wdec;
+    return path == QMLP_PATH_AUTO && M >= kDqMinM ? h->wdec : nullptr;
 }
 
 // stage bit 0: gate/up + SwiGLU (x -> workspace act); bit 1: down (act ->
@@ -473,9 +498,12 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
     const bool gemm = use_gemm(h, path, M);
     if (gemm && !h->has_gemm) return QMLP_ERR_SHAPE;
     if (path == QMLP_PATH_GEMM_PAIR && M < kPairMinM) return QMLP_ERR_SHAPE;
+    if (path == QMLP_PATH_GEMM_DQ && !h->wdec) return QMLP_ERR_SHAPE;
     if (gemm) {
         GemmLaunch g;
         g.pair = path == QMLP_PATH_GEMM_PAIR;
+        g.wdec = dq_buffer(h, path, M);
+        g.wdec_bytes = h->wdec_bytes;
         g.M = M;
         g.err = h->err;
         g.a16 = h->a16;
@@ -706,8 +734,11 @@ qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void*
     if (use_gemm(h, path, M)) {
         if (!h->has_gemm) return QMLP_ERR_SHAPE;
         if (path == QMLP_PATH_GEMM_PAIR && M < kPairMinM) return QMLP_ERR_SHAPE;
+        if (path == QMLP_PATH_GEMM_DQ && !h->wdec) return QMLP_ERR_SHAPE;
         GemmLaunch g;
         g.pair = path == QMLP_PATH_GEMM_PAIR;
+        g.wdec = dq_buffer(h, path, M);
+        g.wdec_bytes = h->wdec_bytes;
         g.epi = kEpiRaw;
         g.raw_sel = which == 1 ? 1 : 0;
         g.w = which < 2 ? h->gm_gu : h->gm_d;

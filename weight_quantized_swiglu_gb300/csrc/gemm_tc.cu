@@ -47,6 +47,14 @@
 //    rows of tile j are gate rows 128j..128j+127 followed by up rows
 //    128j..128j+127, so one accumulator holds both inputs of 128 SwiGLU
 //    outputs per token.
+//  * Dequantise-once instance (PRE; the automatic path from 768 tokens): a
+//    predecode kernel first writes every weight block of the projection as
+//    its bf16 stage image (the swizzled tile the decoders would have written,
+//    bf16 instead of fp16: the decoded values are exact in both), once per
+//    call instead of once per 128-token tile; the GEMM's load stage is then
+//    the bf16 activation tile, loaded by TMA from the input itself (no
+//    prescale), plus the 32 KB image (one cp.async.bulk), 4 stages deep, and
+//    the MMAs are bf16 x bf16 -> fp32. Warps 6-13 have no work there.
 //  * Every wait is bounded (globaltimer); on expiry the kernel records the
 //    error, every role leaves its loop, in-flight copies and MMAs are waited
 //    for (bounded) and TMEM is freed.
@@ -84,12 +92,17 @@ constexpr int kThreads = (2 + kEpiWarps + kDecWarps) * 32;  // 448
 constexpr int kTmemCols = 2 * BN;                           // two accumulators
 constexpr uint64_t kGemmWaitNs = 2000000000ull;             // 2 s
 
+// Dequantise-once instance (PRE): the weights of the call were decoded
+// beforehand into their fp16 stage images, so a load stage is the activation
+// tile plus a 32 KB decoded tile and there is no decoded ring.
+constexpr int kPreStages = 4;
+
 // shared memory map (offsets from a 1024-byte aligned base)
-template <int FMT>
+template <int FMT, bool PRE = false>
 struct Smem {
-    static constexpr int L = lstages<FMT>();
-    static constexpr int BS = bstages<FMT>();
-    static constexpr int R = raw_bytes<FMT>();
+    static constexpr int L = PRE ? kPreStages : lstages<FMT>();
+    static constexpr int BS = PRE ? 0 : bstages<FMT>();
+    static constexpr int R = PRE ? kBBytes : raw_bytes<FMT>();
     static constexpr int A = 0;
     static constexpr int B = A + L * kABytes;
     static constexpr int Raw = B + BS * kBBytes;
@@ -99,6 +112,7 @@ struct Smem {
     static constexpr int Misc = Bar + NumBars * 8;  // tmem address, abort flag
     static constexpr int Bytes = Misc + 16 + 1024;  // + alignment slack
     static_assert(B % 1024 == 0 && Raw % 16 == 0 && Bar % 8 == 0, "smem layout");
+    static_assert(!PRE || (Raw % 1024 == 0 && R % 1024 == 0), "decoded stages sit on the swizzle period");
     static_assert(Bytes <= 227 * 1024, "smem budget");
 };
 
@@ -121,6 +135,8 @@ struct Args {
     int withhold;          // error-path tests: the producer never loads its last k-step
     size_t tiles_bytes;    // index checks: bytes of the weight blocks
     size_t ws_elems;       // index checks: floats of the split-K partial buffer
+    const uint8_t* wdec;   // PRE: decoded stage images [Nt][KS][32 KB]
+    size_t wdec_bytes;     // PRE: bytes of wdec (index checks)
 };
 
 // ---------------------------------------------------------------------------
@@ -195,6 +211,9 @@ constexpr uint32_t kIdesc = (1u << 4)                    // D format fp32
                             | (0u << 7) | (0u << 10)     // A, B fp16
                             | ((uint32_t)(BN >> 3) << 17)  // N >> 3
                             | ((uint32_t)(BM >> 4) << 24); // M >> 4
+
+// The same for bf16 A and B (the dequantise-once instance).
+constexpr uint32_t kIdescBF16 = kIdesc | (1u << 7) | (1u << 10);
 
 // Wait for phase `parity` of `bar`; false if the CTA's abort flag is raised
 // or the wait ran out (which raises it and records `code`).
@@ -345,11 +364,12 @@ QMLP_DEV void store_tile(const Args& a, uint32_t tbase, int m, bool live, int sg
     }
 }
 
-template <int FMT, bool SPLIT>
+template <int FMT, bool SPLIT, bool PRE>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap amap, const Args a) {
-    using S = Smem<FMT>;
+    using S = Smem<FMT, PRE>;
     constexpr int kLStages = S::L;
     constexpr int kBStages = S::BS;
+    constexpr int kBDiv = kBStages > 0 ? kBStages : 1;  // ring arithmetic (unused by PRE)
     constexpr int kRawBytes = S::R;
     constexpr int kOffA = S::A, kOffB = S::B, kOffRaw = S::Raw, kOffBar = S::Bar, kOffMisc = S::Misc;
     extern __shared__ uint8_t dyn_smem_raw[];
@@ -420,8 +440,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         ok = false;
                         break;
                     }
-                    const uint8_t* src = blk + (size_t)ks * kRawBytes;
-                    if (!QMLP_INB((size_t)(src - a.tiles) + kRawBytes - 1, a.tiles_bytes, 11)) src = a.tiles;
+                    const uint8_t* src;
+                    if (PRE) {
+                        src = a.wdec + ((size_t)nt * KS + ks) * kRawBytes;
+                        if (!QMLP_INB((size_t)(src - a.wdec) + kRawBytes - 1, a.wdec_bytes, 16)) src = a.wdec;
+                    } else {
+                        src = blk + (size_t)ks * kRawBytes;
+                        if (!QMLP_INB((size_t)(src - a.tiles) + kRawBytes - 1, a.tiles_bytes, 11)) src = a.tiles;
+                    }
                     mbar_arrive_expect_tx(full(s), kABytes + kRawBytes);
                     tma_load_2d(base_s + kOffA + s * kABytes, &amap, ks * BK, mt * BM, full(s));
                     bulk_g2s(base_s + kOffRaw + s * kRawBytes, src, kRawBytes, full(s));
@@ -451,23 +477,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
                 const int kb = ks_begin(sp), ke = ks_begin(sp + 1);
                 for (int ks = kb; ks < ke; ++ks, ++it) {
-                    const int s = it % kLStages, b = it % kBStages;
+                    const int s = it % kLStages, b = it % kBDiv;
                     if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 13, a.limit) ||
-                        !wait_or_abort(bfull(b), (uint32_t)((it / kBStages) & 1), abort_flag, a.err, 14, a.limit)) {
+                        (!PRE &&
+                         !wait_or_abort(bfull(b), (uint32_t)((it / kBDiv) & 1), abort_flag, a.err, 14, a.limit))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sa = base_s + kOffA + s * kABytes;
-                    const uint32_t sb = base_s + kOffB + b * kBBytes;
+                    const uint32_t sb = PRE ? base_s + kOffRaw + s * kRawBytes : base_s + kOffB + b * kBBytes;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        umma_f16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), kIdesc,
+                        umma_f16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32),
+                                 PRE ? kIdescBF16 : kIdesc,
                                  (ks != kb || k != 0) ? 1u : 0u);
                     }
                     issued = true;
                     umma_commit(empty(s));
-                    umma_commit(bempty(b));
+                    if (!PRE) umma_commit(bempty(b));
                 }
                 if (!ok) break;
                 umma_commit(acc_full(buf));
@@ -493,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc_fence_after();
             const int m = mt * BM + row_in_tile;
             const bool live = m < a.M;
-            const int sg = live ? a.sig[m] : 0;
+            const int sg = live && a.sig ? a.sig[m] : 0;  // no prescale (null sig): bf16 operands
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
             if (SPLIT) {
                 // a k-range of the tile: its fp32 partial, unscaled, in the
@@ -516,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc_fence_before();
             mbar_arrive(acc_empty(buf));
         }
-    } else {
+    } else if (!PRE) {
         // ---------------- decoders ----------------
         const int d = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. kDecThreads-1
         int it = 0;
@@ -525,10 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const int sp = SPLIT ? u % nsp : 0;
             const int ks1 = ks_begin(sp + 1);
             for (int ks = ks_begin(sp); ks < ks1; ++ks, ++it) {
-                const int s = it % kLStages, b = it % kBStages;
+                const int s = it % kLStages, b = it % kBDiv;
                 if (!wait_or_abort(full(s), (uint32_t)((it / kLStages) & 1), abort_flag, a.err, 16, a.limit) ||
-                    (it >= kBStages &&
-                     !wait_or_abort(bempty(b), (uint32_t)((it / kBStages - 1) & 1), abort_flag, a.err, 17, a.limit))) {
+                    (it >= kBDiv &&
+                     !wait_or_abort(bempty(b), (uint32_t)((it / kBDiv - 1) & 1), abort_flag, a.err, 17, a.limit))) {
                     ok = false;
                     break;
                 }
@@ -833,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             tc_fence_after();
             const int m = mt2 * 2 * BM + (int)rank * BM + row_in_tile;
             const bool live = m < a.M;
-            const int sg = live ? a.sig[m] : 0;
+            const int sg = live && a.sig ? a.sig[m] : 0;  // no prescale (null sig): bf16 operands
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
             store_tile<FMT>(a, tbase, m, live, sg, nt);
             tc_fence_before();
@@ -902,7 +930,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const Args a) {
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)a.M * nout) return;
     const int m = (int)(idx / nout), n = (int)(idx % nout);
-    const int sg = a.sig[m];
+    const int sg = a.sig ? a.sig[m] : 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)m * a.ldo + n;
     const size_t plane = (size_t)a.M * a.N;
     const float* ws = a.ws + (size_t)m * a.N;
@@ -924,6 +952,53 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const Args a) {
             if (QMLP_INB((size_t)m * a.N + sp * plane + n, a.ws_elems, 14)) y += ws[sp * plane + n];
         const float f = FMT == kNVFP4 ? a.inv0 : a.cs0[n];
         *out = __float2bfloat16_rn(scalbnf(y, -sg) * f);
+    }
+}
+
+// Dequantise-once prefill: every weight block of a projection -> its decoded
+// stage image, a 128-byte swizzled K-major bf16 tile [256 rows][128 B] that
+// the GEMM copies into shared memory as it is (the swizzle is the one the
+// decoder warps apply: 16-byte chunk c of row n sits at c ^ (n & 7), the
+// image being 1024-byte aligned like a stage). Every decoded weight is exact
+// in bf16 as in fp16 (NVFP4: E2M1 x E4M3, at most six significant bits in
+// [2^-10, 2688]; FP8: four bits in [2^-9, 448]), so the GEMM multiplies the
+// bf16 activations as they are. One thread per 16-byte output chunk (eight
+// weights of one row): a warp stores 512 contiguous bytes (four rows) and
+// loads the 128 packed bytes of those rows.
+template <int FMT>
+__global__ void __launch_bounds__(256) predecode_kernel(const uint8_t* __restrict__ tiles, long nblk,
+                                                        uint8_t* __restrict__ wdec, size_t tiles_bytes,
+                                                        size_t wdec_bytes) {
+    constexpr int kChunks = BN * 8;  // 16-byte chunks of an image
+    const long total = nblk * kChunks;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const long blk = idx / kChunks;
+        const int n = (int)(idx % kChunks) >> 3, p = (int)(idx & 7);  // row, stored chunk
+        const int l = p ^ (n & 7);                                     // its k-chunk: k = 8 l .. 8 l + 7
+        if (!QMLP_INB((blk + 1) * raw_bytes<FMT>() - 1, tiles_bytes, 17) ||
+            !QMLP_INB((blk + 1) * kBBytes - 1, wdec_bytes, 17))
+            continue;
+        const uint8_t* raw = tiles + blk * raw_bytes<FMT>();
+        uint32_t h[4];
+        if (FMT == kNVFP4) {
+            const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(raw + n * 32 + l * 4));
+            const uint32_t sf = e4m3x2_to_f16x2(__ldg(raw + kRawCodes + n * 4 + (l >> 1)));
+            const uint32_t sc = dup_lo16(sf);
+            e2m1x4_to_f16x2x4(w, h[0], h[1], h[2], h[3]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) h[j] = hmul2_u32(h[j], sc);  // exact in fp16
+        } else {
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(raw + n * 64 + l * 8));
+            e4m3x4_to_f16x2x2(w.x, h[0], h[1]);
+            e4m3x4_to_f16x2x2(w.y, h[2], h[3]);
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[j]));
+            o[j] = pack_bf16x2(f.x, f.y);  // exact (see above)
+        }
+        *reinterpret_cast<uint4*>(wdec + blk * kBBytes + n * 128 + p * 16) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -1078,21 +1153,37 @@ cudaError_t launch_pair(const CUtensorMap& map, const Args& a, int pairs_wanted,
     return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<FMT>, map, a);
 }
 
-template <int FMT>
-cudaError_t launch_fmt(const CUtensorMap& map, const Args& a, int grid, cudaStream_t s) {
+template <int FMT, bool PRE>
+cudaError_t launch_inst(const CUtensorMap& map, const Args& a, int grid, cudaStream_t s) {
     static bool attr = false;
+    constexpr int bytes = Smem<FMT, PRE>::Bytes;
     if (!attr) {
         cudaError_t e =
-            cudaFuncSetAttribute(gemm_kernel<FMT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::Bytes);
+            cudaFuncSetAttribute(gemm_kernel<FMT, false, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemm_kernel<FMT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     Smem<FMT>::Bytes);
+            e = cudaFuncSetAttribute(gemm_kernel<FMT, true, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    if (a.splits > 1) gemm_kernel<FMT, true><<<grid, kThreads, Smem<FMT>::Bytes, s>>>(map, a);
-    else gemm_kernel<FMT, false><<<grid, kThreads, Smem<FMT>::Bytes, s>>>(map, a);
-    cudaError_t e = cudaPeekAtLastError();
+    if (a.splits > 1) gemm_kernel<FMT, true, PRE><<<grid, kThreads, bytes, s>>>(map, a);
+    else gemm_kernel<FMT, false, PRE><<<grid, kThreads, bytes, s>>>(map, a);
+    return cudaPeekAtLastError();
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const CUtensorMap& map, const Args& a, int grid, cudaStream_t s, int num_sms) {
+    cudaError_t e;
+    if (a.wdec) {
+        const long nblk = (long)(a.N / BN) * (a.Kd / BK);
+        const long items = nblk * (BN * 8);
+        const int pgrid = (int)std::min<long>((items + 255) / 256, 8L * std::max(num_sms, 1));
+        predecode_kernel<FMT><<<pgrid, 256, 0, s>>>(a.tiles, nblk, const_cast<uint8_t*>(a.wdec), a.tiles_bytes,
+                                                    a.wdec_bytes);
+        if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+        e = launch_inst<FMT, true>(map, a, grid, s);
+    } else {
+        e = launch_inst<FMT, false>(map, a, grid, s);
+    }
     if (e != cudaSuccess || a.splits == 1) return e;
     const long n = (long)a.M * (a.epi == kEpiSwiGLU ? a.N / 2 : a.N);
     splitk_reduce_kernel<FMT><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a);
@@ -1102,6 +1193,8 @@ cudaError_t launch_fmt(const CUtensorMap& map, const Args& a, int grid, cudaStre
 bool gemm_supported(int K, int N) { return K >= BK && K % BK == 0 && N >= BN && N % BN == 0; }
 
 size_t gemm_splitk_ws_elems(int num_sms) { return (size_t)std::max(num_sms, 1) * BM * BN; }
+
+size_t gemm_decoded_bytes(int N, int K) { return (size_t)(N / BN) * (K / BK) * kBBytes; }
 
 size_t gemm_tiles_bytes(int fmt, int N, int K) {
     return (size_t)(N / BN) * (K / BK) * (fmt == kNVFP4 ? raw_bytes<kNVFP4>() : raw_bytes<kFP8>());
@@ -1131,20 +1224,30 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
 
-    // 1. per-token fp16 prescale of the activations
-    const int pgrid = std::min(L.M, 8 * std::max(num_sms, 1));
-    prescale_rows_kernel<<<pgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(L.a),
-                                                static_cast<__half*>(L.a16), L.sig, L.M, P.K);
-    cudaError_t e = cudaPeekAtLastError();
-    if (e != cudaSuccess) return e;
+    // dequantise-once (never with the CTA pair, which decodes its own
+    // halves): bf16 weight images against the bf16 activations as they are
+    const bool dq = L.wdec && !L.pair;
+    if (dq && L.wdec_bytes < gemm_decoded_bytes(P.N, P.K)) return cudaErrorInvalidValue;
 
-    // 2. tensor map of the fp16 activations: [M rows, K] row-major, box 64 x 128
+    // 1. per-token fp16 prescale of the activations (decoder-warp GEMMs,
+    //    whose decoders write fp16 weights)
+    if (!dq) {
+        const int pgrid = std::min(L.M, 8 * std::max(num_sms, 1));
+        prescale_rows_kernel<<<pgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(L.a),
+                                                    static_cast<__half*>(L.a16), L.sig, L.M, P.K);
+        cudaError_t e = cudaPeekAtLastError();
+        if (e != cudaSuccess) return e;
+    }
+
+    // 2. tensor map of the MMA's activations: [M rows, K] row-major, box 64 x
+    //    128 (fp16 prescaled, or the bf16 input itself)
     CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)P.K, (cuuint64_t)L.M};
     const cuuint64_t strides[1] = {(cuuint64_t)P.K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.a16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (enc(&map, dq ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            dq ? const_cast<void*>(L.a) : L.a16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
@@ -1163,7 +1266,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     a.cs0 = P.cs0;
     a.cs1 = P.cs1;
     if (P.fmt == kFP8 && (!P.cs0 || (P.interleaved && !P.cs1))) return cudaErrorInvalidValue;
-    a.sig = L.sig;
+    a.sig = dq ? nullptr : L.sig;
     a.out = L.out;
     a.ldo = L.epi == kEpiSwiGLU ? P.N / 2 : (L.epi == kEpiRaw && P.interleaved ? P.N / 2 : P.N);
     a.err = L.err;
@@ -1171,6 +1274,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     a.withhold = L.withhold ? 1 : 0;
     a.tiles_bytes = gemm_tiles_bytes(P.fmt, P.N, P.K);
     a.ws_elems = L.ws ? gemm_splitk_ws_elems(num_sms) : 0;
+    a.wdec = dq ? L.wdec : nullptr;  // decoded into first, by the predecode kernel
+    a.wdec_bytes = dq ? gemm_decoded_bytes(P.N, P.K) : 0;
     // Split-K when the tiles cannot fill the GPU (small M, or the down
     // projection's few column tiles): each (tile, k-range) unit writes fp32
     // partials and a reduce kernel adds them in split order. The partials
@@ -1189,7 +1294,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
         return P.fmt == kFP8 ? launch_pair<kFP8>(map, a, pairs, s) : launch_pair<kNVFP4>(map, a, pairs, s);
     }
     const int grid = std::min(tiles0 * a.splits, std::max(num_sms, 1));
-    return P.fmt == kFP8 ? launch_fmt<kFP8>(map, a, grid, s) : launch_fmt<kNVFP4>(map, a, grid, s);
+    return P.fmt == kFP8 ? launch_fmt<kFP8>(map, a, grid, s, num_sms) : launch_fmt<kNVFP4>(map, a, grid, s, num_sms);
 }
 
 QMLP_BOUNDS_UNIT(gemm_tc)

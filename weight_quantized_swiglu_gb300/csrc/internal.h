@@ -176,10 +176,13 @@ struct GemmLaunch {
     uint64_t wait_ns = 0;     // bounded-wait limit (0: the kernel's default of 2 s)
     bool withhold = false;    // error-path tests: the last k-step of each CTA is never loaded
     bool pair = false;        // the CTA-pair kernel (M >= kPairMinM; never split-K)
+    uint8_t* wdec = nullptr;  // dequantise-once: decoded stage images of w (null: the decoder warps decode)
+    size_t wdec_bytes = 0;    // bytes of wdec, >= gemm_decoded_bytes(w.N, w.K)
 };
 constexpr int kPairMinM = 256;  // one 256-token tile of a CTA pair
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s);
 size_t gemm_splitk_ws_elems(int num_sms);
+size_t gemm_decoded_bytes(int N, int K);  // fp16 stage images of an [N, K] projection (2 N K bytes)
 bool gemm_supported(int K, int N);
 
 // ---------------------------------------------------------------------------
