@@ -71,11 +71,13 @@ typedef enum { QMLP_META_3B = 3, QMLP_META_4B = 4 } qmlp_meta;
  * 256-token x 256-row tile, each decoding half of its weight rows) for
  * M >= 256; AUTO does not choose it (the single-CTA GEMM measured faster on
  * the 27B-class prefill shape). GEMM_DQ is the dequantise-once GEMM: each
- * projection is first decoded, once per call, into fp16 tiles in a buffer
+ * projection is first decoded, once per call, into bf16 tiles in a buffer
  * the handle holds (4 I K bytes, allocated by qmlp_create when max_M >=
- * 768), and the tensor-core GEMM then reads those tiles with no decoding in
- * its main loop; AUTO takes it from M = 768 on. The products are the same
- * exact fp16 weight values either way. */
+ * 768), and the tensor-core GEMM then multiplies those tiles with the bf16
+ * activations as given (no per-token prescale), with no decoding in its main
+ * loop (on CTA pairs from M = 256, as GEMM_PAIR, each CTA loading
+ * half of every decoded tile); AUTO takes it from M = 768 on. The products
+ * are of the same exact weight values either way. */
 typedef enum {
     QMLP_PATH_AUTO = 0,
     QMLP_PATH_GEMV = 1,

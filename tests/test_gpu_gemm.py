@@ -102,20 +102,24 @@ def test_pair_gemm_one_hot_is_bit_exact(torch_cuda, fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_dq_gemm_one_hot_is_bit_exact(torch_cuda, fmt):
-    """The dequantise-once GEMM (each projection decoded into fp16 stage
+@pytest.mark.parametrize("M", [200, 300])
+def test_dq_gemm_one_hot_is_bit_exact(torch_cuda, fmt, M):
+    """The dequantise-once GEMM (each projection decoded into bf16 stage
     images before the GEMM, which then copies them into shared memory as
     they are): x = e_k rows return the decoded weights bit for bit, for gate,
     up and down, at k positions on scale-group, k-step, swizzle-row and tile
-    boundaries -- a misplaced 16-byte chunk of an image moves a weight."""
+    boundaries -- a misplaced 16-byte chunk of an image moves a weight. M =
+    200 runs on single CTAs, M = 300 on CTA pairs (a full 256-token tile, each
+    CTA holding half of its tokens and half of every image, and a ragged
+    one)."""
     torch = torch_cuda
     case = gen.gen_dense_case(fmt, TK, TI, 1, seed=207)
     mlp = q.QuantMLP.from_case(case, max_M=768)  # the decode buffer exists from max_M = 768
     for which, proj in ((0, case.gate), (1, case.up), (2, case.down)):
         Kp = proj.K
-        M = 200
         ks = [(r * 29 + 3) % Kp for r in range(M)]
         ks[:12] = [0, 7, 8, 15, 16, 31, 32, 63, 64, Kp - 1, Kp - 16, Kp - 64]
+        ks[128:132] = [1, 17, 65, Kp - 2]  # the second CTA's tokens of a pair tile
         x = np.zeros((M, Kp), dtype=np.uint16)
         for r, k in enumerate(ks):
             x[r, k] = 0x3F80
@@ -134,8 +138,10 @@ def test_dq_gemm_one_hot_is_bit_exact(torch_cuda, fmt):
 @pytest.mark.parametrize("M", [17, 129, 300])
 def test_dq_gemm_parity_and_same_bits_as_decoder_warps(torch_cuda, M, fmt):
     """The dequantise-once GEMM against the oracle, and bit for bit against
-    the GEMM whose decoder warps decode in the main loop: both feed the same
-    exact fp16 weights to the same MMA sequence (M = 17 also runs split-K)."""
+    the GEMM whose decoder warps decode in the main loop: both multiply the
+    same exact weight values (bf16 images against the bf16 activations there,
+    fp16 against the prescaled fp16 activations here) in the same k order
+    (M = 17 also runs split-K; M = 300 runs on CTA pairs)."""
     case = gen.gen_dense_case(fmt, TK, TI, M, seed=270 + M)
     mlp = q.QuantMLP.from_case(case, max_M=768)
     out, act = run_forward(torch_cuda, mlp, case.x, q.PATH_GEMM_DQ)

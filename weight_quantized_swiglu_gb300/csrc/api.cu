@@ -147,6 +147,10 @@ static int gemm_min_m(const qmlp_s* h) { return h->sp.G ? split_max_m(h) + 1 : k
 // M = 512 0.322 / 0.345 against 0.357 / 0.386; M = 1024 0.607 / 0.644
 // against 0.552 / 0.578; M = 8192 3.49 / 3.70 against 2.79 / 2.80.
 constexpr int kDqMinM = 768;
+// The dequantise-once GEMM runs on CTA pairs from kPairMinM tokens (measured
+// at M = 8192, NVFP4 / FP8: 2.67 / 2.72 ms against 2.79 / 2.81 on single
+// CTAs; at M = 1024 0.520 / 0.550 against 0.553 / 0.578).
+constexpr bool kDqPair = true;
 
 struct qmlp_moe_s {
     int E = 0, K = 0, I = 0, meta = 0, device = 0, num_sms = 0;
@@ -501,9 +505,9 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
     if (path == QMLP_PATH_GEMM_DQ && !h->wdec) return QMLP_ERR_SHAPE;
     if (gemm) {
         GemmLaunch g;
-        g.pair = path == QMLP_PATH_GEMM_PAIR;
         g.wdec = dq_buffer(h, path, M);
         g.wdec_bytes = h->wdec_bytes;
+        g.pair = path == QMLP_PATH_GEMM_PAIR || (g.wdec && kDqPair && M >= kPairMinM);
         g.M = M;
         g.err = h->err;
         g.a16 = h->a16;
@@ -736,9 +740,9 @@ qmlp_status qmlp_debug_project(qmlp_t* h, int which, qmlp_path path, const void*
         if (path == QMLP_PATH_GEMM_PAIR && M < kPairMinM) return QMLP_ERR_SHAPE;
         if (path == QMLP_PATH_GEMM_DQ && !h->wdec) return QMLP_ERR_SHAPE;
         GemmLaunch g;
-        g.pair = path == QMLP_PATH_GEMM_PAIR;
         g.wdec = dq_buffer(h, path, M);
         g.wdec_bytes = h->wdec_bytes;
+        g.pair = path == QMLP_PATH_GEMM_PAIR || (g.wdec && kDqPair && M >= kPairMinM);
         g.epi = kEpiRaw;
         g.raw_sel = which == 1 ? 1 : 0;
         g.w = which < 2 ? h->gm_gu : h->gm_d;

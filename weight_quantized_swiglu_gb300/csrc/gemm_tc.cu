@@ -598,6 +598,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 // drained an accumulator. Per SM and 64-k step this moves half the decoded
 // weight tile through shared memory (decoder stores 16 KB instead of 32 KB,
 // tensor-core reads 16 KB of B instead of 32 KB) and halves the decode work.
+//
+// Dequantise-once instance (PRE, the automatic path from 768 tokens): no
+// decoders; the leader's producer thread issues, per k-step, the four TMA
+// loads of both CTAs' stages -- each CTA's 128 tokens of the bf16 activation
+// tile and its 128 rows of the decoded image (a tensor map over the images as
+// 128-byte rows) -- into the shared memory of the CTA they belong to, all
+// completing on the leader's barrier (.cta_group::2), so the leader waits on
+// one barrier per stage and no stage needs a signal from the peer. Per SM and
+// step 32 KB arrive instead of the 48 KB of the single-CTA instance. Copies in
+// flight are tracked by the leader's barriers alone.
 // ---------------------------------------------------------------------------
 constexpr int kBHalf = (BN / 2) * BK * 2;  // 16 KB: 128 decoded weight rows of a 64-k step
 constexpr int kDecGroups = 4;              // decoder groups of the pair kernel (one per B stage)
@@ -605,15 +615,15 @@ constexpr int kDecGroups = 4;              // decoder groups of the pair kernel 
 template <int FMT>
 constexpr int raw_half() { return raw_bytes<FMT>() / 2; }  // NVFP4: 4096 codes + 512 scales; FP8: 8192
 
-template <int FMT>
+template <int FMT, bool PRE = false>
 struct SmemP {
-    // load stages: A (16 KB) + the weight half-block. A stage is held from its
-    // TMA until the leader's MMA has used it, which now includes the peer's
-    // signal: measured at M=8192 (NVFP4 / FP8), 3.90 / 3.92 ms with 5 stages,
-    // 3.72 / 3.76 with 6.
+    // load stages: A (16 KB) + the weight half-block (PRE: the 16 KB half of
+    // the decoded image). A stage is held from its TMA until the leader's MMA
+    // has used it, which now includes the peer's signal: measured at M=8192
+    // (NVFP4 / FP8), 3.90 / 3.92 ms with 5 stages, 3.72 / 3.76 with 6.
     static constexpr int L = 6;
-    static constexpr int BS = 4;  // decoded half-B stages
-    static constexpr int R = raw_half<FMT>();
+    static constexpr int BS = PRE ? 0 : 4;  // decoded half-B stages
+    static constexpr int R = PRE ? kBHalf : raw_half<FMT>();
     static constexpr int A = 0;
     static constexpr int B = A + L * kABytes;
     static constexpr int Raw = B + BS * kBHalf;
@@ -626,12 +636,14 @@ struct SmemP {
     static constexpr int Misc = Bar + NumBars * 8;
     static constexpr int Bytes = Misc + 16 + 1024;
     static_assert(B % 1024 == 0 && Raw % 16 == 0 && Bar % 8 == 0 && R % 16 == 0, "smem layout");
+    static_assert(!PRE || (Raw % 1024 == 0 && R % 1024 == 0), "decoded stages sit on the swizzle period");
     static_assert(Bytes <= 227 * 1024, "smem budget");
 };
 
 // Instruction descriptor of the pair MMA: fp32 accumulator, fp16 A and B,
-// K-major, N = 256, M = 256 (128 rows in each CTA).
+// K-major, N = 256, M = 256 (128 rows in each CTA); and with bf16 A and B.
 constexpr uint32_t kIdescPair = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+constexpr uint32_t kIdescPairBF16 = kIdescPair | (1u << 7) | (1u << 10);
 
 QMLP_DEV uint32_t cluster_ctarank() {
     uint32_t r;
@@ -648,6 +660,19 @@ QMLP_DEV void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(bar), "r"(rank));
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
 }
+// TMA tile load into the shared memory of CTA `rank` of the pair (same
+// offset `dst` as in this CTA), completing on this CTA's barrier `bar`
+// (.cta_group::2: the barrier may sit in the destination's peer).
+QMLP_DEV void tma_load_2d_pair(uint32_t dst, uint32_t rank, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+    uint32_t rd;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rd) : "r"(dst), "r"(rank));
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(rd),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
 // Wait for phase `parity` of a barrier that the peer CTA arrives on
 // (acquire at cluster scope); false if the abort flag is raised or the wait
 // ran out (which raises it and records `code`).
@@ -700,10 +725,12 @@ QMLP_DEV void umma_commit_pair(uint32_t bar) {
         : "memory");
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_constant__ CUtensorMap amap, const Args a) {
-    using S = SmemP<FMT>;
+template <int FMT, bool PRE>
+__global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                const __grid_constant__ CUtensorMap bmap, const Args a) {
+    using S = SmemP<FMT, PRE>;
     constexpr int kL = S::L, kBS = S::BS, kR = S::R;
+    constexpr int kBSd = kBS > 0 ? kBS : 1;  // ring arithmetic (unused by PRE)
     extern __shared__ uint8_t dyn_smem_raw[];
     // the same offsets in both CTAs: the MMA addresses the peer's halves, and
     // the commits and remote arrivals its barriers, at this CTA's offsets
@@ -760,8 +787,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         // ---------------- TMA producer: this CTA's A half and weight half ----------------
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&amap)) : "memory");
+            if (PRE) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&bmap)) : "memory");
             int it = 0;
-            bool ok = true;
+            bool ok = !PRE || rank == 0;  // PRE: the leader loads the stages of both CTAs
             for (int u = pair; u < units && ok; u += npairs) {
                 const int nt = u / Mt2, mt2 = u % Mt2;
                 const uint8_t* blk = a.tiles + (size_t)nt * KS * raw_bytes<FMT>();
@@ -773,6 +801,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                         !wait_or_abort(empty(s), (uint32_t)((it / kL - 1) & 1), abort_flag, a.err, 41, a.limit)) {
                         ok = false;
                         break;
+                    }
+                    if (PRE) {
+                        // both CTAs' stage s, on the leader's barrier: tokens
+                        // 128 r.. of the tile and rows 128 r.. of the decoded
+                        // image (image rows, 128 B each, are the tensor map's
+                        // rows; the row swizzle has period 8) into CTA r
+                        mbar_arrive_expect_tx(full(s), 2 * (kABytes + kR));
+                        const int row = (nt * KS + ks) * BN;
+                        const bool in = QMLP_INB(((size_t)row + BN) * 128 - 1, a.wdec_bytes, 16);
+#pragma unroll
+                        for (uint32_t r = 0; r < 2; ++r) {
+                            tma_load_2d_pair(base_s + S::A + s * kABytes, r, &amap, ks * BK, mt2 * 2 * BM + (int)r * BM,
+                                             full(s));
+                            tma_load_2d_pair(base_s + S::Raw + s * kR, r, &bmap, 0, in ? row + (int)r * (BN / 2) : 0,
+                                             full(s));
+                        }
+                        continue;
                     }
                     mbar_arrive_expect_tx(full(s), kABytes + kR);
                     tma_load_2d(base_s + S::A + s * kABytes, &amap, ks * BK, mt2 * 2 * BM + (int)rank * BM, full(s));
@@ -811,24 +856,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     tc_fence_after();
                     const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
                     for (int ks = 0; ks < KS; ++ks, ++it) {
-                        const int s = it % kL, b = it % kBS;
-                        if (!wait_or_abort(full(s), (uint32_t)((it / kL) & 1), abort_flag, a.err, 44, a.limit) ||
-                            !wait_or_abort(bfull(b), (uint32_t)((it / kBS) & 1), abort_flag, a.err, 45, a.limit) ||
-                            !wait_cluster_or_abort(pbfull(b), (uint32_t)((it / kBS) & 1), abort_flag, a.err, 46,
-                                                   a.limit)) {
+                        const int s = it % kL, b = it % kBSd;
+                        const bool ready =
+                            wait_or_abort(full(s), (uint32_t)((it / kL) & 1), abort_flag, a.err, 44, a.limit) &&
+                            (PRE || (wait_or_abort(bfull(b), (uint32_t)((it / kBSd) & 1), abort_flag, a.err, 45,
+                                                   a.limit) &&
+                                     wait_cluster_or_abort(pbfull(b), (uint32_t)((it / kBSd) & 1), abort_flag, a.err,
+                                                           46, a.limit)));
+                        if (!ready) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint32_t sa = base_s + S::A + s * kABytes;
-                        const uint32_t sb = base_s + S::B + b * kBHalf;
+                        const uint32_t sb = PRE ? base_s + S::Raw + s * kR : base_s + S::B + b * kBHalf;
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
-                            umma_f16_pair(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), kIdescPair,
-                                          (ks != 0 || k != 0) ? 1u : 0u);
+                            umma_f16_pair(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32),
+                                          PRE ? kIdescPairBF16 : kIdescPair, (ks != 0 || k != 0) ? 1u : 0u);
                         issued = true;
                         umma_commit_pair(empty(s));
-                        umma_commit_pair(bempty(b));
+                        if (!PRE) umma_commit_pair(bempty(b));
                     }
                     if (!ok) break;
                     umma_commit_pair(acc_full(buf));
@@ -867,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             tc_fence_before();
             mbar_arrive(acc_empty(buf));
         }
-    } else {
+    } else if (!PRE) {
         // ---------------- decoders: rows 128 rank.. of each weight block ----------------
         // kDecGroups groups of warps take turns by step, each decoding a whole
         // half-B stage: the peer's arrival on the leader's barrier is a
@@ -884,10 +932,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         for (int u = pair; u < units && ok; u += npairs) {
             for (int ks = 0; ks < KS; ++ks, ++it) {
                 if (it % kDecGroups != dg) continue;
-                const int s = it % kL, b = it % kBS;
+                const int s = it % kL, b = it % kBSd;
                 if (!wait_or_abort(full(s), (uint32_t)((it / kL) & 1), abort_flag, a.err, 51, a.limit) ||
-                    (it >= kBS &&
-                     !wait_or_abort(bempty(b), (uint32_t)((it / kBS - 1) & 1), abort_flag, a.err, 52, a.limit))) {
+                    (it >= kBSd &&
+                     !wait_or_abort(bempty(b), (uint32_t)((it / kBSd - 1) & 1), abort_flag, a.err, 52, a.limit))) {
                     ok = false;
                     break;
                 }
@@ -1124,12 +1172,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // The CTA-pair GEMM over `pairs_wanted` clusters of two (fewer if fewer fit at
 // once: the pairs loop over the tiles).
-template <int FMT>
-cudaError_t launch_pair(const CUtensorMap& map, const Args& a, int pairs_wanted, cudaStream_t s) {
+template <int FMT, bool PRE>
+cudaError_t launch_pair(const CUtensorMap& map, const CUtensorMap& bmap, const Args& a, int pairs_wanted,
+                        cudaStream_t s) {
     static int max_pairs = -1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = SmemP<FMT>::Bytes;
+    cfg.dynamicSmemBytes = SmemP<FMT, PRE>::Bytes;
     cfg.stream = s;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1139,18 +1188,18 @@ cudaError_t launch_pair(const CUtensorMap& map, const Args& a, int pairs_wanted,
     cfg.attrs = at;
     cfg.numAttrs = 1;
     if (max_pairs < 0) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SmemP<FMT>::Bytes);
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<FMT, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SmemP<FMT, PRE>::Bytes);
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(2);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<FMT>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<FMT, PRE>, &cfg);
         if (e != cudaSuccess) return e;
         if (n < 1) return cudaErrorInvalidConfiguration;
         max_pairs = n;
     }
     cfg.gridDim = dim3((unsigned)(2 * std::min(pairs_wanted, max_pairs)));
-    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<FMT>, map, a);
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<FMT, PRE>, map, bmap, a);
 }
 
 template <int FMT, bool PRE>
@@ -1170,20 +1219,20 @@ cudaError_t launch_inst(const CUtensorMap& map, const Args& a, int grid, cudaStr
     return cudaPeekAtLastError();
 }
 
+// The projection's weight blocks -> their decoded images in a.wdec.
 template <int FMT>
-cudaError_t launch_fmt(const CUtensorMap& map, const Args& a, int grid, cudaStream_t s, int num_sms) {
-    cudaError_t e;
-    if (a.wdec) {
-        const long nblk = (long)(a.N / BN) * (a.Kd / BK);
-        const long items = nblk * (BN * 8);
-        const int pgrid = (int)std::min<long>((items + 255) / 256, 8L * std::max(num_sms, 1));
-        predecode_kernel<FMT><<<pgrid, 256, 0, s>>>(a.tiles, nblk, const_cast<uint8_t*>(a.wdec), a.tiles_bytes,
-                                                    a.wdec_bytes);
-        if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
-        e = launch_inst<FMT, true>(map, a, grid, s);
-    } else {
-        e = launch_inst<FMT, false>(map, a, grid, s);
-    }
+cudaError_t launch_predecode(const Args& a, int num_sms, cudaStream_t s) {
+    const long nblk = (long)(a.N / BN) * (a.Kd / BK);
+    const long items = nblk * (BN * 8);
+    const int pgrid = (int)std::min<long>((items + 255) / 256, 8L * std::max(num_sms, 1));
+    predecode_kernel<FMT><<<pgrid, 256, 0, s>>>(a.tiles, nblk, const_cast<uint8_t*>(a.wdec), a.tiles_bytes,
+                                                a.wdec_bytes);
+    return cudaPeekAtLastError();
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const CUtensorMap& map, const Args& a, int grid, cudaStream_t s) {
+    cudaError_t e = a.wdec ? launch_inst<FMT, true>(map, a, grid, s) : launch_inst<FMT, false>(map, a, grid, s);
     if (e != cudaSuccess || a.splits == 1) return e;
     const long n = (long)a.M * (a.epi == kEpiSwiGLU ? a.N / 2 : a.N);
     splitk_reduce_kernel<FMT><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a);
@@ -1224,9 +1273,9 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
 
-    // dequantise-once (never with the CTA pair, which decodes its own
-    // halves): bf16 weight images against the bf16 activations as they are
-    const bool dq = L.wdec && !L.pair;
+    // dequantise-once: bf16 weight images against the bf16 activations as
+    // they are
+    const bool dq = L.wdec != nullptr;
     if (dq && L.wdec_bytes < gemm_decoded_bytes(P.N, P.K)) return cudaErrorInvalidValue;
 
     // 1. per-token fp16 prescale of the activations (decoder-warp GEMMs,
@@ -1274,8 +1323,13 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     a.withhold = L.withhold ? 1 : 0;
     a.tiles_bytes = gemm_tiles_bytes(P.fmt, P.N, P.K);
     a.ws_elems = L.ws ? gemm_splitk_ws_elems(num_sms) : 0;
-    a.wdec = dq ? L.wdec : nullptr;  // decoded into first, by the predecode kernel
+    a.wdec = dq ? L.wdec : nullptr;
     a.wdec_bytes = dq ? gemm_decoded_bytes(P.N, P.K) : 0;
+    if (dq) {  // the images first
+        const cudaError_t e = P.fmt == kFP8 ? launch_predecode<kFP8>(a, num_sms, s)
+                                            : launch_predecode<kNVFP4>(a, num_sms, s);
+        if (e != cudaSuccess) return e;
+    }
     // Split-K when the tiles cannot fill the GPU (small M, or the down
     // projection's few column tiles): each (tile, k-range) unit writes fp32
     // partials and a reduce kernel adds them in split order. The partials
@@ -1291,10 +1345,24 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     if (L.pair) {
         if (L.M < kPairMinM) return cudaErrorInvalidValue;
         const int pairs = std::min(((L.M + 2 * BM - 1) / (2 * BM)) * (P.N / BN), std::max(num_sms, 2) / 2);
-        return P.fmt == kFP8 ? launch_pair<kFP8>(map, a, pairs, s) : launch_pair<kNVFP4>(map, a, pairs, s);
+        if (!dq)
+            return P.fmt == kFP8 ? launch_pair<kFP8, false>(map, map, a, pairs, s)
+                                 : launch_pair<kNVFP4, false>(map, map, a, pairs, s);
+        // the decoded images as rows of 128 bytes, 128-row boxes (a CTA's
+        // half of a k-step's image), no swizzle (the images carry it)
+        CUtensorMap bmap;
+        const cuuint64_t bdims[2] = {128, (cuuint64_t)(a.wdec_bytes / 128)};
+        const cuuint64_t bstrides[1] = {128};
+        const cuuint32_t bbox[2] = {128, (cuuint32_t)(BN / 2)};
+        if (enc(&bmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wdec), bdims, bstrides, bbox, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        return P.fmt == kFP8 ? launch_pair<kFP8, true>(map, bmap, a, pairs, s)
+                             : launch_pair<kNVFP4, true>(map, bmap, a, pairs, s);
     }
     const int grid = std::min(tiles0 * a.splits, std::max(num_sms, 1));
-    return P.fmt == kFP8 ? launch_fmt<kFP8>(map, a, grid, s, num_sms) : launch_fmt<kNVFP4>(map, a, grid, s, num_sms);
+    return P.fmt == kFP8 ? launch_fmt<kFP8>(map, a, grid, s) : launch_fmt<kNVFP4>(map, a, grid, s);
 }
 
 QMLP_BOUNDS_UNIT(gemm_tc)
