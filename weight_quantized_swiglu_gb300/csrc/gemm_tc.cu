@@ -65,6 +65,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace qmlp {
 namespace {
@@ -139,72 +140,6 @@ struct Args {
     size_t wdec_bytes;     // PRE: bytes of wdec (index checks)
 };
 
-// ---------------------------------------------------------------------------
-// tcgen05 / TMA primitives (inline PTX)
-// ---------------------------------------------------------------------------
-QMLP_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
-QMLP_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-QMLP_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-QMLP_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-QMLP_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16, one thread.
-QMLP_DEV void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
-QMLP_DEV void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// 32 lanes x 32 consecutive fp32 columns: thread = lane, v[j] = column col+j.
-QMLP_DEV void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes with
-// the 128-byte swizzle, 8-row groups 1024 bytes apart (SBO), sm100 version
-// bits, swizzle mode 2 (128B).
-QMLP_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)1u << 16;                    // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(1024u >> 4) << 32;          // stride byte offset
-    d |= (uint64_t)1u << 46;                    // descriptor version
-    d |= (uint64_t)2u << 61;                    // SWIZZLE_128B
-    return d;
-}
-
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
 // K-major, N = BN, M = BM.
 constexpr uint32_t kIdesc = (1u << 4)                    // D format fp32
@@ -214,23 +149,6 @@ constexpr uint32_t kIdesc = (1u << 4)                    // D format fp32
 
 // The same for bf16 A and B (the dequantise-once instance).
 constexpr uint32_t kIdescBF16 = kIdesc | (1u << 7) | (1u << 10);
-
-// Wait for phase `parity` of `bar`; false if the CTA's abort flag is raised
-// or the wait ran out (which raises it and records `code`).
-QMLP_DEV bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, int code,
-                             uint64_t limit) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit) {
-            *abort_flag = 1;
-            atomicExch(err, code);
-            return false;
-        }
-    }
-    return true;
-}
 
 // Decode one (row, 32-k half) item of a packed block into the swizzled fp16
 // B tile: 16 code bytes (32 weights, low nibble = even k) and two E4M3
