@@ -145,7 +145,10 @@ static int gemm_min_m(const qmlp_s* h) { return h->sp.G ? split_max_m(h) + 1 : k
 // decode buffer (4 I K bytes: the larger projection). Measured on the
 // 27B-class shape (NVFP4 / FP8, ms, decoder warps against decoded once):
 // M = 512 0.322 / 0.345 against 0.357 / 0.386; M = 1024 0.607 / 0.644
-// against 0.552 / 0.578; M = 8192 3.49 / 3.70 against 2.79 / 2.80.
+// against 0.552 / 0.578; M = 8192 3.49 / 3.70 against 2.79 / 2.80. With the
+// CTA-pair form: M = 640 0.360 / 0.386 against 0.378 / 0.409, M = 768
+// 0.402 / 0.428 against 0.383 / 0.414 (below, the down projection's few
+// 256-token tiles leave most pairs idle).
 constexpr int kDqMinM = 768;
 // The dequantise-once GEMM runs on CTA pairs from kPairMinM tokens (measured
 // at M = 8192, NVFP4 / FP8: 2.67 / 2.72 ms against 2.79 / 2.81 on single
