@@ -41,6 +41,22 @@ def test_binding_signatures_cover_the_header():
     assert set(declared_symbols()) == set(q._SIGS)
 
 
+def header_enum(prefix):
+    txt = open(os.path.join(ROOT, "include", "qmlp.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return {k: int(v) for k, v in re.findall(r"\b(" + prefix + r"[A-Z0-9_]+)\s*=\s*(\d+)", txt)}
+
+
+def test_binding_constants_match_the_header():
+    """Every kernel-family path and status value the binding names is the
+    header's own (a path added on one side only would call another kernel)."""
+    paths = header_enum("QMLP_PATH_")
+    assert paths == {"QMLP_PATH_AUTO": q.PATH_AUTO, "QMLP_PATH_GEMV": q.PATH_GEMV, "QMLP_PATH_GEMM": q.PATH_GEMM,
+                     "QMLP_PATH_GEMM_PAIR": q.PATH_GEMM_PAIR, "QMLP_PATH_GEMM_DQ": q.PATH_GEMM_DQ}
+    status = {k: v for k, v in header_enum("QMLP_").items() if k.startswith(("QMLP_OK", "QMLP_ERR_"))}
+    assert status == {name: code for code, name in q.STATUS.items()}
+
+
 def test_status_strings(L):
     assert q.qmlp_status_str(0) == "QMLP_OK"
     assert q.qmlp_status_str(8) == "QMLP_ERR_DEVICE_TIMEOUT"

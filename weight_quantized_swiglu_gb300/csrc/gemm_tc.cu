@@ -1137,14 +1137,14 @@ cudaError_t launch_inst(const CUtensorMap& map, const Args& a, int grid, cudaStr
     return cudaPeekAtLastError();
 }
 
-// The projection's weight blocks -> their decoded images in a.wdec.
+// The projection's weight blocks -> their decoded images in wdec (= a.wdec,
+// which the GEMM then only reads).
 template <int FMT>
-cudaError_t launch_predecode(const Args& a, int num_sms, cudaStream_t s) {
+cudaError_t launch_predecode(const Args& a, uint8_t* wdec, int num_sms, cudaStream_t s) {
     const long nblk = (long)(a.N / BN) * (a.Kd / BK);
     const long items = nblk * (BN * 8);
     const int pgrid = (int)std::min<long>((items + 255) / 256, 8L * std::max(num_sms, 1));
-    predecode_kernel<FMT><<<pgrid, 256, 0, s>>>(a.tiles, nblk, const_cast<uint8_t*>(a.wdec), a.tiles_bytes,
-                                                a.wdec_bytes);
+    predecode_kernel<FMT><<<pgrid, 256, 0, s>>>(a.tiles, nblk, wdec, a.tiles_bytes, a.wdec_bytes);
     return cudaPeekAtLastError();
 }
 
@@ -1244,8 +1244,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     a.wdec = dq ? L.wdec : nullptr;
     a.wdec_bytes = dq ? gemm_decoded_bytes(P.N, P.K) : 0;
     if (dq) {  // the images first
-        const cudaError_t e = P.fmt == kFP8 ? launch_predecode<kFP8>(a, num_sms, s)
-                                            : launch_predecode<kNVFP4>(a, num_sms, s);
+        const cudaError_t e = P.fmt == kFP8 ? launch_predecode<kFP8>(a, L.wdec, num_sms, s)
+                                            : launch_predecode<kNVFP4>(a, L.wdec, num_sms, s);
         if (e != cudaSuccess) return e;
     }
     // Split-K when the tiles cannot fill the GPU (small M, or the down
@@ -1272,7 +1272,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
         const cuuint64_t bdims[2] = {128, (cuuint64_t)(a.wdec_bytes / 128)};
         const cuuint64_t bstrides[1] = {128};
         const cuuint32_t bbox[2] = {128, (cuuint32_t)(BN / 2)};
-        if (enc(&bmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wdec), bdims, bstrides, bbox, estr,
+        if (enc(&bmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, L.wdec, bdims, bstrides, bbox, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
