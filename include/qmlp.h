@@ -71,9 +71,13 @@ typedef enum { QMLP_META_3B = 3, QMLP_META_4B = 4 } qmlp_meta;
  * 256-token x 256-row tile, each decoding half of its weight rows) for
  * M >= 256; AUTO does not choose it (the single-CTA GEMM measured faster on
  * the 27B-class prefill shape). GEMM_DQ is the dequantise-once GEMM: each
- * projection is first decoded, once per call, into bf16 tiles in a buffer
- * the handle holds (4 I K bytes, allocated by qmlp_create when max_M >=
- * 768), and the tensor-core GEMM then multiplies those tiles with the bf16
+ * projection is first decoded, once per call, into bf16 tiles in buffers
+ * the handle holds (6 I K bytes, allocated by qmlp_create when max_M >=
+ * 768, with a CUDA stream and two events of the handle's own: in a whole
+ * forward the down projection is decoded on that stream while the gate/up
+ * GEMM runs, forked from and joined back to the caller's stream with
+ * events, so the call stays stream-ordered and can be captured in a CUDA
+ * graph), and the tensor-core GEMM then multiplies those tiles with the bf16
  * activations as given (no per-token prescale), with no decoding in its main
  * loop (on CTA pairs from M = 256, as GEMM_PAIR, each CTA loading
  * half of every decoded tile); AUTO takes it from M = 768 on. The products
@@ -138,7 +142,8 @@ qmlp_status qmlp_forward(qmlp_t* h, const void* x, int M, void* out, qmlp_stream
 /* As qmlp_forward, forcing a kernel family. GEMM, GEMM_PAIR and GEMM_DQ
  * require a handle whose max_M reaches the GEMM threshold (and K % 256,
  * I % 128 == 0); GEMM_PAIR also M >= 256; GEMM_DQ a handle created with
- * max_M >= 768 (any M up to max_M). Otherwise SHAPE. */
+ * max_M >= 768 (any M up to max_M; the handle's buffers and side stream,
+ * see qmlp_path). Otherwise SHAPE. */
 qmlp_status qmlp_forward_path(qmlp_t* h, qmlp_path path, const void* x, int M, void* out,
                               qmlp_stream_t stream);
 

@@ -153,6 +153,42 @@ def test_dq_gemm_parity_and_same_bits_as_decoder_warps(torch_cuda, M, fmt):
     mlp.close()
 
 
+def test_dq_forward_in_a_cuda_graph(torch_cuda):
+    """The dequantise-once forward decodes the down projection on the
+    handle's side stream (forked and joined with events, beside the gate/up
+    GEMM); captured in a CUDA graph and replayed with new x it gives the
+    bytes of an eager call, and a stage call (no fork) agrees too."""
+    torch = torch_cuda
+    M = 300
+    case = gen.gen_dense_case("nvfp4", TK, TI, M, seed=291)
+    mlp = q.QuantMLP.from_case(case, max_M=768)
+    x = to_dev(case.x)
+    out = torch.empty((M, TK), dtype=torch.int16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        mlp.forward(x, out, path=q.PATH_GEMM_DQ, stream=s)  # warm-up (kernel attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mlp.forward(x, out, path=q.PATH_GEMM_DQ, stream=s)
+    for seed in (292, 293):
+        xb = gen.gen_x_only(seed, M, TK)
+        x.copy_(to_dev(xb))
+        g.replay()
+        torch.cuda.synchronize()
+        eager = torch.empty_like(out)
+        mlp.forward(to_dev(xb), eager, path=q.PATH_GEMM_DQ)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits_from_dev(out), bits_from_dev(eager)), seed
+    staged = torch.empty_like(out)
+    mlp.forward_stage(0, x, None, M, path=q.PATH_GEMM_DQ)
+    mlp.forward_stage(1, None, staged, M, path=q.PATH_GEMM_DQ)
+    torch.cuda.synchronize()
+    mlp.check()
+    assert np.array_equal(bits_from_dev(staged), bits_from_dev(out))
+    mlp.close()
+
+
 def test_dq_gemm_needs_the_decode_buffer(torch_cuda):
     """A handle created for fewer than 768 tokens holds no decode buffer:
     the dequantise-once path is refused (SHAPE) before any launch, and the

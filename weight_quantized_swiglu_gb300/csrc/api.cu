@@ -102,8 +102,12 @@ struct qmlp_s {
     bool has_gemm = false;
     GemmProj gm_gu, gm_d;
     void* a16 = nullptr;       // fp16 [max_M, max(K, I)] (GEMM prescaled activations)
-    uint8_t* wdec = nullptr;   // dequantise-once GEMM: one projection's decoded fp16 stage images
+    uint8_t* wdec = nullptr;   // dequantise-once GEMM: one projection's decoded bf16 stage images
     size_t wdec_bytes = 0;
+    uint8_t* wdec2 = nullptr;  // the down projection's images, decoded on `side` beside the gate/up GEMM
+    size_t wdec2_bytes = 0;
+    cudaStream_t side = nullptr;  // the handle's own stream for that predecode
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     float* gemm_ws = nullptr;  // split-K partials of the GEMM (small M)
     int* sig = nullptr;        // [max_M] per-token prescale exponents
     void* act = nullptr;       // bf16 [max_M, I]
@@ -119,6 +123,15 @@ struct qmlp_s {
     bool withhold = false;     // error-path tests: the kernels' producers skip their last step
     Owner mem;
 };
+
+// Frees everything a (possibly half-built) dense handle owns.
+static void release_handle(qmlp_s* h) {
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
+    if (h->side) cudaStreamDestroy(h->side);
+    h->mem.release();
+    delete h;
+}
 
 // Largest token block one launch of the I-partitioned decode kernel takes: 16
 // for FP8 (two 8-token column tiles, x staged in two halves) where the
@@ -314,8 +327,7 @@ qmlp_status qmlp_create_shard(qmlp_t** out, const qmlp_desc* d, int rank, int nr
     }
     if (st != QMLP_OK) {
         cudaStreamSynchronize(s);
-        h->mem.release();
-        delete h;
+        release_handle(h);
         return st;
     }
     sd.down.w = static_cast<const uint8_t*>(dw);
@@ -408,11 +420,22 @@ static qmlp_status create_impl(qmlp_t* h, qmlp_t** out, const qmlp_desc* d, int 
                 st = from_cuda(e);
         }
         if (st == QMLP_OK && d->max_M >= kDqMinM) {
-            const size_t b = std::max(gemm_decoded_bytes(2 * d->I, d->K), gemm_decoded_bytes(d->K, d->I));
-            void* p = nullptr;
+            // one buffer for a projection's images (gate/up, or down alone in
+            // a stage call), one for the down images of a whole forward, and
+            // the side stream that decodes those while the gate/up GEMM runs
+            const size_t b2 = gemm_decoded_bytes(d->K, d->I);
+            const size_t b = std::max(gemm_decoded_bytes(2 * d->I, d->K), b2);
+            void *p = nullptr, *p2 = nullptr;
             if ((e = h->mem.alloc(&p, b)) != cudaSuccess) st = from_cuda(e);
+            else if ((e = h->mem.alloc(&p2, b2)) != cudaSuccess) st = from_cuda(e);
+            else if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+                     cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+                     cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess)
+                st = QMLP_ERR_CUDA;
             h->wdec = static_cast<uint8_t*>(p);
             h->wdec_bytes = b;
+            h->wdec2 = static_cast<uint8_t*>(p2);
+            h->wdec2_bytes = b2;
         }
     }
     // workspace
@@ -454,8 +477,7 @@ static qmlp_status create_impl(qmlp_t* h, qmlp_t** out, const qmlp_desc* d, int 
     }
     if (st != QMLP_OK) {
         cudaStreamSynchronize(s);
-        h->mem.release();
-        delete h;
+        release_handle(h);
         return st;
     }
     *out = h;
@@ -465,8 +487,7 @@ static qmlp_status create_impl(qmlp_t* h, qmlp_t** out, const qmlp_desc* d, int 
 void qmlp_destroy(qmlp_t* h) {
     if (!h) return;
     cudaDeviceSynchronize();
-    h->mem.release();
-    delete h;
+    release_handle(h);
 }
 
 static qmlp_status validate_fwd(qmlp_t* h, const void* x, int M, const void* out, size_t out_elem_bytes,
@@ -518,6 +539,18 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
         g.ws = h->gemm_ws;
         g.wait_ns = h->wait_ns;
         g.withhold = h->withhold;
+        // dequantise-once, whole block: the gate/up images here, then the
+        // down images on the side stream while the gate/up GEMM runs (the
+        // fork follows everything already on s, so the previous call's down
+        // GEMM has finished reading wdec2)
+        const bool fork = g.wdec && stages == 3 && h->wdec2 && h->side;
+        if (fork && (launch_gemm_predecode(h->gm_gu, h->wdec, h->wdec_bytes, h->num_sms, s) != cudaSuccess ||
+                     cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
+                     cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess ||
+                     launch_gemm_predecode(h->gm_d, h->wdec2, h->wdec2_bytes, h->num_sms, h->side) != cudaSuccess ||
+                     cudaEventRecord(h->ev_join, h->side) != cudaSuccess))
+            return QMLP_ERR_CUDA;
+        g.images_ready = fork;
         if (stages & 1) {
             g.epi = kEpiSwiGLU;
             g.w = h->gm_gu;
@@ -526,6 +559,11 @@ static qmlp_status run_stages(qmlp_t* h, qmlp_path path, int stages, const void*
             if (launch_gemm(g, h->num_sms, s) != cudaSuccess) return QMLP_ERR_CUDA;
         }
         if (stages & 2) {
+            if (fork) {
+                if (cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return QMLP_ERR_CUDA;
+                g.wdec = h->wdec2;
+                g.wdec_bytes = h->wdec2_bytes;
+            }
             g.epi = out_f32 ? kEpiRaw : kEpiPlain;
             g.raw_sel = 0;
             g.w = h->gm_d;

@@ -1163,6 +1163,19 @@ size_t gemm_splitk_ws_elems(int num_sms) { return (size_t)std::max(num_sms, 1) *
 
 size_t gemm_decoded_bytes(int N, int K) { return (size_t)(N / BN) * (K / BK) * kBBytes; }
 
+cudaError_t launch_gemm_predecode(const GemmProj& P, uint8_t* wdec, size_t wdec_bytes, int num_sms, cudaStream_t s) {
+    if (!gemm_supported(P.K, P.N) || !P.tiles || !wdec || wdec_bytes < gemm_decoded_bytes(P.N, P.K))
+        return cudaErrorInvalidValue;
+    Args a = {};
+    a.tiles = P.tiles;
+    a.N = P.N;
+    a.Kd = P.K;
+    a.tiles_bytes = gemm_tiles_bytes(P.fmt, P.N, P.K);
+    a.wdec = wdec;
+    a.wdec_bytes = gemm_decoded_bytes(P.N, P.K);
+    return P.fmt == kFP8 ? launch_predecode<kFP8>(a, wdec, num_sms, s) : launch_predecode<kNVFP4>(a, wdec, num_sms, s);
+}
+
 size_t gemm_tiles_bytes(int fmt, int N, int K) {
     return (size_t)(N / BN) * (K / BK) * (fmt == kNVFP4 ? raw_bytes<kNVFP4>() : raw_bytes<kFP8>());
 }
@@ -1243,7 +1256,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s) {
     a.ws_elems = L.ws ? gemm_splitk_ws_elems(num_sms) : 0;
     a.wdec = dq ? L.wdec : nullptr;
     a.wdec_bytes = dq ? gemm_decoded_bytes(P.N, P.K) : 0;
-    if (dq) {  // the images first
+    if (dq && !L.images_ready) {  // the images first
         const cudaError_t e = P.fmt == kFP8 ? launch_predecode<kFP8>(a, L.wdec, num_sms, s)
                                             : launch_predecode<kNVFP4>(a, L.wdec, num_sms, s);
         if (e != cudaSuccess) return e;

@@ -178,11 +178,14 @@ struct GemmLaunch {
     bool pair = false;        // the CTA-pair kernel (M >= kPairMinM; never split-K)
     uint8_t* wdec = nullptr;  // dequantise-once: decoded stage images of w (null: the decoder warps decode)
     size_t wdec_bytes = 0;    // bytes of wdec, >= gemm_decoded_bytes(w.N, w.K)
+    bool images_ready = false;  // dequantise-once: wdec already holds w's images (no predecode launch)
 };
 constexpr int kPairMinM = 256;  // one 256-token tile of a CTA pair
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s);
 size_t gemm_splitk_ws_elems(int num_sms);
-size_t gemm_decoded_bytes(int N, int K);  // fp16 stage images of an [N, K] projection (2 N K bytes)
+size_t gemm_decoded_bytes(int N, int K);  // bf16 stage images of an [N, K] projection (2 N K bytes)
+// The dequantise-once predecode of projection P into wdec, on its own.
+cudaError_t launch_gemm_predecode(const GemmProj& P, uint8_t* wdec, size_t wdec_bytes, int num_sms, cudaStream_t s);
 bool gemm_supported(int K, int N);
 
 // ---------------------------------------------------------------------------
