@@ -94,7 +94,7 @@ constexpr int kTmemCols = 2 * BN;                           // two accumulators
 constexpr uint64_t kGemmWaitNs = 2000000000ull;             // 2 s
 
 // Dequantise-once instance (PRE): the weights of the call were decoded
-// beforehand into their fp16 stage images, so a load stage is the activation
+// beforehand into their bf16 stage images, so a load stage is the activation
 // tile plus a 32 KB decoded tile and there is no decoded ring.
 constexpr int kPreStages = 4;
 
